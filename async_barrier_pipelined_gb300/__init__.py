@@ -1,0 +1,221 @@
+"""Python binding of the gemm_f16 C ABI (include/gemm_f16.h).
+
+Argument marshalling only: every step of the product runs in the CUDA
+kernels of ``csrc/gemm_f16.cu``.  The functions keep the C names; raw
+pointers are Python ints.  ``matmul`` is a convenience that takes torch
+tensors (PyTorch is used only for device memory and streams).
+
+The library is built in-tree by ``async_barrier_pipelined_gb300.build.build()``
+(``__graft_entry__.build()`` calls it).  If it is missing, loading fails
+loudly; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+__all__ = [
+    "GemmError", "load", "gemm_f16_plan", "gemm_f16_run", "gemm_f16_run_host",
+    "gemm_f16_destroy", "gemm_f16_status", "gemm_f16_set_option",
+    "gemm_f16_strerror", "gemm_f16_last_cuda_error", "gemm_f16_validate",
+    "gemm_f16_tile_order", "gemm_f16_tile_shape", "Plan", "matmul",
+    "OK", "ERR_INVALID_ARG", "ERR_MISALIGNED", "ERR_UNSUPPORTED_DEVICE",
+    "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT",
+    "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "EXPORTED_SYMBOLS",
+]
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_MISALIGNED = -2
+ERR_UNSUPPORTED_DEVICE = -3
+ERR_OOM = -4
+ERR_CUDA = -5
+ERR_TIMEOUT = -6
+
+OPT_TIMEOUT_NS = 1
+OPT_TILE_ORDER = 2
+OPT_FAULT_UNIT = 3
+
+_c_int, _c_i64, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
+
+#: name -> (restype, argtypes) for every entry point of include/gemm_f16.h
+_SIGNATURES = {
+    "gemm_f16_plan": (_c_int, [ctypes.POINTER(_vp), _c_int]),
+    "gemm_f16_run": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
+                              _vp, _c_i64, _c_int, _vp]),
+    "gemm_f16_run_host": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
+                                   _vp, _c_i64, _c_int, _vp]),
+    "gemm_f16_destroy": (_c_int, [_vp]),
+    "gemm_f16_status": (_c_int, [_vp]),
+    "gemm_f16_set_option": (_c_int, [_vp, _c_int, _c_i64]),
+    "gemm_f16_strerror": (ctypes.c_char_p, [_c_int]),
+    "gemm_f16_last_cuda_error": (ctypes.c_char_p, []),
+    "gemm_f16_validate": (_c_int, [_c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
+                                   _vp, _c_i64, _c_int]),
+    "gemm_f16_tile_order": (_c_i64, [_c_int, _c_int, _c_int,
+                                     ctypes.POINTER(ctypes.c_uint32), _c_i64]),
+    "gemm_f16_tile_shape": (_c_int, [ctypes.POINTER(_c_int)] * 4),
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmError(RuntimeError):
+    """A negative gemm_f16 return code."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = gemm_f16_strerror(code)
+        if code == ERR_CUDA:
+            msg += f" [{gemm_f16_last_cuda_error()}]"
+        super().__init__(f"{where}: {msg} (code {code})")
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"gemm_f16 library not built ({LIB_PATH} missing); run "
+                    "async_barrier_pipelined_gb300.build.build() first. "
+                    "There is no fallback implementation.")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _check(rc: int, where: str) -> int:
+    if rc < 0:
+        raise GemmError(rc, where)
+    return rc
+
+
+def gemm_f16_strerror(code: int) -> str:
+    return load().gemm_f16_strerror(code).decode()
+
+
+def gemm_f16_last_cuda_error() -> str:
+    return load().gemm_f16_last_cuda_error().decode()
+
+
+def gemm_f16_plan(device: int = 0) -> int:
+    """Create a plan on ``device``; returns the opaque handle as an int."""
+    h = _vp()
+    _check(load().gemm_f16_plan(ctypes.byref(h), device), "gemm_f16_plan")
+    return h.value
+
+
+def gemm_f16_destroy(plan: int) -> None:
+    _check(load().gemm_f16_destroy(plan), "gemm_f16_destroy")
+
+
+def gemm_f16_status(plan: int) -> int:
+    """Device-reported status since the last call (0 or ERR_TIMEOUT); clears it."""
+    return load().gemm_f16_status(plan)
+
+
+def gemm_f16_set_option(plan: int, option: int, value: int) -> None:
+    _check(load().gemm_f16_set_option(plan, option, value), "gemm_f16_set_option")
+
+
+def gemm_f16_run(plan: int, M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int,
+                 C: int, ldc: int, split_k: int = 1, stream: int = 0) -> None:
+    """Enqueue C = A*B (device pointers) on ``stream`` (a cudaStream_t as int)."""
+    _check(load().gemm_f16_run(plan, M, N, K, A, lda, B, ldb, C, ldc, split_k, stream),
+           "gemm_f16_run")
+
+
+def gemm_f16_run_host(plan: int, M: int, N: int, K: int, hA: int, lda: int, hB: int,
+                      ldb: int, hC: int, ldc: int, split_k: int = 1, stream: int = 0) -> None:
+    """Enqueue copy-in, C = A*B and copy-out for HOST pointers on ``stream``."""
+    _check(load().gemm_f16_run_host(plan, M, N, K, hA, lda, hB, ldb, hC, ldc, split_k,
+                                    stream), "gemm_f16_run_host")
+
+
+def gemm_f16_validate(M, N, K, A, lda, B, ldb, C, ldc, split_k) -> int:
+    return load().gemm_f16_validate(M, N, K, A, lda, B, ldb, C, ldc, split_k)
+
+
+def gemm_f16_tile_order(tiles_m: int, tiles_n: int, order: int = 0) -> list:
+    """Tile order as a list of (tile_m, tile_n)."""
+    n = _check(load().gemm_f16_tile_order(tiles_m, tiles_n, order, None, 0),
+               "gemm_f16_tile_order")
+    buf = (ctypes.c_uint32 * n)()
+    _check(load().gemm_f16_tile_order(tiles_m, tiles_n, order, buf, n), "gemm_f16_tile_order")
+    return [(v & 0xFFFF, v >> 16) for v in buf]
+
+
+def gemm_f16_tile_shape() -> tuple:
+    """(BM, BN, BK, STAGES) of the compiled kernel."""
+    vals = [_c_int() for _ in range(4)]
+    load().gemm_f16_tile_shape(*[ctypes.byref(v) for v in vals])
+    return tuple(v.value for v in vals)
+
+
+class Plan:
+    """Owning wrapper of a plan handle."""
+
+    def __init__(self, device: int = 0):
+        self.device = device
+        self.handle = gemm_f16_plan(device)
+
+    def close(self):
+        if self.handle:
+            gemm_f16_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def status(self) -> int:
+        return gemm_f16_status(self.handle)
+
+    def set_option(self, option: int, value: int) -> None:
+        gemm_f16_set_option(self.handle, option, value)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def matmul(plan: Plan, A, B, C=None, split_k: int = 1, stream=None):
+    """C = A @ B for row-major float16 CUDA tensors (C allocated if None)."""
+    import torch
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be torch.float16")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)}")
+    if A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("A and B must be row-major (unit column stride)")
+    M, K = A.shape
+    N = B.shape[1]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    elif C.dtype != torch.float16 or tuple(C.shape) != (M, N) or C.stride(1) != 1:
+        raise ValueError("C must be a row-major float16 M x N tensor")
+    gemm_f16_run(plan.handle, M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
+                 C.data_ptr(), C.stride(0), split_k, _stream_handle(stream))
+    return C

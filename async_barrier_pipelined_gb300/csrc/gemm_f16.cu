@@ -1,0 +1,855 @@
+// Barrier-pipelined FP16 GEMM for GB300 (sm_103a): C = A * B, FP32 accumulate.
+//
+// One persistent CTA per SM, 192 threads in three roles:
+//   warp 0      TMA producer: one elected lane fills a STAGES-deep ring of
+//               shared-memory stages (A tile 128x64, B tile 64x256, 48 KB).
+//               Per stage it arrives on full[s] with expect_tx(48 KB) and
+//               issues the copies, which complete the transaction bytes.
+//   warp 1      allocates 512 TMEM columns (two 128x256 FP32 accumulators)
+//               and one lane issues tcgen05.mma (128x256x16, four per
+//               k-block), releasing each stage with tcgen05.commit -> empty[s]
+//               and handing a finished accumulator over with
+//               tcgen05.commit -> tmem_full[acc].
+//   warps 2..5  epilogue: tcgen05.ld of its 32-lane TMEM quarter, FP16
+//               round-to-nearest-even, swizzled shared staging, TMA store.
+//               (Split runs store FP32 partial tiles instead.)  Each warp
+//               arrives on tmem_empty[acc] when it has read the accumulator,
+//               so the MMA warp can start the next tile in the other one.
+//
+// This is the split-barrier pattern of the "Xe2 Nbarrier Pipelining" page
+// ("Core Concept: Split Barrier"; "Producer-Consumer Pattern") carried over
+// to mbarriers: the producer arrives (expect_tx) and moves on; consumers wait
+// as late as possible.  The barrier rules followed are those of the
+// "mbarrier State and Operations" page ("Phase Completion Condition", "Core
+// APIs", "Three update paths").  One arrive per barrier phase per role, with
+// no second arrive before the phase completes ("Xe2 Nbarrier Pipelining",
+// "What Doesn't Work: Double-Arrive Deadlock"); every role walks the same
+// work units and k-blocks, so arrivals and waits stay balanced on every path
+// ("Xe2 ESIMD GEMM" page, "Hardware limits": equal barrier counts; "Insert
+// Cluster Barrier Pass" page, Rules 4-5: handshakes balanced across tail
+// and drain).  Ragged edges need no tail loop: the tensor copies fill
+// out-of-bounds elements with zero and clip stores at the tensor bounds.
+//
+// Every barrier wait is bounded: past the plan's time limit the role records
+// GEMM_F16_ERR_TIMEOUT, raises a CTA-wide abort flag, stops issuing, waits
+// (bounded) for its own operations in flight, and the CTA frees its TMEM and
+// exits.
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <utility>
+#include <vector>
+
+#include "gemm_f16.h"
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace gf16 {
+
+// ------------------------------------------------------------------ tiling
+constexpr int BM = 128;          // output tile rows (= MMA M, = TMEM lanes)
+constexpr int BN = 256;          // output tile columns (= MMA N)
+constexpr int BK = 64;           // k-block: 64 halves = one 128-byte swizzle row
+constexpr int UMMA_K = 16;       // K of one kind::f16 MMA
+constexpr int STAGES = 4;
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARP0 = 2;
+constexpr int EPI_WARPS = 4;
+
+constexpr uint32_t A_STAGE = BM * BK * 2;        // 16 KB
+constexpr uint32_t B_BOX_N = 64;                 // N extent of one B copy (128 B)
+constexpr uint32_t B_BOX = B_BOX_N * BK * 2;     // 8 KB
+constexpr uint32_t B_STAGE = BN * BK * 2;        // 32 KB
+constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE; // bytes credited per stage
+constexpr uint32_t EPI_BUF = 32 * 64;            // 32 rows x 64 B staging box
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COLS = BN;
+
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
+constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_STAGE;
+constexpr uint32_t OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
+constexpr uint32_t NUM_BARS = 2 * STAGES + 2 + 2 + 1;  // full, empty, tmem_full, tmem_empty, mma_done
+constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
+constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // room to align the base to 1024
+static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit per CTA");
+static_assert(OFF_EPI % 1024 == 0 && OFF_B % 1024 == 0, "swizzled buffers need 1024-B alignment");
+static_assert(2 * ACC_COLS <= TMEM_COLS, "two accumulators must fit in TMEM");
+
+// Instruction descriptor of tcgen05.mma kind::f16: D FP32 (bits 4-5 = 1),
+// A and B FP16 (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B MN-major
+// (bit 16 = 1, row-major B is N-contiguous), N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28.
+constexpr uint32_t make_idesc(int m, int n) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+constexpr uint32_t IDESC = make_idesc(BM, BN);
+
+// Shared-memory matrix descriptor (tcgen05): start address >> 4 (bits 0-13),
+// leading byte offset >> 4 (16-29), stride byte offset >> 4 (32-45), fixed
+// 0b001 at bits 46-48, base offset 0, swizzle mode 2 = 128-byte (bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// A tile (K-major, 128-byte swizzle): 8-row groups 1024 B apart (SBO); the
+// leading offset is unused for swizzled K-major operands.  One MMA K-slice
+// of 16 halves is 32 bytes, so slice k starts 32*k bytes into the rows.
+constexpr uint32_t A_LBO = 16, A_SBO = 1024, A_KSTEP = UMMA_K * 2;
+// B tile (MN-major, 128-byte swizzle): 64-column groups 8 KB apart along N
+// (LBO, one TMA box each), 8-row groups of K 1024 B apart (SBO).  Slice k
+// covers rows 16k .. 16k+15, i.e. 2048 bytes further.
+constexpr uint32_t B_LBO = B_BOX, B_SBO = 1024, B_KSTEP = UMMA_K * 128;
+
+struct Params {
+  int M, N, K;
+  int tiles_m, tiles_n, split_k, kblocks, num_units;
+  const uint32_t* order;   // tile order: tiles_m*tiles_n packed (tm | tn<<16)
+  int* status;             // device-visible status word
+  unsigned long long timeout_ns;
+  int fault_unit;          // test only: unit whose first stage gets no copy
+};
+
+struct Bars {
+  uint32_t full, empty, tfull, tempty, mma_done;  // shared addresses of the arrays
+};
+
+// ------------------------------------------------------------------ waits
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Params& p,
+                                       volatile int* abort_flag) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer() - t0 > p.timeout_ns) {
+      *abort_flag = 1;
+      *(volatile int*)p.status = (int)GEMM_F16_ERR_TIMEOUT;
+      __threadfence_system();
+      return false;
+    }
+  }
+}
+
+// Bounded phase wait; false if it timed out or another role aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
+                                           volatile int* abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, p, abort_flag);
+}
+
+// Bounded wait used while draining after an abort (ignores the abort flag).
+__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ roles
+__device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                              const Params& p, uint32_t base, const Bars& b,
+                                              volatile int* abort_flag) {
+  RingPos pos{0, 0};
+  uint32_t issued = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    int tpos, s, kb0, kb1;
+    decode_unit(u, p.split_k, &tpos, &s);
+    split_range(p.kblocks, p.split_k, s, &kb0, &kb1);
+    const uint32_t packed = p.order[tpos];
+    const int m0 = (int)tile_m_of(packed) * BM;
+    const int n0 = (int)tile_n_of(packed) * BN;
+    const int skip_kb = (u == p.fault_unit) ? kb0 : -1;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!wait_phase(b.empty + 8 * pos.stage, producer_wait_parity(pos), p, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = b.full + 8 * pos.stage;
+      ptx::mbar_arrive_expect_tx(fb, STAGE_TX);
+      if (kb != skip_kb) {
+        const uint32_t sa = base + OFF_A + pos.stage * A_STAGE;
+        const uint32_t sb = base + OFF_B + pos.stage * B_STAGE;
+        const int k0 = kb * BK;
+        ptx::tma_load_2d(sa, tmA, fb, k0, m0);
+#pragma unroll
+        for (int j = 0; j < BN / (int)B_BOX_N; ++j)
+          ptx::tma_load_2d(sb + j * B_BOX, tmB, fb, n0 + j * (int)B_BOX_N, k0);
+      }
+      ++issued;
+      ring_advance(pos, STAGES);
+    }
+  }
+  if (!ok) {
+    // Wait for the copies of the most recent stages (one per stage) so that
+    // no tensor copy still writes this CTA's shared memory when it exits.
+    RingPos q = pos;
+    const uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
+    for (uint32_t i = 0; i < n; ++i) {
+      ring_retreat(q, STAGES);
+      wait_drain(b.full + 8 * q.stage, consumer_wait_parity(q), p.timeout_ns);
+    }
+  }
+}
+
+__device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_t tmem_base,
+                                         const Bars& b, volatile int* abort_flag) {
+  RingPos pos{0, 0};
+  uint32_t local = 0;
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int tpos, s, kb0, kb1;
+    decode_unit(u, p.split_k, &tpos, &s);
+    split_range(p.kblocks, p.split_k, s, &kb0, &kb1);
+    const uint32_t acc = local & 1u;
+    const uint32_t acc_phase = (local >> 1) & 1u;
+    if (!wait_phase(b.tempty + 8 * acc, acc_phase ^ 1u, p, abort_flag)) break;
+    ptx::tc_fence_after();
+    const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+    bool ok = true;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint64_t a_desc =
+          smem_desc_sw128(base + OFF_A + pos.stage * A_STAGE, A_LBO, A_SBO);
+      const uint64_t b_desc =
+          smem_desc_sw128(base + OFF_B + pos.stage * B_STAGE, B_LBO, B_SBO);
+      const uint32_t first = (kb == kb0) ? 1u : 0u;
+#pragma unroll
+      for (int k = 0; k < BK / UMMA_K; ++k) {
+        ptx::mma_f16(d_tmem, a_desc + ((k * A_KSTEP) >> 4), b_desc + ((k * B_KSTEP) >> 4), IDESC,
+                     (first && k == 0) ? 0u : 1u);
+      }
+      ptx::mma_commit(b.empty + 8 * pos.stage);
+      ring_advance(pos, STAGES);
+    }
+    if (!ok) break;
+    ptx::mma_commit(b.tfull + 8 * acc);
+    ++local;
+  }
+  // Every MMA issued so far must be finished before TMEM is freed.
+  ptx::mma_commit(b.mma_done);
+  wait_drain(b.mma_done, 0, p.timeout_ns);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(uint32_t lo, uint32_t hi) {
+  __half2 h = __floats2half2_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUtensorMap* tmW,
+                                              const Params& p, uint32_t base, uint32_t tmem_base,
+                                              const Bars& b, uint32_t warp, uint32_t lane,
+                                              volatile int* abort_flag) {
+  const uint32_t quarter = warp & 3u;  // TMEM lanes 32*quarter .. +31 are this warp's
+  const uint32_t stage0 = base + OFF_EPI + (warp - EPI_WARP0) * 2 * EPI_BUF;
+  // Staging layout = the tensor copy's 64-byte swizzle: row r at r*64, its
+  // 16-byte chunk c at chunk position c ^ ((r >> 1) & 3).
+  const uint32_t row_off = lane * 64u;
+  const uint32_t sw = (lane >> 1) & 3u;
+  uint32_t local = 0, nstore = 0;
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    int tpos, s;
+    decode_unit(u, p.split_k, &tpos, &s);
+    const uint32_t packed = p.order[tpos];
+    const int m0 = (int)tile_m_of(packed) * BM;
+    const int n0 = (int)tile_n_of(packed) * BN;
+    const uint32_t acc = local & 1u;
+    const uint32_t acc_phase = (local >> 1) & 1u;
+    bool got = wait_phase(b.tfull + 8 * acc, acc_phase, p, abort_flag);
+    if (!__all_sync(0xffffffffu, got)) break;
+    ptx::tc_fence_after();
+    const int row0 = m0 + (int)quarter * 32;
+    const uint32_t t_row = tmem_base + acc * ACC_COLS + ((quarter * 32u) << 16);
+    if (row0 < p.M) {
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = n0 + c * 32;
+        if (col0 >= p.N) break;
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c * 32u, r);
+        ptx::tmem_ld_wait();
+        if (p.split_k == 1) {
+          const uint32_t buf = stage0 + (nstore & 1u) * EPI_BUF;
+          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (uint32_t j = 0; j < 4; ++j) {
+            ptx::st_shared_v4(buf + row_off + ((j ^ sw) << 4), pack_half2(r[8 * j + 0], r[8 * j + 1]),
+                              pack_half2(r[8 * j + 2], r[8 * j + 3]),
+                              pack_half2(r[8 * j + 4], r[8 * j + 5]),
+                              pack_half2(r[8 * j + 6], r[8 * j + 7]));
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(tmC, buf, col0, row0);
+            ptx::bulk_commit_group();
+          }
+          ++nstore;
+        } else {
+#pragma unroll
+          for (uint32_t h = 0; h < 2; ++h) {
+            if (col0 + 16 * (int)h >= p.N) break;
+            const uint32_t buf = stage0 + (nstore & 1u) * EPI_BUF;
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j) {
+              const uint32_t* v = &r[16 * h + 4 * j];
+              ptx::st_shared_v4(buf + row_off + ((j ^ sw) << 4), v[0], v[1], v[2], v[3]);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(tmW, buf, col0 + 16 * (int)h, row0, s);
+              ptx::bulk_commit_group();
+            }
+            ++nstore;
+          }
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(b.tempty + 8 * acc);
+    ++local;
+  }
+  if (lane == 0) ptx::bulk_wait_group<0>();
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ kernels
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
+                    const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
+  const uint32_t lane = threadIdx.x & 31u;
+
+  Bars b;
+  b.full = base + OFF_BAR;
+  b.empty = b.full + 8 * STAGES;
+  b.tfull = b.empty + 8 * STAGES;
+  b.tempty = b.tfull + 16;
+  b.mma_done = b.tempty + 16;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmC);
+    if (p.split_k > 1) ptx::prefetch_tmap(&tmW);
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(b.full + 8 * s, 1);   // the producer's arrive.expect_tx (+ tx bytes)
+      ptx::mbar_init(b.empty + 8 * s, 1);  // one tcgen05.commit per use
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(b.tfull + 8 * a, 1);           // one tcgen05.commit per tile
+      ptx::mbar_init(b.tempty + 8 * a, EPI_WARPS);  // one arrive per epilogue warp
+    }
+    ptx::mbar_init(b.mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(base + OFF_TMEM_SLOT, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
+
+  if (warp == 0) {
+    if (lane == 0) producer_role(&tmA, &tmB, p, base, b, abort_flag);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_role(p, base, tmem_base, b, abort_flag);
+    __syncwarp();
+  } else {
+    epilogue_role(&tmC, &tmW, p, base, tmem_base, b, warp, lane, abort_flag);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// Fixed-order split reduction: C[i,j] = fp16_rn(P_0 + P_1 + ... + P_{S-1}),
+// summed left to right in FP32.  Each thread owns 8 consecutive columns.
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float* __restrict__ ws, int M, int N, int64_t ldw, int split_k,
+                         int64_t split_stride, __half* __restrict__ C, int64_t ldc) {
+  const int64_t groups = (N + 7) / 8;
+  const int64_t total = (int64_t)M * groups;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = g / groups;
+    const int j = (int)(g - i * groups) * 8;
+    const float* src = ws + i * ldw + j;
+    float4 lo = *reinterpret_cast<const float4*>(src);
+    float4 hi = *reinterpret_cast<const float4*>(src + 4);
+    for (int s = 1; s < split_k; ++s) {
+      src += split_stride;
+      const float4 a = *reinterpret_cast<const float4*>(src);
+      const float4 c = *reinterpret_cast<const float4*>(src + 4);
+      lo.x += a.x; lo.y += a.y; lo.z += a.z; lo.w += a.w;
+      hi.x += c.x; hi.y += c.y; hi.z += c.z; hi.w += c.w;
+    }
+    const __half2 h0 = __floats2half2_rn(lo.x, lo.y), h1 = __floats2half2_rn(lo.z, lo.w);
+    const __half2 h2 = __floats2half2_rn(hi.x, hi.y), h3 = __floats2half2_rn(hi.z, hi.w);
+    __half* dst = C + i * ldc + j;
+    if (j + 8 <= N) {
+      uint4 v;
+      v.x = *reinterpret_cast<const uint32_t*>(&h0);
+      v.y = *reinterpret_cast<const uint32_t*>(&h1);
+      v.z = *reinterpret_cast<const uint32_t*>(&h2);
+      v.w = *reinterpret_cast<const uint32_t*>(&h3);
+      *reinterpret_cast<uint4*>(dst) = v;
+    } else {
+      const __half vals[8] = {__low2half(h0), __high2half(h0), __low2half(h1), __high2half(h1),
+                              __low2half(h2), __high2half(h2), __low2half(h3), __high2half(h3)};
+      for (int t = 0; t < N - j; ++t) dst[t] = vals[t];
+    }
+  }
+}
+
+}  // namespace gf16
+
+// ====================================================================== host
+using namespace gf16;
+
+namespace {
+
+thread_local char g_last_cuda_error[512] = "no CUDA error recorded";
+
+int cuda_fail(cudaError_t e, const char* what) {
+  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%s)", what,
+                cudaGetErrorName(e), cudaGetErrorString(e));
+  return (e == cudaErrorMemoryAllocation) ? GEMM_F16_ERR_OOM : GEMM_F16_ERR_CUDA;
+}
+
+#define GF16_CUDA(call, what)                          \
+  do {                                                 \
+    cudaError_t e_ = (call);                           \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swz, CUtensorMapL2promotion promo) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "cuTensorMapEncodeTiled entry point not available");
+    return GEMM_F16_ERR_CUDA;
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return GEMM_F16_ERR_CUDA;
+  }
+  return GEMM_F16_OK;
+}
+
+int encode_3d_f32(CUtensorMap* map, const void* ptr, uint64_t n, uint64_t m, uint64_t s,
+                  uint64_t row_bytes, uint64_t plane_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return GEMM_F16_ERR_CUDA;
+  const cuuint64_t dims[3] = {n, m, s};
+  const cuuint64_t strides[2] = {row_bytes, plane_bytes};
+  const cuuint32_t box[3] = {16, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "cuTensorMapEncodeTiled (workspace) failed (CUresult %d)", (int)r);
+    return GEMM_F16_ERR_CUDA;
+  }
+  return GEMM_F16_OK;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool switched = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      switched = (cudaSetDevice(dev) == cudaSuccess);
+    }
+  }
+  ~DeviceGuard() {
+    if (switched) cudaSetDevice(prev);
+  }
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+void build_tile_order(int tiles_m, int tiles_n, int order, std::vector<uint32_t>& out) {
+  out.clear();
+  out.reserve((size_t)tiles_m * tiles_n);
+  if (order == 1) {
+    for (int tm = 0; tm < tiles_m; ++tm)
+      for (int tn = 0; tn < tiles_n; ++tn) out.push_back(pack_tile(tm, tn));
+    return;
+  }
+  std::vector<std::pair<uint32_t, uint32_t>> coded;
+  coded.reserve(out.capacity());
+  for (int tm = 0; tm < tiles_m; ++tm)
+    for (int tn = 0; tn < tiles_n; ++tn)
+      coded.emplace_back(morton_code((uint32_t)tm, (uint32_t)tn), pack_tile(tm, tn));
+  std::sort(coded.begin(), coded.end());
+  for (auto& c : coded) out.push_back(c.second);
+}
+
+struct OrderTable {
+  int tiles_m, tiles_n, order;
+  uint32_t* dev;
+};
+
+}  // namespace
+
+struct gemm_f16_plan_s {
+  int device = 0;
+  int num_sms = 0;
+  int* status_host = nullptr;  // mapped pinned host memory
+  int* status_dev = nullptr;
+  unsigned long long timeout_ns = 1000000000ull;
+  int tile_order = 0;
+  int fault_unit = -1;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  std::vector<OrderTable> orders;
+  void* hbuf[3] = {nullptr, nullptr, nullptr};  // device staging for run_host
+  size_t hcap[3] = {0, 0, 0};
+};
+
+extern "C" {
+
+const char* gemm_f16_strerror(int code) {
+  switch (code) {
+    case GEMM_F16_OK: return "ok";
+    case GEMM_F16_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_F16_ERR_MISALIGNED: return "pointer not 16-byte aligned or leading dimension not a multiple of 8";
+    case GEMM_F16_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    case GEMM_F16_ERR_OOM: return "out of memory";
+    case GEMM_F16_ERR_CUDA: return "CUDA call failed";
+    case GEMM_F16_ERR_TIMEOUT: return "an in-kernel barrier wait timed out";
+    default: return "unknown error code";
+  }
+}
+
+const char* gemm_f16_last_cuda_error(void) { return g_last_cuda_error; }
+
+int gemm_f16_tile_shape(int* bm, int* bn, int* bk, int* stages) {
+  if (bm) *bm = BM;
+  if (bn) *bn = BN;
+  if (bk) *bk = BK;
+  if (stages) *stages = STAGES;
+  return GEMM_F16_OK;
+}
+
+int gemm_f16_validate(int M, int N, int K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                      const void* C, int64_t ldc, int split_k) {
+  if (M <= 0 || N <= 0 || K <= 0) return GEMM_F16_ERR_INVALID_ARG;
+  if (ceil_div(M, BM) > 65535 || ceil_div(N, BN) > 65535) return GEMM_F16_ERR_INVALID_ARG;
+  if (!A || !B || !C) return GEMM_F16_ERR_INVALID_ARG;
+  if (lda < K || ldb < N || ldc < N) return GEMM_F16_ERR_INVALID_ARG;
+  if (split_k < 1 || split_k > ceil_div(K, BK)) return GEMM_F16_ERR_INVALID_ARG;
+  if (((uintptr_t)A | (uintptr_t)B | (uintptr_t)C) & 15u) return GEMM_F16_ERR_MISALIGNED;
+  if ((lda | ldb | ldc) & 7) return GEMM_F16_ERR_MISALIGNED;
+  return GEMM_F16_OK;
+}
+
+int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order, uint32_t* out, int64_t cap) {
+  if (tiles_m < 1 || tiles_n < 1 || tiles_m > 65535 || tiles_n > 65535) return GEMM_F16_ERR_INVALID_ARG;
+  if (order != 0 && order != 1) return GEMM_F16_ERR_INVALID_ARG;
+  if (cap < 0 || (cap > 0 && !out)) return GEMM_F16_ERR_INVALID_ARG;
+  std::vector<uint32_t> v;
+  build_tile_order(tiles_m, tiles_n, order, v);
+  const int64_t n = (int64_t)v.size();
+  std::memcpy(out, v.data(), sizeof(uint32_t) * (size_t)std::min<int64_t>(n, cap));
+  return n;
+}
+
+int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
+  if (!out) return GEMM_F16_ERR_INVALID_ARG;
+  *out = nullptr;
+  int ndev = 0;
+  GF16_CUDA(cudaGetDeviceCount(&ndev), "cudaGetDeviceCount");
+  if (device < 0 || device >= ndev) return GEMM_F16_ERR_INVALID_ARG;
+  cudaDeviceProp prop;
+  GF16_CUDA(cudaGetDeviceProperties(&prop, device), "cudaGetDeviceProperties");
+  if (prop.major != 10 || prop.minor != 3) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+  DeviceGuard g(device);
+  GF16_CUDA(cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES),
+            "cudaFuncSetAttribute(max dynamic smem)");
+  gemm_f16_plan_s* p = new (std::nothrow) gemm_f16_plan_s();
+  if (!p) return GEMM_F16_ERR_OOM;
+  p->device = device;
+  p->num_sms = prop.multiProcessorCount;
+  cudaError_t e = cudaHostAlloc(&p->status_host, sizeof(int), cudaHostAllocMapped);
+  if (e != cudaSuccess) {
+    delete p;
+    return cuda_fail(e, "cudaHostAlloc(status)");
+  }
+  *p->status_host = 0;
+  e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&p->status_dev), p->status_host, 0);
+  if (e != cudaSuccess) {
+    cudaFreeHost(p->status_host);
+    delete p;
+    return cuda_fail(e, "cudaHostGetDevicePointer(status)");
+  }
+  *out = p;
+  return GEMM_F16_OK;
+}
+
+int gemm_f16_destroy(gemm_f16_plan_t p) {
+  if (!p) return GEMM_F16_OK;
+  {
+    DeviceGuard g(p->device);
+    cudaDeviceSynchronize();
+    for (auto& t : p->orders) cudaFree(t.dev);
+    if (p->ws) cudaFree(p->ws);
+    for (int i = 0; i < 3; ++i)
+      if (p->hbuf[i]) cudaFree(p->hbuf[i]);
+    if (p->status_host) cudaFreeHost(p->status_host);
+  }
+  delete p;
+  return GEMM_F16_OK;
+}
+
+int gemm_f16_status(gemm_f16_plan_t p) {
+  if (!p) return GEMM_F16_ERR_INVALID_ARG;
+  volatile int* s = p->status_host;
+  const int v = *s;
+  *s = 0;
+  return v;
+}
+
+int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
+  if (!p) return GEMM_F16_ERR_INVALID_ARG;
+  switch (option) {
+    case GEMM_F16_OPT_TIMEOUT_NS:
+      if (value <= 0) return GEMM_F16_ERR_INVALID_ARG;
+      p->timeout_ns = (unsigned long long)value;
+      return GEMM_F16_OK;
+    case GEMM_F16_OPT_TILE_ORDER:
+      if (value != 0 && value != 1) return GEMM_F16_ERR_INVALID_ARG;
+      p->tile_order = (int)value;
+      return GEMM_F16_OK;
+    case GEMM_F16_OPT_FAULT_UNIT:
+      if (value < -1 || value > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
+      p->fault_unit = (int)value;
+      return GEMM_F16_OK;
+    default:
+      return GEMM_F16_ERR_INVALID_ARG;
+  }
+}
+
+}  // extern "C"
+
+namespace {
+
+int get_order_table(gemm_f16_plan_s* p, int tiles_m, int tiles_n, const uint32_t** out) {
+  for (auto& t : p->orders) {
+    if (t.tiles_m == tiles_m && t.tiles_n == tiles_n && t.order == p->tile_order) {
+      *out = t.dev;
+      return GEMM_F16_OK;
+    }
+  }
+  std::vector<uint32_t> host;
+  build_tile_order(tiles_m, tiles_n, p->tile_order, host);
+  uint32_t* dev = nullptr;
+  GF16_CUDA(cudaMalloc(&dev, host.size() * sizeof(uint32_t)), "cudaMalloc(tile order)");
+  cudaError_t e = cudaMemcpy(dev, host.data(), host.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(dev);
+    return cuda_fail(e, "cudaMemcpy(tile order)");
+  }
+  p->orders.push_back(OrderTable{tiles_m, tiles_n, p->tile_order, dev});
+  *out = dev;
+  return GEMM_F16_OK;
+}
+
+int ensure_buffer(void** buf, size_t* cap, size_t bytes, cudaStream_t stream, const char* what) {
+  if (*cap >= bytes) return GEMM_F16_OK;
+  if (*buf) {
+    GF16_CUDA(cudaFreeAsync(*buf, stream), what);
+    *buf = nullptr;
+    *cap = 0;
+  }
+  GF16_CUDA(cudaMallocAsync(buf, bytes, stream), what);
+  *cap = bytes;
+  return GEMM_F16_OK;
+}
+
+int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t lda, const void* B,
+               int64_t ldb, void* C, int64_t ldc, int split_k, cudaStream_t stream) {
+  const int tiles_m = (int)ceil_div(M, BM);
+  const int tiles_n = (int)ceil_div(N, BN);
+  const int kblocks = (int)ceil_div(K, BK);
+  const int64_t units = (int64_t)tiles_m * tiles_n * split_k;
+  if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
+
+  const uint32_t* order = nullptr;
+  int rc = get_order_table(p, tiles_m, tiles_n, &order);
+  if (rc) return rc;
+
+  alignas(64) CUtensorMap tmA, tmB, tmC, tmW;
+  std::memset(&tmW, 0, sizeof(tmW));
+  rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
+                 (uint64_t)lda * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (rc) return rc;
+  rc = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)N, (uint64_t)K,
+                 (uint64_t)ldb * 2, B_BOX_N, BK, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (rc) return rc;
+  rc = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, (uint64_t)N, (uint64_t)M,
+                 (uint64_t)ldc * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (rc) return rc;
+
+  const int64_t ldw = (N + 7) / 8 * 8;
+  const int64_t split_stride = (int64_t)M * ldw;
+  if (split_k > 1) {
+    const size_t bytes = (size_t)split_k * (size_t)split_stride * sizeof(float);
+    rc = ensure_buffer(&p->ws, &p->ws_bytes, bytes, stream, "workspace allocation");
+    if (rc) return rc;
+    rc = encode_3d_f32(&tmW, p->ws, (uint64_t)N, (uint64_t)M, (uint64_t)split_k,
+                       (uint64_t)ldw * 4, (uint64_t)split_stride * 4);
+    if (rc) return rc;
+  }
+
+  Params prm;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.tiles_m = tiles_m;
+  prm.tiles_n = tiles_n;
+  prm.split_k = split_k;
+  prm.kblocks = kblocks;
+  prm.num_units = (int)units;
+  prm.order = order;
+  prm.status = p->status_dev;
+  prm.timeout_ns = p->timeout_ns;
+  prm.fault_unit = p->fault_unit;
+
+  const int grid = (int)std::min<int64_t>(units, p->num_sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  GF16_CUDA(cudaLaunchKernelEx(&cfg, gemm_f16_kernel, tmA, tmB, tmC, tmW, prm),
+            "launch gemm_f16_kernel");
+
+  if (split_k > 1) {
+    const int64_t groups = (int64_t)M * ((N + 7) / 8);
+    const int rgrid = (int)std::min<int64_t>(ceil_div(groups, 256), (int64_t)p->num_sms * 8);
+    cudaLaunchConfig_t rcfg = {};
+    rcfg.gridDim = dim3(rgrid, 1, 1);
+    rcfg.blockDim = dim3(256, 1, 1);
+    rcfg.stream = stream;
+    GF16_CUDA(cudaLaunchKernelEx(&rcfg, splitk_reduce_kernel, (const float*)p->ws, M, N, ldw,
+                                 split_k, split_stride, (__half*)C, (int64_t)ldc),
+              "launch splitk_reduce_kernel");
+  }
+  return GEMM_F16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f16_run(gemm_f16_plan_t p, int M, int N, int K, const void* A, int64_t lda,
+                 const void* B, int64_t ldb, void* C, int64_t ldc, int split_k,
+                 gemm_f16_stream_t stream) {
+  if (!p) return GEMM_F16_ERR_INVALID_ARG;
+  int rc = gemm_f16_validate(M, N, K, A, lda, B, ldb, C, ldc, split_k);
+  if (rc) return rc;
+  DeviceGuard g(p->device);
+  return run_device(p, M, N, K, A, lda, B, ldb, C, ldc, split_k, (cudaStream_t)stream);
+}
+
+int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, int64_t lda,
+                      const void* hB, int64_t ldb, void* hC, int64_t ldc, int split_k,
+                      gemm_f16_stream_t stream_) {
+  if (!p) return GEMM_F16_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || !hA || !hB || !hC) return GEMM_F16_ERR_INVALID_ARG;
+  if (lda < K || ldb < N || ldc < N) return GEMM_F16_ERR_INVALID_ARG;
+  const int64_t dlda = (K + 7) / 8 * 8, dldb = (N + 7) / 8 * 8, dldc = dldb;
+  int rc = gemm_f16_validate(M, N, K, (const void*)16, dlda, (const void*)16, dldb, (const void*)16,
+                             dldc, split_k);
+  if (rc) return rc;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  DeviceGuard g(p->device);
+  const size_t bytes[3] = {(size_t)M * dlda * 2, (size_t)K * dldb * 2, (size_t)M * dldc * 2};
+  for (int i = 0; i < 3; ++i) {
+    rc = ensure_buffer(&p->hbuf[i], &p->hcap[i], bytes[i], stream, "host-run staging allocation");
+    if (rc) return rc;
+  }
+  GF16_CUDA(cudaMemcpy2DAsync(p->hbuf[0], dlda * 2, hA, lda * 2, (size_t)K * 2, M,
+                              cudaMemcpyHostToDevice, stream),
+            "copy A to device");
+  GF16_CUDA(cudaMemcpy2DAsync(p->hbuf[1], dldb * 2, hB, ldb * 2, (size_t)N * 2, K,
+                              cudaMemcpyHostToDevice, stream),
+            "copy B to device");
+  rc = run_device(p, M, N, K, p->hbuf[0], dlda, p->hbuf[1], dldb, p->hbuf[2], dldc, split_k, stream);
+  if (rc) return rc;
+  GF16_CUDA(cudaMemcpy2DAsync(hC, ldc * 2, p->hbuf[2], dldc * 2, (size_t)N * 2, M,
+                              cudaMemcpyDeviceToHost, stream),
+            "copy C to host");
+  return GEMM_F16_OK;
+}
+
+}  // extern "C"

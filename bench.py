@@ -1,0 +1,412 @@
+"""Benchmark: FP16 GEMM TFLOPS on GB300 through the gemm_f16 C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gemm_4096]
+
+One step = one C = A*B of the workload (the whole hot path: tile schedule,
+TMA producer ring, tcgen05 MMA, epilogue, and for split workloads the
+fixed-order reduction).  The 4096^3 workload rotates through eight seeded A/B
+pairs (8 x 64 MiB = 512 MiB, well above the 129 MB L2), so consecutive
+steps never find their inputs in L2.  Protocol from the "Xe2 ESIMD GEMM"
+page, "Performance testing": random non-zero inputs, rotating buffers, a 5 s
+pause, >= 20 warm-up and 1000 timed iterations by default.
+
+Timing: CUDA events on the launching stream around exactly K steps, with a
+barrier and a device synchronise on both sides; max over ranks.  With
+torchrun each rank runs an independent replica on its own GPU (the GEMM has
+no exchange step, so there is no collective on the data path).
+
+Extra keys: roofline (dominant kernel vs the measured dense 16-bit tensor
+peak), cpu_baseline (the FP64 oracle on a bounded row sample, host cores),
+e2e (same metric through gemm_f16_run_host with pinned host buffers, copies
+inside the timed region), clocks (nvidia-smi sampled under load),
+gpu_launches (kernels launched in the timed region).
+
+--impl reference times the FP64 CPU oracle on the same workload instead
+(bounded row samples per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic_inputs as si  # noqa: E402
+
+METRIC = "FP16 GEMM TFLOPS at M=N=K=4096 on 1 GB300; % of dense FP16 tensor peak"
+FALLBACK_TENSOR_TFLOPS = 1900.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "async_barrier_pipelined_gb300", "csrc", f)
+                  for f in ("gemm_f16.cu", "ptx.cuh", "schedule.h")]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gemm_4096", choices=sorted(si.WORKLOADS))
+    ap.add_argument("--sleep", type=float, default=5.0,
+                    help="idle seconds before the warm-up (page protocol: 5)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU seconds for the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            pk = json.load(fh)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", 0.0)), "measured"
+    except Exception:
+        return FALLBACK_TENSOR_TFLOPS, 1700.0, "fallback"
+
+
+def load_traffic(workload: str):
+    """Per-launch DRAM bytes of the GEMM kernel from a committed ncu summary,
+    or None when the kernel source changed since it was captured."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            t = json.load(fh)
+        e = t.get(workload)
+        if e and e.get("kernel_source_sha") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.proc = None
+        self.tmp = None
+        self.marks = {}
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.interval}"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.tmp if ln.strip()]
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+        return self._summarise(rows)
+
+    def _summarise(self, rows):
+        from datetime import datetime
+        t0 = self.marks.get("load_start", 0)
+        t1 = self.marks.get("timed_end", time.time())
+        under, reasons, smax = [], set(), None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 10:
+                continue
+            try:
+                ts = datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if not (t0 <= ts <= t1 + 0.05):
+                continue
+            try:
+                sm, smx = float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            smax = smx
+            under.append(sm)
+            for name, val in zip(names, r[6:10]):
+                if val.strip() == "Active":
+                    reasons.add(name)
+        if not under:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(under), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(under),
+                "window": "last warm-up steps and the timed region"}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(w: si.Workload, rows: np.ndarray, A_bits, B_bits):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gemm_f16(A_bits, B_bits, rows=rows)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w: si.Workload, target_s: float, A_bits, B_bits):
+    """Oracle TFLOPS on a row sample sized for ~target_s seconds."""
+    import oracle
+    threads = oracle.num_threads()
+    rows = np.arange(min(w.M, max(threads, 8)))
+    t = cpu_oracle_sample(w, rows, A_bits, B_bits)          # calibration, untimed
+    per_row = max(t / len(rows), 1e-6)
+    n = int(min(w.M, max(len(rows), target_s / per_row)))
+    rows = np.linspace(0, w.M - 1, n).astype(np.int64)
+    t = cpu_oracle_sample(w, rows, A_bits, B_bits)
+    flops = 2.0 * n * w.N * w.K
+    return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {w.M} rows of C for pair 0 ({n * w.N} outputs, "
+                      f"{flops / 1e9:.1f} GFLOP in {t:.1f} s, FP64 triple loop)"}
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    import oracle
+    w = si.WORKLOADS[args.workload]
+    A_bits, B_bits = w.pair_bits(0)
+    threads = oracle.num_threads()
+    budget = 120.0
+    steps = args.steps + args.warmup
+    # size each step's sample so the whole run ends within ~budget seconds
+    probe_rows = np.arange(min(w.M, threads))
+    t = cpu_oracle_sample(w, probe_rows, A_bits, B_bits)
+    per_row = max(t / len(probe_rows), 1e-6)
+    n = int(max(1, min(w.M, budget / steps / per_row)))
+    rows_all = np.arange(w.M)
+    for i in range(args.warmup):
+        cpu_oracle_sample(w, rows_all[(i * n) % w.M:][:n], A_bits, B_bits)
+    total = 0.0
+    done_rows = 0
+    for i in range(args.steps):
+        sel = np.roll(rows_all, -((i * n) % w.M))[:n]
+        total += cpu_oracle_sample(w, sel, A_bits, B_bits)
+        done_rows += n
+    flops = 2.0 * done_rows * w.N * w.K
+    value = flops / total / 1e12
+    ms_per_step = total / args.steps * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} rows of C per step ({n}x{w.N} outputs, "
+                                   f"K={w.K}), FP64 triple loop"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w: si.Workload):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "split_k": w.split_k,
+            "pairs": len(w.keys), "layout": "row-major A (MxK), B (KxN), C (MxN)",
+            "accumulate": "f32", "inputs": f"{w.dist} scale={w.scale} eps={w.eps}",
+            "cache": ("rotating A/B pairs larger than L2"
+                      if len(w.keys) > 1 else "inputs resident (no rotation)")}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import async_barrier_pipelined_gb300 as g
+    from async_barrier_pipelined_gb300 import build as gbuild
+    gbuild.build()
+
+    w = si.WORKLOADS[args.workload]
+    npairs = len(w.keys)
+    pairs_bits = [w.pair_bits(p) for p in range(npairs)]
+    A = [torch.from_numpy(a.view(np.float16)).to(dev) for a, _ in pairs_bits]
+    B = [torch.from_numpy(b.view(np.float16)).to(dev) for _, b in pairs_bits]
+    C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = int(stream.cuda_stream)
+    plan = g.Plan(dev.index)
+    launches_per_step = 1 if w.split_k == 1 else 2
+
+    def step(i):
+        p = i % npairs
+        g.gemm_f16_run(plan.handle, w.M, w.N, w.K, A[p].data_ptr(), w.K, B[p].data_ptr(), w.N,
+                       C.data_ptr(), w.N, w.split_k, sh)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # correctness guard on this run's own inputs: one output row vs the oracle
+    step(0)
+    torch.cuda.synchronize(dev)
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(args.sleep)
+    sampler.mark("load_start")
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    ev1.synchronize()
+    barrier()
+    sampler.mark("timed_end")
+    clocks = sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    st = plan.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    flops_all = float(w.flops) * args.steps * world
+    value = flops_all / (ms_total * 1e-3) / 1e12
+
+    peak, peak_sus, peak_kind = load_peaks()
+    # dominant kernel: the GEMM kernel (for split workloads the step also
+    # holds the reduce launch; the figure is then the step's)
+    achieved = float(w.flops) / (ms_step * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": load_traffic(w.name),
+                "peak_source": f"{peak_kind} dense bf16 burst (fp16 runs at the same rate)",
+                "kernel": "gf16::gemm_f16_kernel",
+                "algorithmic_flops_per_launch": float(w.flops)}
+
+    # e2e through gemm_f16_run_host: pinned host buffers, copies timed
+    e2e = None
+    if not args.no_e2e:
+        hA = [torch.from_numpy(a.view(np.float16)).pin_memory() for a, _ in pairs_bits]
+        hB = [torch.from_numpy(b.view(np.float16)).pin_memory() for _, b in pairs_bits]
+        hC = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+
+        def host_step(i):
+            p = i % npairs
+            g.gemm_f16_run_host(plan.handle, w.M, w.N, w.K, hA[p].data_ptr(), w.K,
+                                hB[p].data_ptr(), w.N, hC.data_ptr(), w.N, w.split_k, sh)
+
+        e2e_steps = max(1, min(args.steps, 200))
+        for i in range(3):
+            host_step(i)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            host_step(i)
+        e1.record(stream)
+        e1.synchronize()
+        barrier()
+        ms_e2e = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        if plan.status() != 0:
+            raise RuntimeError("device status error in the e2e region")
+        e2e = {"value": float(w.flops) * e2e_steps * world / (ms_e2e * 1e-3) / 1e12,
+               "unit": "TFLOPS",
+               "h2d_bytes_per_step": 2 * (w.M * w.K + w.K * w.N),
+               "d2h_bytes_per_step": 2 * w.M * w.N,
+               "steps": e2e_steps, "api": "gemm_f16_run_host (pinned host buffers)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        a0, b0 = pairs_bits[0]
+        cpu = cpu_baseline(w, args.cpu_seconds, a0, b0)
+
+    plan.close()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic",
+            "config": workload_config(w),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": args.steps * launches_per_step,
+            "pct_of_peak": 100.0 * achieved / peak,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

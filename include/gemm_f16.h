@@ -1,0 +1,164 @@
+/*
+ * gemm_f16 — a barrier-pipelined FP16 GEMM for NVIDIA GB300 (sm_103a).
+ *
+ *     C = A * B        A: M x K, B: K x N, C: M x N, all row-major IEEE
+ *                      binary16; products accumulated in FP32; C rounded to
+ *                      binary16 with round-to-nearest-even.
+ *
+ * The operation is the half-precision GEMM of the "Xe2 ESIMD GEMM" page
+ * (sections "Inner-loop rules", "Payload CSE", "Tile walk order",
+ * "Correctness testing"), re-designed for Blackwell: its K loop is a ring of
+ * shared-memory stages, each guarded by mbarriers whose phase completes when
+ * the pending-arrival count and the transaction byte count both reach zero
+ * (the "mbarrier State and Operations" page, "Phase Completion Condition"
+ * and "Core APIs").  The optional split of the K range across work units is
+ * the counterpart of the global split ("GSU") named on the "Insert Cluster
+ * Barrier Pass" page, Rule 1; its partial sums are reduced in a fixed order,
+ * so split results are bitwise reproducible run to run.
+ *
+ * Conventions for every entry point below:
+ *   - Pointers named A, B, C are DEVICE pointers on the plan's device unless
+ *     the name says host (hA, hB, hC).  The caller owns them; the library
+ *     never frees them.
+ *   - Leading dimensions (lda, ldb, ldc) count elements, not bytes.
+ *   - Device pointers must be 16-byte aligned and leading dimensions must be
+ *     multiples of 8 elements (the tensor-memory-accelerator's rule for
+ *     global addresses and strides); otherwise GEMM_F16_ERR_MISALIGNED.
+ *   - Return value: GEMM_F16_OK (0) or a negative gemm_f16_error code.  On
+ *     an error no work has been enqueued.
+ *   - A plan may be used from one host thread / one stream at a time (it
+ *     owns a workspace and a status word that concurrent runs would share).
+ */
+#ifndef GEMM_F16_H
+#define GEMM_F16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_f16_plan_s *gemm_f16_plan_t;  /* opaque, library-owned */
+typedef struct CUstream_st *gemm_f16_stream_t;    /* == cudaStream_t; NULL = legacy default stream */
+
+typedef enum gemm_f16_error {
+    GEMM_F16_OK = 0,
+    GEMM_F16_ERR_INVALID_ARG = -1,        /* bad size, null pointer, ld too small, bad split_k, bad option */
+    GEMM_F16_ERR_MISALIGNED = -2,         /* pointer not 16-byte aligned or ld not a multiple of 8 */
+    GEMM_F16_ERR_UNSUPPORTED_DEVICE = -3, /* not a compute-capability 10.3 (sm_103a) device */
+    GEMM_F16_ERR_OOM = -4,                /* device or pinned-host allocation failed */
+    GEMM_F16_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed (see gemm_f16_last_cuda_error) */
+    GEMM_F16_ERR_TIMEOUT = -6             /* a bounded in-kernel wait expired (reported by gemm_f16_status) */
+} gemm_f16_error;
+
+/* Options for gemm_f16_set_option. */
+typedef enum gemm_f16_option {
+    /* Upper bound, in nanoseconds, of every in-kernel barrier wait.  When a
+     * wait runs out the kernel records GEMM_F16_ERR_TIMEOUT, stops issuing
+     * work, waits (bounded) for its own copies in flight, frees its tensor
+     * memory and returns.  Default 1e9 (1 s).  Must be > 0. */
+    GEMM_F16_OPT_TIMEOUT_NS = 1,
+    /* Order in which output tiles are handed to the persistent CTAs:
+     * 0 = Morton (Z-order, "Xe2 ESIMD GEMM" page, "Tile walk order"), the
+     * default; 1 = row-major.  Results do not depend on it. */
+    GEMM_F16_OPT_TILE_ORDER = 2,
+    /* TEST ONLY.  If >= 0, the producer of the given work unit expects the
+     * bytes of its first stage but issues no copy for it, so that stage's
+     * barrier never completes and the bounded waits must run out.  No copy
+     * is left in flight.  Default -1 (off). */
+    GEMM_F16_OPT_FAULT_UNIT = 3
+} gemm_f16_option;
+
+/*
+ * Create a plan on CUDA device `device`.  Checks the device (compute
+ * capability 10.3), sets the kernels' shared-memory limits and allocates the
+ * plan's status word (mapped pinned host memory).  The workspace for split
+ * runs and the tile-order tables are allocated on first use.
+ * `*out` receives the plan, or NULL on error.
+ */
+int gemm_f16_plan(gemm_f16_plan_t *out, int device);
+
+/*
+ * Enqueue C = A * B on `stream` (asynchronous; nothing is synchronised).
+ *   M, N, K  > 0.
+ *   A        device, M x K row-major, row stride lda >= K.
+ *   B        device, K x N row-major, row stride ldb >= N.
+ *   C        device, M x N row-major, row stride ldc >= N.  Overwritten
+ *            (no alpha/beta).  Must not overlap A or B.
+ *   split_k  1 = one pass over K per output tile.  s > 1 = the K range of
+ *            every tile is cut into s contiguous, non-empty ranges of
+ *            64-wide k-blocks (range t covers k-blocks
+ *            [floor(t*KB/s), floor((t+1)*KB/s)), KB = ceil(K/64)); each
+ *            range's FP32 partial tile goes to the plan's workspace and a
+ *            second kernel sums the s partials in order t = 0..s-1 in FP32
+ *            and rounds once to binary16.  Requires s <= KB.
+ * The first run with a new tile grid uploads that grid's tile-order table
+ * and a split run may grow the workspace; both are stream-ordered on
+ * `stream`, so make one such run before capturing the stream in a graph.
+ * Errors found on the device (a wait that timed out) are reported later by
+ * gemm_f16_status.
+ */
+int gemm_f16_run(gemm_f16_plan_t plan, int M, int N, int K,
+                 const void *A, int64_t lda, const void *B, int64_t ldb,
+                 void *C, int64_t ldc, int split_k, gemm_f16_stream_t stream);
+
+/*
+ * Same product with HOST operands: copies hA and hB into plan-owned device
+ * buffers, runs gemm_f16_run on them and copies the result into hC, all
+ * enqueued on `stream`.  Pinned host memory gives asynchronous copies; the
+ * caller must synchronise `stream` before reading hC.  Host buffers need no
+ * alignment; lda/ldb/ldc >= K/N/N (any value).  The device buffers grow on
+ * demand and stay with the plan.
+ */
+int gemm_f16_run_host(gemm_f16_plan_t plan, int M, int N, int K,
+                      const void *hA, int64_t lda, const void *hB, int64_t ldb,
+                      void *hC, int64_t ldc, int split_k,
+                      gemm_f16_stream_t stream);
+
+/* Free everything the plan owns (synchronises the plan's device).  NULL is
+ * accepted and ignored. */
+int gemm_f16_destroy(gemm_f16_plan_t plan);
+
+/*
+ * Device-reported status of the runs completed so far, then cleared:
+ * GEMM_F16_OK or GEMM_F16_ERR_TIMEOUT.  Synchronises nothing: call it after
+ * synchronising the stream of the runs it should cover.
+ */
+int gemm_f16_status(gemm_f16_plan_t plan);
+
+/* Set a gemm_f16_option (see above).  Applies to later runs. */
+int gemm_f16_set_option(gemm_f16_plan_t plan, int option, int64_t value);
+
+/* Static description of an error code (never NULL). */
+const char *gemm_f16_strerror(int code);
+
+/* Text of the last CUDA error seen by this host thread (never NULL). */
+const char *gemm_f16_last_cuda_error(void);
+
+/*
+ * Host-only argument check used by gemm_f16_run (no device needed):
+ * returns GEMM_F16_OK, GEMM_F16_ERR_INVALID_ARG or GEMM_F16_ERR_MISALIGNED.
+ */
+int gemm_f16_validate(int M, int N, int K, const void *A, int64_t lda,
+                      const void *B, int64_t ldb, const void *C, int64_t ldc,
+                      int split_k);
+
+/*
+ * Host-only: the order in which output tiles of a tiles_m x tiles_n grid
+ * are handed out (order 0 = Morton, 1 = row-major).  Writes up to `cap`
+ * entries, each (tile_m | tile_n << 16), into `out` and returns the number
+ * of tiles (tiles_m * tiles_n), or a negative error code.  tiles_m and
+ * tiles_n must be in [1, 65535].
+ */
+int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order,
+                            uint32_t *out, int64_t cap);
+
+/* Compile-time tile shape of the kernel: BM x BN output tile, BK k-block. */
+int gemm_f16_tile_shape(int *bm, int *bn, int *bk, int *stages);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F16_H */

@@ -1,0 +1,143 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every entry point
+that include/gemm_f16.h declares, and its host-side logic (argument
+validation, tile order) behaves as documented.  No compute call is made.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import async_barrier_pipelined_gb300 as g
+from async_barrier_pipelined_gb300 import build as gbuild
+
+HEADER = os.path.join(gbuild.INCLUDE, "gemm_f16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return g.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_f16_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert _declared_functions() == sorted(g.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_strerror_covers_codes(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert g.gemm_f16_strerror(code) != "unknown error code"
+    assert g.gemm_f16_strerror(-99) == "unknown error code"
+
+
+def test_tile_shape(lib):
+    assert g.gemm_f16_tile_shape() == (128, 256, 64, 4)
+
+
+P = 1 << 20  # a 16-byte-aligned fake address (never dereferenced)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((256, 256, 256, P, 256, P, 256, P, 256, 1), g.OK),
+    ((4000, 4104, 3000, P, 3000, P, 4104, P, 4104, 1), g.OK),
+    ((512, 512, 32768, P, 32768, P, 512, P, 512, 16), g.OK),
+    ((1, 1, 1, P, 8, P, 8, P, 8, 1), g.OK),
+    ((0, 8, 8, P, 8, P, 8, P, 8, 1), g.ERR_INVALID_ARG),
+    ((8, 0, 8, P, 8, P, 8, P, 8, 1), g.ERR_INVALID_ARG),
+    ((8, 8, 0, P, 8, P, 8, P, 8, 1), g.ERR_INVALID_ARG),
+    ((8, 8, 8, 0, 8, P, 8, P, 8, 1), g.ERR_INVALID_ARG),
+    ((8, 8, 8, P, 8, 0, 8, P, 8, 1), g.ERR_INVALID_ARG),
+    ((8, 8, 8, P, 8, P, 8, 0, 8, 1), g.ERR_INVALID_ARG),
+    ((8, 8, 16, P, 8, P, 8, P, 8, 1), g.ERR_INVALID_ARG),     # lda < K
+    ((8, 16, 8, P, 8, P, 8, P, 16, 1), g.ERR_INVALID_ARG),    # ldb < N
+    ((8, 16, 8, P, 8, P, 16, P, 8, 1), g.ERR_INVALID_ARG),    # ldc < N
+    ((8, 8, 8, P, 8, P, 8, P, 8, 0), g.ERR_INVALID_ARG),      # split_k < 1
+    ((8, 8, 128, P, 128, P, 8, P, 8, 3), g.ERR_INVALID_ARG),  # split_k > ceil(K/64)
+    ((8, 8, 128, P, 128, P, 8, P, 8, 2), g.OK),
+    ((8, 8, 8, P + 8, 8, P, 8, P, 8, 1), g.ERR_MISALIGNED),
+    ((8, 8, 8, P, 8, P + 2, 8, P, 8, 1), g.ERR_MISALIGNED),
+    ((8, 8, 8, P, 8, P, 8, P + 4, 8, 1), g.ERR_MISALIGNED),
+    ((8, 8, 8, P, 12, P, 8, P, 8, 1), g.ERR_MISALIGNED),
+    ((8, 8, 8, P, 8, P, 12, P, 8, 1), g.ERR_MISALIGNED),
+    ((8, 8, 8, P, 8, P, 8, P, 12, 1), g.ERR_MISALIGNED),
+])
+def test_validate(lib, args, code):
+    assert g.gemm_f16_validate(*args) == code
+
+
+def test_null_plan_is_rejected(lib):
+    assert lib.gemm_f16_run(None, 8, 8, 8, P, 8, P, 8, P, 8, 1, None) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_status(None) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_set_option(None, 1, 5) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_destroy(None) == g.OK
+
+
+def test_plan_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    rc = lib.gemm_f16_plan(ctypes.byref(h), 0)
+    assert rc in (g.ERR_CUDA, g.ERR_INVALID_ARG)
+    assert h.value is None
+
+
+def _deinterleave_even(code):
+    out = 0
+    for b in range(16):
+        out |= ((code >> (2 * b)) & 1) << b
+    return out
+
+
+@pytest.mark.parametrize("tm,tn", [(1, 1), (2, 1), (8, 4), (32, 16), (32, 17), (4, 2),
+                                   (3, 50), (64, 64)])
+def test_tile_order_is_a_permutation(lib, tm, tn):
+    for order in (0, 1):
+        tiles = g.gemm_f16_tile_order(tm, tn, order)
+        assert len(tiles) == tm * tn
+        assert sorted(tiles) == [(i, j) for i in range(tm) for j in range(tn)]
+
+
+def test_row_major_order(lib):
+    assert g.gemm_f16_tile_order(2, 3, 1) == [(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 2)]
+
+
+def test_morton_order_on_square_grid_is_z_order(lib):
+    """On a 2^p x 2^p grid tile number t is (even bits of t, odd bits of t)."""
+    tiles = g.gemm_f16_tile_order(16, 16, 0)
+    for t, (m, n) in enumerate(tiles):
+        assert m == _deinterleave_even(t)
+        assert n == _deinterleave_even(t >> 1)
+
+
+def test_morton_order_rectangular_keeps_z_order(lib):
+    """Ragged grids: the order is the square grid's order with the
+    out-of-range tiles removed (codes strictly increasing)."""
+    def code(m, n):
+        c = 0
+        for b in range(16):
+            c |= ((m >> b) & 1) << (2 * b) | ((n >> b) & 1) << (2 * b + 1)
+        return c
+    tiles = g.gemm_f16_tile_order(32, 17, 0)
+    codes = [code(m, n) for m, n in tiles]
+    assert codes == sorted(codes) and len(set(codes)) == len(codes)
+
+
+def test_tile_order_rejects_bad_grid(lib):
+    assert lib.gemm_f16_tile_order(0, 4, 0, None, 0) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_tile_order(4, 65536, 0, None, 0) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_tile_order(4, 4, 2, None, 0) == g.ERR_INVALID_ARG

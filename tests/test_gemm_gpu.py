@@ -1,0 +1,224 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Criteria ("Xe2 ESIMD GEMM" page, "Correctness testing"): no NaN/Inf in the
+output, checked first; relative RMS error < 0.5%; and every element within
+1e-2 * (|ref| + 1).  Small-integer inputs whose exact products fit binary16
+must come out bit-exact (they localise layout and descriptor errors).
+Split runs must be bitwise reproducible.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic_inputs as si
+from tests import gpu_util, parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def plan():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import async_barrier_pipelined_gb300 as g
+    from async_barrier_pipelined_gb300 import build
+    build.build()
+    p = g.Plan(0)
+    yield p
+    p.close()
+
+
+def _f16(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def _small_int_bits(rng, shape, lo=-2, hi=3):
+    return _f16(rng.integers(lo, hi, size=shape))
+
+
+# ---------------------------------------------------------------- exact cases
+def test_identity_single_tile(plan):
+    rng = np.random.default_rng(1)
+    A = _small_int_bits(rng, (128, 64), -8, 9)
+    c, _ = gpu_util.run(plan, A, _f16(np.eye(64)))
+    assert np.array_equal(c, A.view(np.float16).astype(np.float64))
+
+
+def test_identity_left_multi_tile(plan):
+    rng = np.random.default_rng(2)
+    B = _small_int_bits(rng, (256, 512), -8, 9)
+    c, _ = gpu_util.run(plan, _f16(np.eye(256)), B)
+    assert np.array_equal(c, B.view(np.float16).astype(np.float64))
+
+
+def test_permutations_exact(plan):
+    rng = np.random.default_rng(3)
+    m, k, n = 256, 192, 320
+    A = _small_int_bits(rng, (m, k), -8, 9)
+    pc = rng.permutation(k)
+    Q = np.zeros((k, k))
+    Q[pc, np.arange(k)] = 1.0
+    c, _ = gpu_util.run(plan, A, _f16(Q))
+    assert np.array_equal(c, A.view(np.float16).astype(np.float64)[:, pc])
+
+
+@pytest.mark.parametrize("shape", [(128, 256, 64), (256, 256, 256), (384, 512, 320),
+                                   (300, 700, 200)])
+def test_small_integers_bit_exact(plan, shape):
+    """Entries in {-2..2}: |R| <= 4K <= 2048 is exact in FP32 and binary16."""
+    M, N, K = shape
+    rng = np.random.default_rng(M + N + K)
+    A = _small_int_bits(rng, (M, K))
+    B = _small_int_bits(rng, (K, N))
+    c, full = gpu_util.run(plan, A, B, guard_rows=3, ldc=N + 8)
+    assert np.array_equal(c, oracle.gemm_f16(A, B))
+    gpu_util.assert_untouched_outside(full, M, N)
+
+
+# ---------------------------------------------------------------- workloads
+def test_gemm_256(plan):
+    w = si.WORKLOADS["gemm_256"]
+    A, B = w.pair_bits(0)
+    c, _ = gpu_util.run(plan, A, B)
+    parity.check(c, oracle.gemm_f16(A, B), "gemm_256")
+
+
+def test_gemm_1024(plan):
+    w = si.WORKLOADS["gemm_1024"]
+    A, B = w.pair_bits(0)
+    c, _ = gpu_util.run(plan, A, B)
+    parity.check(c, oracle.gemm_f16(A, B), "gemm_1024")
+
+
+def _sample_rows(M, n, seed):
+    """Rows to check at full size: both edges of every 128-row tile band
+    near the start and the end, plus random rows."""
+    rng = np.random.default_rng(seed)
+    rows = {0, 1, 127, 128, M - 1, M - 2, M - 128 if M > 128 else 0}
+    rows |= set(int(x) for x in rng.choice(M, size=n, replace=False))
+    return np.array(sorted(r for r in rows if 0 <= r < M))
+
+
+def test_gemm_4096_pairs_sampled(plan):
+    """Full 4096^3 in the benchmark's launch configuration, two of the eight
+    rotating pairs, checked on sampled rows (full rows of C)."""
+    w = si.WORKLOADS["gemm_4096"]
+    for p in (0, 7):
+        A, B = w.pair_bits(p)
+        c, _ = gpu_util.run(plan, A, B)
+        rows = _sample_rows(w.M, 48, 40 + p)
+        parity.check(c[rows], oracle.gemm_f16(A, B, rows=rows), f"gemm_4096 pair {p}")
+
+
+def test_gemm_ragged_sampled(plan):
+    w = si.WORKLOADS["gemm_ragged"]
+    A, B = w.pair_bits(0)
+    c, full = gpu_util.run(plan, A, B, guard_rows=5, ldc=w.N + 8)
+    rows = _sample_rows(w.M, 48, 3)
+    parity.check(c[rows], oracle.gemm_f16(A, B, rows=rows), "gemm_ragged")
+    gpu_util.assert_untouched_outside(full, w.M, w.N)
+
+
+def test_gemm_splitk_full_and_reproducible(plan):
+    w = si.WORKLOADS["gemm_splitk"]
+    A, B = w.pair_bits(0)
+    ref = oracle.gemm_f16(A, B)
+    c0, full0 = gpu_util.run(plan, A, B, split_k=w.split_k)
+    parity.check(c0, ref, "gemm_splitk")
+    for _ in range(10):
+        _, full = gpu_util.run(plan, A, B, split_k=w.split_k)
+        assert np.array_equal(full, full0)
+
+
+# ---------------------------------------------------------------- shape sweep
+SWEEP = [
+    (1, 1, 1), (1, 8, 8), (8, 1, 16), (7, 9, 13), (16, 16, 16), (33, 65, 17),
+    (127, 255, 63), (129, 257, 65), (128, 256, 64), (200, 300, 100),
+    (64, 1000, 72), (1000, 64, 200), (385, 513, 1000), (256, 264, 8),
+]
+
+
+@pytest.mark.parametrize("shape", SWEEP, ids=lambda s: "x".join(map(str, s)))
+def test_shape_sweep(plan, shape):
+    M, N, K = shape
+    w = si.custom(M, N, K, seed=M * 7919 + N * 31 + K)
+    A, B = w.pair_bits(0)
+    c, full = gpu_util.run(plan, A, B, guard_rows=2, ldc=(N + 7) // 8 * 8 + 8)
+    parity.check(c, oracle.gemm_f16(A, B), f"{M}x{N}x{K}")
+    gpu_util.assert_untouched_outside(full, M, N)
+
+
+@pytest.mark.parametrize("shape", [(100, 130, 70), (257, 300, 1000)])
+def test_strided_operands(plan, shape):
+    """lda, ldb, ldc larger than the matrix; the padding holds NaN."""
+    M, N, K = shape
+    w = si.custom(M, N, K, seed=5)
+    A, B = w.pair_bits(0)
+    lda = (K + 7) // 8 * 8 + 24
+    ldb = (N + 7) // 8 * 8 + 40
+    c, full = gpu_util.run(plan, A, B, lda=lda, ldb=ldb, ldc=(N + 7) // 8 * 8 + 16,
+                           guard_rows=1)
+    parity.check(c, oracle.gemm_f16(A, B), "strided")
+    gpu_util.assert_untouched_outside(full, M, N)
+
+
+@pytest.mark.parametrize("shape,split", [((256, 256, 256), 2), ((256, 256, 256), 4),
+                                         ((200, 300, 1000), 3), ((129, 40, 640), 10),
+                                         ((1, 1, 128), 2), ((130, 520, 4096), 64)])
+def test_split_k_sweep(plan, shape, split):
+    M, N, K = shape
+    w = si.custom(M, N, K, seed=K + split)
+    A, B = w.pair_bits(0)
+    c, full = gpu_util.run(plan, A, B, split_k=split, guard_rows=2,
+                           ldc=(N + 7) // 8 * 8 + 8)
+    parity.check(c, oracle.gemm_f16(A, B), f"split {split}")
+    gpu_util.assert_untouched_outside(full, M, N)
+    _, full2 = gpu_util.run(plan, A, B, split_k=split, guard_rows=2, ldc=(N + 7) // 8 * 8 + 8)
+    assert np.array_equal(full, full2)
+
+
+def test_row_major_tile_order_same_result(plan):
+    import async_barrier_pipelined_gb300 as g
+    w = si.custom(700, 900, 300, seed=9)
+    A, B = w.pair_bits(0)
+    c0, _ = gpu_util.run(plan, A, B)
+    plan.set_option(g.OPT_TILE_ORDER, 1)
+    try:
+        c1, _ = gpu_util.run(plan, A, B)
+    finally:
+        plan.set_option(g.OPT_TILE_ORDER, 0)
+    assert np.array_equal(c0, c1)
+
+
+def test_run_host_matches_device_path(plan):
+    import torch
+    import async_barrier_pipelined_gb300 as g
+    w = si.custom(300, 260, 200, seed=21)
+    A, B = w.pair_bits(0)
+    c_dev, _ = gpu_util.run(plan, A, B)
+    hA = torch.from_numpy(A.view(np.float16)).pin_memory()
+    hB = torch.from_numpy(B.view(np.float16)).pin_memory()
+    hC = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+    s = torch.cuda.current_stream()
+    g.gemm_f16_run_host(plan.handle, w.M, w.N, w.K, hA.data_ptr(), w.K, hB.data_ptr(), w.N,
+                        hC.data_ptr(), w.N, 1, int(s.cuda_stream))
+    s.synchronize()
+    assert plan.status() == 0
+    assert np.array_equal(hC.numpy().astype(np.float64), c_dev)
+
+
+def test_invalid_arguments_enqueue_nothing(plan):
+    import torch
+    import async_barrier_pipelined_gb300 as g
+    A = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_run(plan.handle, 64, 64, 64, A.data_ptr() + 2, 64, A.data_ptr(), 64,
+                       A.data_ptr(), 64, 1, 0)
+    assert e.value.code == g.ERR_MISALIGNED
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_run(plan.handle, 64, 64, 64, A.data_ptr(), 64, A.data_ptr(), 64,
+                       A.data_ptr(), 64, 2, 0)
+    assert e.value.code == g.ERR_INVALID_ARG
