@@ -158,9 +158,12 @@ __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t 
 }
 
 // ------------------------------------------------------------------ roles
+// Returns, through pos_out / issued_out, where the ring stands when the role
+// stops, so that an aborted CTA can drain its copies in flight.
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                               const Params& p, uint32_t base, const Bars& b,
-                                              volatile int* abort_flag) {
+                                              volatile int* abort_flag, RingPos* pos_out,
+                                              uint32_t* issued_out) {
   RingPos pos{0, 0};
   uint32_t issued = 0;
   bool ok = true;
@@ -192,15 +195,20 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUte
       ring_advance(pos, STAGES);
     }
   }
-  if (!ok) {
-    // Wait for the copies of the most recent stages (one per stage) so that
-    // no tensor copy still writes this CTA's shared memory when it exits.
-    RingPos q = pos;
-    const uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
-    for (uint32_t i = 0; i < n; ++i) {
-      ring_retreat(q, STAGES);
-      wait_drain(b.full + 8 * q.stage, consumer_wait_parity(q), p.timeout_ns);
-    }
+  *pos_out = pos;
+  *issued_out = issued;
+}
+
+// After an abort: wait (bounded) for the copies of the most recently issued
+// stages, one per stage, so that no tensor copy still writes this CTA's
+// shared memory when it exits.  A stage whose phase already completed
+// returns at once.
+__device__ __noinline__ void producer_drain(const Bars& b, RingPos pos, uint32_t issued,
+                                            uint64_t limit_ns) {
+  const uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
+  for (uint32_t i = 0; i < n; ++i) {
+    ring_retreat(pos, STAGES);
+    wait_drain(b.full + 8 * pos.stage, consumer_wait_parity(pos), limit_ns);
   }
 }
 
@@ -378,8 +386,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
 
+  RingPos prod_pos{0, 0};
+  uint32_t prod_issued = 0;
   if (warp == 0) {
-    if (lane == 0) producer_role(&tmA, &tmB, p, base, b, abort_flag);
+    if (lane == 0) producer_role(&tmA, &tmB, p, base, b, abort_flag, &prod_pos, &prod_issued);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) mma_role(p, base, tmem_base, b, abort_flag);
@@ -390,6 +400,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  // Every role has stopped, so the abort flag is final here.
+  if (warp == 0 && lane == 0 && *abort_flag)
+    producer_drain(b, prod_pos, prod_issued, p.timeout_ns);
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, TMEM_COLS);

@@ -191,20 +191,37 @@ def cpu_oracle_sample(w: si.Workload, rows: np.ndarray, A_bits, B_bits):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w: si.Workload, target_s: float, A_bits, B_bits):
-    """Oracle TFLOPS on a row sample sized for ~target_s seconds."""
+def cpu_baseline(w: si.Workload, target_s: float, pairs_bits):
+    """Oracle TFLOPS on a bounded sample of the workload (~target_s seconds).
+
+    If one full product fits the budget, whole products are repeated over
+    the workload's pairs until the budget is spent; otherwise an evenly
+    spaced subset of the rows of C (pair 0) is computed.
+    """
     import oracle
     threads = oracle.num_threads()
-    rows = np.arange(min(w.M, max(threads, 8)))
-    t = cpu_oracle_sample(w, rows, A_bits, B_bits)          # calibration, untimed
-    per_row = max(t / len(rows), 1e-6)
-    n = int(min(w.M, max(len(rows), target_s / per_row)))
-    rows = np.linspace(0, w.M - 1, n).astype(np.int64)
-    t = cpu_oracle_sample(w, rows, A_bits, B_bits)
-    flops = 2.0 * n * w.N * w.K
+    a0, b0 = pairs_bits[0]
+    r0 = int(min(w.M, max(threads, 64)))
+    t_cal = cpu_oracle_sample(w, np.arange(r0), a0, b0)        # calibration, untimed
+    per_row = max(t_cal / r0, 1e-9)
+    if per_row * w.M > target_s:
+        n = int(max(1, target_s / per_row))
+        rows = np.linspace(0, w.M - 1, n).astype(np.int64)
+        t = cpu_oracle_sample(w, rows, a0, b0)
+        flops = 2.0 * n * w.N * w.K
+        sample = (f"{n} of {w.M} rows of C (evenly spaced) for pair 0: "
+                  f"{flops / 1e9:.1f} GFLOP in {t:.1f} s, FP64 triple loop")
+    else:
+        t, flops, products = 0.0, 0.0, 0
+        while t < target_s:
+            a, b = pairs_bits[products % len(pairs_bits)]
+            t += cpu_oracle_sample(w, np.arange(w.M), a, b)
+            flops += 2.0 * w.M * w.N * w.K
+            products += 1
+        sample = (f"{products} full products over {min(products, len(pairs_bits))} "
+                  f"pair(s): {flops / 1e9:.1f} GFLOP in {t:.1f} s, FP64 triple loop")
     return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-            "sample": f"{n} of {w.M} rows of C for pair 0 ({n * w.N} outputs, "
-                      f"{flops / 1e9:.1f} GFLOP in {t:.1f} s, FP64 triple loop)"}
+            "sample": sample}
 
 
 # ------------------------------------------------------------------ arms
@@ -380,8 +397,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        a0, b0 = pairs_bits[0]
-        cpu = cpu_baseline(w, args.cpu_seconds, a0, b0)
+        cpu = cpu_baseline(w, args.cpu_seconds, pairs_bits)
 
     plan.close()
     if rank == 0:

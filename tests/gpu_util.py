@@ -11,7 +11,7 @@ def to_device(bits: np.ndarray, ld: int | None = None, pad_bits: int = SENTINEL_
     """binary16 bit matrix -> (padded) CUDA float16 tensor view, row stride ld."""
     import torch
     rows, cols = bits.shape
-    ld = cols if ld is None else ld
+    ld = (cols + 7) // 8 * 8 if ld is None else ld
     host = np.full((rows, ld), pad_bits, dtype=np.uint16)
     host[:, :cols] = bits
     t = torch.from_numpy(host.view(np.float16)).cuda()
@@ -31,7 +31,7 @@ def run(plan, A_bits, B_bits, split_k=1, lda=None, ldb=None, ldc=None,
     N = B_bits.shape[1]
     A = to_device(A_bits, lda)
     B = to_device(B_bits, ldb)
-    ldc = N if ldc is None else ldc
+    ldc = (N + 7) // 8 * 8 if ldc is None else ldc
     cbuf = torch.from_numpy(
         np.full((M + guard_rows, ldc), SENTINEL_BITS, np.uint16).view(np.float16)).cuda()
     C = cbuf[:M, :N]

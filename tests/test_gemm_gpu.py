@@ -73,7 +73,7 @@ def test_small_integers_bit_exact(plan, shape):
     rng = np.random.default_rng(M + N + K)
     A = _small_int_bits(rng, (M, K))
     B = _small_int_bits(rng, (K, N))
-    c, full = gpu_util.run(plan, A, B, guard_rows=3, ldc=N + 8)
+    c, full = gpu_util.run(plan, A, B, guard_rows=3, ldc=(N + 7) // 8 * 8 + 8)
     assert np.array_equal(c, oracle.gemm_f16(A, B))
     gpu_util.assert_untouched_outside(full, M, N)
 

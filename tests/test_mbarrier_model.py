@@ -1,0 +1,73 @@
+"""Host replay of the kernel's barrier protocol (tests/mbarrier_model/).
+
+The model implements the mbarrier operations as the "mbarrier State and
+Operations" page defines them and drives the producer / MMA / epilogue role
+loops with the kernel's own index and parity helpers (schedule.h) under
+seeded random interleavings of roles, copy completions and tensor-core
+completions.  See model.cpp for the invariants checked.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "mbarrier_model", "model.cpp")
+CSRC = os.path.join(os.path.dirname(HERE), "async_barrier_pipelined_gb300", "csrc")
+BUILD = os.path.join(HERE, "mbarrier_model", "_build")
+EXE = os.path.join(BUILD, "model")
+
+
+@pytest.fixture(scope="module")
+def model():
+    if shutil.which("g++") is None:
+        pytest.skip("g++ not available")
+    os.makedirs(BUILD, exist_ok=True)
+    deps = [SRC, os.path.join(CSRC, "schedule.h")]
+    if not os.path.exists(EXE) or any(os.path.getmtime(d) > os.path.getmtime(EXE) for d in deps):
+        tmp = EXE + f".tmp{os.getpid()}"
+        subprocess.run(["g++", "-std=c++17", "-O2", "-pthread", "-I", CSRC, SRC, "-o", tmp],
+                       check=True)
+        os.replace(tmp, EXE)
+    return EXE
+
+
+def _run(exe, *args):
+    r = subprocess.run([exe, *map(str, args)], capture_output=True, text=True, timeout=300)
+    return r.returncode, r.stdout.strip()
+
+
+# (stages, units, grid, cta, split_k, kblocks, seeds)
+CASES = [
+    (4, 2, 2, 0, 1, 4, 200),        # 256^3: 2 tiles, 4 k-blocks
+    (4, 32, 32, 5, 1, 16, 200),     # 1024^3: 32 tiles on 32 CTAs
+    (4, 512, 152, 0, 1, 64, 30),    # 4096^3, first CTA (4 tiles)
+    (4, 512, 152, 151, 1, 64, 30),  # 4096^3, last CTA (3 tiles)
+    (4, 544, 152, 7, 1, 47, 30),    # ragged 4000x4104x3000
+    (4, 128, 128, 3, 16, 512, 10),  # split-K 512x512x32768, 16 splits of 32
+    (1, 5, 2, 0, 1, 3, 200),        # one stage
+    (2, 9, 4, 1, 3, 7, 200),        # uneven split ranges (7 k-blocks in 3)
+    (3, 6, 1, 0, 2, 2, 200),        # one k-block per split
+    (5, 3, 1, 0, 1, 1, 200),        # single k-block, more stages than fills
+    (4, 1, 1, 0, 1, 1, 200),        # one unit, one k-block
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_protocol_interleavings(model, case):
+    rc, out = _run(model, *case)
+    assert rc == 0 and out.startswith("OK"), out
+
+
+def test_fault_leaves_mma_blocked_on_the_starved_stage(model):
+    # unit 2 belongs to CTA 0 of a 2-CTA grid; its first stage gets no copy
+    rc, out = _run(model, 4, 8, 2, 0, 1, 4, 3, 2)
+    assert rc == 0 and out.startswith("DEADLOCK-AS-EXPECTED"), out
+
+
+def test_fault_on_other_cta_does_not_affect_this_one(model):
+    rc, out = _run(model, 4, 8, 2, 1, 1, 4, 20, 2)
+    assert rc == 0 and out.startswith("OK"), out
