@@ -116,6 +116,8 @@ struct Params {
   int M, N, K;
   int tiles_m, tiles_n, split_k, kblocks, num_units;
   const uint32_t* order;   // tile order: tiles_m*tiles_n packed (tm | tn<<16)
+  __half* C;               // output, for the masked stores of a ragged last chunk
+  int64_t ldc;
   int* status;             // device-visible status word
   unsigned long long timeout_ns;
   int fault_unit;          // test only: unit whose first stage gets no copy
@@ -290,7 +292,19 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c * 32u, r);
         ptx::tmem_ld_wait();
-        if (p.split_k == 1) {
+        if (p.split_k == 1 && col0 + 32 > p.N && (p.N & 7) != 0) {
+          // The chunk straddles a column bound that is not 16-byte aligned.
+          // A tensor store would write on up to the next 16-byte boundary
+          // past N, so this chunk goes out with masked plain stores.
+          const int row = row0 + (int)lane;
+          if (row < p.M) {
+            __half* dst = p.C + (int64_t)row * p.ldc + col0;
+            const int nvalid = p.N - col0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nvalid) dst[j] = __float2half_rn(__uint_as_float(r[j]));
+          }
+        } else if (p.split_k == 1) {
           const uint32_t buf = stage0 + (nstore & 1u) * EPI_BUF;
           if (lane == 0) ptx::bulk_wait_group_read<1>();
           __syncwarp();
@@ -410,39 +424,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // Fixed-order split reduction: C[i,j] = fp16_rn(P_0 + P_1 + ... + P_{S-1}),
-// summed left to right in FP32.  Each thread owns 8 consecutive columns.
+// summed left to right in FP32.  Each thread owns 4 consecutive columns;
+// the partial loads are issued four splits at a time (independent loads),
+// but the additions keep the order t = 0, 1, ..., S-1.
+__device__ __forceinline__ void add4(float4& acc, const float4& v) {
+  acc.x += v.x;
+  acc.y += v.y;
+  acc.z += v.z;
+  acc.w += v.w;
+}
+
 __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ ws, int M, int N, int64_t ldw, int split_k,
                          int64_t split_stride, __half* __restrict__ C, int64_t ldc) {
-  const int64_t groups = (N + 7) / 8;
+  const int64_t groups = (N + 3) / 4;
   const int64_t total = (int64_t)M * groups;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
        g += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = g / groups;
-    const int j = (int)(g - i * groups) * 8;
+    const int j = (int)(g - i * groups) * 4;
     const float* src = ws + i * ldw + j;
-    float4 lo = *reinterpret_cast<const float4*>(src);
-    float4 hi = *reinterpret_cast<const float4*>(src + 4);
-    for (int s = 1; s < split_k; ++s) {
-      src += split_stride;
-      const float4 a = *reinterpret_cast<const float4*>(src);
-      const float4 c = *reinterpret_cast<const float4*>(src + 4);
-      lo.x += a.x; lo.y += a.y; lo.z += a.z; lo.w += a.w;
-      hi.x += c.x; hi.y += c.y; hi.z += c.z; hi.w += c.w;
+    float4 acc = *reinterpret_cast<const float4*>(src);
+    int s = 1;
+    for (; s + 4 <= split_k; s += 4) {
+      const float4 v0 = *reinterpret_cast<const float4*>(src + (int64_t)s * split_stride);
+      const float4 v1 = *reinterpret_cast<const float4*>(src + (int64_t)(s + 1) * split_stride);
+      const float4 v2 = *reinterpret_cast<const float4*>(src + (int64_t)(s + 2) * split_stride);
+      const float4 v3 = *reinterpret_cast<const float4*>(src + (int64_t)(s + 3) * split_stride);
+      add4(acc, v0);
+      add4(acc, v1);
+      add4(acc, v2);
+      add4(acc, v3);
     }
-    const __half2 h0 = __floats2half2_rn(lo.x, lo.y), h1 = __floats2half2_rn(lo.z, lo.w);
-    const __half2 h2 = __floats2half2_rn(hi.x, hi.y), h3 = __floats2half2_rn(hi.z, hi.w);
+    for (; s < split_k; ++s) add4(acc, *reinterpret_cast<const float4*>(src + (int64_t)s * split_stride));
+    const __half2 h0 = __floats2half2_rn(acc.x, acc.y), h1 = __floats2half2_rn(acc.z, acc.w);
     __half* dst = C + i * ldc + j;
-    if (j + 8 <= N) {
-      uint4 v;
+    if (j + 4 <= N) {
+      uint2 v;
       v.x = *reinterpret_cast<const uint32_t*>(&h0);
       v.y = *reinterpret_cast<const uint32_t*>(&h1);
-      v.z = *reinterpret_cast<const uint32_t*>(&h2);
-      v.w = *reinterpret_cast<const uint32_t*>(&h3);
-      *reinterpret_cast<uint4*>(dst) = v;
+      *reinterpret_cast<uint2*>(dst) = v;
     } else {
-      const __half vals[8] = {__low2half(h0), __high2half(h0), __low2half(h1), __high2half(h1),
-                              __low2half(h2), __high2half(h2), __low2half(h3), __high2half(h3)};
+      const __half vals[4] = {__low2half(h0), __high2half(h0), __low2half(h1), __high2half(h1)};
       for (int t = 0; t < N - j; ++t) dst[t] = vals[t];
     }
   }
@@ -793,6 +816,8 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   prm.kblocks = kblocks;
   prm.num_units = (int)units;
   prm.order = order;
+  prm.C = static_cast<__half*>(C);
+  prm.ldc = ldc;
   prm.status = p->status_dev;
   prm.timeout_ns = p->timeout_ns;
   prm.fault_unit = p->fault_unit;
@@ -807,7 +832,7 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
             "launch gemm_f16_kernel");
 
   if (split_k > 1) {
-    const int64_t groups = (int64_t)M * ((N + 7) / 8);
+    const int64_t groups = (int64_t)M * ((N + 3) / 4);
     const int rgrid = (int)std::min<int64_t>(ceil_div(groups, 256), (int64_t)p->num_sms * 8);
     cudaLaunchConfig_t rcfg = {};
     rcfg.gridDim = dim3(rgrid, 1, 1);
