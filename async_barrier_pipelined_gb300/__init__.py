@@ -23,7 +23,7 @@ __all__ = [
     "gemm_f16_strerror", "gemm_f16_last_cuda_error", "gemm_f16_validate",
     "gemm_f16_tile_order", "gemm_f16_tile_shape", "Plan", "matmul",
     "OK", "ERR_INVALID_ARG", "ERR_MISALIGNED", "ERR_UNSUPPORTED_DEVICE",
-    "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT",
+    "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT", "ERR_SCRATCH_TOO_SMALL", "gemm_f16_run_noalloc",
     "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "EXPORTED_SYMBOLS",
 ]
 
@@ -34,6 +34,7 @@ ERR_UNSUPPORTED_DEVICE = -3
 ERR_OOM = -4
 ERR_CUDA = -5
 ERR_TIMEOUT = -6
+ERR_SCRATCH_TOO_SMALL = -7
 
 OPT_TIMEOUT_NS = 1
 OPT_TILE_ORDER = 2
@@ -58,6 +59,8 @@ _SIGNATURES = {
     "gemm_f16_tile_order": (_c_i64, [_c_int, _c_int, _c_int,
                                      ctypes.POINTER(ctypes.c_uint32), _c_i64]),
     "gemm_f16_tile_shape": (_c_int, [ctypes.POINTER(_c_int)] * 4),
+    "gemm_f16_run_noalloc": (_c_int, [_c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
+                                      _vp, _c_i64, _c_int, _vp, _vp]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -141,6 +144,21 @@ def gemm_f16_run_host(plan: int, M: int, N: int, K: int, hA: int, lda: int, hB: 
     """Enqueue copy-in, C = A*B and copy-out for HOST pointers on ``stream``."""
     _check(load().gemm_f16_run_host(plan, M, N, K, hA, lda, hB, ldb, hC, ldc, split_k,
                                     stream), "gemm_f16_run_host")
+
+
+def gemm_f16_run_noalloc(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int,
+                         C: int, ldc: int, split_k: int = 1, status: int = 0,
+                         stream: int = 0) -> None:
+    """Enqueue C = A*B without a plan and without allocating device memory.
+
+    For callers that may not call cudaMalloc (their device memory belongs to
+    another allocator, or they cannot afford its device-wide sync).  Uses the
+    library's fixed scratch array; ``status`` is 0 or the address of a
+    device-visible int that receives ERR_TIMEOUT if a wait runs out.  Calls
+    that overlap on the GPU race on the shared scratch.
+    """
+    _check(load().gemm_f16_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, split_k, status,
+                                       stream), "gemm_f16_run_noalloc")
 
 
 def gemm_f16_validate(M, N, K, A, lda, B, ldb, C, ldc, split_k) -> int:

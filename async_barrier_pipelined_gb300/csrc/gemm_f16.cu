@@ -618,6 +618,7 @@ const char* gemm_f16_strerror(int code) {
     case GEMM_F16_ERR_OOM: return "out of memory";
     case GEMM_F16_ERR_CUDA: return "CUDA call failed";
     case GEMM_F16_ERR_TIMEOUT: return "an in-kernel barrier wait timed out";
+    case GEMM_F16_ERR_SCRATCH_TOO_SMALL: return "problem too large for the fixed no-alloc scratch";
     default: return "unknown error code";
   }
 }
@@ -891,3 +892,163 @@ int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, in
 }
 
 }  // extern "C"
+
+// ====================================================== no-allocation entry
+// gemm_f16_run_noalloc: the plan-free variant for callers that must not
+// allocate device memory (see gemm_f16.h).  Its scratch is one file-scope
+// device array, laid out as
+//   [0, 4*MAX_TILES)            tile-order table (uint32 per tile)
+//   [4*MAX_TILES, +256)         status word used when the caller passes none
+//   [4*MAX_TILES + 256, +32 MiB) FP32 split partials [split][M][ldw]
+// Host code must not use the array's name as an address: the per-device
+// set-up below asks the runtime for its device address.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_F16_NOALLOC_SCRATCH_BYTES];
+
+constexpr size_t NOALLOC_ORDER_OFF = 0;
+constexpr size_t NOALLOC_STATUS_OFF = (size_t)GEMM_F16_NOALLOC_MAX_TILES * 4u;
+constexpr size_t NOALLOC_WS_OFF = NOALLOC_STATUS_OFF + 256u;
+static_assert(NOALLOC_WS_OFF + GEMM_F16_NOALLOC_WS_BYTES == GEMM_F16_NOALLOC_SCRATCH_BYTES,
+              "scratch layout");
+static_assert(NOALLOC_WS_OFF % 256 == 0, "workspace alignment");
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+struct NoallocDevice {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int num_sms = 0;
+  int order_tm = -1, order_tn = -1;  // grid whose order the device table holds
+};
+NoallocDevice g_noalloc_devices[NOALLOC_MAX_DEVICES];
+std::mutex g_noalloc_mutex;
+// Host staging for the tile order, static so that building it allocates nothing.
+uint64_t g_noalloc_keys[GEMM_F16_NOALLOC_MAX_TILES];
+uint32_t g_noalloc_order[GEMM_F16_NOALLOC_MAX_TILES];
+
+// One-time set-up on the current device `dev` (that device is current).
+int noalloc_setup(int dev, NoallocDevice* d) {
+  int major = 0, minor = 0, sms = 0;
+  GF16_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev),
+            "cudaDeviceGetAttribute(major)");
+  GF16_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev),
+            "cudaDeviceGetAttribute(minor)");
+  if (major != 10 || minor != 3) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+  GF16_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+            "cudaDeviceGetAttribute(SM count)");
+  GF16_CUDA(cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES),
+            "cudaFuncSetAttribute(max dynamic smem)");
+  void* ptr = nullptr;
+  GF16_CUDA(cudaGetSymbolAddress(&ptr, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)");
+  d->scratch = static_cast<unsigned char*>(ptr);
+  d->num_sms = sms;
+  d->order_tm = d->order_tn = -1;
+  d->ready = true;
+  return GEMM_F16_OK;
+}
+
+}  // namespace
+
+extern "C" int gemm_f16_run_noalloc(int M, int N, int K, const void* A, int64_t lda,
+                                    const void* B, int64_t ldb, void* C, int64_t ldc,
+                                    int split_k, int* status, gemm_f16_stream_t stream_) {
+  int rc = gemm_f16_validate(M, N, K, A, lda, B, ldb, C, ldc, split_k);
+  if (rc) return rc;
+  const int tiles_m = (int)ceil_div(M, BM);
+  const int tiles_n = (int)ceil_div(N, BN);
+  const int64_t tiles = (int64_t)tiles_m * tiles_n;
+  const int64_t ldw = (N + 7) / 8 * 8;
+  const int64_t split_stride = (int64_t)M * ldw;
+  if (tiles > GEMM_F16_NOALLOC_MAX_TILES) return GEMM_F16_ERR_SCRATCH_TOO_SMALL;
+  if (split_k > 1 &&
+      (uint64_t)split_k * (uint64_t)split_stride * sizeof(float) > GEMM_F16_NOALLOC_WS_BYTES)
+    return GEMM_F16_ERR_SCRATCH_TOO_SMALL;
+  cudaStream_t stream = (cudaStream_t)stream_;
+
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  int dev = 0;
+  GF16_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+  NoallocDevice* d = &g_noalloc_devices[dev];
+  if (!d->ready) {
+    rc = noalloc_setup(dev, d);
+    if (rc) return rc;
+  }
+
+  uint32_t* order = reinterpret_cast<uint32_t*>(d->scratch + NOALLOC_ORDER_OFF);
+  if (d->order_tm != tiles_m || d->order_tn != tiles_n) {
+    int64_t n = 0;
+    for (int tm = 0; tm < tiles_m; ++tm)
+      for (int tn = 0; tn < tiles_n; ++tn)
+        g_noalloc_keys[n++] = ((uint64_t)morton_code((uint32_t)tm, (uint32_t)tn) << 32) |
+                              pack_tile((uint32_t)tm, (uint32_t)tn);
+    std::sort(g_noalloc_keys, g_noalloc_keys + n);  // in place, no allocation
+    for (int64_t t = 0; t < n; ++t) g_noalloc_order[t] = (uint32_t)g_noalloc_keys[t];
+    // Pageable source: the call returns once the bytes are staged, so the
+    // static host buffer may be rebuilt by the next call.
+    GF16_CUDA(cudaMemcpyAsync(order, g_noalloc_order, (size_t)n * sizeof(uint32_t),
+                              cudaMemcpyHostToDevice, stream),
+              "upload tile order (no-alloc)");
+    d->order_tm = tiles_m;
+    d->order_tn = tiles_n;
+  }
+
+  alignas(64) CUtensorMap tmA, tmB, tmC, tmW;
+  std::memset(&tmW, 0, sizeof(tmW));
+  rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
+                 (uint64_t)lda * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (rc) return rc;
+  rc = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)N, (uint64_t)K,
+                 (uint64_t)ldb * 2, B_BOX_N, BK, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (rc) return rc;
+  rc = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, (uint64_t)N, (uint64_t)M,
+                 (uint64_t)ldc * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (rc) return rc;
+  float* ws = reinterpret_cast<float*>(d->scratch + NOALLOC_WS_OFF);
+  if (split_k > 1) {
+    rc = encode_3d_f32(&tmW, ws, (uint64_t)N, (uint64_t)M, (uint64_t)split_k, (uint64_t)ldw * 4,
+                       (uint64_t)split_stride * 4);
+    if (rc) return rc;
+  }
+
+  const int64_t units = tiles * split_k;
+  if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
+  Params prm;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.tiles_m = tiles_m;
+  prm.tiles_n = tiles_n;
+  prm.split_k = split_k;
+  prm.kblocks = (int)ceil_div(K, BK);
+  prm.num_units = (int)units;
+  prm.order = order;
+  prm.C = static_cast<__half*>(C);
+  prm.ldc = ldc;
+  prm.status = status ? status : reinterpret_cast<int*>(d->scratch + NOALLOC_STATUS_OFF);
+  prm.timeout_ns = 1000000000ull;
+  prm.fault_unit = -1;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(units, d->num_sms), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  GF16_CUDA(cudaLaunchKernelEx(&cfg, gemm_f16_kernel, tmA, tmB, tmC, tmW, prm),
+            "launch gemm_f16_kernel (no-alloc)");
+  if (split_k > 1) {
+    const int64_t groups = (int64_t)M * ((N + 3) / 4);
+    cudaLaunchConfig_t rcfg = {};
+    rcfg.gridDim = dim3((unsigned)std::min<int64_t>(ceil_div(groups, 256), (int64_t)d->num_sms * 8), 1, 1);
+    rcfg.blockDim = dim3(256, 1, 1);
+    rcfg.stream = stream;
+    GF16_CUDA(cudaLaunchKernelEx(&rcfg, splitk_reduce_kernel, (const float*)ws, M, N, ldw, split_k,
+                                 split_stride, (__half*)C, (int64_t)ldc),
+              "launch splitk_reduce_kernel (no-alloc)");
+  }
+  return GEMM_F16_OK;
+}

@@ -49,7 +49,8 @@ typedef enum gemm_f16_error {
     GEMM_F16_ERR_UNSUPPORTED_DEVICE = -3, /* not a compute-capability 10.3 (sm_103a) device */
     GEMM_F16_ERR_OOM = -4,                /* device or pinned-host allocation failed */
     GEMM_F16_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed (see gemm_f16_last_cuda_error) */
-    GEMM_F16_ERR_TIMEOUT = -6             /* a bounded in-kernel wait expired (reported by gemm_f16_status) */
+    GEMM_F16_ERR_TIMEOUT = -6,            /* a bounded in-kernel wait expired (reported by gemm_f16_status) */
+    GEMM_F16_ERR_SCRATCH_TOO_SMALL = -7   /* gemm_f16_run_noalloc: problem exceeds its fixed scratch */
 } gemm_f16_error;
 
 /* Options for gemm_f16_set_option. */
@@ -156,6 +157,55 @@ int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order,
 
 /* Compile-time tile shape of the kernel: BM x BN output tile, BK k-block. */
 int gemm_f16_tile_shape(int *bm, int *bn, int *bk, int *stages);
+
+/*
+ * gemm_f16_run_noalloc — the same product as gemm_f16_run, without a plan and
+ * without allocating any memory.  (No counterpart in the paper: this is a
+ * library convenience.)
+ *
+ * Who it is for: callers that must not call cudaMalloc/cudaFree, for example
+ * code whose device memory is owned by another allocator (a framework's
+ * caching pool that has reserved the free HBM, so a direct cudaMalloc can
+ * fail), or latency-critical loops where the implicit device-wide
+ * synchronisation of cudaMalloc/cudaFree would stall every other stream.
+ * gemm_f16_plan allocates (status word, tile tables, the split workspace),
+ * so such callers cannot use it.
+ *
+ * Instead of plan-owned buffers this entry point uses one fixed scratch
+ * array compiled into the library (a file-scope __device__ array), which
+ * every GPU that loads the library holds until the process exits:
+ *   GEMM_F16_NOALLOC_SCRATCH_BYTES bytes = a tile-order table of up to
+ *   GEMM_F16_NOALLOC_MAX_TILES entries plus GEMM_F16_NOALLOC_WS_BYTES of
+ *   FP32 split partials.
+ * Limits: ceil(M/128) * ceil(N/256) <= GEMM_F16_NOALLOC_MAX_TILES, and for
+ * split_k > 1, split_k * M * (N rounded up to 8) * 4 bytes <=
+ * GEMM_F16_NOALLOC_WS_BYTES (32 MiB; e.g. 512 x 512 with 16 splits uses 16
+ * MiB).  Larger problems return GEMM_F16_ERR_SCRATCH_TOO_SMALL and enqueue
+ * nothing.
+ *
+ * Arguments are those of gemm_f16_run (same validation and error codes),
+ * plus `status`: NULL, or a device-visible int the caller owns, into which
+ * the kernel writes GEMM_F16_ERR_TIMEOUT if one of its bounded waits runs
+ * out (it is never cleared by this call).  The device is the current CUDA
+ * device.
+ *
+ * The first call on a device does a one-time set-up with that device
+ * current (shared-memory limit of the kernel, the scratch array's device
+ * address via cudaGetSymbolAddress, SM count); make that first call before
+ * any stream capture.  Every call shares the one scratch array and it keeps
+ * the last call's contents: calls that overlap on the GPU (different
+ * streams, or different host threads) race on it and must not be issued
+ * concurrently.  A call whose tile grid differs from the previous call's on
+ * that device uploads a new tile-order table with a pageable-memory copy on
+ * `stream`, which may wait for the stream's earlier work.
+ */
+#define GEMM_F16_NOALLOC_MAX_TILES 65536
+#define GEMM_F16_NOALLOC_WS_BYTES (32u << 20)
+#define GEMM_F16_NOALLOC_SCRATCH_BYTES \
+    (GEMM_F16_NOALLOC_MAX_TILES * 4u + 256u + GEMM_F16_NOALLOC_WS_BYTES)
+int gemm_f16_run_noalloc(int M, int N, int K, const void *A, int64_t lda,
+                         const void *B, int64_t ldb, void *C, int64_t ldc,
+                         int split_k, int *status, gemm_f16_stream_t stream);
 
 #ifdef __cplusplus
 }
