@@ -24,7 +24,8 @@ __all__ = [
     "gemm_f16_tile_order", "gemm_f16_tile_shape", "Plan", "matmul",
     "OK", "ERR_INVALID_ARG", "ERR_MISALIGNED", "ERR_UNSUPPORTED_DEVICE",
     "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT", "ERR_SCRATCH_TOO_SMALL", "gemm_f16_run_noalloc",
-    "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "EXPORTED_SYMBOLS",
+    "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "INFO_NUM_SMS", "INFO_MAX_PAIRS",
+    "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
 ]
 
 OK = 0
@@ -39,6 +40,9 @@ ERR_SCRATCH_TOO_SMALL = -7
 OPT_TIMEOUT_NS = 1
 OPT_TILE_ORDER = 2
 OPT_FAULT_UNIT = 3
+OPT_KERNEL = 4
+INFO_NUM_SMS = 100
+INFO_MAX_PAIRS = 101
 
 _c_int, _c_i64, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
 
@@ -52,6 +56,7 @@ _SIGNATURES = {
     "gemm_f16_destroy": (_c_int, [_vp]),
     "gemm_f16_status": (_c_int, [_vp]),
     "gemm_f16_set_option": (_c_int, [_vp, _c_int, _c_i64]),
+    "gemm_f16_get_option": (_c_int, [_vp, _c_int, ctypes.POINTER(_c_i64)]),
     "gemm_f16_strerror": (ctypes.c_char_p, [_c_int]),
     "gemm_f16_last_cuda_error": (ctypes.c_char_p, []),
     "gemm_f16_validate": (_c_int, [_c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
@@ -59,6 +64,8 @@ _SIGNATURES = {
     "gemm_f16_tile_order": (_c_i64, [_c_int, _c_int, _c_int,
                                      ctypes.POINTER(ctypes.c_uint32), _c_i64]),
     "gemm_f16_tile_shape": (_c_int, [ctypes.POINTER(_c_int)] * 4),
+    "gemm_f16_pair_tiles": (_c_i64, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                     ctypes.POINTER(ctypes.c_uint32), _c_i64]),
     "gemm_f16_run_noalloc": (_c_int, [_c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
                                       _vp, _c_i64, _c_int, _vp, _vp]),
 }
@@ -132,6 +139,12 @@ def gemm_f16_set_option(plan: int, option: int, value: int) -> None:
     _check(load().gemm_f16_set_option(plan, option, value), "gemm_f16_set_option")
 
 
+def gemm_f16_get_option(plan: int, option: int) -> int:
+    v = _c_i64()
+    _check(load().gemm_f16_get_option(plan, option, ctypes.byref(v)), "gemm_f16_get_option")
+    return v.value
+
+
 def gemm_f16_run(plan: int, M: int, N: int, K: int, A: int, lda: int, B: int, ldb: int,
                  C: int, ldc: int, split_k: int = 1, stream: int = 0) -> None:
     """Enqueue C = A*B (device pointers) on ``stream`` (a cudaStream_t as int)."""
@@ -174,6 +187,16 @@ def gemm_f16_tile_order(tiles_m: int, tiles_n: int, order: int = 0) -> list:
     return [(v & 0xFFFF, v >> 16) for v in buf]
 
 
+def gemm_f16_pair_tiles(M: int, N: int, pairs: int, split_k: int = 1, order: int = 0) -> list:
+    """CTA-pair work list as (row0, col0, width) tuples."""
+    n = _check(load().gemm_f16_pair_tiles(M, N, pairs, split_k, order, None, 0),
+               "gemm_f16_pair_tiles")
+    buf = (ctypes.c_uint32 * n)()
+    _check(load().gemm_f16_pair_tiles(M, N, pairs, split_k, order, buf, n), "gemm_f16_pair_tiles")
+    return [((v & 0xFFFF) * 256, ((v >> 16) & 0x7FFF) * 128, 128 if v >> 31 else 256)
+            for v in buf]
+
+
 def gemm_f16_tile_shape() -> tuple:
     """(BM, BN, BK, STAGES) of the compiled kernel."""
     vals = [_c_int() for _ in range(4)]
@@ -210,6 +233,9 @@ class Plan:
 
     def set_option(self, option: int, value: int) -> None:
         gemm_f16_set_option(self.handle, option, value)
+
+    def get_option(self, option: int) -> int:
+        return gemm_f16_get_option(self.handle, option)
 
 
 def _stream_handle(stream) -> int:

@@ -183,7 +183,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUte
         break;
       }
       const uint32_t fb = b.full + 8 * pos.stage;
-      ptx::mbar_arrive_expect_tx(fb, STAGE_TX);
+      ptx::mbar_arrive_expect_tx_relaxed(fb, STAGE_TX);
       if (kb != skip_kb) {
         const uint32_t sa = base + OFF_A + pos.stage * A_STAGE;
         const uint32_t sb = base + OFF_B + pos.stage * B_STAGE;
@@ -473,6 +473,8 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace gf16
 
+#include "gemm_pair.cuh"
+
 // ====================================================================== host
 using namespace gf16;
 
@@ -585,10 +587,53 @@ void build_tile_order(int tiles_m, int tiles_n, int order, std::vector<uint32_t>
   for (auto& c : coded) out.push_back(c.second);
 }
 
+// Device tile tables cached per plan.  kind 0: single-CTA grid
+// (tiles_m, tiles_n, order); kind 1: pair tiles (M, N, pairs, split, order).
 struct OrderTable {
-  int tiles_m, tiles_n, order;
+  int64_t key[6];
   uint32_t* dev;
+  int64_t count;
 };
+
+double pair_makespan(const std::vector<uint32_t>& tiles, int pairs) {
+  std::vector<double> load((size_t)pairs, 0.0);
+  for (size_t i = 0; i < tiles.size(); ++i)
+    load[i % (size_t)pairs] += pair::narrow_of(tiles[i]) ? 0.5 : 1.0;
+  return *std::max_element(load.begin(), load.end());
+}
+
+// Pair-kernel tile list: 256-row x 256-column tiles over the output, a
+// column remainder of at most 128 as 128-wide tiles, wide tiles in Morton
+// order (pair-row on the even bits) followed by the narrow ones.  With one
+// split, if the wide tiles leave a partial last wave, those tiles are cut
+// into two 128-wide halves when that shortens the busiest pair's work.
+void build_pair_tiles(int M, int N, int pairs, int split_k, int order,
+                      std::vector<uint32_t>& out) {
+  const int tpms = (int)ceil_div(M, pair::PM);
+  const int wide_cols = (N > 128) ? (int)((N - 128 + 255) / 256) : 0;
+  const bool tail = (N - wide_cols * 256) > 0;
+  std::vector<uint32_t> grid;
+  build_tile_order(tpms, std::max(wide_cols, 1), order, grid);
+  std::vector<uint32_t> wide, narrow;
+  if (wide_cols > 0)
+    for (uint32_t e : grid)
+      wide.push_back(pair::pack(tile_m_of(e), 2 * tile_n_of(e), false));
+  if (tail)
+    for (int t = 0; t < tpms; ++t) narrow.push_back(pair::pack(t, 2 * wide_cols, true));
+  out = wide;
+  out.insert(out.end(), narrow.begin(), narrow.end());
+  if (split_k != 1 || pairs <= 0 || wide.empty()) return;
+  const size_t r = wide.size() % (size_t)pairs;
+  if (r == 0) return;
+  std::vector<uint32_t> alt(wide.begin(), wide.end() - r);
+  for (size_t i = wide.size() - r; i < wide.size(); ++i) {
+    const uint32_t e = wide[i];
+    alt.push_back(pair::pack(pair::tpm_of(e), pair::n128_of(e), true));
+    alt.push_back(pair::pack(pair::tpm_of(e), pair::n128_of(e) + 1, true));
+  }
+  alt.insert(alt.end(), narrow.begin(), narrow.end());
+  if (pair_makespan(alt, pairs) < pair_makespan(out, pairs)) out.swap(alt);
+}
 
 }  // namespace
 
@@ -600,6 +645,8 @@ struct gemm_f16_plan_s {
   unsigned long long timeout_ns = 1000000000ull;
   int tile_order = 0;
   int fault_unit = -1;
+  int kernel = 0;      // 0 auto, 1 single CTA, 2 CTA pair
+  int max_pairs = 0;   // co-resident clusters of two for the pair kernel
   void* ws = nullptr;
   size_t ws_bytes = 0;
   std::vector<OrderTable> orders;
@@ -669,10 +716,34 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
   GF16_CUDA(cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SMEM_BYTES),
             "cudaFuncSetAttribute(max dynamic smem)");
+  GF16_CUDA(cudaFuncSetAttribute(pair::gemm_f16_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)pair::SMEM_BYTES),
+            "cudaFuncSetAttribute(pair kernel smem)");
+  int max_clusters = 0;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(prop.multiProcessorCount / 2 * 2), 1, 1);
+    cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, pair::gemm_f16_pair_kernel, &cfg) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      max_clusters = 0;
+    }
+  }
   gemm_f16_plan_s* p = new (std::nothrow) gemm_f16_plan_s();
   if (!p) return GEMM_F16_ERR_OOM;
   p->device = device;
   p->num_sms = prop.multiProcessorCount;
+  p->max_pairs = max_clusters;
   cudaError_t e = cudaHostAlloc(&p->status_host, sizeof(int), cudaHostAllocMapped);
   if (e != cudaSuccess) {
     delete p;
@@ -727,8 +798,39 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
       if (value < -1 || value > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
       p->fault_unit = (int)value;
       return GEMM_F16_OK;
+    case GEMM_F16_OPT_KERNEL:
+      if (value < 0 || value > 2) return GEMM_F16_ERR_INVALID_ARG;
+      if (value == 2 && p->max_pairs <= 0) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+      p->kernel = (int)value;
+      return GEMM_F16_OK;
     default:
       return GEMM_F16_ERR_INVALID_ARG;
+  }
+}
+
+int64_t gemm_f16_pair_tiles(int M, int N, int pairs, int split_k, int order, uint32_t* out,
+                            int64_t cap) {
+  if (M <= 0 || N <= 0 || pairs < 1 || split_k < 1 || (order != 0 && order != 1))
+    return GEMM_F16_ERR_INVALID_ARG;
+  if (ceil_div(M, pair::PM) > 65535 || (N + 127) / 128 >= 0x7FFF) return GEMM_F16_ERR_INVALID_ARG;
+  if (cap < 0 || (cap > 0 && !out)) return GEMM_F16_ERR_INVALID_ARG;
+  std::vector<uint32_t> v;
+  build_pair_tiles(M, N, pairs, split_k, order, v);
+  const int64_t n = (int64_t)v.size();
+  std::memcpy(out, v.data(), sizeof(uint32_t) * (size_t)std::min<int64_t>(n, cap));
+  return n;
+}
+
+int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
+  if (!p || !value) return GEMM_F16_ERR_INVALID_ARG;
+  switch (option) {
+    case GEMM_F16_OPT_TIMEOUT_NS: *value = (int64_t)p->timeout_ns; return GEMM_F16_OK;
+    case GEMM_F16_OPT_TILE_ORDER: *value = p->tile_order; return GEMM_F16_OK;
+    case GEMM_F16_OPT_FAULT_UNIT: *value = p->fault_unit; return GEMM_F16_OK;
+    case GEMM_F16_OPT_KERNEL: *value = p->kernel; return GEMM_F16_OK;
+    case GEMM_F16_INFO_NUM_SMS: *value = p->num_sms; return GEMM_F16_OK;
+    case GEMM_F16_INFO_MAX_PAIRS: *value = p->max_pairs; return GEMM_F16_OK;
+    default: return GEMM_F16_ERR_INVALID_ARG;
   }
 }
 
@@ -736,15 +838,8 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
 
 namespace {
 
-int get_order_table(gemm_f16_plan_s* p, int tiles_m, int tiles_n, const uint32_t** out) {
-  for (auto& t : p->orders) {
-    if (t.tiles_m == tiles_m && t.tiles_n == tiles_n && t.order == p->tile_order) {
-      *out = t.dev;
-      return GEMM_F16_OK;
-    }
-  }
-  std::vector<uint32_t> host;
-  build_tile_order(tiles_m, tiles_n, p->tile_order, host);
+int upload_table(gemm_f16_plan_s* p, const int64_t (&key)[6], const std::vector<uint32_t>& host,
+                 const uint32_t** out) {
   uint32_t* dev = nullptr;
   GF16_CUDA(cudaMalloc(&dev, host.size() * sizeof(uint32_t)), "cudaMalloc(tile order)");
   cudaError_t e = cudaMemcpy(dev, host.data(), host.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
@@ -752,9 +847,44 @@ int get_order_table(gemm_f16_plan_s* p, int tiles_m, int tiles_n, const uint32_t
     cudaFree(dev);
     return cuda_fail(e, "cudaMemcpy(tile order)");
   }
-  p->orders.push_back(OrderTable{tiles_m, tiles_n, p->tile_order, dev});
+  OrderTable t;
+  std::memcpy(t.key, key, sizeof(key));
+  t.dev = dev;
+  t.count = (int64_t)host.size();
+  p->orders.push_back(t);
   *out = dev;
   return GEMM_F16_OK;
+}
+
+const OrderTable* find_table(gemm_f16_plan_s* p, const int64_t (&key)[6]) {
+  for (auto& t : p->orders)
+    if (std::memcmp(t.key, key, sizeof(key)) == 0) return &t;
+  return nullptr;
+}
+
+int get_order_table(gemm_f16_plan_s* p, int tiles_m, int tiles_n, const uint32_t** out) {
+  const int64_t key[6] = {0, tiles_m, tiles_n, p->tile_order, 0, 0};
+  if (const OrderTable* t = find_table(p, key)) {
+    *out = t->dev;
+    return GEMM_F16_OK;
+  }
+  std::vector<uint32_t> host;
+  build_tile_order(tiles_m, tiles_n, p->tile_order, host);
+  return upload_table(p, key, host, out);
+}
+
+int get_pair_table(gemm_f16_plan_s* p, int M, int N, int split_k, const uint32_t** out,
+                   int64_t* count) {
+  const int64_t key[6] = {1, M, N, p->max_pairs, split_k, p->tile_order};
+  if (const OrderTable* t = find_table(p, key)) {
+    *out = t->dev;
+    *count = t->count;
+    return GEMM_F16_OK;
+  }
+  std::vector<uint32_t> host;
+  build_pair_tiles(M, N, p->max_pairs, split_k, p->tile_order, host);
+  *count = (int64_t)host.size();
+  return upload_table(p, key, host, out);
 }
 
 int ensure_buffer(void** buf, size_t* cap, size_t bytes, cudaStream_t stream, const char* what) {
@@ -777,8 +907,17 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   const int64_t units = (int64_t)tiles_m * tiles_n * split_k;
   if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
 
+  // Automatic choice: the pair kernel once its 256 x 256 tiles (times the
+  // splits) fill at least one wave of pairs; below that the single-CTA
+  // kernel's smaller tiles spread the work over more SMs.
+  const bool pair_fits = (N + 127) / 128 < 0x7FFF && p->max_pairs > 0;
+  const int64_t pair_work = ceil_div(M, 256) * ceil_div(N, 256) * (int64_t)split_k;
+  const bool use_pair =
+      pair_fits && (p->kernel == 2 || (p->kernel == 0 && M > BM && pair_work >= p->max_pairs));
   const uint32_t* order = nullptr;
-  int rc = get_order_table(p, tiles_m, tiles_n, &order);
+  int64_t pair_tiles = 0;
+  int rc = use_pair ? get_pair_table(p, M, N, split_k, &order, &pair_tiles)
+                    : get_order_table(p, tiles_m, tiles_n, &order);
   if (rc) return rc;
 
   alignas(64) CUtensorMap tmA, tmB, tmC, tmW;
@@ -807,6 +946,31 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
     if (rc) return rc;
   }
 
+  if (use_pair) {
+    const int64_t punits = pair_tiles * split_k;
+    if (punits > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
+    pair::Params pp;
+    pp.M = M;
+    pp.N = N;
+    pp.K = K;
+    pp.split_k = split_k;
+    pp.kblocks = kblocks;
+    pp.num_units = (int)punits;
+    pp.order = order;
+    pp.C = static_cast<__half*>(C);
+    pp.ldc = ldc;
+    pp.status = p->status_dev;
+    pp.timeout_ns = p->timeout_ns;
+    pp.fault_unit = p->fault_unit;
+    const int64_t npairs = std::min<int64_t>(punits, std::max(p->max_pairs, 1));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * npairs), 1, 1);
+    cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.stream = stream;
+    GF16_CUDA(cudaLaunchKernelEx(&cfg, pair::gemm_f16_pair_kernel, tmA, tmB, tmC, tmW, pp),
+              "launch gemm_f16_pair_kernel");
+  } else {
   Params prm;
   prm.M = M;
   prm.N = N;
@@ -831,6 +995,7 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   cfg.stream = stream;
   GF16_CUDA(cudaLaunchKernelEx(&cfg, gemm_f16_kernel, tmA, tmB, tmC, tmW, prm),
             "launch gemm_f16_kernel");
+  }
 
   if (split_k > 1) {
     const int64_t groups = (int64_t)M * ((N + 3) / 4);

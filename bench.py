@@ -64,6 +64,8 @@ def parse_args():
                     help="idle seconds before the warm-up (page protocol: 5)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU seconds for the oracle baseline sample")
     return ap.parse_args()
@@ -300,6 +302,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     sh = int(stream.cuda_stream)
     plan = g.Plan(dev.index)
+    plan.set_option(g.OPT_KERNEL, args.kernel)
     launches_per_step = 1 if w.split_k == 1 else 2
 
     def step(i):
@@ -399,6 +402,15 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds, pairs_bits)
 
+    plan_sms = plan.get_option(g.INFO_NUM_SMS)
+    plan_pairs = plan.get_option(g.INFO_MAX_PAIRS)
+    pair_work = -(-w.M // 256) * -(-w.N // 256) * w.split_k
+    use_pair = plan_pairs > 0 and (args.kernel == 2 or (
+        args.kernel == 0 and w.M > 128 and pair_work >= plan_pairs))
+    kernel_desc = ("CTA pair (tcgen05 cta_group::2, 256-row tiles)" if use_pair
+                   else "single CTA (tcgen05 cta_group::1, 128x256 tiles)")
+    roofline["kernel"] = ("gf16::pair::gemm_f16_pair_kernel" if use_pair
+                          else "gf16::gemm_f16_kernel")
     plan.close()
     if rank == 0:
         line = {
@@ -406,7 +418,8 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
-            "config": workload_config(w),
+            "config": dict(workload_config(w), kernel=kernel_desc,
+                           sms=plan_sms, max_pairs=plan_pairs),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": args.steps * launches_per_step,
             "pct_of_peak": 100.0 * achieved / peak,

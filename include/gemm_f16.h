@@ -68,7 +68,15 @@ typedef enum gemm_f16_option {
      * bytes of its first stage but issues no copy for it, so that stage's
      * barrier never completes and the bounded waits must run out.  No copy
      * is left in flight.  Default -1 (off). */
-    GEMM_F16_OPT_FAULT_UNIT = 3
+    GEMM_F16_OPT_FAULT_UNIT = 3,
+    /* Which kernel runs the product: 0 = automatic (the CTA-pair kernel when
+     * M > 128 and ceil(M/256) * ceil(N/256) * split_k is at least the number
+     * of co-resident pairs, else the single-CTA kernel), 1 = single-CTA kernel (128 x 256
+     * tiles, tcgen05 cta_group::1), 2 = CTA-pair kernel (256-row tiles,
+     * 256 or 128 columns wide, tcgen05 cta_group::2).  Results agree within
+     * the usual tolerance; split results are bitwise reproducible for a
+     * fixed choice. */
+    GEMM_F16_OPT_KERNEL = 4
 } gemm_f16_option;
 
 /*
@@ -131,6 +139,15 @@ int gemm_f16_status(gemm_f16_plan_t plan);
 /* Set a gemm_f16_option (see above).  Applies to later runs. */
 int gemm_f16_set_option(gemm_f16_plan_t plan, int option, int64_t value);
 
+/* Read-only plan facts for gemm_f16_get_option. */
+enum {
+    GEMM_F16_INFO_NUM_SMS = 100,   /* SMs of the plan's device */
+    GEMM_F16_INFO_MAX_PAIRS = 101  /* co-resident CTA pairs of the pair kernel (0: unavailable) */
+};
+
+/* Read an option's current value, or one of the GEMM_F16_INFO_* facts. */
+int gemm_f16_get_option(gemm_f16_plan_t plan, int option, int64_t *value);
+
 /* Static description of an error code (never NULL). */
 const char *gemm_f16_strerror(int code);
 
@@ -153,6 +170,16 @@ int gemm_f16_validate(int M, int N, int K, const void *A, int64_t lda,
  * tiles_n must be in [1, 65535].
  */
 int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order,
+                            uint32_t *out, int64_t cap);
+
+/*
+ * Host-only: the work list of the CTA-pair kernel for an M x N output with
+ * `pairs` co-resident CTA pairs (see GEMM_F16_INFO_MAX_PAIRS).  Each entry
+ * is (pair_row | col128 << 16 | narrow << 31): rows 256*pair_row .. +255,
+ * columns 128*col128 .. +255 (wide) or .. +127 (narrow).  Writes up to `cap`
+ * entries and returns the count, or a negative error code.
+ */
+int64_t gemm_f16_pair_tiles(int M, int N, int pairs, int split_k, int order,
                             uint32_t *out, int64_t cap);
 
 /* Compile-time tile shape of the kernel: BM x BN output tile, BK k-block. */

@@ -141,3 +141,52 @@ def test_tile_order_rejects_bad_grid(lib):
     assert lib.gemm_f16_tile_order(0, 4, 0, None, 0) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_tile_order(4, 65536, 0, None, 0) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_tile_order(4, 4, 2, None, 0) == g.ERR_INVALID_ARG
+
+
+def _covered(tiles, M, N):
+    """Count how often each output element is covered by the pair tiles."""
+    import numpy as np
+    cov = np.zeros((M, N), np.int32)
+    for r0, c0, w in tiles:
+        cov[r0:min(r0 + 256, M), c0:min(c0 + w, N)] += 1
+    return cov
+
+
+@pytest.mark.parametrize("M,N", [(4096, 4096), (4000, 4104), (1024, 1024), (512, 512),
+                                 (129, 300), (256, 129), (300, 384), (1, 1), (2000, 100),
+                                 (777, 5000)])
+@pytest.mark.parametrize("pairs", [76, 7, 1])
+def test_pair_tiles_cover_output_exactly_once(lib, M, N, pairs):
+    import numpy as np
+    tiles = g.gemm_f16_pair_tiles(M, N, pairs, 1)
+    cov = _covered(tiles, M, N)
+    assert np.all(cov == 1)
+    for r0, c0, w in tiles:            # no tile starts outside the output
+        assert r0 < M and c0 < N and w in (128, 256)
+
+
+def _makespan(tiles, pairs):
+    load = [0.0] * pairs
+    for i, (_, _, w) in enumerate(tiles):
+        load[i % pairs] += w / 256
+    return max(load)
+
+
+def test_pair_tiles_balance_the_last_wave(lib):
+    # 4096^2: 256 wide tiles on 76 pairs = 3 full waves + 28; the 28 become
+    # 56 narrow tiles, so the busiest pair does 3.5 tiles' work instead of 4
+    t = g.gemm_f16_pair_tiles(4096, 4096, 76, 1)
+    assert sum(w == 256 for *_, w in t) == 228 and sum(w == 128 for *_, w in t) == 56
+    assert _makespan(t, 76) == 3.5
+    # ragged 4000 x 4104: a 128-wide column remainder plus the same balancing
+    t = g.gemm_f16_pair_tiles(4000, 4104, 76, 1)
+    assert _makespan(t, 76) == 3.5
+    # splits keep whole tiles (the split units are the parallelism)
+    t = g.gemm_f16_pair_tiles(512, 512, 76, 16)
+    assert len(t) == 4 and all(w == 256 for *_, w in t)
+
+
+def test_pair_tiles_reject_bad_arguments(lib):
+    assert lib.gemm_f16_pair_tiles(0, 8, 76, 1, 0, None, 0) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 0, 1, 0, None, 0) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 76, 0, 0, None, 0) == g.ERR_INVALID_ARG

@@ -18,8 +18,10 @@ from tests import gpu_util, parity
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def plan():
+@pytest.fixture(scope="module", params=[1, 2], ids=["cta1", "pair"])
+def plan(request):
+    """A plan pinned to one kernel: 1 = single-CTA, 2 = CTA pair.  Every
+    test in this file runs once per kernel."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
@@ -27,6 +29,7 @@ def plan():
     from async_barrier_pipelined_gb300 import build
     build.build()
     p = g.Plan(0)
+    p.set_option(g.OPT_KERNEL, request.param)
     yield p
     p.close()
 
@@ -222,3 +225,18 @@ def test_invalid_arguments_enqueue_nothing(plan):
         g.gemm_f16_run(plan.handle, 64, 64, 64, A.data_ptr(), 64, A.data_ptr(), 64,
                        A.data_ptr(), 64, 2, 0)
     assert e.value.code == g.ERR_INVALID_ARG
+
+
+def test_kernels_agree(plan):
+    """The other kernel on the same inputs agrees within the parity bounds."""
+    import async_barrier_pipelined_gb300 as g
+    w = si.custom(1000, 1300, 700, seed=31)
+    A, B = w.pair_bits(0)
+    c0, _ = gpu_util.run(plan, A, B)
+    mine = plan.get_option(g.OPT_KERNEL)
+    plan.set_option(g.OPT_KERNEL, 3 - mine)
+    try:
+        c1, _ = gpu_util.run(plan, A, B)
+    finally:
+        plan.set_option(g.OPT_KERNEL, mine)
+    parity.check(c1, c0, "kernel 1 vs kernel 2")

@@ -16,23 +16,35 @@ import pytest
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "mbarrier_model", "model.cpp")
+PAIR_SRC = os.path.join(HERE, "mbarrier_model", "pair_model.cpp")
 CSRC = os.path.join(os.path.dirname(HERE), "async_barrier_pipelined_gb300", "csrc")
 BUILD = os.path.join(HERE, "mbarrier_model", "_build")
 EXE = os.path.join(BUILD, "model")
+PAIR_EXE = os.path.join(BUILD, "pair_model")
+
+
+def _build(src, exe):
+    if shutil.which("g++") is None:
+        pytest.skip("g++ not available")
+    os.makedirs(BUILD, exist_ok=True)
+    deps = [src, os.path.join(CSRC, "schedule.h"),
+            os.path.join(HERE, "mbarrier_model", "mbar_model.h")]
+    if not os.path.exists(exe) or any(os.path.getmtime(d) > os.path.getmtime(exe) for d in deps):
+        tmp = exe + f".tmp{os.getpid()}"
+        subprocess.run(["g++", "-std=c++17", "-O2", "-pthread", "-I", CSRC, src, "-o", tmp],
+                       check=True)
+        os.replace(tmp, exe)
+    return exe
 
 
 @pytest.fixture(scope="module")
 def model():
-    if shutil.which("g++") is None:
-        pytest.skip("g++ not available")
-    os.makedirs(BUILD, exist_ok=True)
-    deps = [SRC, os.path.join(CSRC, "schedule.h")]
-    if not os.path.exists(EXE) or any(os.path.getmtime(d) > os.path.getmtime(EXE) for d in deps):
-        tmp = EXE + f".tmp{os.getpid()}"
-        subprocess.run(["g++", "-std=c++17", "-O2", "-pthread", "-I", CSRC, SRC, "-o", tmp],
-                       check=True)
-        os.replace(tmp, EXE)
-    return EXE
+    return _build(SRC, EXE)
+
+
+@pytest.fixture(scope="module")
+def pair_model():
+    return _build(PAIR_SRC, PAIR_EXE)
 
 
 def _run(exe, *args):
@@ -71,3 +83,44 @@ def test_fault_leaves_mma_blocked_on_the_starved_stage(model):
 def test_fault_on_other_cta_does_not_affect_this_one(model):
     rc, out = _run(model, 4, 8, 2, 1, 1, 4, 20, 2)
     assert rc == 0 and out.startswith("OK"), out
+
+
+# CTA-pair protocol: (stages, units, pairs, pair, split_k, kblocks, seeds, mode[, arg])
+PAIR_CASES = [
+    (6, 284, 76, 0, 1, 64, 10, "normal"),     # 4096^2: 228 wide + 56 narrow units, first pair
+    (6, 284, 76, 75, 1, 64, 10, "normal"),    # last pair (3 units)
+    (6, 272, 76, 5, 1, 47, 10, "normal"),     # ragged 4000 x 4104 x 3000
+    (6, 64, 64, 3, 16, 512, 4, "normal"),     # split-K units
+    (2, 9, 4, 1, 3, 7, 100, "normal"),        # uneven split ranges
+    (1, 5, 2, 0, 1, 3, 100, "normal"),        # one stage
+    (6, 3, 1, 0, 1, 1, 100, "normal"),        # one k-block per unit
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_pair_protocol_interleavings(pair_model, case):
+    rc, out = _run(pair_model, *case)
+    assert rc == 0 and out.startswith("OK") and "deadlocks=0" in out, out
+
+
+@pytest.mark.parametrize("case", [
+    (6, 8, 2, 0, 1, 4, 50, "fault", 2),          # leader skips one fill's copies
+    (6, 8, 2, 0, 1, 9, 50, "fault", 0),
+    (6, 8, 2, 0, 1, 20, 100, "stop_leader", 5),  # leader producer times out early
+    (3, 8, 2, 0, 1, 20, 100, "stop_leader", 0),
+    (6, 8, 2, 0, 1, 20, 100, "stop_peer", 7),    # peer producer times out early
+    (3, 8, 2, 0, 1, 20, 100, "stop_peer", 0),
+    (4, 8, 1, 0, 2, 20, 100, "stop_peer", 13),
+], ids=lambda c: "-".join(map(str, c)))
+def test_pair_abort_drain_completes_issued_phases(pair_model, case):
+    """Every seed deadlocks (the state the kernel's bounded waits escape);
+    the leader's drain then completes every phase whose copies were issued,
+    and only the faulted fill (whose bytes never come) stays open."""
+    rc, out = _run(pair_model, *case)
+    seeds = case[6]
+    assert rc == 0 and out.startswith("OK") and f"deadlocks={seeds}" in out, out
+
+
+def test_pair_fault_on_other_pair_does_not_affect_this_one(pair_model):
+    rc, out = _run(pair_model, 6, 8, 2, 1, 1, 4, 20, "fault", 2)
+    assert rc == 0 and "deadlocks=0" in out, out

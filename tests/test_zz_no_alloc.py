@@ -37,6 +37,9 @@ def plan():
     from async_barrier_pipelined_gb300 import build
     build.build()
     p = g.Plan(0)
+    # gemm_f16_run_noalloc runs the single-CTA kernel; compare it with the
+    # plan entry point running that same kernel.
+    p.set_option(g.OPT_KERNEL, 1)
     yield p
     p.close()
 
