@@ -56,10 +56,11 @@ namespace gf16 {
 
 // ------------------------------------------------------------------ tiling
 constexpr int BM = 128;          // output tile rows (= MMA M, = TMEM lanes)
-constexpr int BN = 256;          // output tile columns (= MMA N)
+constexpr int BN = 256;          // widest output tile (= MMA N); a launch may use 128 or 64
 constexpr int BK = 64;           // k-block: 64 halves = one 128-byte swizzle row
 constexpr int UMMA_K = 16;       // K of one kind::f16 MMA
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;          // stages of the widest tile; narrower tiles get more
+constexpr int MAX_STAGES = 8;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 4;
@@ -67,34 +68,42 @@ constexpr int EPI_WARPS = 4;
 constexpr uint32_t A_STAGE = BM * BK * 2;        // 16 KB
 constexpr uint32_t B_BOX_N = 64;                 // N extent of one B copy (128 B)
 constexpr uint32_t B_BOX = B_BOX_N * BK * 2;     // 8 KB
-constexpr uint32_t B_STAGE = BN * BK * 2;        // 32 KB
-constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE; // bytes credited per stage
+constexpr uint32_t B_STAGE = BN * BK * 2;        // 32 KB (room for the widest tile)
 constexpr uint32_t EPI_BUF = 32 * 64;            // 32 rows x 64 B staging box
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = BN;
 
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
-constexpr uint32_t OFF_EPI = OFF_B + STAGES * B_STAGE;
+// The ring: `stages` stages of (A tile, B tile) back to back, each stage
+// A_STAGE + W*BK*2 bytes for a W-wide tile; 196,608 bytes hold 4 stages of
+// 256-wide, 6 of 128-wide or 8 of 64-wide tiles.
+constexpr uint32_t RING_BYTES = STAGES * (A_STAGE + B_STAGE);
+constexpr uint32_t OFF_EPI = RING_BYTES;
 constexpr uint32_t OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
-constexpr uint32_t NUM_BARS = 2 * STAGES + 2 + 2 + 1;  // full, empty, tmem_full, tmem_empty, mma_done
+constexpr uint32_t NUM_BARS = 2 * MAX_STAGES + 2 + 2 + 1;  // full, empty, tmem_full, tmem_empty, mma_done
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // room to align the base to 1024
 static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit per CTA");
-static_assert(OFF_EPI % 1024 == 0 && OFF_B % 1024 == 0, "swizzled buffers need 1024-B alignment");
+static_assert(OFF_EPI % 1024 == 0 && A_STAGE % 1024 == 0, "swizzled buffers need 1024-B alignment");
+
+// Stages of the ring for a W-wide tile.
+__host__ __device__ constexpr int stages_for(int w) {
+  return (int)(RING_BYTES / (A_STAGE + (uint32_t)w * BK * 2)) < MAX_STAGES
+             ? (int)(RING_BYTES / (A_STAGE + (uint32_t)w * BK * 2))
+             : MAX_STAGES;
+}
+static_assert(stages_for(256) == 4 && stages_for(128) == 6 && stages_for(64) == 8, "ring sizes");
 static_assert(2 * ACC_COLS <= TMEM_COLS, "two accumulators must fit in TMEM");
 
 // Instruction descriptor of tcgen05.mma kind::f16: D FP32 (bits 4-5 = 1),
 // A and B FP16 (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B MN-major
 // (bit 16 = 1, row-major B is N-contiguous), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
-constexpr uint32_t make_idesc(int m, int n) {
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
   return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) |
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-constexpr uint32_t IDESC = make_idesc(BM, BN);
 
 // Shared-memory matrix descriptor (tcgen05): start address >> 4 (bits 0-13),
 // leading byte offset >> 4 (16-29), stride byte offset >> 4 (32-45), fixed
@@ -114,6 +123,9 @@ constexpr uint32_t B_LBO = B_BOX, B_SBO = 1024, B_KSTEP = UMMA_K * 128;
 
 struct Params {
   int M, N, K;
+  int bn;                  // tile width of this launch: 256, 128 or 64
+  int stages;              // ring depth for that width (stages_for(bn))
+  uint32_t stage_bytes;    // A_STAGE + bn * BK * 2
   int tiles_m, tiles_n, split_k, kblocks, num_units;
   const uint32_t* order;   // tile order: tiles_m*tiles_n packed (tm | tn<<16)
   __half* C;               // output, for the masked stores of a ragged last chunk
@@ -169,13 +181,15 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUte
   RingPos pos{0, 0};
   uint32_t issued = 0;
   bool ok = true;
+  const int boxes = p.bn / (int)B_BOX_N;
+  const uint32_t stage_tx = A_STAGE + (uint32_t)p.bn * BK * 2;
   for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
     int tpos, s, kb0, kb1;
     decode_unit(u, p.split_k, &tpos, &s);
     split_range(p.kblocks, p.split_k, s, &kb0, &kb1);
     const uint32_t packed = p.order[tpos];
     const int m0 = (int)tile_m_of(packed) * BM;
-    const int n0 = (int)tile_n_of(packed) * BN;
+    const int n0 = (int)tile_n_of(packed) * p.bn;
     const int skip_kb = (u == p.fault_unit) ? kb0 : -1;
     for (int kb = kb0; kb < kb1; ++kb) {
       if (!wait_phase(b.empty + 8 * pos.stage, producer_wait_parity(pos), p, abort_flag)) {
@@ -183,18 +197,17 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUte
         break;
       }
       const uint32_t fb = b.full + 8 * pos.stage;
-      ptx::mbar_arrive_expect_tx_relaxed(fb, STAGE_TX);
+      ptx::mbar_arrive_expect_tx_relaxed(fb, stage_tx);
       if (kb != skip_kb) {
-        const uint32_t sa = base + OFF_A + pos.stage * A_STAGE;
-        const uint32_t sb = base + OFF_B + pos.stage * B_STAGE;
+        const uint32_t sa = base + pos.stage * p.stage_bytes;
+        const uint32_t sb = sa + A_STAGE;
         const int k0 = kb * BK;
         ptx::tma_load_2d(sa, tmA, fb, k0, m0);
-#pragma unroll
-        for (int j = 0; j < BN / (int)B_BOX_N; ++j)
+        for (int j = 0; j < boxes; ++j)
           ptx::tma_load_2d(sb + j * B_BOX, tmB, fb, n0 + j * (int)B_BOX_N, k0);
       }
       ++issued;
-      ring_advance(pos, STAGES);
+      ring_advance(pos, (uint32_t)p.stages);
     }
   }
   *pos_out = pos;
@@ -206,10 +219,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUte
 // shared memory when it exits.  A stage whose phase already completed
 // returns at once.
 __device__ __noinline__ void producer_drain(const Bars& b, RingPos pos, uint32_t issued,
-                                            uint64_t limit_ns) {
-  const uint32_t n = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
+                                            uint32_t stages, uint64_t limit_ns) {
+  const uint32_t n = issued < stages ? issued : stages;
   for (uint32_t i = 0; i < n; ++i) {
-    ring_retreat(pos, STAGES);
+    ring_retreat(pos, stages);
     wait_drain(b.full + 8 * pos.stage, consumer_wait_parity(pos), limit_ns);
   }
 }
@@ -218,6 +231,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
                                          const Bars& b, volatile int* abort_flag) {
   RingPos pos{0, 0};
   uint32_t local = 0;
+  const uint32_t idesc = make_idesc(BM, p.bn);
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     int tpos, s, kb0, kb1;
     decode_unit(u, p.split_k, &tpos, &s);
@@ -234,18 +248,17 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
         break;
       }
       ptx::tc_fence_after();
-      const uint64_t a_desc =
-          smem_desc_sw128(base + OFF_A + pos.stage * A_STAGE, A_LBO, A_SBO);
-      const uint64_t b_desc =
-          smem_desc_sw128(base + OFF_B + pos.stage * B_STAGE, B_LBO, B_SBO);
+      const uint32_t sa = base + pos.stage * p.stage_bytes;
+      const uint64_t a_desc = smem_desc_sw128(sa, A_LBO, A_SBO);
+      const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE, B_LBO, B_SBO);
       const uint32_t first = (kb == kb0) ? 1u : 0u;
 #pragma unroll
       for (int k = 0; k < BK / UMMA_K; ++k) {
-        ptx::mma_f16(d_tmem, a_desc + ((k * A_KSTEP) >> 4), b_desc + ((k * B_KSTEP) >> 4), IDESC,
+        ptx::mma_f16(d_tmem, a_desc + ((k * A_KSTEP) >> 4), b_desc + ((k * B_KSTEP) >> 4), idesc,
                      (first && k == 0) ? 0u : 1u);
       }
       ptx::mma_commit(b.empty + 8 * pos.stage);
-      ring_advance(pos, STAGES);
+      ring_advance(pos, (uint32_t)p.stages);
     }
     if (!ok) break;
     ptx::mma_commit(b.tfull + 8 * acc);
@@ -277,7 +290,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
     decode_unit(u, p.split_k, &tpos, &s);
     const uint32_t packed = p.order[tpos];
     const int m0 = (int)tile_m_of(packed) * BM;
-    const int n0 = (int)tile_n_of(packed) * BN;
+    const int n0 = (int)tile_n_of(packed) * p.bn;
     const uint32_t acc = local & 1u;
     const uint32_t acc_phase = (local >> 1) & 1u;
     bool got = wait_phase(b.tfull + 8 * acc, acc_phase, p, abort_flag);
@@ -286,7 +299,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
     const int row0 = m0 + (int)quarter * 32;
     const uint32_t t_row = tmem_base + acc * ACC_COLS + ((quarter * 32u) << 16);
     if (row0 < p.M) {
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < p.bn / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= p.N) break;
         uint32_t r[32];
@@ -368,8 +381,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   Bars b;
   b.full = base + OFF_BAR;
-  b.empty = b.full + 8 * STAGES;
-  b.tfull = b.empty + 8 * STAGES;
+  b.empty = b.full + 8 * MAX_STAGES;
+  b.tfull = b.empty + 8 * MAX_STAGES;
   b.tempty = b.tfull + 16;
   b.mma_done = b.tempty + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
@@ -379,7 +392,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmB);
     ptx::prefetch_tmap(&tmC);
     if (p.split_k > 1) ptx::prefetch_tmap(&tmW);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < p.stages; ++s) {
       ptx::mbar_init(b.full + 8 * s, 1);   // the producer's arrive.expect_tx (+ tx bytes)
       ptx::mbar_init(b.empty + 8 * s, 1);  // one tcgen05.commit per use
     }
@@ -399,6 +412,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
+  // A dependent launch (the split reduction) may be scheduled now; it waits
+  // for this grid's completion before touching the partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   RingPos prod_pos{0, 0};
   uint32_t prod_issued = 0;
@@ -416,7 +432,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   // Every role has stopped, so the abort flag is final here.
   if (warp == 0 && lane == 0 && *abort_flag)
-    producer_drain(b, prod_pos, prod_issued, p.timeout_ns);
+    producer_drain(b, prod_pos, prod_issued, (uint32_t)p.stages, p.timeout_ns);
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, TMEM_COLS);
@@ -437,6 +453,9 @@ __device__ __forceinline__ void add4(float4& acc, const float4& v) {
 __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ ws, int M, int N, int64_t ldw, int split_k,
                          int64_t split_stride, __half* __restrict__ C, int64_t ldc) {
+  // Launched as a programmatic dependent of the GEMM kernel: wait here until
+  // that grid has finished and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t groups = (N + 3) / 4;
   const int64_t total = (int64_t)M * groups;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
@@ -637,6 +656,14 @@ void build_pair_tiles(int M, int N, int pairs, int split_k, int order,
 
 }  // namespace
 
+// Recently encoded tensor maps, keyed by everything the encoding depends on,
+// so that repeated runs on the same buffers skip cuTensorMapEncodeTiled.
+struct TmapEntry {
+  uint64_t key[8];
+  CUtensorMap map;
+};
+constexpr int TMAP_CACHE = 32;
+
 struct gemm_f16_plan_s {
   int device = 0;
   int num_sms = 0;
@@ -646,13 +673,53 @@ struct gemm_f16_plan_s {
   int tile_order = 0;
   int fault_unit = -1;
   int kernel = 0;      // 0 auto, 1 single CTA, 2 CTA pair
+  int tile_width = 0;  // single-CTA tile width: 0 auto, else 256 / 128 / 64
   int max_pairs = 0;   // co-resident clusters of two for the pair kernel
   void* ws = nullptr;
   size_t ws_bytes = 0;
   std::vector<OrderTable> orders;
   void* hbuf[3] = {nullptr, nullptr, nullptr};  // device staging for run_host
   size_t hcap[3] = {0, 0, 0};
+  TmapEntry tmaps[TMAP_CACHE];
+  int tmap_used = 0, tmap_next = 0;
 };
+
+namespace {
+
+// encode_2d through the plan's cache.
+int cached_encode_2d(gemm_f16_plan_s* p, CUtensorMap* map, CUtensorMapDataType dt, const void* ptr,
+                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                     uint32_t box_outer, CUtensorMapSwizzle swz, CUtensorMapL2promotion promo) {
+  const uint64_t key[8] = {(uint64_t)(uintptr_t)ptr, inner, outer, row_bytes,
+                           ((uint64_t)box_inner << 32) | box_outer,
+                           ((uint64_t)dt << 32) | (uint64_t)swz, (uint64_t)promo, 0};
+  for (int i = 0; i < p->tmap_used; ++i) {
+    if (std::memcmp(p->tmaps[i].key, key, sizeof(key)) == 0) {
+      *map = p->tmaps[i].map;
+      return GEMM_F16_OK;
+    }
+  }
+  const int rc = encode_2d(map, dt, ptr, inner, outer, row_bytes, box_inner, box_outer, swz, promo);
+  if (rc) return rc;
+  TmapEntry& e = p->tmaps[p->tmap_next];
+  std::memcpy(e.key, key, sizeof(key));
+  e.map = *map;
+  p->tmap_next = (p->tmap_next + 1) % TMAP_CACHE;
+  if (p->tmap_used < TMAP_CACHE) ++p->tmap_used;
+  return GEMM_F16_OK;
+}
+
+// Host <-> device copy of a row-strided matrix: one plain copy when both
+// sides are contiguous, a pitched copy otherwise.
+cudaError_t copy_rows(void* dst, int64_t dpitch, const void* src, int64_t spitch,
+                      int64_t row_bytes, int64_t rows, cudaMemcpyKind kind, cudaStream_t stream) {
+  if (dpitch == row_bytes && spitch == row_bytes)
+    return cudaMemcpyAsync(dst, src, (size_t)(row_bytes * rows), kind, stream);
+  return cudaMemcpy2DAsync(dst, (size_t)dpitch, src, (size_t)spitch, (size_t)row_bytes,
+                           (size_t)rows, kind, stream);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -798,6 +865,10 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
       if (value < -1 || value > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
       p->fault_unit = (int)value;
       return GEMM_F16_OK;
+    case GEMM_F16_OPT_TILE_WIDTH:
+      if (value != 0 && value != 64 && value != 128 && value != 256) return GEMM_F16_ERR_INVALID_ARG;
+      p->tile_width = (int)value;
+      return GEMM_F16_OK;
     case GEMM_F16_OPT_KERNEL:
       if (value < 0 || value > 2) return GEMM_F16_ERR_INVALID_ARG;
       if (value == 2 && p->max_pairs <= 0) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
@@ -828,6 +899,7 @@ int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
     case GEMM_F16_OPT_TILE_ORDER: *value = p->tile_order; return GEMM_F16_OK;
     case GEMM_F16_OPT_FAULT_UNIT: *value = p->fault_unit; return GEMM_F16_OK;
     case GEMM_F16_OPT_KERNEL: *value = p->kernel; return GEMM_F16_OK;
+    case GEMM_F16_OPT_TILE_WIDTH: *value = p->tile_width; return GEMM_F16_OK;
     case GEMM_F16_INFO_NUM_SMS: *value = p->num_sms; return GEMM_F16_OK;
     case GEMM_F16_INFO_MAX_PAIRS: *value = p->max_pairs; return GEMM_F16_OK;
     default: return GEMM_F16_ERR_INVALID_ARG;
@@ -899,21 +971,48 @@ int ensure_buffer(void** buf, size_t* cap, size_t bytes, cudaStream_t stream, co
   return GEMM_F16_OK;
 }
 
+// Tile width of the single-CTA kernel: 256, 128 or 64 columns.  Estimated
+// time = waves x (k-blocks per unit x cycles per k-block + fixed cost per
+// tile), with cycles per k-block max(W/2, 32 + W/4) for a 128 x W x 64
+// k-block (tensor-core time vs. shared-memory operand reads) and ~2000
+// cycles of pipeline fill and epilogue per tile.  Narrow tiles win when
+// wide ones leave SMs idle.
+int pick_tile_width(int M, int N, int kblocks, int split_k, int num_sms) {
+  const int64_t kb_unit = ceil_div(kblocks, split_k);
+  int best = BN;
+  int64_t best_cost = -1;
+  for (int w : {256, 128, 64}) {
+    if (ceil_div(N, w) > 65535) continue;
+    const int64_t units = ceil_div(M, BM) * ceil_div(N, w) * split_k;
+    const int64_t waves = ceil_div(units, std::max(num_sms, 1));
+    const int64_t per_kb = std::max<int64_t>(w / 2, 32 + w / 4);
+    const int64_t cost = waves * (kb_unit * per_kb + 2000);
+    if (best_cost < 0 || cost < best_cost) {
+      best = w;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t lda, const void* B,
                int64_t ldb, void* C, int64_t ldc, int split_k, cudaStream_t stream) {
   const int tiles_m = (int)ceil_div(M, BM);
-  const int tiles_n = (int)ceil_div(N, BN);
   const int kblocks = (int)ceil_div(K, BK);
+  const int bn = (p->tile_width != 0 && ceil_div(N, p->tile_width) <= 65535)
+                     ? p->tile_width
+                     : pick_tile_width(M, N, kblocks, split_k, p->num_sms);
+  const int tiles_n = (int)ceil_div(N, bn);
   const int64_t units = (int64_t)tiles_m * tiles_n * split_k;
   if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
 
   // Automatic choice: the pair kernel once its 256 x 256 tiles (times the
-  // splits) fill at least one wave of pairs; below that the single-CTA
+  // splits) fill at least half a wave of pairs; below that the single-CTA
   // kernel's smaller tiles spread the work over more SMs.
   const bool pair_fits = (N + 127) / 128 < 0x7FFF && p->max_pairs > 0;
   const int64_t pair_work = ceil_div(M, 256) * ceil_div(N, 256) * (int64_t)split_k;
   const bool use_pair =
-      pair_fits && (p->kernel == 2 || (p->kernel == 0 && M > BM && pair_work >= p->max_pairs));
+      pair_fits && (p->kernel == 2 || (p->kernel == 0 && M > BM && 2 * pair_work >= p->max_pairs));
   const uint32_t* order = nullptr;
   int64_t pair_tiles = 0;
   int rc = use_pair ? get_pair_table(p, M, N, split_k, &order, &pair_tiles)
@@ -922,15 +1021,15 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
 
   alignas(64) CUtensorMap tmA, tmB, tmC, tmW;
   std::memset(&tmW, 0, sizeof(tmW));
-  rc = encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
+  rc = cached_encode_2d(p, &tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
                  (uint64_t)lda * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc) return rc;
-  rc = encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)N, (uint64_t)K,
+  rc = cached_encode_2d(p, &tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)N, (uint64_t)K,
                  (uint64_t)ldb * 2, B_BOX_N, BK, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc) return rc;
-  rc = encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, (uint64_t)N, (uint64_t)M,
+  rc = cached_encode_2d(p, &tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, (uint64_t)N, (uint64_t)M,
                  (uint64_t)ldc * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
                  CU_TENSOR_MAP_L2_PROMOTION_NONE);
   if (rc) return rc;
@@ -975,6 +1074,9 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   prm.M = M;
   prm.N = N;
   prm.K = K;
+  prm.bn = bn;
+  prm.stages = stages_for(bn);
+  prm.stage_bytes = A_STAGE + (uint32_t)bn * BK * 2;
   prm.tiles_m = tiles_m;
   prm.tiles_n = tiles_n;
   prm.split_k = split_k;
@@ -1004,6 +1106,11 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
     rcfg.gridDim = dim3(rgrid, 1, 1);
     rcfg.blockDim = dim3(256, 1, 1);
     rcfg.stream = stream;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    rcfg.attrs = &pdl;
+    rcfg.numAttrs = 1;
     GF16_CUDA(cudaLaunchKernelEx(&rcfg, splitk_reduce_kernel, (const float*)p->ws, M, N, ldw,
                                  split_k, split_stride, (__half*)C, (int64_t)ldc),
               "launch splitk_reduce_kernel");
@@ -1042,16 +1149,16 @@ int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, in
     rc = ensure_buffer(&p->hbuf[i], &p->hcap[i], bytes[i], stream, "host-run staging allocation");
     if (rc) return rc;
   }
-  GF16_CUDA(cudaMemcpy2DAsync(p->hbuf[0], dlda * 2, hA, lda * 2, (size_t)K * 2, M,
-                              cudaMemcpyHostToDevice, stream),
+  GF16_CUDA(copy_rows(p->hbuf[0], dlda * 2, hA, lda * 2, (int64_t)K * 2, M,
+                      cudaMemcpyHostToDevice, stream),
             "copy A to device");
-  GF16_CUDA(cudaMemcpy2DAsync(p->hbuf[1], dldb * 2, hB, ldb * 2, (size_t)N * 2, K,
-                              cudaMemcpyHostToDevice, stream),
+  GF16_CUDA(copy_rows(p->hbuf[1], dldb * 2, hB, ldb * 2, (int64_t)N * 2, K,
+                      cudaMemcpyHostToDevice, stream),
             "copy B to device");
   rc = run_device(p, M, N, K, p->hbuf[0], dlda, p->hbuf[1], dldb, p->hbuf[2], dldc, split_k, stream);
   if (rc) return rc;
-  GF16_CUDA(cudaMemcpy2DAsync(hC, ldc * 2, p->hbuf[2], dldc * 2, (size_t)N * 2, M,
-                              cudaMemcpyDeviceToHost, stream),
+  GF16_CUDA(copy_rows(hC, ldc * 2, p->hbuf[2], dldc * 2, (int64_t)N * 2, M,
+                      cudaMemcpyDeviceToHost, stream),
             "copy C to host");
   return GEMM_F16_OK;
 }
@@ -1186,6 +1293,9 @@ extern "C" int gemm_f16_run_noalloc(int M, int N, int K, const void* A, int64_t 
   prm.M = M;
   prm.N = N;
   prm.K = K;
+  prm.bn = BN;
+  prm.stages = stages_for(BN);
+  prm.stage_bytes = A_STAGE + (uint32_t)BN * BK * 2;
   prm.tiles_m = tiles_m;
   prm.tiles_n = tiles_n;
   prm.split_k = split_k;

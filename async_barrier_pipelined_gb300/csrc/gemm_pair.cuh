@@ -381,6 +381,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
+  // A dependent launch (the split reduction) may be scheduled now; it waits
+  // for this grid's completion before touching the partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   uint32_t issued = 0;
   if (warp == 0) {

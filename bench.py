@@ -50,7 +50,7 @@ METRIC = "FP16 GEMM TFLOPS at M=N=K=4096 on 1 GB300; % of dense FP16 tensor peak
 FALLBACK_TENSOR_TFLOPS = 1900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "async_barrier_pipelined_gb300", "csrc", f)
-                  for f in ("gemm_f16.cu", "ptx.cuh", "schedule.h")]
+                  for f in ("gemm_f16.cu", "gemm_pair.cuh", "ptx.cuh", "schedule.h")]
 
 
 def parse_args():
@@ -406,7 +406,7 @@ def run_ours(args):
     plan_pairs = plan.get_option(g.INFO_MAX_PAIRS)
     pair_work = -(-w.M // 256) * -(-w.N // 256) * w.split_k
     use_pair = plan_pairs > 0 and (args.kernel == 2 or (
-        args.kernel == 0 and w.M > 128 and pair_work >= plan_pairs))
+        args.kernel == 0 and w.M > 128 and 2 * pair_work >= plan_pairs))
     kernel_desc = ("CTA pair (tcgen05 cta_group::2, 256-row tiles)" if use_pair
                    else "single CTA (tcgen05 cta_group::1, 128x256 tiles)")
     roofline["kernel"] = ("gf16::pair::gemm_f16_pair_kernel" if use_pair

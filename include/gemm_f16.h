@@ -70,13 +70,20 @@ typedef enum gemm_f16_option {
      * is left in flight.  Default -1 (off). */
     GEMM_F16_OPT_FAULT_UNIT = 3,
     /* Which kernel runs the product: 0 = automatic (the CTA-pair kernel when
-     * M > 128 and ceil(M/256) * ceil(N/256) * split_k is at least the number
-     * of co-resident pairs, else the single-CTA kernel), 1 = single-CTA kernel (128 x 256
+     * M > 128 and ceil(M/256) * ceil(N/256) * split_k is at least half the
+     * number of co-resident pairs, else the single-CTA kernel),
+     * 1 = single-CTA kernel (128 x 256
      * tiles, tcgen05 cta_group::1), 2 = CTA-pair kernel (256-row tiles,
      * 256 or 128 columns wide, tcgen05 cta_group::2).  Results agree within
      * the usual tolerance; split results are bitwise reproducible for a
      * fixed choice. */
-    GEMM_F16_OPT_KERNEL = 4
+    GEMM_F16_OPT_KERNEL = 4,
+    /* Output tile width of the single-CTA kernel: 0 = automatic (a cost
+     * model picks 256, 128 or 64 columns so that small problems spread over
+     * more SMs), or 256 / 128 / 64.  Narrower tiles get a deeper ring
+     * (4 / 6 / 8 stages in the same shared memory).  Results agree within
+     * the usual tolerance. */
+    GEMM_F16_OPT_TILE_WIDTH = 5
 } gemm_f16_option;
 
 /*

@@ -240,3 +240,22 @@ def test_kernels_agree(plan):
     finally:
         plan.set_option(g.OPT_KERNEL, mine)
     parity.check(c1, c0, "kernel 1 vs kernel 2")
+
+
+@pytest.mark.parametrize("width", [64, 128, 256])
+@pytest.mark.parametrize("shape,split", [((300, 700, 200), 1), ((129, 257, 1000), 3),
+                                         ((1000, 64, 72), 1)])
+def test_single_cta_tile_widths(plan, width, shape, split):
+    """Every tile width of the single-CTA kernel (and its ring depth) against
+    the oracle; the pair kernel ignores the option."""
+    import async_barrier_pipelined_gb300 as g
+    M, N, K = shape
+    w = si.custom(M, N, K, seed=width + M)
+    A, B = w.pair_bits(0)
+    plan.set_option(g.OPT_TILE_WIDTH, width)
+    try:
+        c, full = gpu_util.run(plan, A, B, split_k=split, guard_rows=1, ldc=(N + 7) // 8 * 8 + 8)
+    finally:
+        plan.set_option(g.OPT_TILE_WIDTH, 0)
+    parity.check(c, oracle.gemm_f16(A, B), f"width {width}")
+    gpu_util.assert_untouched_outside(full, M, N)

@@ -65,6 +65,8 @@ CASES = [
     (3, 6, 1, 0, 2, 2, 200),        # one k-block per split
     (5, 3, 1, 0, 1, 1, 200),        # single k-block, more stages than fills
     (4, 1, 1, 0, 1, 1, 200),        # one unit, one k-block
+    (8, 128, 128, 9, 1, 16, 100),   # 1024^3 with 64-wide tiles: 8-stage ring
+    (6, 64, 64, 2, 1, 16, 100),     # 128-wide tiles: 6-stage ring
 ]
 
 
