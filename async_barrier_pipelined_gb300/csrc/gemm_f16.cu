@@ -674,6 +674,7 @@ struct gemm_f16_plan_s {
   int fault_unit = -1;
   int kernel = 0;      // 0 auto, 1 single CTA, 2 CTA pair
   int tile_width = 0;  // single-CTA tile width: 0 auto, else 256 / 128 / 64
+  int sm_limit = 0;    // most SMs a launch may use (0: all)
   int max_pairs = 0;   // co-resident clusters of two for the pair kernel
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -865,6 +866,10 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
       if (value < -1 || value > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
       p->fault_unit = (int)value;
       return GEMM_F16_OK;
+    case GEMM_F16_OPT_SM_LIMIT:
+      if (value < 0 || value > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
+      p->sm_limit = (int)value;
+      return GEMM_F16_OK;
     case GEMM_F16_OPT_TILE_WIDTH:
       if (value != 0 && value != 64 && value != 128 && value != 256) return GEMM_F16_ERR_INVALID_ARG;
       p->tile_width = (int)value;
@@ -900,6 +905,7 @@ int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
     case GEMM_F16_OPT_FAULT_UNIT: *value = p->fault_unit; return GEMM_F16_OK;
     case GEMM_F16_OPT_KERNEL: *value = p->kernel; return GEMM_F16_OK;
     case GEMM_F16_OPT_TILE_WIDTH: *value = p->tile_width; return GEMM_F16_OK;
+    case GEMM_F16_OPT_SM_LIMIT: *value = p->sm_limit; return GEMM_F16_OK;
     case GEMM_F16_INFO_NUM_SMS: *value = p->num_sms; return GEMM_F16_OK;
     case GEMM_F16_INFO_MAX_PAIRS: *value = p->max_pairs; return GEMM_F16_OK;
     default: return GEMM_F16_ERR_INVALID_ARG;
@@ -1061,7 +1067,9 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
     pp.status = p->status_dev;
     pp.timeout_ns = p->timeout_ns;
     pp.fault_unit = p->fault_unit;
-    const int64_t npairs = std::min<int64_t>(punits, std::max(p->max_pairs, 1));
+    int64_t pair_cap = std::max(p->max_pairs, 1);
+    if (p->sm_limit > 0) pair_cap = std::max<int64_t>(1, std::min<int64_t>(pair_cap, p->sm_limit / 2));
+    const int64_t npairs = std::min<int64_t>(punits, pair_cap);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * npairs), 1, 1);
     cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
@@ -1089,7 +1097,8 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   prm.timeout_ns = p->timeout_ns;
   prm.fault_unit = p->fault_unit;
 
-  const int grid = (int)std::min<int64_t>(units, p->num_sms);
+  const int sm_cap = p->sm_limit > 0 ? std::min(p->sm_limit, p->num_sms) : p->num_sms;
+  const int grid = (int)std::min<int64_t>(units, sm_cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);

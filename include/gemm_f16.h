@@ -83,7 +83,11 @@ typedef enum gemm_f16_option {
      * more SMs), or 256 / 128 / 64.  Narrower tiles get a deeper ring
      * (4 / 6 / 8 stages in the same shared memory).  Results agree within
      * the usual tolerance. */
-    GEMM_F16_OPT_TILE_WIDTH = 5
+    GEMM_F16_OPT_TILE_WIDTH = 5,
+    /* Most SMs one launch may occupy (0 = all of them), e.g. to leave SMs
+     * to work on other streams.  The tile schedules are planned for the
+     * full device either way. */
+    GEMM_F16_OPT_SM_LIMIT = 6
 } gemm_f16_option;
 
 /*
