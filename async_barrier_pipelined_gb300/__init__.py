@@ -66,7 +66,7 @@ _SIGNATURES = {
     "gemm_f16_tile_order": (_c_i64, [_c_int, _c_int, _c_int,
                                      ctypes.POINTER(ctypes.c_uint32), _c_i64]),
     "gemm_f16_tile_shape": (_c_int, [ctypes.POINTER(_c_int)] * 4),
-    "gemm_f16_pair_tiles": (_c_i64, [_c_int, _c_int, _c_int, _c_int, _c_int,
+    "gemm_f16_pair_tiles": (_c_i64, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                      ctypes.POINTER(ctypes.c_uint32), _c_i64]),
     "gemm_f16_run_noalloc": (_c_int, [_c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
                                       _vp, _c_i64, _c_int, _vp, _vp]),
@@ -189,14 +189,15 @@ def gemm_f16_tile_order(tiles_m: int, tiles_n: int, order: int = 0) -> list:
     return [(v & 0xFFFF, v >> 16) for v in buf]
 
 
-def gemm_f16_pair_tiles(M: int, N: int, pairs: int, split_k: int = 1, order: int = 0) -> list:
+def gemm_f16_pair_tiles(M: int, N: int, pairs: int, split_k: int = 1, order: int = 0,
+                        tile_width: int = 256) -> list:
     """CTA-pair work list as (row0, col0, width) tuples."""
-    n = _check(load().gemm_f16_pair_tiles(M, N, pairs, split_k, order, None, 0),
+    n = _check(load().gemm_f16_pair_tiles(M, N, pairs, split_k, order, tile_width, None, 0),
                "gemm_f16_pair_tiles")
     buf = (ctypes.c_uint32 * n)()
-    _check(load().gemm_f16_pair_tiles(M, N, pairs, split_k, order, buf, n), "gemm_f16_pair_tiles")
-    return [((v & 0xFFFF) * 256, ((v >> 16) & 0x7FFF) * 128, 128 if v >> 31 else 256)
-            for v in buf]
+    _check(load().gemm_f16_pair_tiles(M, N, pairs, split_k, order, tile_width, buf, n),
+           "gemm_f16_pair_tiles")
+    return [((v & 0xFFFF) * 256, ((v >> 16) & 0x3FFF) * 128, 128 << (v >> 30)) for v in buf]
 
 
 def gemm_f16_tile_shape() -> tuple:

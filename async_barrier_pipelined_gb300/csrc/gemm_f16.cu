@@ -614,46 +614,59 @@ struct OrderTable {
   int64_t count;
 };
 
-double pair_makespan(const std::vector<uint32_t>& tiles, int pairs) {
+double pair_makespan(const std::vector<uint32_t>& tiles, int pairs, int tn) {
   std::vector<double> load((size_t)pairs, 0.0);
   for (size_t i = 0; i < tiles.size(); ++i)
-    load[i % (size_t)pairs] += pair::narrow_of(tiles[i]) ? 0.5 : 1.0;
+    load[i % (size_t)pairs] += (double)pair::width_of(tiles[i]) / tn;
   return *std::max_element(load.begin(), load.end());
 }
 
-// Pair-kernel tile list: 256-row x 256-column tiles over the output, a
-// column remainder of at most 128 as 128-wide tiles, wide tiles in Morton
-// order (pair-row on the even bits) followed by the narrow ones.  With one
-// split, if the wide tiles leave a partial last wave, those tiles are cut
-// into two 128-wide halves when that shortens the busiest pair's work.
-void build_pair_tiles(int M, int N, int pairs, int split_k, int order,
+// Pair-kernel tile list for tiles TN (256 or 512) columns wide: full tiles
+// over the output in Morton order (pair-row on the even bits), then the
+// column remainder as tiles of TN/2 or TN/4 (never under 128).  With one
+// split, if the full tiles leave a partial last wave, those tiles are cut
+// into halves or quarters when that shortens the busiest pair's work.
+void build_pair_tiles(int M, int N, int pairs, int split_k, int order, int tn,
                       std::vector<uint32_t>& out) {
   const int tpms = (int)ceil_div(M, pair::PM);
-  const int wide_cols = (N > 128) ? (int)((N - 128 + 255) / 256) : 0;
-  const bool tail = (N - wide_cols * 256) > 0;
+  const int min_w = 128;
+  // full-width column tiles while more than TN/2 columns remain
+  int full_cols = 0;
+  while (N - full_cols * tn > tn / 2) ++full_cols;
   std::vector<uint32_t> grid;
-  build_tile_order(tpms, std::max(wide_cols, 1), order, grid);
-  std::vector<uint32_t> wide, narrow;
-  if (wide_cols > 0)
+  build_tile_order(tpms, std::max(full_cols, 1), order, grid);
+  std::vector<uint32_t> full, rest;
+  if (full_cols > 0)
     for (uint32_t e : grid)
-      wide.push_back(pair::pack(tile_m_of(e), 2 * tile_n_of(e), false));
-  if (tail)
-    for (int t = 0; t < tpms; ++t) narrow.push_back(pair::pack(t, 2 * wide_cols, true));
-  out = wide;
-  out.insert(out.end(), narrow.begin(), narrow.end());
-  if (split_k != 1 || pairs <= 0 || wide.empty()) return;
-  const size_t r = wide.size() % (size_t)pairs;
-  if (r == 0) return;
-  std::vector<uint32_t> alt(wide.begin(), wide.end() - r);
-  for (size_t i = wide.size() - r; i < wide.size(); ++i) {
-    const uint32_t e = wide[i];
-    alt.push_back(pair::pack(pair::tpm_of(e), pair::n128_of(e), true));
-    alt.push_back(pair::pack(pair::tpm_of(e), pair::n128_of(e) + 1, true));
+      full.push_back(pair::pack(tile_m_of(e), tile_n_of(e) * (tn / 128), tn));
+  const int rem = N - full_cols * tn;  // <= tn/2
+  if (rem > 0) {
+    const int w = (rem > tn / 4 || tn / 4 < min_w) ? tn / 2 : tn / 4;
+    for (int t = 0; t < tpms; ++t) rest.push_back(pair::pack(t, full_cols * (tn / 128), w));
   }
-  alt.insert(alt.end(), narrow.begin(), narrow.end());
-  if (pair_makespan(alt, pairs) < pair_makespan(out, pairs)) out.swap(alt);
+  out = full;
+  out.insert(out.end(), rest.begin(), rest.end());
+  if (split_k != 1 || pairs <= 0 || full.empty()) return;
+  const size_t r = full.size() % (size_t)pairs;
+  if (r == 0) return;
+  double best = pair_makespan(out, pairs, tn);
+  for (int parts : {2, 4}) {
+    const int w = tn / parts;
+    if (w < min_w) continue;
+    std::vector<uint32_t> alt(full.begin(), full.end() - r);
+    for (size_t i = full.size() - r; i < full.size(); ++i)
+      for (int k = 0; k < parts; ++k) {
+        const uint32_t n128 = pair::n128_of(full[i]) + k * (w / 128);
+        if ((int64_t)n128 * 128 < N) alt.push_back(pair::pack(pair::tpm_of(full[i]), n128, w));
+      }
+    alt.insert(alt.end(), rest.begin(), rest.end());
+    const double m = pair_makespan(alt, pairs, tn);
+    if (m < best) {
+      best = m;
+      out.swap(alt);
+    }
+  }
 }
-
 }  // namespace
 
 // Recently encoded tensor maps, keyed by everything the encoding depends on,
@@ -784,16 +797,21 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
   GF16_CUDA(cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SMEM_BYTES),
             "cudaFuncSetAttribute(max dynamic smem)");
-  GF16_CUDA(cudaFuncSetAttribute(pair::gemm_f16_pair_kernel,
+  GF16_CUDA(cudaFuncSetAttribute(pair::gemm_f16_pair_kernel<256>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)pair::SMEM_BYTES),
+                                 (int)pair::Cfg<256>::SMEM_BYTES),
             "cudaFuncSetAttribute(pair kernel smem)");
+  GF16_CUDA(cudaFuncSetAttribute(pair::gemm_f16_pair_kernel<512>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)pair::Cfg<512>::SMEM_BYTES),
+            "cudaFuncSetAttribute(pair kernel smem)");
+  // Co-resident clusters of two for each pair-kernel instance; keep the
+  // smaller count (0 if the query fails: the pair kernel is then not used).
   int max_clusters = 0;
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(prop.multiProcessorCount / 2 * 2), 1, 1);
     cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = 2;
@@ -801,11 +819,18 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, pair::gemm_f16_pair_kernel, &cfg) !=
-        cudaSuccess) {
+    int n256 = 0, n512 = 0;
+    cfg.dynamicSmemBytes = pair::Cfg<256>::SMEM_BYTES;
+    if (cudaOccupancyMaxActiveClusters(&n256, pair::gemm_f16_pair_kernel<256>, &cfg) != cudaSuccess) {
       cudaGetLastError();
-      max_clusters = 0;
+      n256 = 0;
     }
+    cfg.dynamicSmemBytes = pair::Cfg<512>::SMEM_BYTES;
+    if (cudaOccupancyMaxActiveClusters(&n512, pair::gemm_f16_pair_kernel<512>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n512 = 0;
+    }
+    max_clusters = std::min(n256, n512);
   }
   gemm_f16_plan_s* p = new (std::nothrow) gemm_f16_plan_s();
   if (!p) return GEMM_F16_ERR_OOM;
@@ -875,8 +900,8 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
       p->tile_width = (int)value;
       return GEMM_F16_OK;
     case GEMM_F16_OPT_KERNEL:
-      if (value < 0 || value > 2) return GEMM_F16_ERR_INVALID_ARG;
-      if (value == 2 && p->max_pairs <= 0) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+      if (value < 0 || value > 3) return GEMM_F16_ERR_INVALID_ARG;
+      if (value >= 2 && p->max_pairs <= 0) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
       p->kernel = (int)value;
       return GEMM_F16_OK;
     default:
@@ -884,14 +909,15 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
   }
 }
 
-int64_t gemm_f16_pair_tiles(int M, int N, int pairs, int split_k, int order, uint32_t* out,
-                            int64_t cap) {
+int64_t gemm_f16_pair_tiles(int M, int N, int pairs, int split_k, int order, int tile_width,
+                            uint32_t* out, int64_t cap) {
   if (M <= 0 || N <= 0 || pairs < 1 || split_k < 1 || (order != 0 && order != 1))
     return GEMM_F16_ERR_INVALID_ARG;
-  if (ceil_div(M, pair::PM) > 65535 || (N + 127) / 128 >= 0x7FFF) return GEMM_F16_ERR_INVALID_ARG;
+  if (tile_width != 256 && tile_width != 512) return GEMM_F16_ERR_INVALID_ARG;
+  if (ceil_div(M, pair::PM) > 65535 || (N + 127) / 128 >= 0x3FFF) return GEMM_F16_ERR_INVALID_ARG;
   if (cap < 0 || (cap > 0 && !out)) return GEMM_F16_ERR_INVALID_ARG;
   std::vector<uint32_t> v;
-  build_pair_tiles(M, N, pairs, split_k, order, v);
+  build_pair_tiles(M, N, pairs, split_k, order, tile_width, v);
   const int64_t n = (int64_t)v.size();
   std::memcpy(out, v.data(), sizeof(uint32_t) * (size_t)std::min<int64_t>(n, cap));
   return n;
@@ -951,16 +977,16 @@ int get_order_table(gemm_f16_plan_s* p, int tiles_m, int tiles_n, const uint32_t
   return upload_table(p, key, host, out);
 }
 
-int get_pair_table(gemm_f16_plan_s* p, int M, int N, int split_k, const uint32_t** out,
+int get_pair_table(gemm_f16_plan_s* p, int M, int N, int split_k, int tn, const uint32_t** out,
                    int64_t* count) {
-  const int64_t key[6] = {1, M, N, p->max_pairs, split_k, p->tile_order};
+  const int64_t key[6] = {tn, M, N, p->max_pairs, split_k, p->tile_order};
   if (const OrderTable* t = find_table(p, key)) {
     *out = t->dev;
     *count = t->count;
     return GEMM_F16_OK;
   }
   std::vector<uint32_t> host;
-  build_pair_tiles(M, N, p->max_pairs, split_k, p->tile_order, host);
+  build_pair_tiles(M, N, p->max_pairs, split_k, p->tile_order, tn, host);
   *count = (int64_t)host.size();
   return upload_table(p, key, host, out);
 }
@@ -1015,13 +1041,14 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   // Automatic choice: the pair kernel once its 256 x 256 tiles (times the
   // splits) fill at least half a wave of pairs; below that the single-CTA
   // kernel's smaller tiles spread the work over more SMs.
-  const bool pair_fits = (N + 127) / 128 < 0x7FFF && p->max_pairs > 0;
+  const bool pair_fits = (N + 127) / 128 < 0x3FFF && p->max_pairs > 0;
   const int64_t pair_work = ceil_div(M, 256) * ceil_div(N, 256) * (int64_t)split_k;
-  const bool use_pair =
-      pair_fits && (p->kernel == 2 || (p->kernel == 0 && M > BM && 2 * pair_work >= p->max_pairs));
+  const bool use_pair = pair_fits && (p->kernel == 2 || p->kernel == 3 ||
+                                      (p->kernel == 0 && M > BM && 2 * pair_work >= p->max_pairs));
+  const int pair_tn = (p->kernel == 3) ? 512 : 256;
   const uint32_t* order = nullptr;
   int64_t pair_tiles = 0;
-  int rc = use_pair ? get_pair_table(p, M, N, split_k, &order, &pair_tiles)
+  int rc = use_pair ? get_pair_table(p, M, N, split_k, pair_tn, &order, &pair_tiles)
                     : get_order_table(p, tiles_m, tiles_n, &order);
   if (rc) return rc;
 
@@ -1073,10 +1100,16 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * npairs), 1, 1);
     cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
     cfg.stream = stream;
-    GF16_CUDA(cudaLaunchKernelEx(&cfg, pair::gemm_f16_pair_kernel, tmA, tmB, tmC, tmW, pp),
-              "launch gemm_f16_pair_kernel");
+    if (pair_tn == 512) {
+      cfg.dynamicSmemBytes = pair::Cfg<512>::SMEM_BYTES;
+      GF16_CUDA(cudaLaunchKernelEx(&cfg, pair::gemm_f16_pair_kernel<512>, tmA, tmB, tmC, tmW, pp),
+                "launch gemm_f16_pair_kernel<512>");
+    } else {
+      cfg.dynamicSmemBytes = pair::Cfg<256>::SMEM_BYTES;
+      GF16_CUDA(cudaLaunchKernelEx(&cfg, pair::gemm_f16_pair_kernel<256>, tmA, tmB, tmC, tmW, pp),
+                "launch gemm_f16_pair_kernel<256>");
+    }
   } else {
   Params prm;
   prm.M = M;

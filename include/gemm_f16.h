@@ -72,11 +72,13 @@ typedef enum gemm_f16_option {
     /* Which kernel runs the product: 0 = automatic (the CTA-pair kernel when
      * M > 128 and ceil(M/256) * ceil(N/256) * split_k is at least half the
      * number of co-resident pairs, else the single-CTA kernel),
-     * 1 = single-CTA kernel (128 x 256
-     * tiles, tcgen05 cta_group::1), 2 = CTA-pair kernel (256-row tiles,
-     * 256 or 128 columns wide, tcgen05 cta_group::2).  Results agree within
-     * the usual tolerance; split results are bitwise reproducible for a
-     * fixed choice. */
+     * 1 = single-CTA kernel (128-row tiles, tcgen05 cta_group::1),
+     * 2 = CTA-pair kernel with 256-row x 256-column tiles (two TMEM
+     * accumulators, epilogue overlapped; 128-wide tiles in the last wave),
+     * 3 = CTA-pair kernel with 256 x 512 tiles (less load traffic per MMA,
+     * one accumulator; 256- and 128-wide tiles in the last wave).  Results
+     * agree within the usual tolerance; split results are bitwise
+     * reproducible for a fixed choice. */
     GEMM_F16_OPT_KERNEL = 4,
     /* Output tile width of the single-CTA kernel: 0 = automatic (a cost
      * model picks 256, 128 or 64 columns so that small problems spread over
@@ -184,14 +186,15 @@ int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order,
                             uint32_t *out, int64_t cap);
 
 /*
- * Host-only: the work list of the CTA-pair kernel for an M x N output with
- * `pairs` co-resident CTA pairs (see GEMM_F16_INFO_MAX_PAIRS).  Each entry
- * is (pair_row | col128 << 16 | narrow << 31): rows 256*pair_row .. +255,
- * columns 128*col128 .. +255 (wide) or .. +127 (narrow).  Writes up to `cap`
- * entries and returns the count, or a negative error code.
+ * Host-only: the work list of the CTA-pair kernel with full tiles
+ * `tile_width` (256 or 512) columns wide, for an M x N output with `pairs`
+ * co-resident CTA pairs (see GEMM_F16_INFO_MAX_PAIRS).  Each entry is
+ * (pair_row | col128 << 16 | log2(width/128) << 30): rows 256*pair_row ..
+ * +255, columns 128*col128 .. +width-1.  Writes up to `cap` entries and
+ * returns the count, or a negative error code.
  */
 int64_t gemm_f16_pair_tiles(int M, int N, int pairs, int split_k, int order,
-                            uint32_t *out, int64_t cap);
+                            int tile_width, uint32_t *out, int64_t cap);
 
 /* Compile-time tile shape of the kernel: BM x BN output tile, BK k-block. */
 int gemm_f16_tile_shape(int *bm, int *bn, int *bk, int *stages);

@@ -156,19 +156,20 @@ def _covered(tiles, M, N):
                                  (129, 300), (256, 129), (300, 384), (1, 1), (2000, 100),
                                  (777, 5000)])
 @pytest.mark.parametrize("pairs", [76, 7, 1])
-def test_pair_tiles_cover_output_exactly_once(lib, M, N, pairs):
+@pytest.mark.parametrize("tw", [256, 512])
+def test_pair_tiles_cover_output_exactly_once(lib, M, N, pairs, tw):
     import numpy as np
-    tiles = g.gemm_f16_pair_tiles(M, N, pairs, 1)
+    tiles = g.gemm_f16_pair_tiles(M, N, pairs, 1, 0, tw)
     cov = _covered(tiles, M, N)
     assert np.all(cov == 1)
     for r0, c0, w in tiles:            # no tile starts outside the output
-        assert r0 < M and c0 < N and w in (128, 256)
+        assert r0 < M and c0 < N and w in ((128, 256) if tw == 256 else (128, 256, 512))
 
 
-def _makespan(tiles, pairs):
+def _makespan(tiles, pairs, tw=256):
     load = [0.0] * pairs
     for i, (_, _, w) in enumerate(tiles):
-        load[i % pairs] += w / 256
+        load[i % pairs] += w / tw
     return max(load)
 
 
@@ -184,9 +185,14 @@ def test_pair_tiles_balance_the_last_wave(lib):
     # splits keep whole tiles (the split units are the parallelism)
     t = g.gemm_f16_pair_tiles(512, 512, 76, 16)
     assert len(t) == 4 and all(w == 256 for *_, w in t)
+    # 512-wide tiles: 128 tiles on 76 pairs; the second wave is cut into
+    # quarters (3 per pair at most), 1.75 instead of 2 tiles' work
+    t = g.gemm_f16_pair_tiles(4096, 4096, 76, 1, 0, 512)
+    assert _makespan(t, 76, 512) == 1.75
 
 
 def test_pair_tiles_reject_bad_arguments(lib):
-    assert lib.gemm_f16_pair_tiles(0, 8, 76, 1, 0, None, 0) == g.ERR_INVALID_ARG
-    assert lib.gemm_f16_pair_tiles(8, 8, 0, 1, 0, None, 0) == g.ERR_INVALID_ARG
-    assert lib.gemm_f16_pair_tiles(8, 8, 76, 0, 0, None, 0) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(0, 8, 76, 1, 0, 256, None, 0) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 0, 1, 0, 256, None, 0) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 76, 0, 0, 256, None, 0) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 76, 1, 0, 384, None, 0) == g.ERR_INVALID_ARG

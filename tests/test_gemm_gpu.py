@@ -18,10 +18,11 @@ from tests import gpu_util, parity
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[1, 2], ids=["cta1", "pair"])
+@pytest.fixture(scope="module", params=[1, 2, 3], ids=["cta1", "pair256", "pair512"])
 def plan(request):
-    """A plan pinned to one kernel: 1 = single-CTA, 2 = CTA pair.  Every
-    test in this file runs once per kernel."""
+    """A plan pinned to one kernel: 1 = single-CTA, 2 = CTA pair with
+    256-wide tiles, 3 = CTA pair with 512-wide tiles.  Every test in this
+    file runs once per kernel."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
@@ -234,7 +235,7 @@ def test_kernels_agree(plan):
     A, B = w.pair_bits(0)
     c0, _ = gpu_util.run(plan, A, B)
     mine = plan.get_option(g.OPT_KERNEL)
-    plan.set_option(g.OPT_KERNEL, 3 - mine)
+    plan.set_option(g.OPT_KERNEL, 2 if mine == 1 else 1)
     try:
         c1, _ = gpu_util.run(plan, A, B)
     finally:
