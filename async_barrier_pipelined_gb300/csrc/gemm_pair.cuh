@@ -130,15 +130,15 @@ __device__ __forceinline__ uint32_t cta_stage_bytes(int width) {
   return A_STAGE + (uint32_t)(width / 2) * BK * 2;
 }
 
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Params& p,
-                                       volatile int* abort_flag) {
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                       int* status, volatile int* abort_flag) {
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (ptx::globaltimer() - t0 > p.timeout_ns) {
+    if (ptx::globaltimer() - t0 > timeout_ns) {
       *abort_flag = 1;
-      *(volatile int*)p.status = (int)GEMM_F16_ERR_TIMEOUT;
+      *(volatile int*)status = (int)GEMM_F16_ERR_TIMEOUT;
       __threadfence_system();
       return false;
     }
@@ -148,7 +148,7 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Para
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
                                            volatile int* abort_flag) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, p, abort_flag);
+  return wait_slow(bar, parity, p.timeout_ns, p.status, abort_flag);
 }
 
 __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -351,21 +351,25 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
 // bytes.  A fill the peer never issued leaves the peer's bytes expected:
 // take them off with complete_tx.
 template <int TN>
-__device__ __noinline__ void leader_drain(const Params& p, const Bars& b, uint32_t pair,
-                                          uint32_t npairs, uint32_t mine, uint32_t peer) {
+__device__ __noinline__ void leader_drain(const uint32_t* order, int num_units, int split_k,
+                                          int kblocks, uint32_t full_bar, uint32_t pair,
+                                          uint32_t npairs, uint32_t mine, uint32_t peer,
+                                          uint64_t limit_ns) {
   using C = Cfg<TN>;
   const uint32_t hi = mine > peer ? mine : peer;
   const uint32_t lo = hi > (uint32_t)C::STAGES ? hi - (uint32_t)C::STAGES : 0u;
   uint32_t fill = 0;
-  for (int u = (int)pair; u < p.num_units && fill < hi; u += (int)npairs) {
-    const UnitGeom g = unit_geom(p, u, 0);
-    const uint32_t bytes = cta_stage_bytes(g.width);
-    for (int kb = g.kb0; kb < g.kb1 && fill < hi; ++kb, ++fill) {
+  for (int u = (int)pair; u < num_units && fill < hi; u += (int)npairs) {
+    int tpos, s, kb0, kb1;
+    decode_unit(u, split_k, &tpos, &s);
+    split_range(kblocks, split_k, s, &kb0, &kb1);
+    const uint32_t bytes = cta_stage_bytes(width_of(order[tpos]));
+    for (int kb = kb0; kb < kb1 && fill < hi; ++kb, ++fill) {
       if (fill < lo) continue;
-      const uint32_t bar = b.full + 8 * (fill % C::STAGES);
+      const uint32_t bar = full_bar + 8 * (fill % C::STAGES);
       if (fill >= mine) ptx::mbar_arrive_expect_tx_relaxed(bar, bytes);
       if (fill >= peer) ptx::mbar_complete_tx(bar, bytes);
-      wait_drain(bar, (fill / C::STAGES) & 1u, p.timeout_ns);
+      wait_drain(bar, (fill / C::STAGES) & 1u, limit_ns);
     }
   }
 }
@@ -446,7 +450,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   ptx::cluster_sync();  // both CTAs have stopped issuing
   if (warp == 0 && lane == 0 && rank == 0) {
     const uint32_t peer = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_PEER_ISSUED);
-    leader_drain<TN>(p, b, pair, npairs, issued, peer);
+    leader_drain<TN>(p.order, p.num_units, p.split_k, p.kblocks, b.full, pair, npairs, issued, peer,
+                     p.timeout_ns);
   }
   ptx::cluster_sync();  // no copy into either CTA is still in flight
   if (warp == 1) {
