@@ -493,6 +493,7 @@ __global__ void __launch_bounds__(256)
 }  // namespace gf16
 
 #include "gemm_pair.cuh"
+#include "gemm_pair_wide.cuh"
 
 // ====================================================================== host
 using namespace gf16;
@@ -617,7 +618,7 @@ struct OrderTable {
 double pair_makespan(const std::vector<uint32_t>& tiles, int pairs, int tn) {
   std::vector<double> load((size_t)pairs, 0.0);
   for (size_t i = 0; i < tiles.size(); ++i)
-    load[i % (size_t)pairs] += (double)pair::width_of(tiles[i]) / tn;
+    load[i % (size_t)pairs] += (double)pairw::width_of(tiles[i]) / tn;
   return *std::max_element(load.begin(), load.end());
 }
 
@@ -628,7 +629,7 @@ double pair_makespan(const std::vector<uint32_t>& tiles, int pairs, int tn) {
 // into halves or quarters when that shortens the busiest pair's work.
 void build_pair_tiles(int M, int N, int pairs, int split_k, int order, int tn,
                       std::vector<uint32_t>& out) {
-  const int tpms = (int)ceil_div(M, pair::PM);
+  const int tpms = (int)ceil_div(M, pairw::PM);
   const int min_w = 128;
   // full-width column tiles while more than TN/2 columns remain
   int full_cols = 0;
@@ -638,11 +639,11 @@ void build_pair_tiles(int M, int N, int pairs, int split_k, int order, int tn,
   std::vector<uint32_t> full, rest;
   if (full_cols > 0)
     for (uint32_t e : grid)
-      full.push_back(pair::pack(tile_m_of(e), tile_n_of(e) * (tn / 128), tn));
+      full.push_back(pairw::pack(tile_m_of(e), tile_n_of(e) * (tn / 128), tn));
   const int rem = N - full_cols * tn;  // <= tn/2
   if (rem > 0) {
     const int w = (rem > tn / 4 || tn / 4 < min_w) ? tn / 2 : tn / 4;
-    for (int t = 0; t < tpms; ++t) rest.push_back(pair::pack(t, full_cols * (tn / 128), w));
+    for (int t = 0; t < tpms; ++t) rest.push_back(pairw::pack(t, full_cols * (tn / 128), w));
   }
   out = full;
   out.insert(out.end(), rest.begin(), rest.end());
@@ -656,8 +657,8 @@ void build_pair_tiles(int M, int N, int pairs, int split_k, int order, int tn,
     std::vector<uint32_t> alt(full.begin(), full.end() - r);
     for (size_t i = full.size() - r; i < full.size(); ++i)
       for (int k = 0; k < parts; ++k) {
-        const uint32_t n128 = pair::n128_of(full[i]) + k * (w / 128);
-        if ((int64_t)n128 * 128 < N) alt.push_back(pair::pack(pair::tpm_of(full[i]), n128, w));
+        const uint32_t n128 = pairw::n128_of(full[i]) + k * (w / 128);
+        if ((int64_t)n128 * 128 < N) alt.push_back(pairw::pack(pairw::tpm_of(full[i]), n128, w));
       }
     alt.insert(alt.end(), rest.begin(), rest.end());
     const double m = pair_makespan(alt, pairs, tn);
@@ -797,14 +798,14 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
   GF16_CUDA(cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SMEM_BYTES),
             "cudaFuncSetAttribute(max dynamic smem)");
-  GF16_CUDA(cudaFuncSetAttribute(pair::gemm_f16_pair_kernel<256>,
+  GF16_CUDA(cudaFuncSetAttribute(pair::gemm_f16_pair_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)pair::Cfg<256>::SMEM_BYTES),
+                                 (int)pair::SMEM_BYTES),
             "cudaFuncSetAttribute(pair kernel smem)");
-  GF16_CUDA(cudaFuncSetAttribute(pair::gemm_f16_pair_kernel<512>,
+  GF16_CUDA(cudaFuncSetAttribute(pairw::gemm_f16_pair_kernel<512>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)pair::Cfg<512>::SMEM_BYTES),
-            "cudaFuncSetAttribute(pair kernel smem)");
+                                 (int)pairw::Cfg<512>::SMEM_BYTES),
+            "cudaFuncSetAttribute(wide pair kernel smem)");
   // Co-resident clusters of two for each pair-kernel instance; keep the
   // smaller count (0 if the query fails: the pair kernel is then not used).
   int max_clusters = 0;
@@ -820,13 +821,13 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n256 = 0, n512 = 0;
-    cfg.dynamicSmemBytes = pair::Cfg<256>::SMEM_BYTES;
-    if (cudaOccupancyMaxActiveClusters(&n256, pair::gemm_f16_pair_kernel<256>, &cfg) != cudaSuccess) {
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    if (cudaOccupancyMaxActiveClusters(&n256, pair::gemm_f16_pair_kernel, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n256 = 0;
     }
-    cfg.dynamicSmemBytes = pair::Cfg<512>::SMEM_BYTES;
-    if (cudaOccupancyMaxActiveClusters(&n512, pair::gemm_f16_pair_kernel<512>, &cfg) != cudaSuccess) {
+    cfg.dynamicSmemBytes = pairw::Cfg<512>::SMEM_BYTES;
+    if (cudaOccupancyMaxActiveClusters(&n512, pairw::gemm_f16_pair_kernel<512>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n512 = 0;
     }
@@ -914,7 +915,7 @@ int64_t gemm_f16_pair_tiles(int M, int N, int pairs, int split_k, int order, int
   if (M <= 0 || N <= 0 || pairs < 1 || split_k < 1 || (order != 0 && order != 1))
     return GEMM_F16_ERR_INVALID_ARG;
   if (tile_width != 256 && tile_width != 512) return GEMM_F16_ERR_INVALID_ARG;
-  if (ceil_div(M, pair::PM) > 65535 || (N + 127) / 128 >= 0x3FFF) return GEMM_F16_ERR_INVALID_ARG;
+  if (ceil_div(M, pairw::PM) > 65535 || (N + 127) / 128 >= 0x3FFF) return GEMM_F16_ERR_INVALID_ARG;
   if (cap < 0 || (cap > 0 && !out)) return GEMM_F16_ERR_INVALID_ARG;
   std::vector<uint32_t> v;
   build_pair_tiles(M, N, pairs, split_k, order, tile_width, v);
@@ -987,6 +988,9 @@ int get_pair_table(gemm_f16_plan_s* p, int M, int N, int split_k, int tn, const 
   }
   std::vector<uint32_t> host;
   build_pair_tiles(M, N, p->max_pairs, split_k, p->tile_order, tn, host);
+  if (tn == 256)  // the 256-wide kernel's entry format: narrow flag in bit 31
+    for (uint32_t& e : host)
+      e = pair::pack(pairw::tpm_of(e), pairw::n128_of(e), pairw::width_of(e) == 128);
   *count = (int64_t)host.size();
   return upload_table(p, key, host, out);
 }
@@ -1045,6 +1049,9 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   const int64_t pair_work = ceil_div(M, 256) * ceil_div(N, 256) * (int64_t)split_k;
   const bool use_pair = pair_fits && (p->kernel == 2 || p->kernel == 3 ||
                                       (p->kernel == 0 && M > BM && 2 * pair_work >= p->max_pairs));
+  // 512-wide tiles (less load traffic per MMA, but one accumulator and so
+  // no epilogue overlap) only on request: measured slower than 256-wide
+  // tiles from 2048^3 to 8192^3.
   const int pair_tn = (p->kernel == 3) ? 512 : 256;
   const uint32_t* order = nullptr;
   int64_t pair_tiles = 0;
@@ -1102,13 +1109,26 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
     cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
     cfg.stream = stream;
     if (pair_tn == 512) {
-      cfg.dynamicSmemBytes = pair::Cfg<512>::SMEM_BYTES;
-      GF16_CUDA(cudaLaunchKernelEx(&cfg, pair::gemm_f16_pair_kernel<512>, tmA, tmB, tmC, tmW, pp),
-                "launch gemm_f16_pair_kernel<512>");
+      pairw::Params pw;
+      pw.M = pp.M;
+      pw.N = pp.N;
+      pw.K = pp.K;
+      pw.split_k = pp.split_k;
+      pw.kblocks = pp.kblocks;
+      pw.num_units = pp.num_units;
+      pw.order = pp.order;
+      pw.C = pp.C;
+      pw.ldc = pp.ldc;
+      pw.status = pp.status;
+      pw.timeout_ns = pp.timeout_ns;
+      pw.fault_unit = pp.fault_unit;
+      cfg.dynamicSmemBytes = pairw::Cfg<512>::SMEM_BYTES;
+      GF16_CUDA(cudaLaunchKernelEx(&cfg, pairw::gemm_f16_pair_kernel<512>, tmA, tmB, tmC, tmW, pw),
+                "launch wide gemm_f16_pair_kernel<512>");
     } else {
-      cfg.dynamicSmemBytes = pair::Cfg<256>::SMEM_BYTES;
-      GF16_CUDA(cudaLaunchKernelEx(&cfg, pair::gemm_f16_pair_kernel<256>, tmA, tmB, tmC, tmW, pp),
-                "launch gemm_f16_pair_kernel<256>");
+      cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+      GF16_CUDA(cudaLaunchKernelEx(&cfg, pair::gemm_f16_pair_kernel, tmA, tmB, tmC, tmW, pp),
+                "launch gemm_f16_pair_kernel");
     }
   } else {
   Params prm;

@@ -50,7 +50,7 @@ METRIC = "FP16 GEMM TFLOPS at M=N=K=4096 on 1 GB300; % of dense FP16 tensor peak
 FALLBACK_TENSOR_TFLOPS = 1900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "async_barrier_pipelined_gb300", "csrc", f)
-                  for f in ("gemm_f16.cu", "gemm_pair.cuh", "ptx.cuh", "schedule.h")]
+                  for f in ("gemm_f16.cu", "gemm_pair.cuh", "gemm_pair_wide.cuh", "ptx.cuh", "schedule.h")]
 
 
 def parse_args():
@@ -64,8 +64,8 @@ def parse_args():
                     help="idle seconds before the warm-up (page protocol: 5)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2],
-                    help="0 automatic, 1 single-CTA kernel, 2 CTA-pair kernel")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="0 automatic, 1 single-CTA kernel, 2 CTA pair 256x256, 3 CTA pair 256x512")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU seconds for the oracle baseline sample")
     return ap.parse_args()
@@ -407,9 +407,12 @@ def run_ours(args):
     pair_work = -(-w.M // 256) * -(-w.N // 256) * w.split_k
     use_pair = plan_pairs > 0 and (args.kernel == 2 or (
         args.kernel == 0 and w.M > 128 and 2 * pair_work >= plan_pairs))
-    kernel_desc = ("CTA pair (tcgen05 cta_group::2, 256-row tiles)" if use_pair
-                   else "single CTA (tcgen05 cta_group::1, 128x256 tiles)")
-    roofline["kernel"] = ("gf16::pair::gemm_f16_pair_kernel" if use_pair
+    use_wide = use_pair and args.kernel == 3
+    kernel_desc = ("CTA pair (tcgen05 cta_group::2, 256x512 tiles)" if use_wide else
+                   "CTA pair (tcgen05 cta_group::2, 256x256 tiles)" if use_pair
+                   else "single CTA (tcgen05 cta_group::1, 128-row tiles)")
+    roofline["kernel"] = ("gf16::pairw::gemm_f16_pair_kernel<512>" if use_wide else
+                          "gf16::pair::gemm_f16_pair_kernel" if use_pair
                           else "gf16::gemm_f16_kernel")
     plan.close()
     if rank == 0:
