@@ -693,8 +693,14 @@ struct gemm_f16_plan_s {
   void* ws = nullptr;
   size_t ws_bytes = 0;
   std::vector<OrderTable> orders;
-  void* hbuf[3] = {nullptr, nullptr, nullptr};  // device staging for run_host
-  size_t hcap[3] = {0, 0, 0};
+  // run_host: two slots of device staging (A, B, C) used by alternate calls,
+  // a stream for the input copies and the events that order the slots.
+  void* hbuf[2][3] = {{nullptr, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
+  size_t hcap[2][3] = {{0, 0, 0}, {0, 0, 0}};
+  cudaStream_t in_stream = nullptr;
+  cudaEvent_t in_done[2] = {nullptr, nullptr};
+  cudaEvent_t gemm_done[2] = {nullptr, nullptr};
+  int host_slot = 0;
   TmapEntry tmaps[TMAP_CACHE];
   int tmap_used = 0, tmap_next = 0;
 };
@@ -861,8 +867,14 @@ int gemm_f16_destroy(gemm_f16_plan_t p) {
     cudaDeviceSynchronize();
     for (auto& t : p->orders) cudaFree(t.dev);
     if (p->ws) cudaFree(p->ws);
-    for (int i = 0; i < 3; ++i)
-      if (p->hbuf[i]) cudaFree(p->hbuf[i]);
+    for (int sl = 0; sl < 2; ++sl)
+      for (int i = 0; i < 3; ++i)
+        if (p->hbuf[sl][i]) cudaFree(p->hbuf[sl][i]);
+    for (int sl = 0; sl < 2; ++sl) {
+      if (p->in_done[sl]) cudaEventDestroy(p->in_done[sl]);
+      if (p->gemm_done[sl]) cudaEventDestroy(p->gemm_done[sl]);
+    }
+    if (p->in_stream) cudaStreamDestroy(p->in_stream);
     if (p->status_host) cudaFreeHost(p->status_host);
   }
   delete p;
@@ -1206,21 +1218,47 @@ int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, in
   if (rc) return rc;
   cudaStream_t stream = (cudaStream_t)stream_;
   DeviceGuard g(p->device);
-  const size_t bytes[3] = {(size_t)M * dlda * 2, (size_t)K * dldb * 2, (size_t)M * dldc * 2};
-  for (int i = 0; i < 3; ++i) {
-    rc = ensure_buffer(&p->hbuf[i], &p->hcap[i], bytes[i], stream, "host-run staging allocation");
-    if (rc) return rc;
+  if (!p->in_stream) {
+    GF16_CUDA(cudaStreamCreateWithFlags(&p->in_stream, cudaStreamNonBlocking),
+              "create input-copy stream");
+    for (int sl = 0; sl < 2; ++sl) {
+      GF16_CUDA(cudaEventCreateWithFlags(&p->in_done[sl], cudaEventDisableTiming), "create event");
+      GF16_CUDA(cudaEventCreateWithFlags(&p->gemm_done[sl], cudaEventDisableTiming), "create event");
+    }
   }
-  GF16_CUDA(copy_rows(p->hbuf[0], dlda * 2, hA, lda * 2, (int64_t)K * 2, M,
-                      cudaMemcpyHostToDevice, stream),
+  const int slot = p->host_slot;
+  p->host_slot ^= 1;
+  void** buf = p->hbuf[slot];
+  const size_t bytes[3] = {(size_t)M * dlda * 2, (size_t)K * dldb * 2, (size_t)M * dldc * 2};
+  if (p->hcap[slot][0] < bytes[0] || p->hcap[slot][1] < bytes[1] || p->hcap[slot][2] < bytes[2]) {
+    // Growing a slot: let everything that may still use it finish first.
+    GF16_CUDA(cudaDeviceSynchronize(), "synchronise before growing run_host staging");
+    for (int i = 0; i < 3; ++i) {
+      if (p->hcap[slot][i] >= bytes[i]) continue;
+      if (buf[i]) cudaFree(buf[i]);
+      buf[i] = nullptr;
+      p->hcap[slot][i] = 0;
+      GF16_CUDA(cudaMalloc(&buf[i], bytes[i]), "run_host staging allocation");
+      p->hcap[slot][i] = bytes[i];
+    }
+  }
+  // Input copies on the plan's own stream, once the product that last read
+  // this slot (two calls ago) has finished; the product on `stream` waits
+  // for them; the result copy follows the product on `stream`.
+  GF16_CUDA(cudaStreamWaitEvent(p->in_stream, p->gemm_done[slot], 0), "order input copies");
+  GF16_CUDA(copy_rows(buf[0], dlda * 2, hA, lda * 2, (int64_t)K * 2, M, cudaMemcpyHostToDevice,
+                      p->in_stream),
             "copy A to device");
-  GF16_CUDA(copy_rows(p->hbuf[1], dldb * 2, hB, ldb * 2, (int64_t)N * 2, K,
-                      cudaMemcpyHostToDevice, stream),
+  GF16_CUDA(copy_rows(buf[1], dldb * 2, hB, ldb * 2, (int64_t)N * 2, K, cudaMemcpyHostToDevice,
+                      p->in_stream),
             "copy B to device");
-  rc = run_device(p, M, N, K, p->hbuf[0], dlda, p->hbuf[1], dldb, p->hbuf[2], dldc, split_k, stream);
+  GF16_CUDA(cudaEventRecord(p->in_done[slot], p->in_stream), "record input copies");
+  GF16_CUDA(cudaStreamWaitEvent(stream, p->in_done[slot], 0), "order product after inputs");
+  rc = run_device(p, M, N, K, buf[0], dlda, buf[1], dldb, buf[2], dldc, split_k, stream);
   if (rc) return rc;
-  GF16_CUDA(copy_rows(hC, ldc * 2, p->hbuf[2], dldc * 2, (int64_t)N * 2, M,
-                      cudaMemcpyDeviceToHost, stream),
+  GF16_CUDA(cudaEventRecord(p->gemm_done[slot], stream), "record product");
+  GF16_CUDA(copy_rows(hC, ldc * 2, buf[2], dldc * 2, (int64_t)N * 2, M, cudaMemcpyDeviceToHost,
+                      stream),
             "copy C to host");
   return GEMM_F16_OK;
 }

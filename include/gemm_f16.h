@@ -127,11 +127,16 @@ int gemm_f16_run(gemm_f16_plan_t plan, int M, int N, int K,
 
 /*
  * Same product with HOST operands: copies hA and hB into plan-owned device
- * buffers, runs gemm_f16_run on them and copies the result into hC, all
- * enqueued on `stream`.  Pinned host memory gives asynchronous copies; the
- * caller must synchronise `stream` before reading hC.  Host buffers need no
- * alignment; lda/ldb/ldc >= K/N/N (any value).  The device buffers grow on
- * demand and stay with the plan.
+ * buffers, runs gemm_f16_run on them and copies the result into hC.
+ * Consecutive calls overlap: the input copies run on a plan-internal stream
+ * into one of two alternating device slots, so the next call's input copies
+ * proceed while this call's product and result copy (both on `stream`)
+ * run.  Hence hA and hB must be ready on the host when the call is made
+ * (work enqueued earlier on `stream` is not waited for before they are
+ * read); synchronise `stream` before reading hC or reusing hA / hB.
+ * Pinned host memory gives asynchronous copies.  Host buffers need no
+ * alignment; lda/ldb/ldc >= K/N/N (any value).  The device slots grow on
+ * demand (growing synchronises the device) and stay with the plan.
  */
 int gemm_f16_run_host(gemm_f16_plan_t plan, int M, int N, int K,
                       const void *hA, int64_t lda, const void *hB, int64_t ldb,

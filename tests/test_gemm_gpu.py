@@ -260,3 +260,28 @@ def test_single_cta_tile_widths(plan, width, shape, split):
         plan.set_option(g.OPT_TILE_WIDTH, 0)
     parity.check(c, oracle.gemm_f16(A, B), f"width {width}")
     gpu_util.assert_untouched_outside(full, M, N)
+
+
+def test_run_host_back_to_back_calls(plan):
+    """Consecutive run_host calls overlap (input copies of call i+1 during the
+    product of call i, two alternating device slots): every result must still
+    be its own product, including when a slot grows mid-sequence."""
+    import torch
+    import async_barrier_pipelined_gb300 as g
+    shapes = [(300, 260, 200), (300, 260, 200), (520, 300, 330), (300, 260, 200),
+              (129, 64, 1000), (520, 300, 330)]
+    s = torch.cuda.current_stream()
+    jobs = []
+    for t, (M, N, K) in enumerate(shapes):
+        w = si.custom(M, N, K, seed=100 + t)
+        A, B = w.pair_bits(0)
+        hA = torch.from_numpy(A.view(np.float16)).pin_memory()
+        hB = torch.from_numpy(B.view(np.float16)).pin_memory()
+        hC = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+        g.gemm_f16_run_host(plan.handle, M, N, K, hA.data_ptr(), K, hB.data_ptr(), N,
+                            hC.data_ptr(), N, 1, int(s.cuda_stream))
+        jobs.append((A, B, hA, hB, hC))
+    s.synchronize()
+    assert plan.status() == 0
+    for A, B, _, _, hC in jobs:
+        parity.check(hC.numpy().astype(np.float64), oracle.gemm_f16(A, B), "run_host chain")
