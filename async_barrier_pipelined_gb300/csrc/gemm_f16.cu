@@ -363,7 +363,9 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
     if (lane == 0) ptx::mbar_arrive(b.tempty + 8 * acc);
     ++local;
   }
-  if (lane == 0) ptx::bulk_wait_group<0>();
+  // Only the shared-memory reads of the stores must end before the CTA
+  // exits; their writes are complete when the grid is.
+  if (lane == 0) ptx::bulk_wait_group_read<0>();
   __syncwarp();
 }
 
@@ -415,6 +417,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // A dependent launch (the split reduction) may be scheduled now; it waits
   // for this grid's completion before touching the partials.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Launched as a programmatic dependent: everything above (barriers, TMEM,
+  // tensor-map prefetch) may overlap the previous kernel's tail; no global
+  // memory is touched before that kernel has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   RingPos prod_pos{0, 0};
   uint32_t prod_issued = 0;
@@ -1120,6 +1126,11 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
     cfg.gridDim = dim3((unsigned)(2 * npairs), 1, 1);
     cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
     cfg.stream = stream;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
     if (pair_tn == 512) {
       pairw::Params pw;
       pw.M = pp.M;
@@ -1169,6 +1180,11 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
   GF16_CUDA(cudaLaunchKernelEx(&cfg, gemm_f16_kernel, tmA, tmB, tmC, tmW, prm),
             "launch gemm_f16_kernel");
   }

@@ -341,7 +341,9 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
     if (lane == 0) ptx::mbar_arrive_cluster(leader_tempty + 8 * acc);
     ++local;
   }
-  if (lane == 0) ptx::bulk_wait_group<0>();
+  // Only the shared-memory reads of the stores must end before the CTA
+  // exits; their writes are complete when the grid is.
+  if (lane == 0) ptx::bulk_wait_group_read<0>();
   __syncwarp();
 }
 
@@ -431,6 +433,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   // A dependent launch (the split reduction) may be scheduled now; it waits
   // for this grid's completion before touching the partials.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Launched as a programmatic dependent: everything above (barriers, TMEM,
+  // tensor-map prefetch) may overlap the previous kernel's tail; no global
+  // memory is touched before that kernel has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   uint32_t issued = 0;
   if (warp == 0) {
