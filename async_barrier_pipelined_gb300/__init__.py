@@ -26,6 +26,8 @@ __all__ = [
     "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT", "ERR_SCRATCH_TOO_SMALL", "gemm_f16_run_noalloc",
     "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "INFO_NUM_SMS", "INFO_MAX_PAIRS",
     "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
+    "gemm_f16_run_ex", "gemm_f16_validate_ex",
+    "LAYOUT_NN", "LAYOUT_TN", "LAYOUT_NT", "LAYOUT_TT",
 ]
 
 OK = 0
@@ -46,6 +48,11 @@ OPT_SM_LIMIT = 6
 INFO_NUM_SMS = 100
 INFO_MAX_PAIRS = 101
 
+LAYOUT_NN = 0
+LAYOUT_TN = 1   # A stored K x M
+LAYOUT_NT = 2   # B stored N x K
+LAYOUT_TT = 3
+
 _c_int, _c_i64, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
 
 #: name -> (restype, argtypes) for every entry point of include/gemm_f16.h
@@ -53,6 +60,8 @@ _SIGNATURES = {
     "gemm_f16_plan": (_c_int, [ctypes.POINTER(_vp), _c_int]),
     "gemm_f16_run": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
                               _vp, _c_i64, _c_int, _vp]),
+    "gemm_f16_run_ex": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _c_i64, _vp,
+                                 _c_i64, _vp, _c_i64, _c_int, _vp]),
     "gemm_f16_run_host": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
                                    _vp, _c_i64, _c_int, _vp]),
     "gemm_f16_destroy": (_c_int, [_vp]),
@@ -63,6 +72,8 @@ _SIGNATURES = {
     "gemm_f16_last_cuda_error": (ctypes.c_char_p, []),
     "gemm_f16_validate": (_c_int, [_c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
                                    _vp, _c_i64, _c_int]),
+    "gemm_f16_validate_ex": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _c_i64, _vp,
+                                      _c_i64, _vp, _c_i64, _c_int]),
     "gemm_f16_tile_order": (_c_i64, [_c_int, _c_int, _c_int,
                                      ctypes.POINTER(ctypes.c_uint32), _c_i64]),
     "gemm_f16_tile_shape": (_c_int, [ctypes.POINTER(_c_int)] * 4),
@@ -154,6 +165,13 @@ def gemm_f16_run(plan: int, M: int, N: int, K: int, A: int, lda: int, B: int, ld
            "gemm_f16_run")
 
 
+def gemm_f16_run_ex(plan: int, layout: int, M: int, N: int, K: int, A: int, lda: int, B: int,
+                    ldb: int, C: int, ldc: int, split_k: int = 1, stream: int = 0) -> None:
+    """gemm_f16_run with an operand layout (LAYOUT_NN / TN / NT / TT)."""
+    _check(load().gemm_f16_run_ex(plan, layout, M, N, K, A, lda, B, ldb, C, ldc, split_k,
+                                  stream), "gemm_f16_run_ex")
+
+
 def gemm_f16_run_host(plan: int, M: int, N: int, K: int, hA: int, lda: int, hB: int,
                       ldb: int, hC: int, ldc: int, split_k: int = 1, stream: int = 0) -> None:
     """Enqueue copy-in, C = A*B and copy-out for HOST pointers on ``stream``."""
@@ -178,6 +196,10 @@ def gemm_f16_run_noalloc(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: 
 
 def gemm_f16_validate(M, N, K, A, lda, B, ldb, C, ldc, split_k) -> int:
     return load().gemm_f16_validate(M, N, K, A, lda, B, ldb, C, ldc, split_k)
+
+
+def gemm_f16_validate_ex(layout, M, N, K, A, lda, B, ldb, C, ldc, split_k) -> int:
+    return load().gemm_f16_validate_ex(layout, M, N, K, A, lda, B, ldb, C, ldc, split_k)
 
 
 def gemm_f16_tile_order(tiles_m: int, tiles_n: int, order: int = 0) -> list:
@@ -248,21 +270,36 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _operand(X, rows: int, cols: int, name: str):
+    """(transposed, leading dimension) of a rows x cols view, or raise."""
+    if X.stride(1) == 1 and (rows == 1 or X.stride(0) >= cols):
+        return False, X.stride(0) if rows > 1 else cols
+    if X.stride(0) == 1 and (cols == 1 or X.stride(1) >= rows):
+        return True, X.stride(1) if cols > 1 else rows
+    raise ValueError(f"{name} must be row-major or a transposed row-major view")
+
+
 def matmul(plan: Plan, A, B, C=None, split_k: int = 1, stream=None):
-    """C = A @ B for row-major float16 CUDA tensors (C allocated if None)."""
+    """C = A @ B for float16 CUDA tensors (C allocated if None).
+
+    A and B may each be row-major or the transpose of a row-major tensor
+    (``X.t()``); the matching operand layout is passed to the kernel, so no
+    copy is made.  C must be row-major.
+    """
     import torch
     if A.dtype != torch.float16 or B.dtype != torch.float16:
         raise TypeError("A and B must be torch.float16")
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)}")
-    if A.stride(1) != 1 or B.stride(1) != 1:
-        raise ValueError("A and B must be row-major (unit column stride)")
     M, K = A.shape
     N = B.shape[1]
+    at, lda = _operand(A, M, K, "A")
+    bt, ldb = _operand(B, K, N, "B")
     if C is None:
         C = torch.empty((M, N), dtype=torch.float16, device=A.device)
     elif C.dtype != torch.float16 or tuple(C.shape) != (M, N) or C.stride(1) != 1:
         raise ValueError("C must be a row-major float16 M x N tensor")
-    gemm_f16_run(plan.handle, M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
-                 C.data_ptr(), C.stride(0), split_k, _stream_handle(stream))
+    layout = (LAYOUT_TN if at else 0) | (LAYOUT_NT if bt else 0)
+    gemm_f16_run_ex(plan.handle, layout, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
+                    C.data_ptr(), C.stride(0) if M > 1 else N, split_k, _stream_handle(stream))
     return C

@@ -105,6 +105,16 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// Operand layouts (the `layout` of gemm_f16_run_ex): bit 0 = A is stored
+// K x M (M contiguous), bit 1 = B is stored N x K (K contiguous).  Row-major
+// A is K-major for the MMA and row-major B is MN-major; a stored-transposed
+// operand flips that.  Instruction-descriptor bits 15 / 16: A / B MN-major.
+constexpr int LAYOUT_AT = 1, LAYOUT_BT = 2;
+__host__ __device__ constexpr uint32_t idesc_for_layout(uint32_t idesc, int layout) {
+  return (idesc & ~((1u << 15) | (1u << 16))) | ((layout & LAYOUT_AT) ? (1u << 15) : 0u) |
+         ((layout & LAYOUT_BT) ? 0u : (1u << 16));
+}
+
 // Shared-memory matrix descriptor (tcgen05): start address >> 4 (bits 0-13),
 // leading byte offset >> 4 (16-29), stride byte offset >> 4 (32-45), fixed
 // 0b001 at bits 46-48, base offset 0, swizzle mode 2 = 128-byte (bits 61-63).
@@ -120,6 +130,21 @@ constexpr uint32_t A_LBO = 16, A_SBO = 1024, A_KSTEP = UMMA_K * 2;
 // (LBO, one TMA box each), 8-row groups of K 1024 B apart (SBO).  Slice k
 // covers rows 16k .. 16k+15, i.e. 2048 bytes further.
 constexpr uint32_t B_LBO = B_BOX, B_SBO = 1024, B_KSTEP = UMMA_K * 128;
+// Stored-transposed operands: an M-contiguous A tile is MN-major like
+// row-major B (two 64-row copies 8 KB apart, 8-row groups of K 1 KB apart,
+// 2048 bytes per K slice); an N x K (K-contiguous) B tile is K-major like
+// row-major A (rows 128 B, 8-row groups 1 KB apart, 32 bytes per K slice).
+constexpr uint32_t AT_LBO = 8192, AT_SBO = 1024, AT_KSTEP = UMMA_K * 128;
+constexpr uint32_t BT_LBO = 16, BT_SBO = 1024, BT_KSTEP = UMMA_K * 2;
+template <int LAYOUT>
+struct OperandDesc {
+  static constexpr uint32_t a_lbo = (LAYOUT & LAYOUT_AT) ? AT_LBO : A_LBO;
+  static constexpr uint32_t a_sbo = (LAYOUT & LAYOUT_AT) ? AT_SBO : A_SBO;
+  static constexpr uint32_t a_kstep = (LAYOUT & LAYOUT_AT) ? AT_KSTEP : A_KSTEP;
+  static constexpr uint32_t b_lbo = (LAYOUT & LAYOUT_BT) ? BT_LBO : B_LBO;
+  static constexpr uint32_t b_sbo = (LAYOUT & LAYOUT_BT) ? BT_SBO : B_SBO;
+  static constexpr uint32_t b_kstep = (LAYOUT & LAYOUT_BT) ? BT_KSTEP : B_KSTEP;
+};
 
 struct Params {
   int M, N, K;
@@ -174,6 +199,7 @@ __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t 
 // ------------------------------------------------------------------ roles
 // Returns, through pos_out / issued_out, where the ring stands when the role
 // stops, so that an aborted CTA can drain its copies in flight.
+template <int LAYOUT>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                               const Params& p, uint32_t base, const Bars& b,
                                               volatile int* abort_flag, RingPos* pos_out,
@@ -202,9 +228,18 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUte
         const uint32_t sa = base + pos.stage * p.stage_bytes;
         const uint32_t sb = sa + A_STAGE;
         const int k0 = kb * BK;
-        ptx::tma_load_2d(sa, tmA, fb, k0, m0);
-        for (int j = 0; j < boxes; ++j)
-          ptx::tma_load_2d(sb + j * B_BOX, tmB, fb, n0 + j * (int)B_BOX_N, k0);
+        if constexpr ((LAYOUT & LAYOUT_AT) != 0) {
+          ptx::tma_load_2d(sa, tmA, fb, m0, k0);            // 64 rows of M x 64 of K
+          ptx::tma_load_2d(sa + 8192, tmA, fb, m0 + 64, k0);
+        } else {
+          ptx::tma_load_2d(sa, tmA, fb, k0, m0);
+        }
+        if constexpr ((LAYOUT & LAYOUT_BT) != 0) {
+          ptx::tma_load_2d(sb, tmB, fb, k0, n0);            // bn rows of N x 64 of K
+        } else {
+          for (int j = 0; j < boxes; ++j)
+            ptx::tma_load_2d(sb + j * B_BOX, tmB, fb, n0 + j * (int)B_BOX_N, k0);
+        }
       }
       ++issued;
       ring_advance(pos, (uint32_t)p.stages);
@@ -227,11 +262,13 @@ __device__ __noinline__ void producer_drain(const Bars& b, RingPos pos, uint32_t
   }
 }
 
+template <int LAYOUT>
 __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_t tmem_base,
                                          const Bars& b, volatile int* abort_flag) {
+  using D = OperandDesc<LAYOUT>;
   RingPos pos{0, 0};
   uint32_t local = 0;
-  const uint32_t idesc = make_idesc(BM, p.bn);
+  const uint32_t idesc = idesc_for_layout(make_idesc(BM, p.bn), LAYOUT);
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     int tpos, s, kb0, kb1;
     decode_unit(u, p.split_k, &tpos, &s);
@@ -249,13 +286,13 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
       }
       ptx::tc_fence_after();
       const uint32_t sa = base + pos.stage * p.stage_bytes;
-      const uint64_t a_desc = smem_desc_sw128(sa, A_LBO, A_SBO);
-      const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE, B_LBO, B_SBO);
+      const uint64_t a_desc = smem_desc_sw128(sa, D::a_lbo, D::a_sbo);
+      const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE, D::b_lbo, D::b_sbo);
       const uint32_t first = (kb == kb0) ? 1u : 0u;
 #pragma unroll
       for (int k = 0; k < BK / UMMA_K; ++k) {
-        ptx::mma_f16(d_tmem, a_desc + ((k * A_KSTEP) >> 4), b_desc + ((k * B_KSTEP) >> 4), idesc,
-                     (first && k == 0) ? 0u : 1u);
+        ptx::mma_f16(d_tmem, a_desc + ((k * D::a_kstep) >> 4), b_desc + ((k * D::b_kstep) >> 4),
+                     idesc, (first && k == 0) ? 0u : 1u);
       }
       ptx::mma_commit(b.empty + 8 * pos.stage);
       ring_advance(pos, (uint32_t)p.stages);
@@ -370,6 +407,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
 }
 
 // ------------------------------------------------------------------ kernels
+template <int LAYOUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
@@ -425,10 +463,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   RingPos prod_pos{0, 0};
   uint32_t prod_issued = 0;
   if (warp == 0) {
-    if (lane == 0) producer_role(&tmA, &tmB, p, base, b, abort_flag, &prod_pos, &prod_issued);
+    if (lane == 0)
+      producer_role<LAYOUT>(&tmA, &tmB, p, base, b, abort_flag, &prod_pos, &prod_issued);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) mma_role(p, base, tmem_base, b, abort_flag);
+    if (lane == 0) mma_role<LAYOUT>(p, base, tmem_base, b, abort_flag);
     __syncwarp();
   } else {
     epilogue_role(&tmC, &tmW, p, base, tmem_base, b, warp, lane, abort_flag);
@@ -774,16 +813,24 @@ int gemm_f16_tile_shape(int* bm, int* bn, int* bk, int* stages) {
   return GEMM_F16_OK;
 }
 
-int gemm_f16_validate(int M, int N, int K, const void* A, int64_t lda, const void* B, int64_t ldb,
-                      const void* C, int64_t ldc, int split_k) {
+int gemm_f16_validate_ex(int layout, int M, int N, int K, const void* A, int64_t lda,
+                         const void* B, int64_t ldb, const void* C, int64_t ldc, int split_k) {
+  if (layout < 0 || layout > 3) return GEMM_F16_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0) return GEMM_F16_ERR_INVALID_ARG;
   if (ceil_div(M, BM) > 65535 || ceil_div(N, BN) > 65535) return GEMM_F16_ERR_INVALID_ARG;
   if (!A || !B || !C) return GEMM_F16_ERR_INVALID_ARG;
-  if (lda < K || ldb < N || ldc < N) return GEMM_F16_ERR_INVALID_ARG;
+  const int64_t a_row = (layout & LAYOUT_AT) ? M : K;   // elements in a stored row of A
+  const int64_t b_row = (layout & LAYOUT_BT) ? K : N;   // ... of B
+  if (lda < a_row || ldb < b_row || ldc < N) return GEMM_F16_ERR_INVALID_ARG;
   if (split_k < 1 || split_k > ceil_div(K, BK)) return GEMM_F16_ERR_INVALID_ARG;
   if (((uintptr_t)A | (uintptr_t)B | (uintptr_t)C) & 15u) return GEMM_F16_ERR_MISALIGNED;
   if ((lda | ldb | ldc) & 7) return GEMM_F16_ERR_MISALIGNED;
   return GEMM_F16_OK;
+}
+
+int gemm_f16_validate(int M, int N, int K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                      const void* C, int64_t ldc, int split_k) {
+  return gemm_f16_validate_ex(0, M, N, K, A, lda, B, ldb, C, ldc, split_k);
 }
 
 int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order, uint32_t* out, int64_t cap) {
@@ -807,13 +854,20 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
   GF16_CUDA(cudaGetDeviceProperties(&prop, device), "cudaGetDeviceProperties");
   if (prop.major != 10 || prop.minor != 3) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
   DeviceGuard g(device);
-  GF16_CUDA(cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES),
-            "cudaFuncSetAttribute(max dynamic smem)");
-  GF16_CUDA(cudaFuncSetAttribute(pair::gemm_f16_pair_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)pair::SMEM_BYTES),
-            "cudaFuncSetAttribute(pair kernel smem)");
+  {
+    void* const single[4] = {(void*)gemm_f16_kernel<0>, (void*)gemm_f16_kernel<1>,
+                             (void*)gemm_f16_kernel<2>, (void*)gemm_f16_kernel<3>};
+    void* const pairs[4] = {(void*)pair::gemm_f16_pair_kernel<0>, (void*)pair::gemm_f16_pair_kernel<1>,
+                            (void*)pair::gemm_f16_pair_kernel<2>, (void*)pair::gemm_f16_pair_kernel<3>};
+    for (int l = 0; l < 4; ++l) {
+      GF16_CUDA(cudaFuncSetAttribute(single[l], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_BYTES),
+                "cudaFuncSetAttribute(max dynamic smem)");
+      GF16_CUDA(cudaFuncSetAttribute(pairs[l], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)pair::SMEM_BYTES),
+                "cudaFuncSetAttribute(pair kernel smem)");
+    }
+  }
   GF16_CUDA(cudaFuncSetAttribute(pairw::gemm_f16_pair_kernel<512>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)pairw::Cfg<512>::SMEM_BYTES),
@@ -834,7 +888,7 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
     cfg.numAttrs = 1;
     int n256 = 0, n512 = 0;
     cfg.dynamicSmemBytes = pair::SMEM_BYTES;
-    if (cudaOccupancyMaxActiveClusters(&n256, pair::gemm_f16_pair_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n256, pair::gemm_f16_pair_kernel<0>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n256 = 0;
     }
@@ -1049,8 +1103,20 @@ int pick_tile_width(int M, int N, int kblocks, int split_k, int num_sms) {
   return best;
 }
 
-int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t lda, const void* B,
-               int64_t ldb, void* C, int64_t ldc, int split_k, cudaStream_t stream) {
+// Kernel instance for a layout (template parameter 0..3).
+template <typename F0, typename F1, typename F2, typename F3>
+inline void* pick_instance(int layout, F0 f0, F1 f1, F2 f2, F3 f3) {
+  switch (layout) {
+    case 1: return (void*)f1;
+    case 2: return (void*)f2;
+    case 3: return (void*)f3;
+    default: return (void*)f0;
+  }
+}
+
+int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* A, int64_t lda,
+               const void* B, int64_t ldb, void* C, int64_t ldc, int split_k,
+               cudaStream_t stream) {
   const int tiles_m = (int)ceil_div(M, BM);
   const int kblocks = (int)ceil_div(K, BK);
   const int bn = (p->tile_width != 0 && ceil_div(N, p->tile_width) <= 65535)
@@ -1070,7 +1136,7 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   // 512-wide tiles (less load traffic per MMA, but one accumulator and so
   // no epilogue overlap) only on request: measured slower than 256-wide
   // tiles from 2048^3 to 8192^3.
-  const int pair_tn = (p->kernel == 3) ? 512 : 256;
+  const int pair_tn = (p->kernel == 3 && layout == 0) ? 512 : 256;
   const uint32_t* order = nullptr;
   int64_t pair_tiles = 0;
   int rc = use_pair ? get_pair_table(p, M, N, split_k, pair_tn, &order, &pair_tiles)
@@ -1079,13 +1145,27 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
 
   alignas(64) CUtensorMap tmA, tmB, tmC, tmW;
   std::memset(&tmW, 0, sizeof(tmW));
-  rc = cached_encode_2d(p, &tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
-                 (uint64_t)lda * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  // A: row-major M x K -> boxes of 64 K x 128 rows; stored K x M -> boxes
+  // of 64 M x 64 K (two per tile).  B: row-major K x N -> boxes of 64 N x
+  // 64 K; stored N x K -> one box of 64 K x the tile's (or, in the pair
+  // kernel, the CTA's) columns.
+  if (layout & LAYOUT_AT)
+    rc = cached_encode_2d(p, &tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)M, (uint64_t)K,
+                          (uint64_t)lda * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  else
+    rc = cached_encode_2d(p, &tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
+                          (uint64_t)lda * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc) return rc;
-  rc = cached_encode_2d(p, &tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)N, (uint64_t)K,
-                 (uint64_t)ldb * 2, B_BOX_N, BK, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (layout & LAYOUT_BT)
+    rc = cached_encode_2d(p, &tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,
+                          (uint64_t)ldb * 2, BK, use_pair ? 128u : (uint32_t)bn,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  else
+    rc = cached_encode_2d(p, &tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)N, (uint64_t)K,
+                          (uint64_t)ldb * 2, B_BOX_N, BK, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc) return rc;
   rc = cached_encode_2d(p, &tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, (uint64_t)N, (uint64_t)M,
                  (uint64_t)ldc * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -1150,8 +1230,10 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
                 "launch wide gemm_f16_pair_kernel<512>");
     } else {
       cfg.dynamicSmemBytes = pair::SMEM_BYTES;
-      GF16_CUDA(cudaLaunchKernelEx(&cfg, pair::gemm_f16_pair_kernel, tmA, tmB, tmC, tmW, pp),
-                "launch gemm_f16_pair_kernel");
+      void* fn = pick_instance(layout, pair::gemm_f16_pair_kernel<0>, pair::gemm_f16_pair_kernel<1>,
+                               pair::gemm_f16_pair_kernel<2>, pair::gemm_f16_pair_kernel<3>);
+      void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmC, (void*)&tmW, (void*)&pp};
+      GF16_CUDA(cudaLaunchKernelExC(&cfg, fn, args), "launch gemm_f16_pair_kernel");
     }
   } else {
   Params prm;
@@ -1185,8 +1267,12 @@ int run_device(gemm_f16_plan_s* p, int M, int N, int K, const void* A, int64_t l
   pdl.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &pdl;
   cfg.numAttrs = 1;
-  GF16_CUDA(cudaLaunchKernelEx(&cfg, gemm_f16_kernel, tmA, tmB, tmC, tmW, prm),
-            "launch gemm_f16_kernel");
+  {
+    void* fn = pick_instance(layout, gemm_f16_kernel<0>, gemm_f16_kernel<1>, gemm_f16_kernel<2>,
+                             gemm_f16_kernel<3>);
+    void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmC, (void*)&tmW, (void*)&prm};
+    GF16_CUDA(cudaLaunchKernelExC(&cfg, fn, args), "launch gemm_f16_kernel");
+  }
   }
 
   if (split_k > 1) {
@@ -1219,7 +1305,17 @@ int gemm_f16_run(gemm_f16_plan_t p, int M, int N, int K, const void* A, int64_t 
   int rc = gemm_f16_validate(M, N, K, A, lda, B, ldb, C, ldc, split_k);
   if (rc) return rc;
   DeviceGuard g(p->device);
-  return run_device(p, M, N, K, A, lda, B, ldb, C, ldc, split_k, (cudaStream_t)stream);
+  return run_device(p, 0, M, N, K, A, lda, B, ldb, C, ldc, split_k, (cudaStream_t)stream);
+}
+
+int gemm_f16_run_ex(gemm_f16_plan_t p, int layout, int M, int N, int K, const void* A,
+                    int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int split_k,
+                    gemm_f16_stream_t stream) {
+  if (!p) return GEMM_F16_ERR_INVALID_ARG;
+  int rc = gemm_f16_validate_ex(layout, M, N, K, A, lda, B, ldb, C, ldc, split_k);
+  if (rc) return rc;
+  DeviceGuard g(p->device);
+  return run_device(p, layout, M, N, K, A, lda, B, ldb, C, ldc, split_k, (cudaStream_t)stream);
 }
 
 int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, int64_t lda,
@@ -1270,7 +1366,7 @@ int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, in
             "copy B to device");
   GF16_CUDA(cudaEventRecord(p->in_done[slot], p->in_stream), "record input copies");
   GF16_CUDA(cudaStreamWaitEvent(stream, p->in_done[slot], 0), "order product after inputs");
-  rc = run_device(p, M, N, K, buf[0], dlda, buf[1], dldb, buf[2], dldc, split_k, stream);
+  rc = run_device(p, 0, M, N, K, buf[0], dlda, buf[1], dldb, buf[2], dldc, split_k, stream);
   if (rc) return rc;
   GF16_CUDA(cudaEventRecord(p->gemm_done[slot], stream), "record product");
   GF16_CUDA(copy_rows(hC, ldc * 2, buf[2], dldc * 2, (int64_t)N * 2, M, cudaMemcpyDeviceToHost,
@@ -1324,7 +1420,7 @@ int noalloc_setup(int dev, NoallocDevice* d) {
   if (major != 10 || minor != 3) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
   GF16_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
             "cudaDeviceGetAttribute(SM count)");
-  GF16_CUDA(cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  GF16_CUDA(cudaFuncSetAttribute(gemm_f16_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SMEM_BYTES),
             "cudaFuncSetAttribute(max dynamic smem)");
   void* ptr = nullptr;
@@ -1429,7 +1525,7 @@ extern "C" int gemm_f16_run_noalloc(int M, int N, int K, const void* A, int64_t 
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  GF16_CUDA(cudaLaunchKernelEx(&cfg, gemm_f16_kernel, tmA, tmB, tmC, tmW, prm),
+  GF16_CUDA(cudaLaunchKernelEx(&cfg, gemm_f16_kernel<0>, tmA, tmB, tmC, tmW, prm),
             "launch gemm_f16_kernel (no-alloc)");
   if (split_k > 1) {
     const int64_t groups = (int64_t)M * ((N + 3) / 4);

@@ -10,6 +10,9 @@
 // the single-CTA kernel.  Tiles are W = 256 columns wide, or 128 ("narrow")
 // where that balances the last wave or covers a thin column remainder.
 //
+// Operand layouts are a template parameter (bit 0: A stored K x M, bit 1: B
+// stored N x K): only the copies' boxes and the MMA descriptors differ.
+//
 // Barrier protocol ("mbarrier State and Operations": phase completes when
 // pending arrivals and transaction bytes are both zero):
 //   full[s]        leader only, 1 arrival per phase: the leader's producer
@@ -148,6 +151,7 @@ __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t 
 }
 
 // ------------------------------------------------------------------ roles
+template <int LAYOUT>
 __device__ __forceinline__ uint32_t producer_role(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                                   const Params& p, uint32_t base, uint32_t rank,
                                                   uint32_t pair, uint32_t npairs, const Bars& b,
@@ -171,10 +175,20 @@ __device__ __forceinline__ uint32_t producer_role(const CUtensorMap* tmA, const 
       if (kb != skip_kb) {
         const uint32_t fb = leader_full + 8 * pos.stage;
         const int k0 = kb * BK;
-        ptx::tma_load_2d_pair(base + OFF_A + pos.stage * A_STAGE, tmA, fb, k0, g.m0);
+        const uint32_t sa = base + OFF_A + pos.stage * A_STAGE;
+        if constexpr ((LAYOUT & LAYOUT_AT) != 0) {   // A stored K x M
+          ptx::tma_load_2d_pair(sa, tmA, fb, g.m0, k0);
+          ptx::tma_load_2d_pair(sa + 8192, tmA, fb, g.m0 + 64, k0);
+        } else {
+          ptx::tma_load_2d_pair(sa, tmA, fb, k0, g.m0);
+        }
         const uint32_t sb = base + OFF_B + pos.stage * B_STAGE;
-        ptx::tma_load_2d_pair(sb, tmB, fb, nb0, k0);
-        ptx::tma_load_2d_pair(sb + B_BOX, tmB, fb, nb0 + (int)B_BOX_N, k0);
+        if constexpr ((LAYOUT & LAYOUT_BT) != 0) {   // B stored N x K: 128 rows of N
+          ptx::tma_load_2d_pair(sb, tmB, fb, k0, nb0);
+        } else {
+          ptx::tma_load_2d_pair(sb, tmB, fb, nb0, k0);
+          ptx::tma_load_2d_pair(sb + B_BOX, tmB, fb, nb0 + (int)B_BOX_N, k0);
+        }
       }
       ++issued;
       ring_advance(pos, STAGES);
@@ -183,14 +197,16 @@ __device__ __forceinline__ uint32_t producer_role(const CUtensorMap* tmA, const 
   return issued;
 }
 
+template <int LAYOUT>
 __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_t tmem_base,
                                          uint32_t pair, uint32_t npairs, const Bars& b,
                                          volatile int* abort_flag) {
+  using D = OperandDesc<LAYOUT>;
   RingPos pos{0, 0};
   uint32_t local = 0;
   for (int u = (int)pair; u < p.num_units; u += (int)npairs) {
     const UnitGeom g = unit_geom(p, u, 0);
-    const uint32_t idesc = idesc_for(g.width);
+    const uint32_t idesc = idesc_for_layout(idesc_for(g.width), LAYOUT);
     const uint32_t acc = local & 1u;
     const uint32_t acc_phase = (local >> 1) & 1u;
     if (!wait_phase(b.tempty + 8 * acc, acc_phase ^ 1u, p, abort_flag)) break;
@@ -203,13 +219,13 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
         break;
       }
       ptx::tc_fence_after();
-      const uint64_t a_desc = smem_desc_sw128(base + OFF_A + pos.stage * A_STAGE, A_LBO, A_SBO);
-      const uint64_t b_desc = smem_desc_sw128(base + OFF_B + pos.stage * B_STAGE, B_BOX, 1024);
+      const uint64_t a_desc = smem_desc_sw128(base + OFF_A + pos.stage * A_STAGE, D::a_lbo, D::a_sbo);
+      const uint64_t b_desc = smem_desc_sw128(base + OFF_B + pos.stage * B_STAGE, D::b_lbo, D::b_sbo);
       const uint32_t first = (kb == g.kb0) ? 1u : 0u;
 #pragma unroll
       for (int k = 0; k < BK / UMMA_K; ++k) {
-        ptx::mma_f16_pair(d_tmem, a_desc + ((k * A_KSTEP) >> 4), b_desc + ((k * B_KSTEP) >> 4),
-                          idesc, (first && k == 0) ? 0u : 1u);
+        ptx::mma_f16_pair(d_tmem, a_desc + ((k * D::a_kstep) >> 4),
+                          b_desc + ((k * D::b_kstep) >> 4), idesc, (first && k == 0) ? 0u : 1u);
       }
       ptx::mma_commit_pair(b.empty + 8 * pos.stage, 0x3);
       ring_advance(pos, STAGES);
@@ -333,6 +349,7 @@ __device__ __noinline__ void leader_drain(const Bars& b, uint32_t mine, uint32_t
   }
 }
 
+template <int LAYOUT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
@@ -393,10 +410,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
   uint32_t issued = 0;
   if (warp == 0) {
-    if (lane == 0) issued = producer_role(&tmA, &tmB, p, base, rank, pair, npairs, b, abort_flag);
+    if (lane == 0)
+      issued = producer_role<LAYOUT>(&tmA, &tmB, p, base, rank, pair, npairs, b, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role(p, base, tmem_base, pair, npairs, b, abort_flag);
+    if (lane == 0 && rank == 0) mma_role<LAYOUT>(p, base, tmem_base, pair, npairs, b, abort_flag);
     __syncwarp();
   } else {
     epilogue_role(&tmC, &tmW, p, base, tmem_base, rank, pair, npairs, b, warp, lane, abort_flag);

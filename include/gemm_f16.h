@@ -126,6 +126,41 @@ int gemm_f16_run(gemm_f16_plan_t plan, int M, int N, int K,
                  void *C, int64_t ldc, int split_k, gemm_f16_stream_t stream);
 
 /*
+ * Operand storage for gemm_f16_run_ex.  The product is always C = A * B
+ * with A of M x K and B of K x N (element (i, k) of A, (k, j) of B); the
+ * layout says how each operand sits in memory:
+ *   GEMM_F16_LAYOUT_NN  A row-major (M rows of K, stride lda >= K),
+ *                       B row-major (K rows of N, stride ldb >= N);
+ *   GEMM_F16_LAYOUT_TN  A stored transposed: K rows of M, A(i, k) at
+ *                       A[k * lda + i], lda >= M; B as in NN;
+ *   GEMM_F16_LAYOUT_NT  A as in NN; B stored transposed: N rows of K,
+ *                       B(k, j) at B[j * ldb + k], ldb >= K;
+ *   GEMM_F16_LAYOUT_TT  both stored transposed.
+ * A transposed operand is read by the same tensor copies with the other
+ * dimension innermost and handed to the tensor core with the other major
+ * mode: no copy or transpose kernel is run.  These layouts are not in the
+ * pages' kernel, whose operands are row-major A and B; they cover the
+ * usual "transposed operand" cases of a GEMM library.
+ */
+enum {
+    GEMM_F16_LAYOUT_NN = 0,
+    GEMM_F16_LAYOUT_TN = 1,   /* bit 0: A stored K x M */
+    GEMM_F16_LAYOUT_NT = 2,   /* bit 1: B stored N x K */
+    GEMM_F16_LAYOUT_TT = 3
+};
+
+/*
+ * gemm_f16_run with an operand layout (above).  gemm_f16_run is
+ * gemm_f16_run_ex with GEMM_F16_LAYOUT_NN.  Same semantics, workspace,
+ * split-K order and errors; GEMM_F16_ERR_INVALID_ARG also for a layout
+ * outside 0..3.  Option GEMM_F16_OPT_KERNEL 3 (512-wide pair tiles) is
+ * honoured for layout NN only; other layouts then use 256-wide pair tiles.
+ */
+int gemm_f16_run_ex(gemm_f16_plan_t plan, int layout, int M, int N, int K,
+                    const void *A, int64_t lda, const void *B, int64_t ldb,
+                    void *C, int64_t ldc, int split_k, gemm_f16_stream_t stream);
+
+/*
  * Same product with HOST operands: copies hA and hB into plan-owned device
  * buffers, runs gemm_f16_run on them and copies the result into hC.
  * Consecutive calls overlap: the input copies run on a plan-internal stream
@@ -179,6 +214,11 @@ const char *gemm_f16_last_cuda_error(void);
 int gemm_f16_validate(int M, int N, int K, const void *A, int64_t lda,
                       const void *B, int64_t ldb, const void *C, int64_t ldc,
                       int split_k);
+
+/* Host-only argument check used by gemm_f16_run_ex for `layout`. */
+int gemm_f16_validate_ex(int layout, int M, int N, int K, const void *A,
+                         int64_t lda, const void *B, int64_t ldb,
+                         const void *C, int64_t ldc, int split_k);
 
 /*
  * Host-only: the order in which output tiles of a tiles_m x tiles_n grid

@@ -196,3 +196,22 @@ def test_pair_tiles_reject_bad_arguments(lib):
     assert lib.gemm_f16_pair_tiles(8, 8, 0, 1, 0, 256, None, 0) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_pair_tiles(8, 8, 76, 0, 0, 256, None, 0) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_pair_tiles(8, 8, 76, 1, 0, 384, None, 0) == g.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("layout,args,code", [
+    (0, (16, 32, 64, P, 64, P, 32, P, 32, 1), g.OK),
+    (1, (16, 32, 64, P, 16, P, 32, P, 32, 1), g.OK),       # A stored K x M: lda >= M
+    (1, (16, 32, 64, P, 8, P, 32, P, 32, 1), g.ERR_INVALID_ARG),
+    (1, (24, 32, 64, P, 24, P, 32, P, 32, 1), g.OK),       # lda need not reach K
+    (2, (16, 32, 64, P, 64, P, 64, P, 32, 1), g.OK),       # B stored N x K: ldb >= K
+    (2, (16, 32, 64, P, 64, P, 32, P, 32, 1), g.ERR_INVALID_ARG),
+    (3, (16, 32, 64, P, 16, P, 64, P, 32, 1), g.OK),
+    (3, (16, 32, 64, P, 64, P, 32, P, 32, 1), g.ERR_INVALID_ARG),
+    (3, (16, 32, 64, P, 20, P, 64, P, 32, 1), g.ERR_MISALIGNED),
+    (4, (16, 32, 64, P, 64, P, 32, P, 32, 1), g.ERR_INVALID_ARG),
+    (-1, (16, 32, 64, P, 64, P, 32, P, 32, 1), g.ERR_INVALID_ARG),
+])
+def test_validate_layouts(lib, layout, args, code):
+    assert g.gemm_f16_validate_ex(layout, *args) == code
+    if layout == 0:
+        assert g.gemm_f16_validate(*args) == code
