@@ -26,7 +26,8 @@ __all__ = [
     "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT", "ERR_SCRATCH_TOO_SMALL", "gemm_f16_run_noalloc",
     "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "INFO_NUM_SMS", "INFO_MAX_PAIRS",
     "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
-    "gemm_f16_run_ex", "gemm_f16_validate_ex",
+    "gemm_f16_run_ex", "gemm_f16_validate_ex", "attn_f16_fwd", "attn_f16_validate",
+    "attention", "ATTN_HEAD_DIM",
     "LAYOUT_NN", "LAYOUT_TN", "LAYOUT_NT", "LAYOUT_TT",
 ]
 
@@ -47,6 +48,8 @@ OPT_TILE_WIDTH = 5
 OPT_SM_LIMIT = 6
 INFO_NUM_SMS = 100
 INFO_MAX_PAIRS = 101
+
+ATTN_HEAD_DIM = 256
 
 LAYOUT_NN = 0
 LAYOUT_TN = 1   # A stored K x M
@@ -81,6 +84,14 @@ _SIGNATURES = {
                                      ctypes.POINTER(ctypes.c_uint32), _c_i64]),
     "gemm_f16_run_noalloc": (_c_int, [_c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
                                       _vp, _c_i64, _c_int, _vp, _vp]),
+    "attn_f16_fwd": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                              _vp, ctypes.POINTER(_c_i64), _vp, ctypes.POINTER(_c_i64),
+                              _vp, ctypes.POINTER(_c_i64), _vp, ctypes.POINTER(_c_i64),
+                              ctypes.c_float, _vp]),
+    "attn_f16_validate": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                   _vp, ctypes.POINTER(_c_i64), _vp, ctypes.POINTER(_c_i64),
+                                   _vp, ctypes.POINTER(_c_i64), _vp, ctypes.POINTER(_c_i64),
+                                   ctypes.c_float]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -202,6 +213,30 @@ def gemm_f16_validate_ex(layout, M, N, K, A, lda, B, ldb, C, ldc, split_k) -> in
     return load().gemm_f16_validate_ex(layout, M, N, K, A, lda, B, ldb, C, ldc, split_k)
 
 
+def _strides3(st):
+    if st is None or len(st) != 3:
+        raise ValueError("strides are (batch, head, row) in elements")
+    return (_c_i64 * 3)(*[int(x) for x in st])
+
+
+def attn_f16_fwd(plan: int, batch: int, heads: int, seq_q: int, seq_kv: int, head_dim: int,
+                 Q: int, q_strides, K: int, k_strides, V: int, v_strides, O: int, o_strides,
+                 scale: float, stream: int = 0) -> None:
+    """Enqueue attention forward (device pointers; strides (batch, head, row))."""
+    _check(load().attn_f16_fwd(plan, batch, heads, seq_q, seq_kv, head_dim,
+                               Q, _strides3(q_strides), K, _strides3(k_strides),
+                               V, _strides3(v_strides), O, _strides3(o_strides),
+                               float(scale), stream), "attn_f16_fwd")
+
+
+def attn_f16_validate(batch, heads, seq_q, seq_kv, head_dim, Q, q_strides, K, k_strides,
+                      V, v_strides, O, o_strides, scale) -> int:
+    return load().attn_f16_validate(batch, heads, seq_q, seq_kv, head_dim,
+                                    Q, _strides3(q_strides), K, _strides3(k_strides),
+                                    V, _strides3(v_strides), O, _strides3(o_strides),
+                                    float(scale))
+
+
 def gemm_f16_tile_order(tiles_m: int, tiles_n: int, order: int = 0) -> list:
     """Tile order as a list of (tile_m, tile_n)."""
     n = _check(load().gemm_f16_tile_order(tiles_m, tiles_n, order, None, 0),
@@ -303,3 +338,28 @@ def matmul(plan: Plan, A, B, C=None, split_k: int = 1, stream=None):
     gemm_f16_run_ex(plan.handle, layout, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
                     C.data_ptr(), C.stride(0) if M > 1 else N, split_k, _stream_handle(stream))
     return C
+
+
+def attention(plan: Plan, Q, K, V, O=None, scale=None, stream=None):
+    """softmax(scale * Q K^T) V for float16 CUDA tensors of shape
+    [batch, heads, seq, 256] (the last dimension contiguous; other strides
+    free, so ``x.transpose(1, 2)`` of a [batch, seq, heads, 256] tensor works).
+    ``scale`` defaults to 1/sqrt(256).  O is allocated if None."""
+    import torch
+    for name, X in (("Q", Q), ("K", K), ("V", V)):
+        if X.dtype != torch.float16 or X.dim() != 4 or X.stride(3) != 1:
+            raise ValueError(f"{name} must be a float16 [B, H, S, D] tensor with D contiguous")
+    B, H, Sq, D = Q.shape
+    Skv = K.shape[2]
+    if tuple(K.shape) != (B, H, Skv, D) or tuple(V.shape) != (B, H, Skv, D):
+        raise ValueError(f"shape mismatch {tuple(Q.shape)} {tuple(K.shape)} {tuple(V.shape)}")
+    if O is None:
+        O = torch.empty((B, H, Sq, D), dtype=torch.float16, device=Q.device)
+    elif O.dtype != torch.float16 or tuple(O.shape) != (B, H, Sq, D) or O.stride(3) != 1:
+        raise ValueError("O must be a float16 [B, H, Sq, D] tensor with D contiguous")
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    st = lambda X: (X.stride(0), X.stride(1), X.stride(2))
+    attn_f16_fwd(plan.handle, B, H, Sq, Skv, D, Q.data_ptr(), st(Q), K.data_ptr(), st(K),
+                 V.data_ptr(), st(V), O.data_ptr(), st(O), scale, _stream_handle(stream))
+    return O

@@ -1,0 +1,435 @@
+// Scaled dot-product attention forward for head dimension 256 on GB300
+// (sm_103a): O = softmax(scale * Q K^T) V per batch and head, binary16 in and
+// out, FP32 scores, accumulator and softmax statistics.
+//
+// The schedule is the "SDP Kernel Split Barrier B" pattern of the "Xe2
+// Nbarrier Pipelining" page, carried over to mbarriers and tensor memory.
+// Per block of 64 keys: S = Q K^T (tensor core) -> softmax with a running
+// row maximum -> P stored to shared memory -> ARRIVE -> [window: the deferred
+// sum update; the next K and V tiles arrive through the copy ring; the next
+// S = Q K^T runs on the tensor core] -> the MMA thread WAITS -> O += P V.
+// The output rescale ("compensation") is applied to the TMEM accumulator
+// before P is published, and only when some row's maximum moved (else the
+// factor is exactly 1).
+//
+// One CTA per (128 query rows, head, batch), 192 threads:
+//   warp 0      TMA producer: Q once (128 x 256, four 64-column boxes), then
+//               K and V tiles (64 x 256, 32 KB) into a 4-slot ring in the
+//               order the MMA thread consumes them: K0, K1, V0, K2, V1, ...
+//   warp 1      allocates 512 TMEM columns (S double buffer 2 x 64, O 256)
+//               and one lane issues the MMAs: S_j+1 = Q K_j+1^T (128x64x16,
+//               x16) ahead of O += P_j V_j (128x256x16, x4), releasing ring
+//               slots with tcgen05.commit.
+//   warps 2..5  softmax + epilogue: one query row per thread (its TMEM
+//               lane).  Row max / exp2 / row sum in FP32, P rounded to
+//               binary16 into shared memory, final O / l rounded to binary16
+//               and written with tensor stores.
+//
+// Barriers ("mbarrier State and Operations" page): q_full and full[s] (one
+// arrive.expect_tx + the copies' bytes), empty[s] (one commit), s_full[b]
+// (one commit per S block), p_full (128 softmax threads), o_done (one commit
+// per P V block), mma_done.  Every wait is bounded as in the GEMM kernels:
+// past the time limit the role records GEMM_F16_ERR_TIMEOUT, raises the
+// CTA's abort flag and stops; the CTA drains its copies and MMAs in flight
+// and frees its TMEM before it exits.
+
+#pragma once
+
+namespace gf16 {
+namespace attn {
+
+constexpr int HD = 256;                 // head dimension
+constexpr int BQ = 128;                 // query rows per CTA (MMA M, TMEM lanes)
+constexpr int BKV = 64;                 // keys per block
+constexpr int RING = 4;                 // K / V tiles in flight
+constexpr int NUM_THREADS = 192;
+constexpr int SM_WARP0 = 2;             // softmax warps 2..5
+constexpr int SM_THREADS = 128;
+
+constexpr uint32_t CHUNK_Q = BQ * 128;            // 64 d-columns x 128 rows: 16 KB
+constexpr uint32_t CHUNK_KV = BKV * 128;          // 64 d-columns x 64 rows: 8 KB
+constexpr uint32_t Q_BYTES = (HD / 64) * CHUNK_Q;       // 64 KB
+constexpr uint32_t TILE_BYTES = (HD / 64) * CHUNK_KV;   // 32 KB
+constexpr uint32_t P_BYTES = BQ * BKV * 2;              // 16 KB
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_RING = OFF_Q + Q_BYTES;
+constexpr uint32_t OFF_P = OFF_RING + RING * TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
+// q_full, full[RING], empty[RING], s_full[2], p_full, o_done, mma_done
+constexpr uint32_t NUM_BARS = 1 + 2 * RING + 2 + 3;
+constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
+constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + room to align the base to 1024
+static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit per CTA");
+static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "swizzled buffers need 1024-B alignment");
+
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL = 0;     // S buffers at columns 0 and 64
+constexpr uint32_t O_COL = 256;   // O: columns 256 .. 511
+
+// Instruction descriptors (kind::f16, FP32 accumulate): S = Q K^T has both
+// operands K-major (Q rows and K rows both run along d); O += P V has A
+// (P) K-major and B (V, rows along d = N) MN-major.
+constexpr uint32_t IDESC_QK = make_idesc(BQ, BKV) & ~(1u << 16);
+constexpr uint32_t IDESC_PV = make_idesc(BQ, HD);
+
+struct Params {
+  int seq_q, seq_kv;
+  int nkv;                      // key blocks: ceil(seq_kv / 64)
+  float scale_log2;             // scale * log2(e): scores go to base 2
+  int* status;
+  unsigned long long timeout_ns;
+  int fault_cta;                // test only: CTA whose first K tile gets no copy
+};
+
+struct Bars {
+  uint32_t q_full, full, empty, s_full, p_full, o_done, mma_done;
+};
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* status,
+                                       unsigned long long timeout_ns, volatile int* abort_flag) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      *(volatile int*)status = (int)GEMM_F16_ERR_TIMEOUT;
+      __threadfence_system();
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
+                                           volatile int* abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, p.status, p.timeout_ns, abort_flag);
+}
+
+// ------------------------------------------------------------------ producer
+// Issues the copies in consumption order; returns how many ring slots it
+// filled (for the drain after an abort) through `issued`, and its ring
+// position through `pos_out`.
+__device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                              const CUtensorMap* tmV, const Params& p,
+                                              uint32_t base, const Bars& b, int q0, int h,
+                                              int bz, bool fault, volatile int* abort_flag,
+                                              RingPos* pos_out, uint32_t* issued_out) {
+  ptx::mbar_arrive_expect_tx_relaxed(b.q_full, Q_BYTES);
+#pragma unroll
+  for (int c = 0; c < HD / 64; ++c)
+    ptx::tma_load_4d(base + OFF_Q + c * CHUNK_Q, tmQ, b.q_full, 64 * c, q0, h, bz);
+
+  RingPos pos{0, 0};
+  uint32_t issued = 0;
+  // Tile t of the consumption order: K_0, then for each j: K_{j+1}, V_j.
+  const int ntiles = 2 * p.nkv;
+  for (int t = 0; t < ntiles; ++t) {
+    int j;
+    bool is_k;
+    if (t == 0) {
+      j = 0;
+      is_k = true;
+    } else if (t == ntiles - 1) {
+      j = p.nkv - 1;
+      is_k = false;
+    } else {
+      is_k = (t & 1) != 0;              // odd: K_{(t+1)/2}; even: V_{t/2 - 1}
+      j = is_k ? (t + 1) / 2 : t / 2 - 1;
+    }
+    if (!wait_phase(b.empty + 8 * pos.stage, producer_wait_parity(pos), p, abort_flag)) break;
+    const uint32_t fb = b.full + 8 * pos.stage;
+    ptx::mbar_arrive_expect_tx_relaxed(fb, TILE_BYTES);
+    if (!(fault && t == 0)) {
+      const uint32_t dst = base + OFF_RING + pos.stage * TILE_BYTES;
+      const CUtensorMap* tm = is_k ? tmK : tmV;
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c)
+        ptx::tma_load_4d(dst + c * CHUNK_KV, tm, fb, 64 * c, j * BKV, h, bz);
+    }
+    ++issued;
+    ring_advance(pos, RING);
+  }
+  *pos_out = pos;
+  *issued_out = issued;
+}
+
+// ------------------------------------------------------------------ MMA issuer
+__device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_t tmem_base,
+                                         const Bars& b, volatile int* abort_flag) {
+  if (!wait_phase(b.q_full, 0, p, abort_flag)) return;
+  ptx::tc_fence_after();
+  RingPos pos{0, 0};
+  const uint32_t q_addr = base + OFF_Q;
+  const uint32_t o_tmem = tmem_base + O_COL;
+
+  // S_j = Q K_j^T into S buffer `sb`: 16 MMAs of K = 16 along d.
+  auto issue_qk = [&](uint32_t sb) -> bool {
+    if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag))
+      return false;
+    ptx::tc_fence_after();
+    const uint32_t k_addr = base + OFF_RING + pos.stage * TILE_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      const uint32_t off_q = (uint32_t)(kk >> 2) * CHUNK_Q + (uint32_t)(kk & 3) * 32u;
+      const uint32_t off_k = (uint32_t)(kk >> 2) * CHUNK_KV + (uint32_t)(kk & 3) * 32u;
+      ptx::mma_f16(tmem_base + S_COL + sb * BKV, smem_desc_sw128(q_addr + off_q, 16, 1024),
+                   smem_desc_sw128(k_addr + off_k, 16, 1024), IDESC_QK, kk > 0 ? 1u : 0u);
+    }
+    ptx::mma_commit(b.empty + 8 * pos.stage);
+    ptx::mma_commit(b.s_full + 8 * sb);
+    ring_advance(pos, RING);
+    return true;
+  };
+
+  bool ok = issue_qk(0);
+  for (int j = 0; j < p.nkv && ok; ++j) {
+    if (j + 1 < p.nkv && !issue_qk((uint32_t)(j + 1) & 1u)) break;
+    // The split barrier's WAIT: P_j is in shared memory and O is rescaled.
+    if (!wait_phase(b.p_full, (uint32_t)j & 1u, p, abort_flag)) break;
+    ptx::tc_fence_after();
+    if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag)) break;
+    ptx::tc_fence_after();
+    const uint32_t v_addr = base + OFF_RING + pos.stage * TILE_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < BKV / 16; ++kk) {
+      ptx::mma_f16(o_tmem, smem_desc_sw128(base + OFF_P + (uint32_t)kk * 32u, 16, 1024),
+                   smem_desc_sw128(v_addr + (uint32_t)kk * 2048u, CHUNK_KV, 1024), IDESC_PV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+    }
+    ptx::mma_commit(b.empty + 8 * pos.stage);
+    ptx::mma_commit(b.o_done);
+    ring_advance(pos, RING);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Sum of a packed pair of binary16 values, in FP32.
+__device__ __forceinline__ float half2_sum(uint32_t v) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+  return f.x + f.y;
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+__device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Params& p,
+                                             uint32_t base, uint32_t tmem_base, const Bars& b,
+                                             uint32_t warp, uint32_t lane, int q0, int h, int bz,
+                                             volatile int* abort_flag) {
+  const uint32_t quarter = warp & 3u;             // TMEM lanes 32*quarter .. +31
+  const uint32_t row = quarter * 32u + lane;      // query row within the tile
+  const uint32_t t_lane = (quarter * 32u) << 16;
+  const uint32_t p_row = base + OFF_P + row * 128u;
+  const uint32_t sw = row & 7u;
+  float m = -INFINITY;                            // running row max (base-2 units)
+  float l = 0.f;                                  // running row sum
+  bool ok = true;
+  for (int j = 0; j < p.nkv; ++j) {
+    const uint32_t sb = (uint32_t)j & 1u;
+    bool got = wait_phase(b.s_full + 8 * sb, ((uint32_t)j >> 1) & 1u, p, abort_flag);
+    if (!__all_sync(0xffffffffu, got)) {
+      ok = false;
+      break;
+    }
+    ptx::tc_fence_after();
+    uint32_t s[64];
+    ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + S_COL + sb * BKV,
+                            *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + S_COL + sb * BKV + 32,
+                            *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    ptx::tmem_ld_wait();
+    float x[64];
+    const int valid = p.seq_kv - j * BKV;  // keys of this block inside the sequence
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      x[c] = (c < valid) ? __uint_as_float(s[c]) * p.scale_log2 : -INFINITY;
+      mx = fmaxf(mx, x[c]);
+    }
+    const float m_new = fmaxf(m, mx);
+    const float alpha = (m_new == m) ? 1.f : ptx::ex2_approx(m - m_new);
+    uint32_t pk[32];
+    float lsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      pk[c] = pack_half2(ptx::ex2_approx(x[2 * c] - m_new), ptx::ex2_approx(x[2 * c + 1] - m_new));
+      lsum += half2_sum(pk[c]);
+    }
+    if (j > 0) {
+      // P V of the previous block must be done: it reads the P buffer and
+      // writes the O this thread may rescale.
+      got = wait_phase(b.o_done, (uint32_t)(j - 1) & 1u, p, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          const uint32_t ta = tmem_base + t_lane + O_COL + (uint32_t)c * 32u;
+          ptx::tmem_ld_32x32b_x32(ta, o);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          ptx::tmem_st_32x32b_x32(ta, o);
+        }
+        ptx::tmem_st_wait();
+      }
+    }
+    // P row -> shared memory, 128-byte swizzle (16-byte chunk g of row r at
+    // chunk position g ^ (r mod 8)), the K-major layout the MMA reads.
+#pragma unroll
+    for (uint32_t g = 0; g < 8; ++g)
+      ptx::st_shared_v4(p_row + ((g ^ sw) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
+                        pk[4 * g + 3]);
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    // The split barrier's ARRIVE ...
+    ptx::mbar_arrive(b.p_full);
+    // ... and the window: the deferred sum update.
+    l = l * alpha + lsum;
+    m = m_new;
+  }
+  if (ok) {
+    const bool got = wait_phase(b.o_done, (uint32_t)(p.nkv - 1) & 1u, p, abort_flag);
+    ok = __all_sync(0xffffffffu, got);
+  }
+  if (ok) {
+    ptx::tc_fence_after();
+    const float inv_l = 1.f / l;
+    // Staging in the Q buffer (every MMA has completed): per warp 4 boxes of
+    // 32 rows x 64 columns, 128-byte swizzle.
+    const uint32_t stage = base + OFF_Q + quarter * 4u * 4096u;
+    const uint32_t lsw = lane & 7u;
+#pragma unroll 1
+    for (int c = 0; c < HD / 32; ++c) {
+      uint32_t o[32];
+      ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + O_COL + (uint32_t)c * 32u, o);
+      ptx::tmem_ld_wait();
+      const uint32_t box = stage + (uint32_t)(c >> 1) * 4096u + lane * 128u;
+#pragma unroll
+      for (uint32_t i = 0; i < 4; ++i) {
+        const uint32_t g = (uint32_t)(c & 1) * 4u + i;
+        const float* f = reinterpret_cast<const float*>(&o[8 * i]);
+        ptx::st_shared_v4(box + ((g ^ lsw) << 4), pack_half2(f[0] * inv_l, f[1] * inv_l),
+                          pack_half2(f[2] * inv_l, f[3] * inv_l),
+                          pack_half2(f[4] * inv_l, f[5] * inv_l),
+                          pack_half2(f[6] * inv_l, f[7] * inv_l));
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    const int r0 = q0 + (int)quarter * 32;
+    if (lane == 0 && r0 < p.seq_q) {
+#pragma unroll
+      for (int bx = 0; bx < HD / 64; ++bx)
+        ptx::tma_store_4d(tmO, stage + (uint32_t)bx * 4096u, 64 * bx, r0, h, bz);
+      ptx::bulk_commit_group();
+      ptx::bulk_wait_group_read<0>();
+    }
+    __syncwarp();
+  }
+}
+
+// After an abort: wait (bounded) for the copies still in flight into the
+// ring (at most the last RING slots) and for Q.
+__device__ __noinline__ void producer_drain(const Bars& b, RingPos pos, uint32_t issued,
+                                            uint64_t limit_ns) {
+  const uint32_t n = issued < (uint32_t)RING ? issued : (uint32_t)RING;
+  for (uint32_t i = 0; i < n; ++i) {
+    ring_retreat(pos, RING);
+    wait_drain(b.full + 8 * pos.stage, consumer_wait_parity(pos), limit_ns);
+  }
+  wait_drain(b.q_full, 0, limit_ns);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_f16_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmO, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
+  const uint32_t lane = threadIdx.x & 31u;
+  const int q0 = (int)blockIdx.x * BQ;
+  const int h = (int)blockIdx.y;
+  const int bz = (int)blockIdx.z;
+  const int cta = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+
+  Bars b;
+  b.q_full = base + OFF_BAR;
+  b.full = b.q_full + 8;
+  b.empty = b.full + 8 * RING;
+  b.s_full = b.empty + 8 * RING;
+  b.p_full = b.s_full + 16;
+  b.o_done = b.p_full + 8;
+  b.mma_done = b.o_done + 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+    ptx::prefetch_tmap(&tmO);
+    ptx::mbar_init(b.q_full, 1);
+    for (int s = 0; s < RING; ++s) {
+      ptx::mbar_init(b.full + 8 * s, 1);
+      ptx::mbar_init(b.empty + 8 * s, 1);
+    }
+    ptx::mbar_init(b.s_full, 1);
+    ptx::mbar_init(b.s_full + 8, 1);
+    ptx::mbar_init(b.p_full, SM_THREADS);
+    ptx::mbar_init(b.o_done, 1);
+    ptx::mbar_init(b.mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(base + OFF_TMEM_SLOT, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
+
+  RingPos prod_pos{0, 0};
+  uint32_t prod_issued = 0;
+  if (warp == 0) {
+    if (lane == 0)
+      producer_role(&tmQ, &tmK, &tmV, p, base, b, q0, h, bz, cta == p.fault_cta, abort_flag,
+                    &prod_pos, &prod_issued);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      mma_role(p, base, tmem_base, b, abort_flag);
+      // Every MMA issued must be finished before TMEM is freed.
+      ptx::mma_commit(b.mma_done);
+      wait_drain(b.mma_done, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    softmax_role(&tmO, p, base, tmem_base, b, warp, lane, q0, h, bz, abort_flag);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag)
+    producer_drain(b, prod_pos, prod_issued, p.timeout_ns);
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace attn
+}  // namespace gf16

@@ -48,6 +48,7 @@
 #include <utility>
 #include <vector>
 
+#include "attn_f16.h"
 #include "gemm_f16.h"
 #include "ptx.cuh"
 #include "schedule.h"
@@ -539,6 +540,7 @@ __global__ void __launch_bounds__(256)
 
 #include "gemm_pair.cuh"
 #include "gemm_pair_wide.cuh"
+#include "attn_f16.cuh"
 
 // ====================================================================== host
 using namespace gf16;
@@ -872,6 +874,10 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)pairw::Cfg<512>::SMEM_BYTES),
             "cudaFuncSetAttribute(wide pair kernel smem)");
+  GF16_CUDA(cudaFuncSetAttribute(attn::attn_f16_fwd_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn::SMEM_BYTES),
+            "cudaFuncSetAttribute(attention kernel smem)");
   // Co-resident clusters of two for each pair-kernel instance; keep the
   // smaller count (0 if the query fails: the pair kernel is then not used).
   int max_clusters = 0;
@@ -1539,3 +1545,99 @@ extern "C" int gemm_f16_run_noalloc(int M, int N, int K, const void* A, int64_t 
   }
   return GEMM_F16_OK;
 }
+
+// ====================================================================== attention
+namespace {
+
+// [batch, head, row, 256] binary16 view as a 4-D tensor map: dims (d, row,
+// head, batch), box (64, box_rows, 1, 1), 128-byte swizzle.
+int encode_bhsd(CUtensorMap* map, const void* ptr, int batch, int heads, int rows,
+                const int64_t st[3], uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "cuTensorMapEncodeTiled entry point not available");
+    return GEMM_F16_ERR_CUDA;
+  }
+  // A stride of an extent-1 dimension is never used; give the map a valid one.
+  const int64_t row_st = st[2];
+  const int64_t head_st = heads > 1 ? st[1] : row_st * rows;
+  const int64_t batch_st = batch > 1 ? st[0] : head_st * heads;
+  const cuuint64_t dims[4] = {(cuuint64_t)attn::HD, (cuuint64_t)rows, (cuuint64_t)heads,
+                              (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {(cuuint64_t)row_st * 2, (cuuint64_t)head_st * 2,
+                                 (cuuint64_t)batch_st * 2};
+  const cuuint32_t box[4] = {64, box_rows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "cuTensorMapEncodeTiled (attention operand) failed (CUresult %d)", (int)r);
+    return GEMM_F16_ERR_CUDA;
+  }
+  return GEMM_F16_OK;
+}
+
+bool strides_ok(const int64_t* st) {
+  if (!st) return false;
+  for (int i = 0; i < 3; ++i)
+    if (st[i] <= 0 || st[i] >= ((int64_t)1 << 38)) return false;
+  return st[2] >= attn::HD;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_f16_validate(int batch, int heads, int seq_q, int seq_kv, int head_dim, const void* Q,
+                      const int64_t q_strides[3], const void* K, const int64_t k_strides[3],
+                      const void* V, const int64_t v_strides[3], const void* O,
+                      const int64_t o_strides[3], float scale) {
+  if (batch < 1 || heads < 1 || batch > 65535 || heads > 65535) return GEMM_F16_ERR_INVALID_ARG;
+  if (seq_q < 1 || seq_kv < 1) return GEMM_F16_ERR_INVALID_ARG;
+  if (head_dim != attn::HD) return GEMM_F16_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !O) return GEMM_F16_ERR_INVALID_ARG;
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return GEMM_F16_ERR_INVALID_ARG;
+  const int64_t* sts[4] = {q_strides, k_strides, v_strides, o_strides};
+  for (const int64_t* st : sts)
+    if (!strides_ok(st)) return GEMM_F16_ERR_INVALID_ARG;
+  const void* ptrs[4] = {Q, K, V, O};
+  for (const void* ptr : ptrs)
+    if ((uintptr_t)ptr & 15) return GEMM_F16_ERR_MISALIGNED;
+  for (const int64_t* st : sts)
+    if ((st[0] | st[1] | st[2]) & 7) return GEMM_F16_ERR_MISALIGNED;
+  return GEMM_F16_OK;
+}
+
+int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv, int head_dim,
+                 const void* Q, const int64_t q_strides[3], const void* K,
+                 const int64_t k_strides[3], const void* V, const int64_t v_strides[3], void* O,
+                 const int64_t o_strides[3], float scale, gemm_f16_stream_t stream) {
+  if (!p) return GEMM_F16_ERR_INVALID_ARG;
+  int rc = attn_f16_validate(batch, heads, seq_q, seq_kv, head_dim, Q, q_strides, K, k_strides,
+                             V, v_strides, O, o_strides, scale);
+  if (rc) return rc;
+  DeviceGuard g(p->device);
+  CUtensorMap tmQ, tmK, tmV, tmO;
+  if ((rc = encode_bhsd(&tmQ, Q, batch, heads, seq_q, q_strides, attn::BQ))) return rc;
+  if ((rc = encode_bhsd(&tmK, K, batch, heads, seq_kv, k_strides, attn::BKV))) return rc;
+  if ((rc = encode_bhsd(&tmV, V, batch, heads, seq_kv, v_strides, attn::BKV))) return rc;
+  if ((rc = encode_bhsd(&tmO, O, batch, heads, seq_q, o_strides, 32))) return rc;
+  attn::Params prm;
+  prm.seq_q = seq_q;
+  prm.seq_kv = seq_kv;
+  prm.nkv = (int)ceil_div(seq_kv, attn::BKV);
+  prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  prm.status = p->status_dev;
+  prm.timeout_ns = p->timeout_ns;
+  prm.fault_cta = p->fault_unit;
+  const dim3 grid((unsigned)ceil_div(seq_q, attn::BQ), (unsigned)heads, (unsigned)batch);
+  attn::attn_f16_fwd_kernel<<<grid, attn::NUM_THREADS, attn::SMEM_BYTES, (cudaStream_t)stream>>>(
+      tmQ, tmK, tmV, tmO, prm);
+  GF16_CUDA(cudaGetLastError(), "launch attn_f16_fwd_kernel");
+  return GEMM_F16_OK;
+}
+
+}  // extern "C"

@@ -1,4 +1,4 @@
-"""Seeded synthetic FP16 inputs for the GEMM workloads.
+"""Seeded synthetic FP16 inputs for the GEMM and attention workloads.
 
 This module only draws numbers; it holds none of the GEMM's arithmetic, and
 both the oracle side (tests) and the GPU side (tests, bench) take their
@@ -25,6 +25,12 @@ numpy's float64 -> float16 conversion):
 
 Workloads: see ``WORKLOADS`` below.  Each has a fixed stream key; the 4096^3
 case has eight A/B pairs for cache busting, pair p keyed (2 << 32) + p.
+
+Attention workloads (``ATTN_WORKLOADS``): Q, K, V of shape [batch, heads,
+seq, 256] in one stream: Q takes the first B*H*Sq*256 draws (row-major over
+b, h, i, d), K the next B*H*Skv*256, V the next.  Q and K are normal with
+sigma 1 (so a score q.k / 16 has unit variance), V uniform on
+[-1, -1e-3] U [1e-3, 1].
 """
 from __future__ import annotations
 
@@ -152,3 +158,77 @@ def custom(M: int, N: int, K: int, seed: int, split_k: int = 1,
     """
     return _w(f"custom_{M}x{N}x{K}_s{seed}", M, N, K, split_k, dist, scale,
               eps * scale if dist == "uniform_nonzero" else 0.0, [seed])
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """One attention workload: [B, H, S, D] shapes, distributions, seed."""
+    name: str
+    B: int
+    H: int
+    Sq: int
+    Skv: int
+    D: int
+    key: int
+    qk_sigma: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.D))
+
+    @property
+    def flops(self) -> int:
+        """Two products per head: S = Q K^T and O = P V."""
+        return 4 * self.B * self.H * self.Sq * self.Skv * self.D
+
+    def _q0(self):
+        return 0
+
+    def _k0(self):
+        return self.B * self.H * self.Sq * self.D
+
+    def _v0(self):
+        return self._k0() + self.B * self.H * self.Skv * self.D
+
+    def bits(self):
+        """(Q, K, V) as uint16 arrays of shape [B, H, S, D]."""
+        B, H, D = self.B, self.H, self.D
+        q = normal_bits(self.key, self._q0(), B * H * self.Sq * D, self.qk_sigma)
+        k = normal_bits(self.key, self._k0(), B * H * self.Skv * D, self.qk_sigma)
+        v = uniform_nonzero_bits(self.key, self._v0(), B * H * self.Skv * D, 1.0, 1e-3)
+        return (q.reshape(B, H, self.Sq, D), k.reshape(B, H, self.Skv, D),
+                v.reshape(B, H, self.Skv, D))
+
+    def head_bits(self, b: int, h: int, rows=None):
+        """(Q rows, K, V) of one (batch, head), each [1, 1, S, D]; ``rows``
+        selects query rows (same values as in the full tensor)."""
+        D, H = self.D, self.H
+        bh = b * H + h
+        if rows is None:
+            rows = np.arange(self.Sq)
+        rows = np.asarray(rows, dtype=np.int64)
+        q = np.stack([normal_bits(self.key, self._q0() + (bh * self.Sq + int(i)) * D, D,
+                                  self.qk_sigma) for i in rows]) if len(rows) else \
+            np.zeros((0, D), np.uint16)
+        k = normal_bits(self.key, self._k0() + bh * self.Skv * D, self.Skv * D, self.qk_sigma)
+        v = uniform_nonzero_bits(self.key, self._v0() + bh * self.Skv * D, self.Skv * D, 1.0,
+                                 1e-3)
+        return (q.reshape(1, 1, len(rows), D), k.reshape(1, 1, self.Skv, D),
+                v.reshape(1, 1, self.Skv, D))
+
+
+#: Attention forward at head dimension 256 (the pages' HD=256 kernel; they
+#: state no batch, head count or sequence length): a small case the oracle
+#: finishes at once, a ragged case (query and key counts not multiples of
+#: the 128 / 64 blocks) and a throughput case, 4 x 16 heads x 4096 x 4096.
+ATTN_WORKLOADS = {
+    "attn_256": AttnWorkload("attn_256", 1, 2, 256, 256, 256, 10),
+    "attn_ragged": AttnWorkload("attn_ragged", 2, 3, 1000, 1500, 256, 11),
+    "attn_4096": AttnWorkload("attn_4096", 4, 16, 4096, 4096, 256, 12),
+}
+
+
+def attn_custom(B: int, H: int, Sq: int, Skv: int, seed: int, qk_sigma: float = 1.0,
+                D: int = 256) -> AttnWorkload:
+    """An attention workload of any shape with the same generator."""
+    return AttnWorkload(f"attn_{B}x{H}x{Sq}x{Skv}_s{seed}", B, H, Sq, Skv, D, seed, qk_sigma)

@@ -1,5 +1,5 @@
 """CPU-only checks of the C-ABI library: it loads, exports every entry point
-that include/gemm_f16.h declares, and its host-side logic (argument
+that include/gemm_f16.h and include/attn_f16.h declare, and its host-side logic (argument
 validation, tile order) behaves as documented.  No compute call is made.
 """
 from __future__ import annotations
@@ -14,6 +14,7 @@ import async_barrier_pipelined_gb300 as g
 from async_barrier_pipelined_gb300 import build as gbuild
 
 HEADER = os.path.join(gbuild.INCLUDE, "gemm_f16.h")
+HEADERS = [HEADER, os.path.join(gbuild.INCLUDE, "attn_f16.h")]
 
 
 @pytest.fixture(scope="module")
@@ -23,9 +24,11 @@ def lib():
 
 
 def _declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_f16_\w+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:gemm|attn)_f16_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_and_binding_agree():
@@ -215,3 +218,35 @@ def test_validate_layouts(lib, layout, args, code):
     assert g.gemm_f16_validate_ex(layout, *args) == code
     if layout == 0:
         assert g.gemm_f16_validate(*args) == code
+
+
+_ST = (64 * 256, 64 * 256, 256)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 1, 64, 64, 256, P, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.OK),
+    ((4, 16, 4096, 4096, 256, P, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.OK),
+    ((1, 1, 64, 64, 128, P, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.ERR_INVALID_ARG),
+    ((0, 1, 64, 64, 256, P, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.ERR_INVALID_ARG),
+    ((1, 0, 64, 64, 256, P, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.ERR_INVALID_ARG),
+    ((1, 1, 0, 64, 256, P, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.ERR_INVALID_ARG),
+    ((1, 1, 64, 0, 256, P, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.ERR_INVALID_ARG),
+    ((65536, 1, 64, 64, 256, P, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.ERR_INVALID_ARG),
+    ((1, 1, 64, 64, 256, 0, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.ERR_INVALID_ARG),
+    ((1, 1, 64, 64, 256, P, _ST, P, _ST, P, _ST, 0, _ST, 0.0625), g.ERR_INVALID_ARG),
+    ((1, 1, 64, 64, 256, P, (64 * 256, 64 * 256, 128), P, _ST, P, _ST, P, _ST, 0.0625),
+     g.ERR_INVALID_ARG),                                   # row stride < 256
+    ((1, 1, 64, 64, 256, P, (0, 64 * 256, 256), P, _ST, P, _ST, P, _ST, 0.0625),
+     g.ERR_INVALID_ARG),                                   # zero stride
+    ((1, 1, 64, 64, 256, P, _ST, P, _ST, P, _ST, P, _ST, float("inf")), g.ERR_INVALID_ARG),
+    ((1, 1, 64, 64, 256, P + 8, _ST, P, _ST, P, _ST, P, _ST, 0.0625), g.ERR_MISALIGNED),
+    ((1, 1, 64, 64, 256, P, _ST, P, (64 * 256, 64 * 256, 260), P, _ST, P, _ST, 0.0625),
+     g.ERR_MISALIGNED),
+    ((1, 2, 64, 64, 256, P, (64 * 256, 64 * 256 + 4, 256), P, _ST, P, _ST, P, _ST, 0.0625),
+     g.ERR_MISALIGNED),
+    # [B, S, H, D] storage: head stride 256, row stride H * 256
+    ((2, 8, 100, 300, 256, P, (100 * 8 * 256, 256, 8 * 256), P, (300 * 8 * 256, 256, 8 * 256),
+      P, (300 * 8 * 256, 256, 8 * 256), P, (100 * 8 * 256, 256, 8 * 256), 0.0625), g.OK),
+])
+def test_attn_validate(lib, args, code):
+    assert g.attn_f16_validate(*args) == code

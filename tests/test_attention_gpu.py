@@ -1,0 +1,243 @@
+"""GPU parity of the attention forward kernel (attn_f16_fwd) against the FP64
+oracle (oracle.attention_f16).
+
+Criteria as for the GEMM ("Xe2 ESIMD GEMM" page, "Correctness testing"):
+no NaN/Inf first, then relative RMS error < 0.5% and every element within
+1e-2 * (|ref| + 1).  Exact cases pin the data paths: with all keys equal
+the output is the mean of the value rows (exact for small integers and a
+power-of-two key count), and with one-hot keys and a dominant score each
+query copies one value row (exact).  A ramp of scores makes the running
+maximum move in every key block, so the output rescale runs every time.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic_inputs as si
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+D = 256
+
+
+@pytest.fixture(scope="module")
+def plan():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import async_barrier_pipelined_gb300 as g
+    from async_barrier_pipelined_gb300 import build
+    build.build()
+    p = g.Plan(0)
+    yield p
+    p.close()
+
+
+def _dev(bits, layout="bhsd", pad=0):
+    """uint16 [B, H, S, D] bits -> CUDA float16 [B, H, S, D] view.
+
+    layout "bhsd": rows of one head contiguous (row stride D + pad);
+    "bshd": [B, S, H, D] storage seen as [B, H, S, D]."""
+    import torch
+    B, H, S, Dd = bits.shape
+    if layout == "bhsd":
+        host = np.full((B, H, S, Dd + pad), 0x7E00, np.uint16)
+        host[..., :Dd] = bits
+        t = torch.from_numpy(host.view(np.float16)).cuda()
+        return t[..., :Dd]
+    host = np.full((B, S, H, Dd + pad), 0x7E00, np.uint16)
+    host[..., :Dd] = bits.transpose(0, 2, 1, 3)
+    t = torch.from_numpy(host.view(np.float16)).cuda()
+    return t[..., :Dd].transpose(1, 2)
+
+
+def _run(plan, Qb, Kb, Vb, scale=None, layout="bhsd", pad=0, o_layout=None):
+    import torch
+    import async_barrier_pipelined_gb300 as g
+    Q, K, V = _dev(Qb, layout, pad), _dev(Kb, layout, pad), _dev(Vb, layout, pad)
+    B, H, Sq, _ = Qb.shape
+    O = _dev(np.full((B, H, Sq, D), 0x7E00, np.uint16), o_layout or layout, pad)
+    g.attention(plan, Q, K, V, O, scale=scale)
+    torch.cuda.synchronize()
+    st = plan.status()
+    assert st == g.OK, g.gemm_f16_strerror(st)
+    return O.cpu().numpy().astype(np.float64)
+
+
+def _f16(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+# ---------------------------------------------------------------- exact cases
+@pytest.mark.parametrize("shape", [(1, 1, 128, 64), (2, 3, 200, 256), (1, 2, 1, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_equal_keys_give_the_exact_mean(plan, shape):
+    """K = 0: every score is 0, every weight 1, the output the mean of V.
+    Small integers over a power-of-two key count: exact in binary16."""
+    B, H, Sq, Skv = shape
+    rng = np.random.default_rng(Skv)
+    Q = _f16(rng.standard_normal((B, H, Sq, D)))
+    K = np.zeros((B, H, Skv, D), np.uint16)
+    Vv = rng.integers(-8, 9, (B, H, Skv, D)).astype(np.float64)
+    o = _run(plan, Q, K, _f16(Vv))
+    # the exact mean (an integer sum over a power of two), rounded once
+    want = np.broadcast_to(Vv.mean(axis=2, keepdims=True), o.shape)
+    assert np.array_equal(o, want.astype(np.float16).astype(np.float64))
+
+
+@pytest.mark.parametrize("skv", [1, 63, 100, 1000])
+def test_equal_keys_ragged_key_count_masks_the_tail(plan, skv):
+    """A key count that is not a multiple of the 64-key block: the padded
+    keys must get weight 0 (else the mean is taken over too many rows)."""
+    rng = np.random.default_rng(skv + 1)
+    Q = _f16(rng.standard_normal((1, 2, 130, D)))
+    K = np.zeros((1, 2, skv, D), np.uint16)
+    Vb = _f16(rng.integers(-8, 9, (1, 2, skv, D)))
+    o = _run(plan, Q, K, Vb)
+    ref = oracle.attention_f16(Q, K, Vb, 1 / 16)
+    parity.check(o, ref, f"equal keys skv={skv}")
+    # the mean rounded once to binary16, up to one unit in the last place
+    assert np.max(np.abs(o - ref)) <= np.max(np.abs(ref)) * 2 ** -10 + 1e-7
+
+
+@pytest.mark.parametrize("sq,skv", [(256, 256), (300, 200), (129, 65)])
+def test_one_hot_keys_select_value_rows_exactly(plan, sq, skv):
+    """Key j = e_(j mod 256); query i = 320 e_(pi(i)): the matching score is
+    20, every other 0, so every other key's weight is below exp(-20) ~ 2e-9
+    of the match's.  Their total pull on the output is then far below half
+    a binary16 unit of any value row entry of magnitude >= 1/8, so each query
+    returns value row pi(i) exactly (entries are nonzero multiples of 1/8)."""
+    rng = np.random.default_rng(sq * skv)
+    pi = rng.integers(0, skv, sq)
+    Q = np.zeros((1, 1, sq, D))
+    Q[0, 0, np.arange(sq), pi % D] = 320.0
+    K = np.zeros((1, 1, skv, D))
+    K[0, 0, np.arange(skv), np.arange(skv) % D] = 1.0      # skv <= 256: distinct keys
+    Vv = rng.integers(1, 101, (1, 1, skv, D)) * rng.choice([-1.0, 1.0], (1, 1, skv, D)) / 8.0
+    o = _run(plan, _f16(Q), _f16(K), _f16(Vv))
+    assert np.array_equal(o[0, 0], Vv[0, 0, pi])
+
+
+# ---------------------------------------------------------------- workloads
+@pytest.mark.parametrize("name", ["attn_256", "attn_ragged"])
+def test_workloads_full(plan, name):
+    w = si.ATTN_WORKLOADS[name]
+    Qb, Kb, Vb = w.bits()
+    o = _run(plan, Qb, Kb, Vb)
+    parity.check(o, oracle.attention_f16(Qb, Kb, Vb, w.scale), name)
+
+
+def test_attn_4096_sampled_heads(plan):
+    """The throughput workload (4 x 16 x 4096 x 4096) in the launch
+    configuration the benchmark times; sampled rows of three heads."""
+    import torch
+    import async_barrier_pipelined_gb300 as g
+    w = si.ATTN_WORKLOADS["attn_4096"]
+    Qb, Kb, Vb = w.bits()
+    Q, K, V = (torch.from_numpy(x.view(np.float16)).cuda() for x in (Qb, Kb, Vb))
+    O = g.attention(plan, Q, K, V)
+    torch.cuda.synchronize()
+    assert plan.status() == g.OK
+    rng = np.random.default_rng(21)
+    for b, h in ((0, 0), (1, 7), (3, 15)):
+        rows = np.unique(np.concatenate([[0, 1, 127, 128, 4095], rng.choice(4096, 24)]))
+        q, k, v = w.head_bits(b, h, rows)
+        ref = oracle.attention_f16(q, k, v, w.scale)[0, 0]
+        got = O[b, h, torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+        parity.check(got, ref, f"attn_4096 b{b} h{h}")
+
+
+SHAPES = [(1, 1, 1, 1), (1, 1, 1, 1000), (1, 1, 129, 65), (2, 2, 64, 64), (1, 3, 513, 127),
+          (3, 1, 257, 2049)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_shape_sweep(plan, shape):
+    B, H, Sq, Skv = shape
+    w = si.attn_custom(B, H, Sq, Skv, seed=Sq * 31 + Skv)
+    Qb, Kb, Vb = w.bits()
+    parity.check(_run(plan, Qb, Kb, Vb), oracle.attention_f16(Qb, Kb, Vb, w.scale),
+                 f"{shape}")
+
+
+def test_running_max_moves_every_block(plan):
+    """Scores ramp up along the keys, so the row maximum grows in every key
+    block and the accumulator is rescaled every time."""
+    rng = np.random.default_rng(2)
+    Sq, Skv = 200, 1100
+    Q = rng.standard_normal((1, 2, Sq, D))
+    Q[..., 0] = 16.0
+    K = rng.standard_normal((1, 2, Skv, D)) * 0.5
+    K[..., 0] = np.linspace(0, 24, Skv)
+    Vb = _f16(rng.uniform(-1, 1, (1, 2, Skv, D)))
+    Qb, Kb = _f16(Q), _f16(K)
+    parity.check(_run(plan, Qb, Kb, Vb), oracle.attention_f16(Qb, Kb, Vb, 1 / 16), "ramp")
+
+
+@pytest.mark.parametrize("sigma,scale", [(3.0, 1 / 16), (1.0, 0.2), (1.0, -0.05), (1.0, 0.0)])
+def test_peaked_and_odd_scales(plan, sigma, scale):
+    w = si.attn_custom(1, 2, 300, 700, seed=int(sigma * 10 + scale * 100), qk_sigma=sigma)
+    Qb, Kb, Vb = w.bits()
+    parity.check(_run(plan, Qb, Kb, Vb, scale=scale),
+                 oracle.attention_f16(Qb, Kb, Vb, np.float32(scale)), f"sigma {sigma} scale {scale}")
+
+
+@pytest.mark.parametrize("layout,pad", [("bshd", 0), ("bhsd", 40), ("bshd", 8)])
+def test_strided_layouts(plan, layout, pad):
+    """[B, S, H, D] storage and padded rows (padding holds NaN)."""
+    w = si.attn_custom(2, 3, 150, 333, seed=17 + pad)
+    Qb, Kb, Vb = w.bits()
+    o = _run(plan, Qb, Kb, Vb, layout=layout, pad=pad)
+    parity.check(o, oracle.attention_f16(Qb, Kb, Vb, w.scale), f"{layout} pad {pad}")
+
+
+def test_output_rows_outside_untouched(plan):
+    """O with padded rows: the NaN padding and the rows of other heads stay
+    as they were (a ragged last query block must not spill over)."""
+    import torch
+    import async_barrier_pipelined_gb300 as g
+    w = si.attn_custom(1, 2, 100, 80, seed=5)
+    Qb, Kb, Vb = w.bits()
+    Q, K, V = (_dev(x) for x in (Qb, Kb, Vb))
+    big = torch.from_numpy(np.full((1, 2, 100, D + 16), 0x7E00, np.uint16).view(np.float16)).cuda()
+    O = big[..., :D]
+    g.attention(plan, Q, K, V, O)
+    torch.cuda.synchronize()
+    full = big.cpu().numpy().view(np.uint16)
+    assert np.all(full[..., D:] == 0x7E00)
+    parity.check(full[..., :D].view(np.float16).astype(np.float64),
+                 oracle.attention_f16(Qb, Kb, Vb, w.scale), "padded O")
+
+
+def test_repeat_runs_bitwise_identical(plan):
+    w = si.attn_custom(1, 4, 384, 1024, seed=3)
+    Qb, Kb, Vb = w.bits()
+    o0 = _run(plan, Qb, Kb, Vb)
+    for _ in range(5):
+        assert np.array_equal(_run(plan, Qb, Kb, Vb).view(np.uint64), o0.view(np.uint64))
+
+
+def test_invalid_arguments_enqueue_nothing(plan):
+    import torch
+    import async_barrier_pipelined_gb300 as g
+    Q = torch.zeros((1, 1, 64, D), dtype=torch.float16, device="cuda")
+    st = (64 * D, 64 * D, D)
+    ptr = Q.data_ptr()
+    cases = [
+        ((1, 1, 64, 64, 128, ptr, st, ptr, st, ptr, st, ptr, st, 1.0), g.ERR_INVALID_ARG),
+        ((0, 1, 64, 64, D, ptr, st, ptr, st, ptr, st, ptr, st, 1.0), g.ERR_INVALID_ARG),
+        ((1, 1, 0, 64, D, ptr, st, ptr, st, ptr, st, ptr, st, 1.0), g.ERR_INVALID_ARG),
+        ((1, 1, 64, 64, D, ptr + 2, st, ptr, st, ptr, st, ptr, st, 1.0), g.ERR_MISALIGNED),
+        ((1, 1, 64, 64, D, ptr, (64 * D, 64 * D, D + 4), ptr, st, ptr, st, ptr, st, 1.0),
+         g.ERR_MISALIGNED),
+        ((1, 1, 64, 64, D, ptr, st, ptr, st, ptr, st, ptr, st, float("nan")), g.ERR_INVALID_ARG),
+    ]
+    for args, code in cases:
+        with pytest.raises(g.GemmError) as e:
+            g.attn_f16_fwd(plan.handle, *args, stream=0)
+        assert e.value.code == code
+    torch.cuda.synchronize()
+    assert plan.status() == g.OK

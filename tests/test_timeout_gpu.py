@@ -54,3 +54,34 @@ def test_bounded_wait_reports_timeout_and_context_survives(kernel):
             c, _ = gpu_util.run(plan, A, B)
             assert np.array_equal(c, want)
             assert plan.status() == g.OK
+
+
+def test_attention_bounded_wait_reports_timeout_and_context_survives():
+    """The attention kernel: CTA 1's first key tile gets no copy, so the MMA
+    thread's wait runs out; the run must return with ERR_TIMEOUT and the
+    next run on the same context must be correct."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import async_barrier_pipelined_gb300 as g
+    import synthetic_inputs as si
+    from tests import parity
+    from async_barrier_pipelined_gb300 import build
+    build.build()
+    w = si.attn_custom(1, 2, 256, 200, seed=9)
+    Qb, Kb, Vb = w.bits()
+    Q, K, V = (torch.from_numpy(x.view(np.float16)).cuda() for x in (Qb, Kb, Vb))
+    with g.Plan(0) as plan:
+        plan.set_option(g.OPT_TIMEOUT_NS, 20_000_000)
+        plan.set_option(g.OPT_FAULT_UNIT, 1)
+        g.attention(plan, Q, K, V)
+        torch.cuda.synchronize()
+        assert plan.status() == g.ERR_TIMEOUT
+        assert plan.status() == g.OK
+        plan.set_option(g.OPT_FAULT_UNIT, -1)
+        want = oracle.attention_f16(Qb, Kb, Vb, w.scale)
+        for _ in range(2):
+            O = g.attention(plan, Q, K, V)
+            torch.cuda.synchronize()
+            assert plan.status() == g.OK
+            parity.check(O.cpu().numpy().astype(np.float64), want, "after timeout")
