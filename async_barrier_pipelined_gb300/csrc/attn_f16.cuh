@@ -8,9 +8,14 @@
 // row maximum -> P stored to shared memory -> ARRIVE -> [window: the deferred
 // sum update; the next K and V tiles arrive through the copy ring; the next
 // S = Q K^T runs on the tensor core] -> the MMA thread WAITS -> O += P V.
+// P is double-buffered, so the softmax of block j+1 overlaps P V of block j.
+//
 // The output rescale ("compensation") is applied to the TMEM accumulator
-// before P is published, and only when some row's maximum moved (else the
-// factor is exactly 1).
+// before P is published.  Here it is lazy: the exponent offset m a row uses
+// only moves when the block maximum exceeds it by more than RESCALE_LOG2
+// (base-2 units), so weights stay <= 2^RESCALE_LOG2 and the accumulator is
+// touched only when some row of a warp moved its offset.  Numerator and
+// denominator use the same offset, so the result is the same softmax.
 //
 // One CTA per (128 query rows, head, batch), 192 threads:
 //   warp 0      TMA producer: Q once (128 x 256, four 64-column boxes), then
@@ -27,11 +32,11 @@
 //
 // Barriers ("mbarrier State and Operations" page): q_full and full[s] (one
 // arrive.expect_tx + the copies' bytes), empty[s] (one commit), s_full[b]
-// (one commit per S block), p_full (128 softmax threads), o_done (one commit
-// per P V block), mma_done.  Every wait is bounded as in the GEMM kernels:
-// past the time limit the role records GEMM_F16_ERR_TIMEOUT, raises the
-// CTA's abort flag and stops; the CTA drains its copies and MMAs in flight
-// and frees its TMEM before it exits.
+// (one commit per S block), p_full[b] (128 softmax threads), o_done[b] (one
+// commit per P V block) for P buffer b, mma_done.  Every wait is bounded as
+// in the GEMM kernels: past the time limit the role records
+// GEMM_F16_ERR_TIMEOUT, raises the CTA's abort flag and stops; the CTA
+// drains its copies and MMAs in flight and frees its TMEM before it exits.
 
 #pragma once
 
@@ -50,13 +55,13 @@ constexpr uint32_t CHUNK_Q = BQ * 128;            // 64 d-columns x 128 rows: 16
 constexpr uint32_t CHUNK_KV = BKV * 128;          // 64 d-columns x 64 rows: 8 KB
 constexpr uint32_t Q_BYTES = (HD / 64) * CHUNK_Q;       // 64 KB
 constexpr uint32_t TILE_BYTES = (HD / 64) * CHUNK_KV;   // 32 KB
-constexpr uint32_t P_BYTES = BQ * BKV * 2;              // 16 KB
+constexpr uint32_t P_BYTES = BQ * BKV * 2;              // 16 KB per P buffer
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_P = OFF_RING + RING * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
-// q_full, full[RING], empty[RING], s_full[2], p_full, o_done, mma_done
-constexpr uint32_t NUM_BARS = 1 + 2 * RING + 2 + 3;
+constexpr uint32_t OFF_P = OFF_RING + RING * TILE_BYTES;  // two P buffers
+constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+// q_full, full[RING], empty[RING], s_full[2], p_full[2], o_done[2], mma_done
+constexpr uint32_t NUM_BARS = 1 + 2 * RING + 2 + 2 + 2 + 1;
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + room to align the base to 1024
@@ -66,6 +71,10 @@ static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "swizzled buffers need 
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t S_COL = 0;     // S buffers at columns 0 and 64
 constexpr uint32_t O_COL = 256;   // O: columns 256 .. 511
+
+// Lazy rescale threshold: a row's exponent offset moves only when its block
+// maximum (base-2 units) exceeds the offset by more than this.
+constexpr float RESCALE_LOG2 = 8.f;
 
 // Instruction descriptors (kind::f16, FP32 accumulate): S = Q K^T has both
 // operands K-major (Q rows and K rows both run along d); O += P V has A
@@ -187,19 +196,21 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
   for (int j = 0; j < p.nkv && ok; ++j) {
     if (j + 1 < p.nkv && !issue_qk((uint32_t)(j + 1) & 1u)) break;
     // The split barrier's WAIT: P_j is in shared memory and O is rescaled.
-    if (!wait_phase(b.p_full, (uint32_t)j & 1u, p, abort_flag)) break;
+    const uint32_t pb = (uint32_t)j & 1u;
+    if (!wait_phase(b.p_full + 8 * pb, ((uint32_t)j >> 1) & 1u, p, abort_flag)) break;
     ptx::tc_fence_after();
     if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag)) break;
     ptx::tc_fence_after();
     const uint32_t v_addr = base + OFF_RING + pos.stage * TILE_BYTES;
 #pragma unroll
     for (int kk = 0; kk < BKV / 16; ++kk) {
-      ptx::mma_f16(o_tmem, smem_desc_sw128(base + OFF_P + (uint32_t)kk * 32u, 16, 1024),
+      ptx::mma_f16(o_tmem,
+                   smem_desc_sw128(base + OFF_P + pb * P_BYTES + (uint32_t)kk * 32u, 16, 1024),
                    smem_desc_sw128(v_addr + (uint32_t)kk * 2048u, CHUNK_KV, 1024), IDESC_PV,
                    (j > 0 || kk > 0) ? 1u : 0u);
     }
     ptx::mma_commit(b.empty + 8 * pos.stage);
-    ptx::mma_commit(b.o_done);
+    ptx::mma_commit(b.o_done + 8 * pb);
     ring_advance(pos, RING);
   }
 }
@@ -215,6 +226,27 @@ __device__ __forceinline__ float half2_sum(uint32_t v) {
   return f.x + f.y;
 }
 
+// P = 2^(scale*log2(e)*s - m) for one row of a key block, packed to binary16
+// pairs; returns the FP32 sum of the weights (four partial sums).  MASK:
+// keys from `valid` on are past the sequence end and get weight 0.
+template <bool MASK>
+__device__ __forceinline__ float block_weights(const uint32_t (&s)[64], float sl2, float neg_m,
+                                               int valid, uint32_t (&pk)[32]) {
+  float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[2 * c]), sl2, neg_m));
+    float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), sl2, neg_m));
+    if (MASK) {
+      p0 = (2 * c < valid) ? p0 : 0.f;
+      p1 = (2 * c + 1 < valid) ? p1 : 0.f;
+    }
+    pk[c] = pack_half2(p0, p1);
+    l4[c & 3] += p0 + p1;
+  }
+  return (l4[0] + l4[1]) + (l4[2] + l4[3]);
+}
+
 // ------------------------------------------------------------------ softmax + epilogue
 __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Params& p,
                                              uint32_t base, uint32_t tmem_base, const Bars& b,
@@ -223,13 +255,13 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
   const uint32_t quarter = warp & 3u;             // TMEM lanes 32*quarter .. +31
   const uint32_t row = quarter * 32u + lane;      // query row within the tile
   const uint32_t t_lane = (quarter * 32u) << 16;
-  const uint32_t p_row = base + OFF_P + row * 128u;
   const uint32_t sw = row & 7u;
-  float m = -INFINITY;                            // running row max (base-2 units)
+  const float sl2 = p.scale_log2;
+  float m = -INFINITY;                            // exponent offset in use (base-2 units)
   float l = 0.f;                                  // running row sum
   bool ok = true;
   for (int j = 0; j < p.nkv; ++j) {
-    const uint32_t sb = (uint32_t)j & 1u;
+    const uint32_t sb = (uint32_t)j & 1u;         // S buffer = P buffer = j mod 2
     bool got = wait_phase(b.s_full + 8 * sb, ((uint32_t)j >> 1) & 1u, p, abort_flag);
     if (!__all_sync(0xffffffffu, got)) {
       ok = false;
@@ -242,62 +274,83 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
     ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + S_COL + sb * BKV + 32,
                             *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     ptx::tmem_ld_wait();
-    float x[64];
     const int valid = p.seq_kv - j * BKV;  // keys of this block inside the sequence
-    float mx = -INFINITY;
+    const bool ragged = valid < BKV;       // last block of a ragged key count
+    if (ragged) {                          // keep padded keys out of the maximum
+      const float fill = sl2 >= 0.f ? -INFINITY : INFINITY;
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      x[c] = (c < valid) ? __uint_as_float(s[c]) * p.scale_log2 : -INFINITY;
-      mx = fmaxf(mx, x[c]);
+      for (int c = 0; c < 64; ++c)
+        if (c >= valid) s[c] = __float_as_uint(fill);
     }
-    const float m_new = fmaxf(m, mx);
+    // Block maximum of scale * s: eight independent chains over the raw
+    // scores (the minimum when the scale is negative), scaled once.
+    float r8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r8[k] = __uint_as_float(s[k]);
+    if (sl2 >= 0.f) {
+#pragma unroll
+      for (int c = 8; c < 64; ++c) r8[c & 7] = fmaxf(r8[c & 7], __uint_as_float(s[c]));
+#pragma unroll
+      for (int k = 1; k < 8; ++k) r8[0] = fmaxf(r8[0], r8[k]);
+    } else {
+#pragma unroll
+      for (int c = 8; c < 64; ++c) r8[c & 7] = fminf(r8[c & 7], __uint_as_float(s[c]));
+#pragma unroll
+      for (int k = 1; k < 8; ++k) r8[0] = fminf(r8[0], r8[k]);
+    }
+    const float mx = (sl2 == 0.f) ? 0.f : r8[0] * sl2;
+    const float m_new = (mx > m + RESCALE_LOG2) ? mx : m;
     const float alpha = (m_new == m) ? 1.f : ptx::ex2_approx(m - m_new);
     uint32_t pk[32];
-    float lsum = 0.f;
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      pk[c] = pack_half2(ptx::ex2_approx(x[2 * c] - m_new), ptx::ex2_approx(x[2 * c + 1] - m_new));
-      lsum += half2_sum(pk[c]);
+    const float lsum = ragged ? block_weights<true>(s, sl2, -m_new, valid, pk)
+                              : block_weights<false>(s, sl2, -m_new, valid, pk);
+    // P buffer sb was last read by P V of block j-2.
+    if (j >= 2) {
+      got = wait_phase(b.o_done + 8 * sb, ((uint32_t)(j - 2) >> 1) & 1u, p, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
     }
-    if (j > 0) {
-      // P V of the previous block must be done: it reads the P buffer and
-      // writes the O this thread may rescale.
-      got = wait_phase(b.o_done, (uint32_t)(j - 1) & 1u, p, abort_flag);
+    // P row -> shared memory, 128-byte swizzle (16-byte chunk g of row r at
+    // chunk position g ^ (r mod 8)), the K-major layout the MMA reads.
+    const uint32_t p_row = base + OFF_P + sb * P_BYTES + row * 128u;
+#pragma unroll
+    for (uint32_t g = 0; g < 8; ++g)
+      ptx::st_shared_v4(p_row + ((g ^ sw) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
+                        pk[4 * g + 3]);
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // Compensation: O *= alpha once P V of block j-1 has landed in O.
+      const uint32_t ob = (uint32_t)(j - 1) & 1u;
+      got = wait_phase(b.o_done + 8 * ob, ((uint32_t)(j - 1) >> 1) & 1u, p, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t o[32];
-          const uint32_t ta = tmem_base + t_lane + O_COL + (uint32_t)c * 32u;
-          ptx::tmem_ld_32x32b_x32(ta, o);
-          ptx::tmem_ld_wait();
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        const uint32_t ta = tmem_base + t_lane + O_COL + (uint32_t)c * 32u;
+        ptx::tmem_ld_32x32b_x32(ta, o);
+        ptx::tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          ptx::tmem_st_32x32b_x32(ta, o);
-        }
-        ptx::tmem_st_wait();
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        ptx::tmem_st_32x32b_x32(ta, o);
       }
+      ptx::tmem_st_wait();
     }
-    // P row -> shared memory, 128-byte swizzle (16-byte chunk g of row r at
-    // chunk position g ^ (r mod 8)), the K-major layout the MMA reads.
-#pragma unroll
-    for (uint32_t g = 0; g < 8; ++g)
-      ptx::st_shared_v4(p_row + ((g ^ sw) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
-                        pk[4 * g + 3]);
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     // The split barrier's ARRIVE ...
-    ptx::mbar_arrive(b.p_full);
+    ptx::mbar_arrive(b.p_full + 8 * sb);
     // ... and the window: the deferred sum update.
     l = l * alpha + lsum;
     m = m_new;
   }
   if (ok) {
-    const bool got = wait_phase(b.o_done, (uint32_t)(p.nkv - 1) & 1u, p, abort_flag);
+    const uint32_t ob = (uint32_t)(p.nkv - 1) & 1u;
+    const bool got = wait_phase(b.o_done + 8 * ob, ((uint32_t)(p.nkv - 1) >> 1) & 1u, p, abort_flag);
     ok = __all_sync(0xffffffffu, got);
   }
   if (ok) {
@@ -371,8 +424,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   b.empty = b.full + 8 * RING;
   b.s_full = b.empty + 8 * RING;
   b.p_full = b.s_full + 16;
-  b.o_done = b.p_full + 8;
-  b.mma_done = b.o_done + 8;
+  b.o_done = b.p_full + 16;
+  b.mma_done = b.o_done + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
 
   if (warp == 0 && lane == 0) {
@@ -387,8 +440,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     ptx::mbar_init(b.s_full, 1);
     ptx::mbar_init(b.s_full + 8, 1);
-    ptx::mbar_init(b.p_full, SM_THREADS);
-    ptx::mbar_init(b.o_done, 1);
+    for (int k = 0; k < 2; ++k) {
+      ptx::mbar_init(b.p_full + 8 * k, SM_THREADS);
+      ptx::mbar_init(b.o_done + 8 * k, 1);
+    }
     ptx::mbar_init(b.mma_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
