@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(LIB_DIR, "libgemm_f16.so")
 SOURCES = [os.path.join(CSRC, "gemm_f16.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "schedule.h"),
                      os.path.join(CSRC, "gemm_pair.cuh"), os.path.join(CSRC, "gemm_pair_wide.cuh"),
-                     os.path.join(CSRC, "attn_f16.cuh"), os.path.join(INCLUDE, "gemm_f16.h"),
+                     os.path.join(CSRC, "attn_f16.cuh"),
+                     os.path.join(CSRC, "attn_pair.cuh"), os.path.join(INCLUDE, "gemm_f16.h"),
                      os.path.join(INCLUDE, "attn_f16.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

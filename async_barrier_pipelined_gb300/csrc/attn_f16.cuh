@@ -20,11 +20,11 @@
 // One CTA per (128 query rows, head, batch), 192 threads:
 //   warp 0      TMA producer: Q once (128 x 256, four 64-column boxes), then
 //               K and V tiles (64 x 256, 32 KB) into a 4-slot ring in the
-//               order the MMA thread consumes them: K0, K1, V0, K2, V1, ...
-//   warp 1      allocates 512 TMEM columns (S double buffer 2 x 64, O 256)
-//               and one lane issues the MMAs: S_j+1 = Q K_j+1^T (128x64x16,
-//               x16) ahead of O += P_j V_j (128x256x16, x4), releasing ring
-//               slots with tcgen05.commit.
+//               order the MMA thread consumes them: K0, K1, K2, V0, K3, V1, ...
+//   warp 1      allocates 512 TMEM columns (three 64-column S buffers, O in
+//               256) and one lane issues the MMAs: S_j+2 = Q K_j+2^T
+//               (128x64x16, x16) two blocks ahead of O += P_j V_j
+//               (128x256x16, x4), releasing ring slots with tcgen05.commit.
 //   warps 2..5  softmax + epilogue: one query row per thread (its TMEM
 //               lane).  Row max / exp2 / row sum in FP32, P rounded to
 //               binary16 into shared memory, final O / l rounded to binary16
@@ -60,17 +60,22 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = OFF_Q + Q_BYTES;
 constexpr uint32_t OFF_P = OFF_RING + RING * TILE_BYTES;  // two P buffers
 constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
-// q_full, full[RING], empty[RING], s_full[2], p_full[2], o_done[2], mma_done
-constexpr uint32_t NUM_BARS = 1 + 2 * RING + 2 + 2 + 2 + 1;
+// q_full, full[RING], empty[RING], s_full[3], p_full[2], o_done[2], mma_done
+constexpr uint32_t NUM_BARS = 1 + 2 * RING + 3 + 2 + 2 + 1;
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + room to align the base to 1024
 static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit per CTA");
 static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "swizzled buffers need 1024-B alignment");
 
+// S = Q K^T runs LOOKAHEAD key blocks ahead of the softmax, so S needs
+// LOOKAHEAD + 1 buffers in TMEM.
+constexpr int LOOKAHEAD = 2;
+constexpr int S_BUFS = LOOKAHEAD + 1;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 0;     // S buffers at columns 0 and 64
+constexpr uint32_t S_COL = 0;     // S buffers at columns 0, 64, 128
 constexpr uint32_t O_COL = 256;   // O: columns 256 .. 511
+static_assert(S_COL + S_BUFS * BKV <= O_COL, "S buffers overlap O in TMEM");
 
 // Lazy rescale threshold: a row's exponent offset moves only when its block
 // maximum (base-2 units) exceeds the offset by more than this.
@@ -132,33 +137,29 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmQ, const CUte
 
   RingPos pos{0, 0};
   uint32_t issued = 0;
-  // Tile t of the consumption order: K_0, then for each j: K_{j+1}, V_j.
-  const int ntiles = 2 * p.nkv;
-  for (int t = 0; t < ntiles; ++t) {
-    int j;
-    bool is_k;
-    if (t == 0) {
-      j = 0;
-      is_k = true;
-    } else if (t == ntiles - 1) {
-      j = p.nkv - 1;
-      is_k = false;
-    } else {
-      is_k = (t & 1) != 0;              // odd: K_{(t+1)/2}; even: V_{t/2 - 1}
-      j = is_k ? (t + 1) / 2 : t / 2 - 1;
-    }
-    if (!wait_phase(b.empty + 8 * pos.stage, producer_wait_parity(pos), p, abort_flag)) break;
+  // One K or V tile into the next ring slot.
+  auto load = [&](const CUtensorMap* tm, int j) -> bool {
+    if (!wait_phase(b.empty + 8 * pos.stage, producer_wait_parity(pos), p, abort_flag))
+      return false;
     const uint32_t fb = b.full + 8 * pos.stage;
     ptx::mbar_arrive_expect_tx_relaxed(fb, TILE_BYTES);
-    if (!(fault && t == 0)) {
+    if (!(fault && issued == 0)) {
       const uint32_t dst = base + OFF_RING + pos.stage * TILE_BYTES;
-      const CUtensorMap* tm = is_k ? tmK : tmV;
 #pragma unroll
       for (int c = 0; c < HD / 64; ++c)
         ptx::tma_load_4d(dst + c * CHUNK_KV, tm, fb, 64 * c, j * BKV, h, bz);
     }
     ++issued;
     ring_advance(pos, RING);
+    return true;
+  };
+  // The MMA thread's consumption order: K_0 .. K_{LOOKAHEAD-1}, then for
+  // each block j: K_{j+LOOKAHEAD}, V_j.
+  bool ok = true;
+  for (int t = 0; t < LOOKAHEAD && t < p.nkv && ok; ++t) ok = load(tmK, t);
+  for (int j = 0; j < p.nkv && ok; ++j) {
+    if (j + LOOKAHEAD < p.nkv) ok = load(tmK, j + LOOKAHEAD);
+    if (ok) ok = load(tmV, j);
   }
   *pos_out = pos;
   *issued_out = issued;
@@ -192,9 +193,12 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
     return true;
   };
 
-  bool ok = issue_qk(0);
+  bool ok = true;
+  for (int t = 0; t < LOOKAHEAD && t < p.nkv && ok; ++t) ok = issue_qk((uint32_t)t % S_BUFS);
   for (int j = 0; j < p.nkv && ok; ++j) {
-    if (j + 1 < p.nkv && !issue_qk((uint32_t)(j + 1) & 1u)) break;
+    // S two blocks ahead: it runs on the tensor core while the softmax
+    // warps work on block j and P V of block j-1 drains.
+    if (j + LOOKAHEAD < p.nkv && !issue_qk((uint32_t)(j + LOOKAHEAD) % S_BUFS)) break;
     // The split barrier's WAIT: P_j is in shared memory and O is rescaled.
     const uint32_t pb = (uint32_t)j & 1u;
     if (!wait_phase(b.p_full + 8 * pb, ((uint32_t)j >> 1) & 1u, p, abort_flag)) break;
@@ -226,15 +230,16 @@ __device__ __forceinline__ float half2_sum(uint32_t v) {
   return f.x + f.y;
 }
 
-// P = 2^(scale*log2(e)*s - m) for one row of a key block, packed to binary16
-// pairs; returns the FP32 sum of the weights (four partial sums).  MASK:
-// keys from `valid` on are past the sequence end and get weight 0.
-template <bool MASK>
-__device__ __forceinline__ float block_weights(const uint32_t (&s)[64], float sl2, float neg_m,
-                                               int valid, uint32_t (&pk)[32]) {
+// P = 2^(scale*log2(e)*s - m) for one row of a key block of NCOL keys,
+// packed to binary16 pairs; returns the FP32 sum of the weights (four
+// partial sums).  MASK: keys from `valid` on are past the sequence end and
+// get weight 0.
+template <int NCOL, bool MASK>
+__device__ __forceinline__ float block_weights(const uint32_t (&s)[NCOL], float sl2, float neg_m,
+                                               int valid, uint32_t (&pk)[NCOL / 2]) {
   float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
+  for (int c = 0; c < NCOL / 2; ++c) {
     float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[2 * c]), sl2, neg_m));
     float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), sl2, neg_m));
     if (MASK) {
@@ -245,6 +250,41 @@ __device__ __forceinline__ float block_weights(const uint32_t (&s)[64], float sl
     l4[c & 3] += p0 + p1;
   }
   return (l4[0] + l4[1]) + (l4[2] + l4[3]);
+}
+
+// Exponent offset update of one row for a key block (base-2 units):
+// `s` holds the raw scores, keys from `valid` on excluded.  Returns the new
+// offset (moved only when the block maximum passes m + RESCALE_LOG2) and
+// sets `alpha` = 2^(m - m_new), exactly 1 when the offset stays.
+template <int NCOL>
+__device__ __forceinline__ float block_offset(uint32_t (&s)[NCOL], float sl2, int valid, float m,
+                                              float* alpha) {
+  if (valid < NCOL) {  // keep padded keys out of the maximum
+    const float fill = sl2 >= 0.f ? -INFINITY : INFINITY;
+#pragma unroll
+    for (int c = 0; c < NCOL; ++c)
+      if (c >= valid) s[c] = __float_as_uint(fill);
+  }
+  // eight independent chains over the raw scores (the minimum when the
+  // scale is negative), scaled once
+  float r8[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) r8[k] = __uint_as_float(s[k]);
+  if (sl2 >= 0.f) {
+#pragma unroll
+    for (int c = 8; c < NCOL; ++c) r8[c & 7] = fmaxf(r8[c & 7], __uint_as_float(s[c]));
+#pragma unroll
+    for (int k = 1; k < 8; ++k) r8[0] = fmaxf(r8[0], r8[k]);
+  } else {
+#pragma unroll
+    for (int c = 8; c < NCOL; ++c) r8[c & 7] = fminf(r8[c & 7], __uint_as_float(s[c]));
+#pragma unroll
+    for (int k = 1; k < 8; ++k) r8[0] = fminf(r8[0], r8[k]);
+  }
+  const float mx = (sl2 == 0.f) ? 0.f : r8[0] * sl2;
+  const float m_new = (mx > m + RESCALE_LOG2) ? mx : m;
+  *alpha = (m_new == m) ? 1.f : ptx::ex2_approx(m - m_new);
+  return m_new;
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
@@ -261,8 +301,9 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
   float l = 0.f;                                  // running row sum
   bool ok = true;
   for (int j = 0; j < p.nkv; ++j) {
-    const uint32_t sb = (uint32_t)j & 1u;         // S buffer = P buffer = j mod 2
-    bool got = wait_phase(b.s_full + 8 * sb, ((uint32_t)j >> 1) & 1u, p, abort_flag);
+    const uint32_t sb = (uint32_t)j % S_BUFS;     // S buffer
+    const uint32_t pb = (uint32_t)j & 1u;         // P buffer
+    bool got = wait_phase(b.s_full + 8 * sb, ((uint32_t)j / S_BUFS) & 1u, p, abort_flag);
     if (!__all_sync(0xffffffffu, got)) {
       ok = false;
       break;
@@ -275,38 +316,14 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
                             *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     ptx::tmem_ld_wait();
     const int valid = p.seq_kv - j * BKV;  // keys of this block inside the sequence
-    const bool ragged = valid < BKV;       // last block of a ragged key count
-    if (ragged) {                          // keep padded keys out of the maximum
-      const float fill = sl2 >= 0.f ? -INFINITY : INFINITY;
-#pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (c >= valid) s[c] = __float_as_uint(fill);
-    }
-    // Block maximum of scale * s: eight independent chains over the raw
-    // scores (the minimum when the scale is negative), scaled once.
-    float r8[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) r8[k] = __uint_as_float(s[k]);
-    if (sl2 >= 0.f) {
-#pragma unroll
-      for (int c = 8; c < 64; ++c) r8[c & 7] = fmaxf(r8[c & 7], __uint_as_float(s[c]));
-#pragma unroll
-      for (int k = 1; k < 8; ++k) r8[0] = fmaxf(r8[0], r8[k]);
-    } else {
-#pragma unroll
-      for (int c = 8; c < 64; ++c) r8[c & 7] = fminf(r8[c & 7], __uint_as_float(s[c]));
-#pragma unroll
-      for (int k = 1; k < 8; ++k) r8[0] = fminf(r8[0], r8[k]);
-    }
-    const float mx = (sl2 == 0.f) ? 0.f : r8[0] * sl2;
-    const float m_new = (mx > m + RESCALE_LOG2) ? mx : m;
-    const float alpha = (m_new == m) ? 1.f : ptx::ex2_approx(m - m_new);
+    float alpha;
+    const float m_new = block_offset<BKV>(s, sl2, valid, m, &alpha);
     uint32_t pk[32];
-    const float lsum = ragged ? block_weights<true>(s, sl2, -m_new, valid, pk)
-                              : block_weights<false>(s, sl2, -m_new, valid, pk);
-    // P buffer sb was last read by P V of block j-2.
+    const float lsum = valid < BKV ? block_weights<BKV, true>(s, sl2, -m_new, valid, pk)
+                                   : block_weights<BKV, false>(s, sl2, -m_new, valid, pk);
+    // P buffer pb was last read by P V of block j-2.
     if (j >= 2) {
-      got = wait_phase(b.o_done + 8 * sb, ((uint32_t)(j - 2) >> 1) & 1u, p, abort_flag);
+      got = wait_phase(b.o_done + 8 * pb, ((uint32_t)(j - 2) >> 1) & 1u, p, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
@@ -314,7 +331,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
     }
     // P row -> shared memory, 128-byte swizzle (16-byte chunk g of row r at
     // chunk position g ^ (r mod 8)), the K-major layout the MMA reads.
-    const uint32_t p_row = base + OFF_P + sb * P_BYTES + row * 128u;
+    const uint32_t p_row = base + OFF_P + pb * P_BYTES + row * 128u;
 #pragma unroll
     for (uint32_t g = 0; g < 8; ++g)
       ptx::st_shared_v4(p_row + ((g ^ sw) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
@@ -343,7 +360,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     // The split barrier's ARRIVE ...
-    ptx::mbar_arrive(b.p_full + 8 * sb);
+    ptx::mbar_arrive(b.p_full + 8 * pb);
     // ... and the window: the deferred sum update.
     l = l * alpha + lsum;
     m = m_new;
@@ -423,7 +440,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   b.full = b.q_full + 8;
   b.empty = b.full + 8 * RING;
   b.s_full = b.empty + 8 * RING;
-  b.p_full = b.s_full + 16;
+  b.p_full = b.s_full + 8 * S_BUFS;
   b.o_done = b.p_full + 16;
   b.mma_done = b.o_done + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
@@ -438,8 +455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(b.full + 8 * s, 1);
       ptx::mbar_init(b.empty + 8 * s, 1);
     }
-    ptx::mbar_init(b.s_full, 1);
-    ptx::mbar_init(b.s_full + 8, 1);
+    for (int k = 0; k < S_BUFS; ++k) ptx::mbar_init(b.s_full + 8 * k, 1);
     for (int k = 0; k < 2; ++k) {
       ptx::mbar_init(b.p_full + 8 * k, SM_THREADS);
       ptx::mbar_init(b.o_done + 8 * k, 1);

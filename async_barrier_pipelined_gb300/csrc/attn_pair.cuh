@@ -1,0 +1,444 @@
+// CTA-pair variant of the attention forward kernel (tcgen05 cta_group::2),
+// head dimension 256, blocks of 128 keys.
+//
+// A cluster of two CTAs handles 256 query rows of one (batch, head): CTA r
+// holds rows 128r .. 128r+127 (its Q tile in shared memory, its rows of S
+// and O in its tensor memory) and the even CTA ("leader") issues the MMAs
+// for both:
+//   S = Q K^T   256 x 128 x 16, 16 per key block; B (the key block) is split
+//               by keys: CTA r holds keys 64r .. 64r+63 of the block.
+//   O += P V    256 x 256 x 16, 8 per key block; B (the value block) is
+//               split by columns: CTA r holds d = 128r .. 128r+127.
+// Each SM so takes in 32 KB of K and 32 KB of V per 128 keys -- half of
+// what the single-CTA kernel needs for the same work -- and the S MMAs are
+// 128 keys wide (a 64-wide S MMA runs at two thirds of the tensor rate).
+// The softmax (one query row per thread, four warps per CTA) and the
+// split-barrier schedule are those of the single-CTA kernel: S of block
+// j+1 runs on the tensor core while the softmax works on block j; P is
+// published with an ARRIVE and the leader's MMA thread WAITs for both CTAs
+// before O += P V.
+//
+// Barriers ("mbarrier State and Operations" page):
+//   q_full, full[s]  leader only: its producer's arrive.expect_tx for both
+//                    CTAs' bytes; both CTAs' copies complete them.
+//   empty[s]         both: the leader's commit, multicast to the pair.
+//   s_full[b]        both: multicast commit when S buffer b is written.
+//   p_full           leader only: one arrival per softmax warp of either
+//                    CTA (8 per phase) once its P rows are in shared memory.
+//   o_done           both: multicast commit when O += P V of a block ends.
+//   mma_done         leader only: the last commit, waited before TMEM is freed.
+// Every wait is bounded; after an abort the leader completes the phases of
+// copies in flight (as the pair GEMM kernel does) before either CTA exits.
+
+#pragma once
+
+namespace gf16 {
+namespace attnp {
+
+using attn::block_offset;
+using attn::block_weights;
+using attn::HD;
+using attn::pack_half2;
+
+constexpr int CQ = 128;                 // query rows per CTA
+constexpr int PQ = 2 * CQ;              // query rows per pair
+constexpr int BKV = 128;                // keys per block
+constexpr int RING = 4;                 // K / V half-tiles in flight per CTA
+constexpr int NUM_THREADS = 192;
+constexpr int SM_WARPS = 4;             // softmax warps 2..5
+
+constexpr uint32_t CHUNK_Q = CQ * 128;                 // 64 d x 128 rows: 16 KB
+constexpr uint32_t Q_BYTES = (HD / 64) * CHUNK_Q;      // 64 KB
+constexpr uint32_t K_CHUNK = (BKV / 2) * 128;          // 64 d x 64 keys: 8 KB
+constexpr uint32_t V_CHUNK = BKV * 128;                // 64 d x 128 keys: 16 KB
+constexpr uint32_t SLOT_BYTES = 32768;                 // a K half (4 chunks) or a V half (2)
+constexpr uint32_t P_CHUNK = CQ * 128;                 // 64 keys x 128 rows: 16 KB
+constexpr uint32_t P_BYTES = 2 * P_CHUNK;              // 32 KB
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_RING = OFF_Q + Q_BYTES;
+constexpr uint32_t OFF_P = OFF_RING + RING * SLOT_BYTES;
+constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
+// q_full, full[RING], empty[RING], s_full[2], p_full, o_done, mma_done
+constexpr uint32_t NUM_BARS = 1 + 2 * RING + 2 + 3;
+constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
+constexpr uint32_t OFF_PEER_ISSUED = OFF_ABORT + 4;
+constexpr uint32_t SMEM_BYTES = OFF_PEER_ISSUED + 4 + 1024;
+static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit per CTA");
+static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "swizzled buffers need 1024-B alignment");
+static_assert((HD / 64) * K_CHUNK == SLOT_BYTES && 2 * V_CHUNK == SLOT_BYTES, "slot sizes");
+
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL = 0;     // S buffers at columns 0 and 128
+constexpr uint32_t O_COL = 256;   // O: columns 256 .. 511
+
+// kind::f16, FP32 accumulate, M = 256 (the pair): S = Q K^T with both
+// operands K-major; O += P V with P K-major and V MN-major.
+constexpr uint32_t IDESC_QK = (1u << 4) | ((uint32_t)(BKV >> 3) << 17) | ((uint32_t)(PQ >> 4) << 24);
+constexpr uint32_t IDESC_PV =
+    (1u << 4) | (1u << 16) | ((uint32_t)(HD >> 3) << 17) | ((uint32_t)(PQ >> 4) << 24);
+
+struct Params {
+  int seq_q, seq_kv;
+  int nkv;                      // key blocks: ceil(seq_kv / 128)
+  float scale_log2;
+  int* status;
+  unsigned long long timeout_ns;
+  int fault_pair;               // test only: pair whose first ring fill gets no copy
+};
+
+struct Bars {
+  uint32_t q_full, full, empty, s_full, p_full, o_done, mma_done;
+};
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
+                                           volatile int* abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return attn::wait_slow(bar, parity, p.status, p.timeout_ns, abort_flag);
+}
+
+// Wait for a phase completed by release arrivals from either CTA.
+__device__ __noinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, const Params& p,
+                                                volatile int* abort_flag) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer() - t0 > p.timeout_ns) {
+      *abort_flag = 1;
+      *(volatile int*)p.status = (int)GEMM_F16_ERR_TIMEOUT;
+      __threadfence_system();
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ producer
+// Both CTAs: copy this CTA's halves of the K and V blocks, in the order the
+// MMA thread consumes them (K_0, then per block j: K_{j+1}, V_j), crediting
+// the leader's barriers; the leader also arrives (expect_tx) for the pair.
+// Returns the ring fills issued.
+__device__ __forceinline__ uint32_t producer_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                                  const CUtensorMap* tmV, const Params& p,
+                                                  uint32_t base, const Bars& b, uint32_t rank,
+                                                  int q0, int h, int bz, bool fault,
+                                                  volatile int* abort_flag) {
+  const uint32_t leader_q = ptx::map_to_cta(b.q_full, 0);
+  const uint32_t leader_full = ptx::map_to_cta(b.full, 0);
+  if (rank == 0) ptx::mbar_arrive_expect_tx_relaxed(b.q_full, 2 * Q_BYTES);
+#pragma unroll
+  for (int c = 0; c < HD / 64; ++c)
+    ptx::tma_load_4d_pair(base + OFF_Q + c * CHUNK_Q, tmQ, leader_q, 64 * c, q0 + (int)rank * CQ,
+                          h, bz);
+
+  RingPos pos{0, 0};
+  uint32_t issued = 0;
+  auto fill = [&](bool is_k, int j) -> bool {
+    if (!wait_phase(b.empty + 8 * pos.stage, producer_wait_parity(pos), p, abort_flag))
+      return false;
+    if (rank == 0) ptx::mbar_arrive_expect_tx_relaxed(b.full + 8 * pos.stage, 2 * SLOT_BYTES);
+    if (!(fault && issued == 0 && rank == 0)) {
+      const uint32_t dst = base + OFF_RING + pos.stage * SLOT_BYTES;
+      const uint32_t fb = leader_full + 8 * pos.stage;
+      if (is_k) {
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c)
+          ptx::tma_load_4d_pair(dst + c * K_CHUNK, tmK, fb, 64 * c, j * BKV + (int)rank * (BKV / 2),
+                                h, bz);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_4d_pair(dst + c * V_CHUNK, tmV, fb, (int)rank * 128 + 64 * c, j * BKV, h,
+                                bz);
+      }
+    }
+    ++issued;
+    ring_advance(pos, RING);
+    return true;
+  };
+  bool ok = fill(true, 0);
+  for (int j = 0; j < p.nkv && ok; ++j) {
+    if (j + 1 < p.nkv) ok = fill(true, j + 1);
+    if (ok) ok = fill(false, j);
+  }
+  return issued;
+}
+
+// ------------------------------------------------------------------ MMA issuer (leader)
+__device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_t tmem_base,
+                                         const Bars& b, volatile int* abort_flag) {
+  if (!wait_phase(b.q_full, 0, p, abort_flag)) return;
+  ptx::tc_fence_after();
+  RingPos pos{0, 0};
+  const uint32_t q_addr = base + OFF_Q;
+  const uint32_t o_tmem = tmem_base + O_COL;
+
+  auto issue_qk = [&](uint32_t sb) -> bool {
+    if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag))
+      return false;
+    ptx::tc_fence_after();
+    const uint32_t k_addr = base + OFF_RING + pos.stage * SLOT_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      const uint32_t off_q = (uint32_t)(kk >> 2) * CHUNK_Q + (uint32_t)(kk & 3) * 32u;
+      const uint32_t off_k = (uint32_t)(kk >> 2) * K_CHUNK + (uint32_t)(kk & 3) * 32u;
+      ptx::mma_f16_pair(tmem_base + S_COL + sb * BKV, smem_desc_sw128(q_addr + off_q, 16, 1024),
+                        smem_desc_sw128(k_addr + off_k, 16, 1024), IDESC_QK, kk > 0 ? 1u : 0u);
+    }
+    ptx::mma_commit_pair(b.empty + 8 * pos.stage, 0x3);
+    ptx::mma_commit_pair(b.s_full + 8 * sb, 0x3);
+    ring_advance(pos, RING);
+    return true;
+  };
+
+  bool ok = issue_qk(0);
+  for (int j = 0; j < p.nkv && ok; ++j) {
+    if (j + 1 < p.nkv && !issue_qk((uint32_t)(j + 1) & 1u)) break;
+    // The split barrier's WAIT: both CTAs' P rows are in shared memory.
+    if (!wait_phase_cluster(b.p_full, (uint32_t)j & 1u, p, abort_flag)) break;
+    ptx::tc_fence_after();
+    if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag)) break;
+    ptx::tc_fence_after();
+    const uint32_t v_addr = base + OFF_RING + pos.stage * SLOT_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < BKV / 16; ++kk) {
+      const uint32_t off_p = (uint32_t)(kk >> 2) * P_CHUNK + (uint32_t)(kk & 3) * 32u;
+      ptx::mma_f16_pair(o_tmem, smem_desc_sw128(base + OFF_P + off_p, 16, 1024),
+                        smem_desc_sw128(v_addr + (uint32_t)kk * 2048u, V_CHUNK, 1024), IDESC_PV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+    }
+    ptx::mma_commit_pair(b.empty + 8 * pos.stage, 0x3);
+    ptx::mma_commit_pair(b.o_done, 0x3);
+    ring_advance(pos, RING);
+  }
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+__device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Params& p,
+                                             uint32_t base, uint32_t tmem_base, const Bars& b,
+                                             uint32_t rank, uint32_t warp, uint32_t lane, int q0,
+                                             int h, int bz, volatile int* abort_flag) {
+  const uint32_t quarter = warp & 3u;
+  const uint32_t row = quarter * 32u + lane;      // row within this CTA's 128
+  const uint32_t t_lane = (quarter * 32u) << 16;
+  const uint32_t sw = row & 7u;
+  const uint32_t leader_p_full = ptx::map_to_cta(b.p_full, 0);
+  const float sl2 = p.scale_log2;
+  float m = -INFINITY;
+  float l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < p.nkv; ++j) {
+    const uint32_t sb = (uint32_t)j & 1u;
+    bool got = wait_phase(b.s_full + 8 * sb, ((uint32_t)j >> 1) & 1u, p, abort_flag);
+    if (!__all_sync(0xffffffffu, got)) {
+      ok = false;
+      break;
+    }
+    ptx::tc_fence_after();
+    uint32_t s[BKV];
+#pragma unroll
+    for (int c = 0; c < BKV / 32; ++c)
+      ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + S_COL + sb * BKV + 32u * c,
+                              *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
+    ptx::tmem_ld_wait();
+    const int valid = p.seq_kv - j * BKV;
+    float alpha;
+    const float m_new = block_offset<BKV>(s, sl2, valid, m, &alpha);
+    uint32_t pk[BKV / 2];
+    const float lsum = valid < BKV ? block_weights<BKV, true>(s, sl2, -m_new, valid, pk)
+                                   : block_weights<BKV, false>(s, sl2, -m_new, valid, pk);
+    if (j > 0) {
+      // O += P V of block j-1 has ended: the P buffer is free and O stable.
+      got = wait_phase(b.o_done, (uint32_t)(j - 1) & 1u, p, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+    }
+    // P row -> shared memory: keys 0-63 and 64-127 in two 128-byte-swizzled
+    // chunks (16-byte group g of row r at position g ^ (r mod 8)).
+#pragma unroll
+    for (uint32_t g = 0; g < 16; ++g)
+      ptx::st_shared_v4(base + OFF_P + (g >> 3) * P_CHUNK + row * 128u + (((g & 7u) ^ sw) << 4),
+                        pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        const uint32_t ta = tmem_base + t_lane + O_COL + (uint32_t)c * 32u;
+        ptx::tmem_ld_32x32b_x32(ta, o);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        ptx::tmem_st_32x32b_x32(ta, o);
+      }
+      ptx::tmem_st_wait();
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncwarp();
+    // The split barrier's ARRIVE (one per warp, on the leader's barrier) ...
+    if (lane == 0) {
+      if (rank == 0)
+        ptx::mbar_arrive(b.p_full);
+      else
+        ptx::mbar_arrive_cluster(leader_p_full);
+    }
+    // ... and the window: the deferred sum update.
+    l = l * alpha + lsum;
+    m = m_new;
+  }
+  if (ok) {
+    const bool got = wait_phase(b.o_done, (uint32_t)(p.nkv - 1) & 1u, p, abort_flag);
+    ok = __all_sync(0xffffffffu, got);
+  }
+  if (ok) {
+    ptx::tc_fence_after();
+    const float inv_l = 1.f / l;
+    // Staging in the Q buffer (every MMA has completed): per warp 4 boxes of
+    // 32 rows x 64 columns, 128-byte swizzle.
+    const uint32_t stage = base + OFF_Q + quarter * 4u * 4096u;
+    const uint32_t lsw = lane & 7u;
+#pragma unroll 1
+    for (int c = 0; c < HD / 32; ++c) {
+      uint32_t o[32];
+      ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + O_COL + (uint32_t)c * 32u, o);
+      ptx::tmem_ld_wait();
+      const uint32_t box = stage + (uint32_t)(c >> 1) * 4096u + lane * 128u;
+#pragma unroll
+      for (uint32_t i = 0; i < 4; ++i) {
+        const uint32_t g = (uint32_t)(c & 1) * 4u + i;
+        const float* f = reinterpret_cast<const float*>(&o[8 * i]);
+        ptx::st_shared_v4(box + ((g ^ lsw) << 4), pack_half2(f[0] * inv_l, f[1] * inv_l),
+                          pack_half2(f[2] * inv_l, f[3] * inv_l),
+                          pack_half2(f[4] * inv_l, f[5] * inv_l),
+                          pack_half2(f[6] * inv_l, f[7] * inv_l));
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    const int r0 = q0 + (int)rank * CQ + (int)quarter * 32;
+    if (lane == 0 && r0 < p.seq_q) {
+#pragma unroll
+      for (int bx = 0; bx < HD / 64; ++bx)
+        ptx::tma_store_4d(tmO, stage + (uint32_t)bx * 4096u, 64 * bx, r0, h, bz);
+      ptx::bulk_commit_group();
+      ptx::bulk_wait_group_read<0>();
+    }
+    __syncwarp();
+  }
+}
+
+// After both CTAs stopped issuing: complete every ring phase a producer
+// opened and wait (bounded) for the copies that were issued, then for Q.
+// Fill f used slot f % RING in phase parity (f / RING) & 1.  A fill the
+// leader never reached lacks its arrival: arrive expecting only the peer's
+// bytes.  A fill the peer never issued leaves its bytes expected: take them
+// off with complete_tx.
+__device__ __noinline__ void leader_drain(const Bars& b, uint32_t mine, uint32_t peer,
+                                          uint64_t limit_ns) {
+  const uint32_t hi = mine > peer ? mine : peer;
+  const uint32_t lo = hi > (uint32_t)RING ? hi - (uint32_t)RING : 0u;
+  for (uint32_t f = lo; f < hi; ++f) {
+    const uint32_t bar = b.full + 8 * (f % RING);
+    if (f >= mine) ptx::mbar_arrive_expect_tx_relaxed(bar, SLOT_BYTES);
+    if (f >= peer) ptx::mbar_complete_tx(bar, SLOT_BYTES);
+    wait_drain(bar, (f / RING) & 1u, limit_ns);
+  }
+  wait_drain(b.q_full, 0, limit_ns);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    attn_f16_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
+                             const __grid_constant__ CUtensorMap tmK,
+                             const __grid_constant__ CUtensorMap tmV,
+                             const __grid_constant__ CUtensorMap tmO, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t warp = __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int pair_x = (int)(blockIdx.x >> 1);
+  const int q0 = pair_x * PQ;
+  const int h = (int)blockIdx.y;
+  const int bz = (int)blockIdx.z;
+  const int pair_id = pair_x + (int)(gridDim.x >> 1) * (h + (int)gridDim.y * bz);
+
+  Bars b;
+  b.q_full = base + OFF_BAR;
+  b.full = b.q_full + 8;
+  b.empty = b.full + 8 * RING;
+  b.s_full = b.empty + 8 * RING;
+  b.p_full = b.s_full + 16;
+  b.o_done = b.p_full + 8;
+  b.mma_done = b.o_done + 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+    ptx::prefetch_tmap(&tmO);
+    ptx::mbar_init(b.q_full, 1);
+    for (int s = 0; s < RING; ++s) {
+      ptx::mbar_init(b.full + 8 * s, 1);
+      ptx::mbar_init(b.empty + 8 * s, 1);
+    }
+    ptx::mbar_init(b.s_full, 1);
+    ptx::mbar_init(b.s_full + 8, 1);
+    ptx::mbar_init(b.p_full, 2 * SM_WARPS);
+    ptx::mbar_init(b.o_done, 1);
+    ptx::mbar_init(b.mma_done, 1);
+    *abort_flag = 0;
+    *reinterpret_cast<volatile uint32_t*>(smem + OFF_PEER_ISSUED) = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(base + OFF_TMEM_SLOT, TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
+
+  uint32_t issued = 0;
+  if (warp == 0) {
+    if (lane == 0)
+      issued = producer_role(&tmQ, &tmK, &tmV, p, base, b, rank, q0, h, bz,
+                             pair_id == p.fault_pair, abort_flag);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      mma_role(p, base, tmem_base, b, abort_flag);
+      // Every MMA issued must be finished before TMEM is freed.
+      ptx::mma_commit_pair(b.mma_done, 0x1);
+      wait_drain(b.mma_done, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    softmax_role(&tmO, p, base, tmem_base, b, rank, warp, lane, q0, h, bz, abort_flag);
+  }
+
+  if (warp == 0 && lane == 0 && rank == 1)
+    ptx::st_cluster_u32(ptx::map_to_cta(base + OFF_PEER_ISSUED, 0), issued);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs have stopped issuing
+  if (warp == 0 && lane == 0 && rank == 0) {
+    const uint32_t peer = *reinterpret_cast<volatile uint32_t*>(smem + OFF_PEER_ISSUED);
+    leader_drain(b, issued, peer, p.timeout_ns);
+  }
+  ptx::cluster_sync();  // no copy into either CTA is still in flight
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace attnp
+}  // namespace gf16

@@ -541,6 +541,7 @@ __global__ void __launch_bounds__(256)
 #include "gemm_pair.cuh"
 #include "gemm_pair_wide.cuh"
 #include "attn_f16.cuh"
+#include "attn_pair.cuh"
 
 // ====================================================================== host
 using namespace gf16;
@@ -736,6 +737,7 @@ struct gemm_f16_plan_s {
   int kernel = 0;      // 0 auto, 1 single CTA, 2 CTA pair
   int tile_width = 0;  // single-CTA tile width: 0 auto, else 256 / 128 / 64
   int sm_limit = 0;    // most SMs a launch may use (0: all)
+  int attn_kernel = 0; // attention: 0 auto (CTA pair), 1 single CTA, 2 CTA pair
   int max_pairs = 0;   // co-resident clusters of two for the pair kernel
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -878,6 +880,10 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)attn::SMEM_BYTES),
             "cudaFuncSetAttribute(attention kernel smem)");
+  GF16_CUDA(cudaFuncSetAttribute(attnp::attn_f16_fwd_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attnp::SMEM_BYTES),
+            "cudaFuncSetAttribute(pair attention kernel smem)");
   // Co-resident clusters of two for each pair-kernel instance; keep the
   // smaller count (0 if the query fails: the pair kernel is then not used).
   int max_clusters = 0;
@@ -974,6 +980,10 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
       if (value < 0 || value > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
       p->sm_limit = (int)value;
       return GEMM_F16_OK;
+    case GEMM_F16_OPT_ATTN_KERNEL:
+      if (value < 0 || value > 2) return GEMM_F16_ERR_INVALID_ARG;
+      p->attn_kernel = (int)value;
+      return GEMM_F16_OK;
     case GEMM_F16_OPT_TILE_WIDTH:
       if (value != 0 && value != 64 && value != 128 && value != 256) return GEMM_F16_ERR_INVALID_ARG;
       p->tile_width = (int)value;
@@ -1011,6 +1021,7 @@ int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
     case GEMM_F16_OPT_KERNEL: *value = p->kernel; return GEMM_F16_OK;
     case GEMM_F16_OPT_TILE_WIDTH: *value = p->tile_width; return GEMM_F16_OK;
     case GEMM_F16_OPT_SM_LIMIT: *value = p->sm_limit; return GEMM_F16_OK;
+    case GEMM_F16_OPT_ATTN_KERNEL: *value = p->attn_kernel; return GEMM_F16_OK;
     case GEMM_F16_INFO_NUM_SMS: *value = p->num_sms; return GEMM_F16_OK;
     case GEMM_F16_INFO_MAX_PAIRS: *value = p->max_pairs; return GEMM_F16_OK;
     default: return GEMM_F16_ERR_INVALID_ARG;
@@ -1620,11 +1631,28 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
                              V, v_strides, O, o_strides, scale);
   if (rc) return rc;
   DeviceGuard g(p->device);
+  const bool use_pair = p->attn_kernel != 1;
   CUtensorMap tmQ, tmK, tmV, tmO;
   if ((rc = encode_bhsd(&tmQ, Q, batch, heads, seq_q, q_strides, attn::BQ))) return rc;
-  if ((rc = encode_bhsd(&tmK, K, batch, heads, seq_kv, k_strides, attn::BKV))) return rc;
-  if ((rc = encode_bhsd(&tmV, V, batch, heads, seq_kv, v_strides, attn::BKV))) return rc;
+  if ((rc = encode_bhsd(&tmK, K, batch, heads, seq_kv, k_strides, 64))) return rc;
+  if ((rc = encode_bhsd(&tmV, V, batch, heads, seq_kv, v_strides, use_pair ? 128u : 64u)))
+    return rc;
   if ((rc = encode_bhsd(&tmO, O, batch, heads, seq_q, o_strides, 32))) return rc;
+  if (use_pair) {
+    attnp::Params prm;
+    prm.seq_q = seq_q;
+    prm.seq_kv = seq_kv;
+    prm.nkv = (int)ceil_div(seq_kv, attnp::BKV);
+    prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    prm.status = p->status_dev;
+    prm.timeout_ns = p->timeout_ns;
+    prm.fault_pair = p->fault_unit;
+    const dim3 grid((unsigned)(2 * ceil_div(seq_q, attnp::PQ)), (unsigned)heads, (unsigned)batch);
+    attnp::attn_f16_fwd_pair_kernel<<<grid, attnp::NUM_THREADS, attnp::SMEM_BYTES,
+                                      (cudaStream_t)stream>>>(tmQ, tmK, tmV, tmO, prm);
+    GF16_CUDA(cudaGetLastError(), "launch attn_f16_fwd_pair_kernel");
+    return GEMM_F16_OK;
+  }
   attn::Params prm;
   prm.seq_q = seq_q;
   prm.seq_kv = seq_kv;

@@ -89,7 +89,12 @@ typedef enum gemm_f16_option {
     /* Most SMs one launch may occupy (0 = all of them), e.g. to leave SMs
      * to work on other streams.  The tile schedules are planned for the
      * full device either way. */
-    GEMM_F16_OPT_SM_LIMIT = 6
+    GEMM_F16_OPT_SM_LIMIT = 6,
+    /* Attention kernel (attn_f16_fwd in attn_f16.h): 0 = automatic (the
+     * CTA-pair kernel), 1 = single-CTA kernel (128 query rows, blocks of 64
+     * keys), 2 = CTA-pair kernel (256 query rows over two SMs, blocks of
+     * 128 keys).  Results agree within the usual tolerance. */
+    GEMM_F16_OPT_ATTN_KERNEL = 7
 } gemm_f16_option;
 
 /*

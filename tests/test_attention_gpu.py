@@ -24,8 +24,11 @@ pytestmark = pytest.mark.gpu
 D = 256
 
 
-@pytest.fixture(scope="module")
-def plan():
+@pytest.fixture(scope="module", params=[1, 2], ids=["cta1", "pair"])
+def plan(request):
+    """A plan pinned to one attention kernel: 1 = single CTA (128 query
+    rows, 64-key blocks), 2 = CTA pair (256 query rows, 128-key blocks).
+    Every test in this file runs on both."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
@@ -33,6 +36,7 @@ def plan():
     from async_barrier_pipelined_gb300 import build
     build.build()
     p = g.Plan(0)
+    p.set_option(g.OPT_ATTN_KERNEL, request.param)
     yield p
     p.close()
 

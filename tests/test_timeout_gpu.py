@@ -56,10 +56,11 @@ def test_bounded_wait_reports_timeout_and_context_survives(kernel):
             assert plan.status() == g.OK
 
 
-def test_attention_bounded_wait_reports_timeout_and_context_survives():
-    """The attention kernel: CTA 1's first key tile gets no copy, so the MMA
-    thread's wait runs out; the run must return with ERR_TIMEOUT and the
-    next run on the same context must be correct."""
+@pytest.mark.parametrize("kernel", [1, 2], ids=["cta1", "pair"])
+def test_attention_bounded_wait_reports_timeout_and_context_survives(kernel):
+    """The attention kernels: the first key tile of CTA (or CTA pair) 1 gets
+    no copy, so the MMA thread's wait runs out; the run must return with
+    ERR_TIMEOUT and the next run on the same context must be correct."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
@@ -68,10 +69,11 @@ def test_attention_bounded_wait_reports_timeout_and_context_survives():
     from tests import parity
     from async_barrier_pipelined_gb300 import build
     build.build()
-    w = si.attn_custom(1, 2, 256, 200, seed=9)
+    w = si.attn_custom(1, 2, 512, 300, seed=9)
     Qb, Kb, Vb = w.bits()
     Q, K, V = (torch.from_numpy(x.view(np.float16)).cuda() for x in (Qb, Kb, Vb))
     with g.Plan(0) as plan:
+        plan.set_option(g.OPT_ATTN_KERNEL, kernel)
         plan.set_option(g.OPT_TIMEOUT_NS, 20_000_000)
         plan.set_option(g.OPT_FAULT_UNIT, 1)
         g.attention(plan, Q, K, V)
