@@ -23,9 +23,14 @@
 //                    CTAs' bytes; both CTAs' copies complete them.
 //   empty[s]         both: the leader's commit, multicast to the pair.
 //   s_full[b]        both: multicast commit when S buffer b is written.
-//   p_full           leader only: one arrival per softmax warp of either
-//                    CTA (8 per phase) once its P rows are in shared memory.
-//   o_done           both: multicast commit when O += P V of a block ends.
+//   p_full[b]        leader only, for P buffer b: one arrival per leader
+//                    softmax warp, each expecting 16 bytes; each peer softmax
+//                    warp publishes its P rows with a 16-byte shared-memory
+//                    copy into the leader that completes 16 bytes on it.
+//                    (A release arrival across the cluster took ~0.8 us;
+//                    the copy is ordered after the warp's proxy fence like a
+//                    tensor store and lands in a fraction of that.)
+//   o_done[b]        both: multicast commit when O += P V from P buffer b ends.
 //   mma_done         leader only: the last commit, waited before TMEM is freed.
 // Every wait is bounded; after an abort the leader completes the phases of
 // copies in flight (as the pair GEMM kernel does) before either CTA exits.
@@ -43,7 +48,7 @@ using attn::pack_half2;
 constexpr int CQ = 128;                 // query rows per CTA
 constexpr int PQ = 2 * CQ;              // query rows per pair
 constexpr int BKV = 128;                // keys per block
-constexpr int RING = 4;                 // K / V half-tiles in flight per CTA
+constexpr int RING = 3;                 // K / V half-tiles in flight per CTA
 constexpr int NUM_THREADS = 192;
 constexpr int SM_WARPS = 4;             // softmax warps 2..5
 
@@ -53,17 +58,21 @@ constexpr uint32_t K_CHUNK = (BKV / 2) * 128;          // 64 d x 64 keys: 8 KB
 constexpr uint32_t V_CHUNK = BKV * 128;                // 64 d x 128 keys: 16 KB
 constexpr uint32_t SLOT_BYTES = 32768;                 // a K half (4 chunks) or a V half (2)
 constexpr uint32_t P_CHUNK = CQ * 128;                 // 64 keys x 128 rows: 16 KB
-constexpr uint32_t P_BYTES = 2 * P_CHUNK;              // 32 KB
+constexpr uint32_t P_BYTES = 2 * P_CHUNK;              // 32 KB per P buffer
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_P = OFF_RING + RING * SLOT_BYTES;
-constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
-// q_full, full[RING], empty[RING], s_full[2], p_full, o_done, mma_done
-constexpr uint32_t NUM_BARS = 1 + 2 * RING + 2 + 3;
+constexpr uint32_t OFF_P = OFF_RING + RING * SLOT_BYTES;  // two P buffers
+constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
+// q_full, full[RING], empty[RING], s_full[2], p_full[2], o_done[2], mma_done
+constexpr uint32_t NUM_BARS = 1 + 2 * RING + 2 + 2 + 2 + 1;
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr uint32_t OFF_PEER_ISSUED = OFF_ABORT + 4;
-constexpr uint32_t SMEM_BYTES = OFF_PEER_ISSUED + 4 + 1024;
+// P-ready signals: per softmax warp a 16-byte source (in the peer) and
+// destination (in the leader) of the signalling copy.
+constexpr uint32_t OFF_SIG = (OFF_PEER_ISSUED + 4 + 15) / 16 * 16;
+constexpr uint32_t SIG_BYTES = 16;
+constexpr uint32_t SMEM_BYTES = OFF_SIG + 2 * SM_WARPS * SIG_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit per CTA");
 static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "swizzled buffers need 1024-B alignment");
 static_assert((HD / 64) * K_CHUNK == SLOT_BYTES && 2 * V_CHUNK == SLOT_BYTES, "slot sizes");
@@ -95,22 +104,6 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
                                            volatile int* abort_flag) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   return attn::wait_slow(bar, parity, p.status, p.timeout_ns, abort_flag);
-}
-
-// Wait for a phase completed by release arrivals from either CTA.
-__device__ __noinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, const Params& p,
-                                                volatile int* abort_flag) {
-  const uint64_t t0 = ptx::globaltimer();
-  while (true) {
-    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (ptx::globaltimer() - t0 > p.timeout_ns) {
-      *abort_flag = 1;
-      *(volatile int*)p.status = (int)GEMM_F16_ERR_TIMEOUT;
-      __threadfence_system();
-      return false;
-    }
-  }
 }
 
 // ------------------------------------------------------------------ producer
@@ -195,20 +188,21 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
   for (int j = 0; j < p.nkv && ok; ++j) {
     if (j + 1 < p.nkv && !issue_qk((uint32_t)(j + 1) & 1u)) break;
     // The split barrier's WAIT: both CTAs' P rows are in shared memory.
-    if (!wait_phase_cluster(b.p_full, (uint32_t)j & 1u, p, abort_flag)) break;
+    const uint32_t pb = (uint32_t)j & 1u;
+    if (!wait_phase(b.p_full + 8 * pb, ((uint32_t)j >> 1) & 1u, p, abort_flag)) break;
     ptx::tc_fence_after();
     if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag)) break;
     ptx::tc_fence_after();
     const uint32_t v_addr = base + OFF_RING + pos.stage * SLOT_BYTES;
 #pragma unroll
     for (int kk = 0; kk < BKV / 16; ++kk) {
-      const uint32_t off_p = (uint32_t)(kk >> 2) * P_CHUNK + (uint32_t)(kk & 3) * 32u;
+      const uint32_t off_p = pb * P_BYTES + (uint32_t)(kk >> 2) * P_CHUNK + (uint32_t)(kk & 3) * 32u;
       ptx::mma_f16_pair(o_tmem, smem_desc_sw128(base + OFF_P + off_p, 16, 1024),
                         smem_desc_sw128(v_addr + (uint32_t)kk * 2048u, V_CHUNK, 1024), IDESC_PV,
                         (j > 0 || kk > 0) ? 1u : 0u);
     }
     ptx::mma_commit_pair(b.empty + 8 * pos.stage, 0x3);
-    ptx::mma_commit_pair(b.o_done, 0x3);
+    ptx::mma_commit_pair(b.o_done + 8 * pb, 0x3);
     ring_advance(pos, RING);
   }
 }
@@ -223,6 +217,8 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
   const uint32_t t_lane = (quarter * 32u) << 16;
   const uint32_t sw = row & 7u;
   const uint32_t leader_p_full = ptx::map_to_cta(b.p_full, 0);
+  const uint32_t sig_dst = ptx::map_to_cta(base + OFF_SIG + (warp - 2) * SIG_BYTES, 0);
+  const uint32_t sig_src = base + OFF_SIG + (SM_WARPS + warp - 2) * SIG_BYTES;
   const float sl2 = p.scale_log2;
   float m = -INFINITY;
   float l = 0.f;
@@ -247,22 +243,31 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
     uint32_t pk[BKV / 2];
     const float lsum = valid < BKV ? block_weights<BKV, true>(s, sl2, -m_new, valid, pk)
                                    : block_weights<BKV, false>(s, sl2, -m_new, valid, pk);
-    if (j > 0) {
-      // O += P V of block j-1 has ended: the P buffer is free and O stable.
-      got = wait_phase(b.o_done, (uint32_t)(j - 1) & 1u, p, abort_flag);
+    const uint32_t pb = (uint32_t)j & 1u;
+    if (j >= 2) {
+      // P buffer pb was last read by O += P V of block j-2.
+      got = wait_phase(b.o_done + 8 * pb, ((uint32_t)(j - 2) >> 1) & 1u, p, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+    }
+    // P row -> shared memory: keys 0-63 and 64-127 in two 128-byte-swizzled
+    // chunks (16-byte group g of row r at position g ^ (r mod 8)).
+    const uint32_t p_row = base + OFF_P + pb * P_BYTES + row * 128u;
+#pragma unroll
+    for (uint32_t g = 0; g < 16; ++g)
+      ptx::st_shared_v4(p_row + (g >> 3) * P_CHUNK + (((g & 7u) ^ sw) << 4), pk[4 * g],
+                        pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // Compensation: O *= alpha once O += P V of block j-1 has landed.
+      const uint32_t ob = (uint32_t)(j - 1) & 1u;
+      got = wait_phase(b.o_done + 8 * ob, ((uint32_t)(j - 1) >> 1) & 1u, p, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-    }
-    // P row -> shared memory: keys 0-63 and 64-127 in two 128-byte-swizzled
-    // chunks (16-byte group g of row r at position g ^ (r mod 8)).
-#pragma unroll
-    for (uint32_t g = 0; g < 16; ++g)
-      ptx::st_shared_v4(base + OFF_P + (g >> 3) * P_CHUNK + row * 128u + (((g & 7u) ^ sw) << 4),
-                        pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t o[32];
@@ -281,16 +286,17 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
     // The split barrier's ARRIVE (one per warp, on the leader's barrier) ...
     if (lane == 0) {
       if (rank == 0)
-        ptx::mbar_arrive(b.p_full);
+        ptx::mbar_arrive_expect_tx(b.p_full + 8 * pb, SIG_BYTES);
       else
-        ptx::mbar_arrive_cluster(leader_p_full);
+        ptx::bulk_copy_to_cluster(sig_dst, sig_src, SIG_BYTES, leader_p_full + 8 * pb);
     }
     // ... and the window: the deferred sum update.
     l = l * alpha + lsum;
     m = m_new;
   }
   if (ok) {
-    const bool got = wait_phase(b.o_done, (uint32_t)(p.nkv - 1) & 1u, p, abort_flag);
+    const uint32_t ob = (uint32_t)(p.nkv - 1) & 1u;
+    const bool got = wait_phase(b.o_done + 8 * ob, ((uint32_t)(p.nkv - 1) >> 1) & 1u, p, abort_flag);
     ok = __all_sync(0xffffffffu, got);
   }
   if (ok) {
@@ -373,8 +379,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   b.empty = b.full + 8 * RING;
   b.s_full = b.empty + 8 * RING;
   b.p_full = b.s_full + 16;
-  b.o_done = b.p_full + 8;
-  b.mma_done = b.o_done + 8;
+  b.o_done = b.p_full + 16;
+  b.mma_done = b.o_done + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
 
   if (warp == 0 && lane == 0) {
@@ -389,8 +395,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     ptx::mbar_init(b.s_full, 1);
     ptx::mbar_init(b.s_full + 8, 1);
-    ptx::mbar_init(b.p_full, 2 * SM_WARPS);
-    ptx::mbar_init(b.o_done, 1);
+    for (int k = 0; k < 2; ++k) {
+      ptx::mbar_init(b.p_full + 8 * k, SM_WARPS);  // leader warps (+ the peer's bytes)
+      ptx::mbar_init(b.o_done + 8 * k, 1);
+    }
     ptx::mbar_init(b.mma_done, 1);
     *abort_flag = 0;
     *reinterpret_cast<volatile uint32_t*>(smem + OFF_PEER_ISSUED) = 0;

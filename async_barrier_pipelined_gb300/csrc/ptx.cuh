@@ -316,18 +316,16 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
-// try_wait with acquire at cluster scope: for phases completed by release
-// arrivals from the peer CTA that publish generic shared-memory writes.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t done;
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// a shared-memory address of another CTA in the cluster, completing the
+// bytes on a barrier in that CTA.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
+                                                     uint32_t bytes, uint32_t bar_cluster) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+      " [%0], [%1], %2, [%3];" ::"r"(dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
       : "memory");
-  return done != 0;
 }
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
