@@ -24,6 +24,11 @@ gpu_launches (kernels launched in the timed region).
 
 --impl reference times the FP64 CPU oracle on the same workload instead
 (bounded row samples per step).
+
+--workload attn_256 / attn_ragged / attn_4096 measures the attention
+forward kernel (attn_f16_fwd, head dimension 256) instead: one step = one
+O = softmax(Q K^T / 16) V over all batches and heads, TFLOPS counted as
+4 * B * H * Sq * Skv * 256.
 """
 from __future__ import annotations
 
@@ -47,10 +52,12 @@ import numpy as np  # noqa: E402
 import synthetic_inputs as si  # noqa: E402
 
 METRIC = "FP16 GEMM TFLOPS at M=N=K=4096 on 1 GB300; % of dense FP16 tensor peak"
+ATTN_METRIC = "FP16 attention forward TFLOPS, head dim 256, on 1 GB300"
 FALLBACK_TENSOR_TFLOPS = 1900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "async_barrier_pipelined_gb300", "csrc", f)
-                  for f in ("gemm_f16.cu", "gemm_pair.cuh", "gemm_pair_wide.cuh", "ptx.cuh", "schedule.h")]
+                  for f in ("gemm_f16.cu", "gemm_pair.cuh", "gemm_pair_wide.cuh", "ptx.cuh", "schedule.h",
+                            "attn_f16.cuh", "attn_pair.cuh")]
 
 
 def parse_args():
@@ -59,13 +66,15 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gemm_4096", choices=sorted(si.WORKLOADS))
+    ap.add_argument("--workload", default="gemm_4096",
+                    choices=sorted(si.WORKLOADS) + sorted(si.ATTN_WORKLOADS))
     ap.add_argument("--sleep", type=float, default=5.0,
                     help="idle seconds before the warm-up (page protocol: 5)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
-                    help="0 automatic, 1 single-CTA kernel, 2 CTA pair 256x256, 3 CTA pair 256x512")
+                    help="GEMM: 0 automatic, 1 single-CTA kernel, 2 CTA pair 256x256, "
+                         "3 CTA pair 256x512; attention: 0 automatic, 1 single CTA, 2 CTA pair")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU seconds for the oracle baseline sample")
     return ap.parse_args()
@@ -237,10 +246,85 @@ def cpu_baseline(w: si.Workload, target_s: float, pairs_bits):
 
 
 # ------------------------------------------------------------------ arms
+def attn_oracle_rows(w, b: int, h: int, rows):
+    """Seconds for the FP64 oracle on `rows` of head (b, h)."""
+    import oracle
+    q, k, v = w.head_bits(b, h, rows)
+    t0 = time.perf_counter()
+    oracle.attention_f16(q, k, v, w.scale)
+    return time.perf_counter() - t0
+
+
+def attn_cpu_baseline(w, target_s: float):
+    """Oracle TFLOPS on a bounded sample: evenly spaced query rows of the
+    heads (b, h) taken in order until ~target_s seconds are spent."""
+    import oracle
+    threads = oracle.num_threads()
+    r0 = int(min(w.Sq, max(threads, 16)))
+    t_cal = attn_oracle_rows(w, 0, 0, np.arange(r0))            # calibration, untimed
+    per_row = max(t_cal / r0, 1e-9)
+    n = int(max(1, min(w.Sq, target_s / per_row / 4)))
+    rows = np.linspace(0, w.Sq - 1, n).astype(np.int64)
+    t, done, heads = 0.0, 0, 0
+    while t < target_s and heads < w.B * w.H:
+        t += attn_oracle_rows(w, heads // w.H, heads % w.H, rows)
+        done += n
+        heads += 1
+    flops = 4.0 * done * w.Skv * w.D
+    return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {w.Sq} query rows (evenly spaced) of {heads} head(s): "
+                      f"{flops / 1e9:.1f} GFLOP in {t:.1f} s, FP64 plain softmax"}
+
+
+def attn_config(w):
+    return {"workload": w.name, "batch": w.B, "heads": w.H, "seq_q": w.Sq, "seq_kv": w.Skv,
+            "head_dim": w.D, "scale": w.scale, "mask": "none",
+            "layout": "[batch, head, seq, 256] contiguous, binary16",
+            "inputs": f"Q, K normal sigma={w.qk_sigma}; V uniform non-zero on [-1, 1]",
+            "cache": "inputs larger than L2 (Q, K, V, O %.0f MB)" % (
+                2.0 * w.D * w.B * w.H * (2 * w.Sq + 2 * w.Skv) / 1e6)}
+
+
+def run_reference_attention(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    import oracle
+    w = si.ATTN_WORKLOADS[args.workload]
+    threads = oracle.num_threads()
+    budget = 120.0
+    steps = args.steps + args.warmup
+    probe = np.arange(min(w.Sq, max(threads, 16)))
+    per_row = max(attn_oracle_rows(w, 0, 0, probe) / len(probe), 1e-6)
+    n = int(max(1, min(w.Sq, budget / steps / per_row)))
+    for i in range(args.warmup):
+        attn_oracle_rows(w, 0, i % w.H, (np.arange(n) + i * n) % w.Sq)
+    total = 0.0
+    for i in range(args.steps):
+        hh = i % (w.B * w.H)
+        total += attn_oracle_rows(w, hh // w.H, hh % w.H, (np.arange(n) + i * n) % w.Sq)
+    flops = 4.0 * n * args.steps * w.Skv * w.D
+    value = flops / total / 1e12
+    line = {
+        "metric": ATTN_METRIC, "value": value, "unit": "TFLOPS", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": attn_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} query rows of one head per step, FP64 plain softmax"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return 0
+    if args.workload in si.ATTN_WORKLOADS:
+        return run_reference_attention(args)
     import oracle
     w = si.WORKLOADS[args.workload]
     A_bits, B_bits = w.pair_bits(0)
@@ -288,9 +372,145 @@ def workload_config(w: si.Workload):
                       if len(w.keys) > 1 else "inputs resident (no rotation)")}
 
 
+def run_attention(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import async_barrier_pipelined_gb300 as g
+    from async_barrier_pipelined_gb300 import build as gbuild
+    gbuild.build()
+
+    w = si.ATTN_WORKLOADS[args.workload]
+    qb, kb, vb = w.bits()
+    Q, K, V = (torch.from_numpy(x.view(np.float16)).to(dev) for x in (qb, kb, vb))
+    O = torch.empty_like(Q)
+    stream = torch.cuda.Stream(device=dev)
+    plan = g.Plan(dev.index)
+    plan.set_option(g.OPT_ATTN_KERNEL, min(args.kernel, 2))
+    use_pair = args.kernel != 1
+
+    def step(i):
+        g.attention(plan, Q, K, V, O, scale=w.scale, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    step(0)
+    torch.cuda.synchronize(dev)
+    if plan.status() != 0:
+        raise RuntimeError("device status error")
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(args.sleep)
+    sampler.mark("load_start")
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    ev1.synchronize()
+    barrier()
+    sampler.mark("timed_end")
+    clocks = sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    if plan.status() != 0:
+        raise RuntimeError("device status error after the timed region")
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = float(w.flops) * args.steps * world / (ms_total * 1e-3) / 1e12
+
+    peak, peak_sus, peak_hbm, peak_kind = load_peaks()
+    achieved = float(w.flops) / (ms_step * 1e-3) / 1e12
+    cbytes = 2.0 * w.D * w.B * w.H * (2 * w.Sq + 2 * w.Skv)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_source": f"{peak_kind} dense bf16 burst (fp16 runs at the same rate)",
+                "algorithmic_flops_per_launch": float(w.flops),
+                "traffic": load_traffic(w.name) if use_pair else None,
+                "flop_per_byte": float(w.flops) / cbytes,
+                "kernel": ("gf16::attnp::attn_f16_fwd_pair_kernel" if use_pair
+                           else "gf16::attn::attn_f16_fwd_kernel")}
+
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (torch.from_numpy(x.view(np.float16)).pin_memory() for x in (qb, kb, vb))
+        ho = torch.empty(O.shape, dtype=torch.float16).pin_memory()
+
+        def host_step(i):
+            with torch.cuda.stream(stream):
+                Q.copy_(hq, non_blocking=True)
+                K.copy_(hk, non_blocking=True)
+                V.copy_(hv, non_blocking=True)
+                g.attention(plan, Q, K, V, O, scale=w.scale, stream=stream)
+                ho.copy_(O, non_blocking=True)
+
+        e2e_steps = max(1, min(args.steps, 20))
+        for i in range(2):
+            host_step(i)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            host_step(i)
+        e1.record(stream)
+        e1.synchronize()
+        barrier()
+        ms_e2e = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": float(w.flops) * e2e_steps * world / (ms_e2e * 1e-3) / 1e12,
+               "unit": "TFLOPS", "h2d_bytes_per_step": int(qb.nbytes + kb.nbytes + vb.nbytes),
+               "d2h_bytes_per_step": int(qb.nbytes), "steps": e2e_steps,
+               "api": "attention() with pinned host Q, K, V copied in and O copied out"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = attn_cpu_baseline(w, args.cpu_seconds)
+    plan.close()
+    if rank == 0:
+        line = {
+            "metric": ATTN_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic",
+            "config": dict(attn_config(w), kernel=("CTA pair (tcgen05 cta_group::2, 256 query "
+                                                   "rows, 128-key blocks)" if use_pair else
+                                                   "single CTA (128 query rows, 64-key blocks)")),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": args.steps, "pct_of_peak": 100.0 * achieved / peak,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
+
+    if args.workload in si.ATTN_WORKLOADS:
+        return run_attention(args)
 
     world, rank, local = dist_setup(args)
     if world > 1:
