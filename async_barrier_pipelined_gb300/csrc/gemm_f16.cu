@@ -1591,6 +1591,29 @@ int encode_bhsd(CUtensorMap* map, const void* ptr, int batch, int heads, int row
   return GEMM_F16_OK;
 }
 
+// encode_bhsd through the plan's tensor-map cache (keys tagged apart from
+// the 2-D GEMM maps).
+int cached_encode_bhsd(gemm_f16_plan_s* p, CUtensorMap* map, const void* ptr, int batch,
+                       int heads, int rows, const int64_t st[3], uint32_t box_rows) {
+  const uint64_t key[8] = {(uint64_t)(uintptr_t)ptr, ((uint64_t)(uint32_t)batch << 32) | (uint32_t)heads,
+                           (uint64_t)(uint32_t)rows, (uint64_t)st[0], (uint64_t)st[1],
+                           (uint64_t)st[2], (uint64_t)box_rows, 0x4D00000000000000ull};
+  for (int i = 0; i < p->tmap_used; ++i) {
+    if (std::memcmp(p->tmaps[i].key, key, sizeof(key)) == 0) {
+      *map = p->tmaps[i].map;
+      return GEMM_F16_OK;
+    }
+  }
+  const int rc = encode_bhsd(map, ptr, batch, heads, rows, st, box_rows);
+  if (rc) return rc;
+  TmapEntry& e = p->tmaps[p->tmap_next];
+  std::memcpy(e.key, key, sizeof(key));
+  e.map = *map;
+  p->tmap_next = (p->tmap_next + 1) % TMAP_CACHE;
+  if (p->tmap_used < TMAP_CACHE) ++p->tmap_used;
+  return GEMM_F16_OK;
+}
+
 bool strides_ok(const int64_t* st) {
   if (!st) return false;
   for (int i = 0; i < 3; ++i)
@@ -1633,11 +1656,11 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
   DeviceGuard g(p->device);
   const bool use_pair = p->attn_kernel != 1;
   CUtensorMap tmQ, tmK, tmV, tmO;
-  if ((rc = encode_bhsd(&tmQ, Q, batch, heads, seq_q, q_strides, attn::BQ))) return rc;
-  if ((rc = encode_bhsd(&tmK, K, batch, heads, seq_kv, k_strides, 64))) return rc;
-  if ((rc = encode_bhsd(&tmV, V, batch, heads, seq_kv, v_strides, use_pair ? 128u : 64u)))
+  if ((rc = cached_encode_bhsd(p, &tmQ, Q, batch, heads, seq_q, q_strides, attn::BQ))) return rc;
+  if ((rc = cached_encode_bhsd(p, &tmK, K, batch, heads, seq_kv, k_strides, 64))) return rc;
+  if ((rc = cached_encode_bhsd(p, &tmV, V, batch, heads, seq_kv, v_strides, use_pair ? 128u : 64u)))
     return rc;
-  if ((rc = encode_bhsd(&tmO, O, batch, heads, seq_q, o_strides, 32))) return rc;
+  if ((rc = cached_encode_bhsd(p, &tmO, O, batch, heads, seq_q, o_strides, 32))) return rc;
   if (use_pair) {
     attnp::Params prm;
     prm.seq_q = seq_q;
