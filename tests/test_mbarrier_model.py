@@ -4,7 +4,11 @@ The model implements the mbarrier operations as the "mbarrier State and
 Operations" page defines them and drives the producer / MMA / epilogue role
 loops with the kernel's own index and parity helpers (schedule.h) under
 seeded random interleavings of roles, copy completions and tensor-core
-completions.  See model.cpp for the invariants checked.
+completions.  See model.cpp for the invariants checked.  attn_pair_model.cpp
+replays the CTA-pair attention kernel's protocol (copy ring, S / P / O
+hand-over between the MMA thread and the softmax warps of both CTAs, the
+peer's P signalling copies) and also checks that every parity wait returns
+with exactly the phase it waited for.
 """
 from __future__ import annotations
 
@@ -17,10 +21,12 @@ import pytest
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "mbarrier_model", "model.cpp")
 PAIR_SRC = os.path.join(HERE, "mbarrier_model", "pair_model.cpp")
+ATTN_SRC = os.path.join(HERE, "mbarrier_model", "attn_pair_model.cpp")
 CSRC = os.path.join(os.path.dirname(HERE), "async_barrier_pipelined_gb300", "csrc")
 BUILD = os.path.join(HERE, "mbarrier_model", "_build")
 EXE = os.path.join(BUILD, "model")
 PAIR_EXE = os.path.join(BUILD, "pair_model")
+ATTN_EXE = os.path.join(BUILD, "attn_pair_model")
 
 
 def _build(src, exe):
@@ -45,6 +51,11 @@ def model():
 @pytest.fixture(scope="module")
 def pair_model():
     return _build(PAIR_SRC, PAIR_EXE)
+
+
+@pytest.fixture(scope="module")
+def attn_model():
+    return _build(ATTN_SRC, ATTN_EXE)
 
 
 def _run(exe, *args):
@@ -126,3 +137,20 @@ def test_pair_abort_drain_completes_issued_phases(pair_model, case):
 def test_pair_fault_on_other_pair_does_not_affect_this_one(pair_model):
     rc, out = _run(pair_model, 6, 8, 2, 1, 1, 4, 20, "fault", 2)
     assert rc == 0 and "deadlocks=0" in out, out
+
+
+# (ring slots, key blocks, seeds): 1 and 2 blocks (no reuse), odd / even
+# counts, the kernel's 3-slot ring and others
+ATTN_CASES = [(3, 1, 100), (3, 2, 100), (3, 5, 100), (3, 8, 60), (2, 6, 100), (4, 7, 60),
+              (1, 4, 60)]
+
+
+@pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_attention_pair_protocol_interleavings(attn_model, case):
+    rc, out = _run(attn_model, *case)
+    assert rc == 0 and out.startswith("OK"), out
+
+
+def test_attention_pair_fault_blocks_the_mma_on_the_starved_fill(attn_model):
+    rc, out = _run(attn_model, 3, 4, 20, "fault")
+    assert rc == 0 and out.startswith("DEADLOCK-AS-EXPECTED"), out
