@@ -198,6 +198,24 @@ class ClockSampler:
                 "window": "last warm-up steps and the timed region"}
 
 
+def max_over_ranks(ms: float, world: int, dev=None) -> float:
+    """The slowest rank's time: every rank contributes its own event time
+    and all receive the maximum (a no-op for one process)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms_total: float) -> float:
+    """Work of all ranks (each runs `steps` steps of its own replica) over
+    the slowest rank's time."""
+    return flops_per_step * steps * world / (ms_total * 1e-3) / 1e12
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -440,12 +458,9 @@ def run_attention(args):
     ms_total = ev0.elapsed_time(ev1)
     if plan.status() != 0:
         raise RuntimeError("device status error after the timed region")
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
-    value = float(w.flops) * args.steps * world / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(float(w.flops), args.steps, world, ms_total)
 
     peak, peak_sus, peak_hbm, peak_kind = load_peaks()
     achieved = float(w.flops) / (ms_step * 1e-3) / 1e12
@@ -485,11 +500,8 @@ def run_attention(args):
         e1.synchronize()
         barrier()
         ms_e2e = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": float(w.flops) * e2e_steps * world / (ms_e2e * 1e-3) / 1e12,
+        ms_e2e = max_over_ranks(ms_e2e, world, dev)
+        e2e = {"value": whole_job_tflops(float(w.flops), e2e_steps, world, ms_e2e),
                "unit": "TFLOPS", "h2d_bytes_per_step": int(qb.nbytes + kb.nbytes + vb.nbytes),
                "d2h_bytes_per_step": int(qb.nbytes), "steps": e2e_steps,
                "api": "attention() with pinned host Q, K, V copied in and O copied out"}
@@ -584,13 +596,9 @@ def run_ours(args):
     st = plan.status()
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed region")
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
-    flops_all = float(w.flops) * args.steps * world
-    value = flops_all / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(float(w.flops), args.steps, world, ms_total)
 
     peak, peak_sus, peak_hbm, peak_kind = load_peaks()
     # Dominant kernel: the GEMM kernel.  For split workloads the step also
@@ -640,13 +648,10 @@ def run_ours(args):
         e1.synchronize()
         barrier()
         ms_e2e = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
+        ms_e2e = max_over_ranks(ms_e2e, world, dev)
         if plan.status() != 0:
             raise RuntimeError("device status error in the e2e region")
-        e2e = {"value": float(w.flops) * e2e_steps * world / (ms_e2e * 1e-3) / 1e12,
+        e2e = {"value": whole_job_tflops(float(w.flops), e2e_steps, world, ms_e2e),
                "unit": "TFLOPS",
                "h2d_bytes_per_step": 2 * (w.M * w.K + w.K * w.N),
                "d2h_bytes_per_step": 2 * w.M * w.N,
