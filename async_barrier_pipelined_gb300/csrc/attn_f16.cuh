@@ -48,7 +48,6 @@ constexpr int BQ = 128;                 // query rows per CTA (MMA M, TMEM lanes
 constexpr int BKV = 64;                 // keys per block
 constexpr int RING = 4;                 // K / V tiles in flight
 constexpr int NUM_THREADS = 192;
-constexpr int SM_WARP0 = 2;             // softmax warps 2..5
 constexpr int SM_THREADS = 128;
 
 constexpr uint32_t CHUNK_Q = BQ * 128;            // 64 d-columns x 128 rows: 16 KB
