@@ -779,6 +779,41 @@ int cached_encode_2d(gemm_f16_plan_s* p, CUtensorMap* map, CUtensorMapDataType d
   return GEMM_F16_OK;
 }
 
+// Row-major B (K x N, N a multiple of 64) as a 3-D tensor (64 columns, K
+// rows, N / 64 column groups; strides: row, 128 bytes), boxes of 64 x 64 x 2:
+// one copy fetches both 64-column groups of a pair CTA's half of a B stage,
+// in the same shared-memory layout as two 2-D boxes.  Cached in the plan.
+int cached_encode_b3d(gemm_f16_plan_s* p, CUtensorMap* map, const void* ptr, uint64_t K,
+                      uint64_t N, uint64_t ldb) {
+  const uint64_t key[8] = {(uint64_t)(uintptr_t)ptr, K, N, ldb, 0, 0, 0, 0x3D00000000000000ull};
+  for (int i = 0; i < p->tmap_used; ++i) {
+    if (std::memcmp(p->tmaps[i].key, key, sizeof(key)) == 0) {
+      *map = p->tmaps[i].map;
+      return GEMM_F16_OK;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return GEMM_F16_ERR_CUDA;
+  const cuuint64_t dims[3] = {64, K, N / 64};
+  const cuuint64_t strides[2] = {ldb * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)BK, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                  "cuTensorMapEncodeTiled (3-D B) failed (CUresult %d)", (int)r);
+    return GEMM_F16_ERR_CUDA;
+  }
+  TmapEntry& e = p->tmaps[p->tmap_next];
+  std::memcpy(e.key, key, sizeof(key));
+  e.map = *map;
+  p->tmap_next = (p->tmap_next + 1) % TMAP_CACHE;
+  if (p->tmap_used < TMAP_CACHE) ++p->tmap_used;
+  return GEMM_F16_OK;
+}
+
 // Host <-> device copy of a row-strided matrix: one plain copy when both
 // sides are contiguous, a pitched copy otherwise.
 cudaError_t copy_rows(void* dst, int64_t dpitch, const void* src, int64_t spitch,
@@ -1175,10 +1210,13 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
                           (uint64_t)lda * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc) return rc;
+  const bool b3d = use_pair && pair_tn == 256 && !(layout & LAYOUT_BT) && (N % 64) == 0;
   if (layout & LAYOUT_BT)
     rc = cached_encode_2d(p, &tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,
                           (uint64_t)ldb * 2, BK, use_pair ? 128u : (uint32_t)bn,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  else if (b3d)
+    rc = cached_encode_b3d(p, &tmB, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb);
   else
     rc = cached_encode_2d(p, &tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)N, (uint64_t)K,
                           (uint64_t)ldb * 2, B_BOX_N, BK, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1216,6 +1254,7 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
     pp.status = p->status_dev;
     pp.timeout_ns = p->timeout_ns;
     pp.fault_unit = p->fault_unit;
+    pp.b3d = b3d ? 1 : 0;
     int64_t pair_cap = std::max(p->max_pairs, 1);
     if (p->sm_limit > 0) pair_cap = std::max<int64_t>(1, std::min<int64_t>(pair_cap, p->sm_limit / 2));
     const int64_t npairs = std::min<int64_t>(punits, pair_cap);

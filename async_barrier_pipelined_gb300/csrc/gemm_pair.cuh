@@ -95,6 +95,7 @@ struct Params {
   int* status;
   unsigned long long timeout_ns;
   int fault_unit;
+  int b3d;       // row-major B seen as 3-D (64 columns, K, column groups): one copy per stage
 };
 
 struct Bars {
@@ -185,6 +186,9 @@ __device__ __forceinline__ uint32_t producer_role(const CUtensorMap* tmA, const 
         const uint32_t sb = base + OFF_B + pos.stage * B_STAGE;
         if constexpr ((LAYOUT & LAYOUT_BT) != 0) {   // B stored N x K: 128 rows of N
           ptx::tma_load_2d_pair(sb, tmB, fb, k0, nb0);
+        } else if (p.b3d) {
+          // both 64-column groups of this CTA's half in one copy
+          ptx::tma_load_3d_pair(sb, tmB, fb, 0, k0, nb0 / (int)B_BOX_N);
         } else {
           ptx::tma_load_2d_pair(sb, tmB, fb, nb0, k0);
           ptx::tma_load_2d_pair(sb + B_BOX, tmB, fb, nb0 + (int)B_BOX_N, k0);

@@ -304,6 +304,18 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// 3-D tensor load into this CTA's shared memory crediting a barrier that
+// may live in the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
+                                                 uint32_t cluster_bar, int32_t x, int32_t y,
+                                                 int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(cluster_bar)
+      : "memory");
+}
+
 // 4-D tensor load into this CTA's shared memory crediting a barrier that
 // may live in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap,
