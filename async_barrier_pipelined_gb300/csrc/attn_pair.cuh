@@ -2,34 +2,40 @@
 // head dimension 256, blocks of 128 keys.
 //
 // A cluster of two CTAs handles 256 query rows of one (batch, head): CTA r
-// holds rows 128r .. 128r+127 (its Q tile in shared memory, its rows of S
-// and O in its tensor memory) and the even CTA ("leader") issues the MMAs
+// holds rows 128r .. 128r+127 (its Q tile in shared memory, its rows of S,
+// P and O in its tensor memory) and the even CTA ("leader") issues the MMAs
 // for both:
 //   S = Q K^T   256 x 128 x 16, 16 per key block; B (the key block) is split
 //               by keys: CTA r holds keys 64r .. 64r+63 of the block.
-//   O += P V    256 x 256 x 16, 8 per key block; B (the value block) is
-//               split by columns: CTA r holds d = 128r .. 128r+127.
+//   O += P V    256 x 256 x 16, 8 per key block; A (P, FP16) is read from
+//               each CTA's tensor memory, B (the value block) is split by
+//               columns: CTA r holds d = 128r .. 128r+127.
 // Each SM so takes in 32 KB of K and 32 KB of V per 128 keys -- half of
 // what the single-CTA kernel needs for the same work -- and the S MMAs are
 // 128 keys wide (a 64-wide S MMA runs at two thirds of the tensor rate).
-// The softmax (one query row per thread, four warps per CTA) and the
-// split-barrier schedule are those of the single-CTA kernel: S of block
-// j+1 runs on the tensor core while the softmax works on block j; P is
-// published with an ARRIVE and the leader's MMA thread WAITs for both CTAs
-// before O += P V.
+// P never passes through shared memory: per block and CTA that saves 32 KB
+// of softmax stores and 32 KB of MMA operand reads, a quarter of the
+// shared-memory traffic, and frees room for a 5-slot copy ring.
+// The softmax (one query row per thread, four warps per CTA) is that of the
+// single-CTA kernel.  Per block j it loads S_j into registers and says so
+// (s_free), which lets the leader issue S_{j+1} into the one S buffer while
+// O += P V of block j-1 runs; it then writes P_j into one of two P buffers
+// in tensor memory and publishes it (the split barrier's ARRIVE); the
+// leader's MMA thread WAITs for both CTAs before O += P V.
 //
 // Barriers ("mbarrier State and Operations" page):
 //   q_full, full[s]  leader only: its producer's arrive.expect_tx for both
 //                    CTAs' bytes; both CTAs' copies complete them.
 //   empty[s]         both: the leader's commit, multicast to the pair.
-//   s_full[b]        both: multicast commit when S buffer b is written.
-//   p_full[b]        leader only, for P buffer b: one arrival per leader
-//                    softmax warp, each expecting 16 bytes; each peer softmax
-//                    warp publishes its P rows with a 16-byte shared-memory
-//                    copy into the leader that completes 16 bytes on it.
-//                    (A release arrival across the cluster took ~0.8 us;
-//                    the copy is ordered after the warp's proxy fence like a
-//                    tensor store and lands in a fraction of that.)
+//   s_full           both: multicast commit when S is written.
+//   s_free, p_full[b]
+//                    leader only: one arrival per leader softmax warp, each
+//                    expecting 16 bytes; each peer softmax warp signals with
+//                    a 16-byte shared-memory copy into the leader that
+//                    completes 16 bytes on it.  (A release arrival across
+//                    the cluster took ~0.8 us; the copy lands in a fraction
+//                    of that.)  s_free: S is in registers in both CTAs;
+//                    p_full[b]: P buffer b is written in both CTAs.
 //   o_done[b]        both: multicast commit when O += P V from P buffer b ends.
 //   mma_done         leader only: the last commit, waited before TMEM is freed.
 // Every wait is bounded; after an abort the leader completes the phases of
@@ -48,7 +54,7 @@ using attn::pack_half2;
 constexpr int CQ = 128;                 // query rows per CTA
 constexpr int PQ = 2 * CQ;              // query rows per pair
 constexpr int BKV = 128;                // keys per block
-constexpr int RING = 3;                 // K / V half-tiles in flight per CTA
+constexpr int RING = 5;                 // K / V half-tiles in flight per CTA
 constexpr int NUM_THREADS = 192;
 constexpr int SM_WARPS = 4;             // softmax warps 2..5
 
@@ -57,32 +63,31 @@ constexpr uint32_t Q_BYTES = (HD / 64) * CHUNK_Q;      // 64 KB
 constexpr uint32_t K_CHUNK = (BKV / 2) * 128;          // 64 d x 64 keys: 8 KB
 constexpr uint32_t V_CHUNK = BKV * 128;                // 64 d x 128 keys: 16 KB
 constexpr uint32_t SLOT_BYTES = 32768;                 // a K half (4 chunks) or a V half (2)
-constexpr uint32_t P_CHUNK = CQ * 128;                 // 64 keys x 128 rows: 16 KB
-constexpr uint32_t P_BYTES = 2 * P_CHUNK;              // 32 KB per P buffer
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_P = OFF_RING + RING * SLOT_BYTES;  // two P buffers
-constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
-// q_full, full[RING], empty[RING], s_full[2], p_full[2], o_done[2], mma_done
-constexpr uint32_t NUM_BARS = 1 + 2 * RING + 2 + 2 + 2 + 1;
+constexpr uint32_t OFF_BAR = OFF_RING + RING * SLOT_BYTES;
+// q_full, full[RING], empty[RING], s_full, s_free, p_full[2], o_done[2], mma_done
+constexpr uint32_t NUM_BARS = 1 + 2 * RING + 1 + 1 + 2 + 2 + 1;
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 constexpr uint32_t OFF_PEER_ISSUED = OFF_ABORT + 4;
-// P-ready signals: per softmax warp a 16-byte source (in the peer) and
-// destination (in the leader) of the signalling copy.
+// Signalling copies, 16 bytes per softmax warp: destinations in the leader
+// for p_full and for s_free, then the sources (read in the peer).
 constexpr uint32_t OFF_SIG = (OFF_PEER_ISSUED + 4 + 15) / 16 * 16;
 constexpr uint32_t SIG_BYTES = 16;
-constexpr uint32_t SMEM_BYTES = OFF_SIG + 2 * SM_WARPS * SIG_BYTES + 1024;
+constexpr uint32_t SIG_P = 0, SIG_S = SM_WARPS * SIG_BYTES, SIG_SRC = 2 * SM_WARPS * SIG_BYTES;
+constexpr uint32_t SMEM_BYTES = OFF_SIG + 3 * SM_WARPS * SIG_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "over the 227 KB shared-memory limit per CTA");
-static_assert(OFF_RING % 1024 == 0 && OFF_P % 1024 == 0, "swizzled buffers need 1024-B alignment");
+static_assert(OFF_RING % 1024 == 0, "swizzled buffers need 1024-B alignment");
 static_assert((HD / 64) * K_CHUNK == SLOT_BYTES && 2 * V_CHUNK == SLOT_BYTES, "slot sizes");
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 0;     // S buffers at columns 0 and 128
+constexpr uint32_t S_COL = 0;     // S: columns 0 .. 127 (FP32)
+constexpr uint32_t P_COL = 128;   // P buffers: columns 128 and 192, 64 each (FP16 pairs)
 constexpr uint32_t O_COL = 256;   // O: columns 256 .. 511
 
 // kind::f16, FP32 accumulate, M = 256 (the pair): S = Q K^T with both
-// operands K-major; O += P V with P K-major and V MN-major.
+// operands K-major; O += P V with P K-major (tensor memory) and V MN-major.
 constexpr uint32_t IDESC_QK = (1u << 4) | ((uint32_t)(BKV >> 3) << 17) | ((uint32_t)(PQ >> 4) << 24);
 constexpr uint32_t IDESC_PV =
     (1u << 4) | (1u << 16) | ((uint32_t)(HD >> 3) << 17) | ((uint32_t)(PQ >> 4) << 24);
@@ -97,7 +102,7 @@ struct Params {
 };
 
 struct Bars {
-  uint32_t q_full, full, empty, s_full, p_full, o_done, mma_done;
+  uint32_t q_full, full, empty, s_full, s_free, p_full, o_done, mma_done;
 };
 
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
@@ -166,7 +171,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
   const uint32_t q_addr = base + OFF_Q;
   const uint32_t o_tmem = tmem_base + O_COL;
 
-  auto issue_qk = [&](uint32_t sb) -> bool {
+  auto issue_qk = [&]() -> bool {
     if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag))
       return false;
     ptx::tc_fence_after();
@@ -175,32 +180,36 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
     for (int kk = 0; kk < HD / 16; ++kk) {
       const uint32_t off_q = (uint32_t)(kk >> 2) * CHUNK_Q + (uint32_t)(kk & 3) * 32u;
       const uint32_t off_k = (uint32_t)(kk >> 2) * K_CHUNK + (uint32_t)(kk & 3) * 32u;
-      ptx::mma_f16_pair(tmem_base + S_COL + sb * BKV, smem_desc_sw128(q_addr + off_q, 16, 1024),
+      ptx::mma_f16_pair(tmem_base + S_COL, smem_desc_sw128(q_addr + off_q, 16, 1024),
                         smem_desc_sw128(k_addr + off_k, 16, 1024), IDESC_QK, kk > 0 ? 1u : 0u);
     }
     ptx::mma_commit_pair(b.empty + 8 * pos.stage, 0x3);
-    ptx::mma_commit_pair(b.s_full + 8 * sb, 0x3);
+    ptx::mma_commit_pair(b.s_full, 0x3);
     ring_advance(pos, RING);
     return true;
   };
 
-  bool ok = issue_qk(0);
+  bool ok = issue_qk();
   for (int j = 0; j < p.nkv && ok; ++j) {
-    if (j + 1 < p.nkv && !issue_qk((uint32_t)(j + 1) & 1u)) break;
-    // The split barrier's WAIT: both CTAs' P rows are in shared memory.
+    if (j + 1 < p.nkv) {
+      // S_{j+1} overwrites S_j once both CTAs hold S_j in registers.
+      if (!wait_phase(b.s_free, (uint32_t)j & 1u, p, abort_flag)) break;
+      ptx::tc_fence_after();
+      if (!issue_qk()) break;
+    }
+    // The split barrier's WAIT: both CTAs' P rows are in tensor memory.
     const uint32_t pb = (uint32_t)j & 1u;
     if (!wait_phase(b.p_full + 8 * pb, ((uint32_t)j >> 1) & 1u, p, abort_flag)) break;
     ptx::tc_fence_after();
     if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag)) break;
     ptx::tc_fence_after();
     const uint32_t v_addr = base + OFF_RING + pos.stage * SLOT_BYTES;
+    const uint32_t p_tmem = tmem_base + P_COL + pb * (BKV / 2);
 #pragma unroll
-    for (int kk = 0; kk < BKV / 16; ++kk) {
-      const uint32_t off_p = pb * P_BYTES + (uint32_t)(kk >> 2) * P_CHUNK + (uint32_t)(kk & 3) * 32u;
-      ptx::mma_f16_pair(o_tmem, smem_desc_sw128(base + OFF_P + off_p, 16, 1024),
-                        smem_desc_sw128(v_addr + (uint32_t)kk * 2048u, V_CHUNK, 1024), IDESC_PV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-    }
+    for (int kk = 0; kk < BKV / 16; ++kk)   // 16 keys = 8 columns of P per MMA
+      ptx::mma_f16_pair_tmem_a(o_tmem, p_tmem + (uint32_t)kk * 8u,
+                               smem_desc_sw128(v_addr + (uint32_t)kk * 2048u, V_CHUNK, 1024),
+                               IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
     ptx::mma_commit_pair(b.empty + 8 * pos.stage, 0x3);
     ptx::mma_commit_pair(b.o_done + 8 * pb, 0x3);
     ring_advance(pos, RING);
@@ -213,19 +222,30 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
                                              uint32_t rank, uint32_t warp, uint32_t lane, int q0,
                                              int h, int bz, volatile int* abort_flag) {
   const uint32_t quarter = warp & 3u;
-  const uint32_t row = quarter * 32u + lane;      // row within this CTA's 128
   const uint32_t t_lane = (quarter * 32u) << 16;
-  const uint32_t sw = row & 7u;
   const uint32_t leader_p_full = ptx::map_to_cta(b.p_full, 0);
-  const uint32_t sig_dst = ptx::map_to_cta(base + OFF_SIG + (warp - 2) * SIG_BYTES, 0);
-  const uint32_t sig_src = base + OFF_SIG + (SM_WARPS + warp - 2) * SIG_BYTES;
+  const uint32_t leader_s_free = ptx::map_to_cta(b.s_free, 0);
+  const uint32_t sig_p = ptx::map_to_cta(base + OFF_SIG + SIG_P + (warp - 2) * SIG_BYTES, 0);
+  const uint32_t sig_s = ptx::map_to_cta(base + OFF_SIG + SIG_S + (warp - 2) * SIG_BYTES, 0);
+  const uint32_t sig_src = base + OFF_SIG + SIG_SRC + (warp - 2) * SIG_BYTES;
+  // One arrival on a leader barrier per warp: the leader's warps arrive
+  // expecting 16 bytes, the peer's send them.
+  auto signal = [&](uint32_t local_bar, uint32_t leader_bar, uint32_t dst) {
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (rank == 0)
+        ptx::mbar_arrive_expect_tx(local_bar, SIG_BYTES);
+      else
+        ptx::bulk_copy_to_cluster(dst, sig_src, SIG_BYTES, leader_bar);
+    }
+  };
   const float sl2 = p.scale_log2;
   float m = -INFINITY;
   float l = 0.f;
   bool ok = true;
   for (int j = 0; j < p.nkv; ++j) {
-    const uint32_t sb = (uint32_t)j & 1u;
-    bool got = wait_phase(b.s_full + 8 * sb, ((uint32_t)j >> 1) & 1u, p, abort_flag);
+    bool got = wait_phase(b.s_full, (uint32_t)j & 1u, p, abort_flag);
     if (!__all_sync(0xffffffffu, got)) {
       ok = false;
       break;
@@ -234,9 +254,11 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
     uint32_t s[BKV];
 #pragma unroll
     for (int c = 0; c < BKV / 32; ++c)
-      ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + S_COL + sb * BKV + 32u * c,
+      ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + S_COL + 32u * c,
                               *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
     ptx::tmem_ld_wait();
+    // S_j is in registers: S_{j+1} may overwrite it.
+    if (j + 1 < p.nkv) signal(b.s_free, leader_s_free, sig_s);
     const int valid = p.seq_kv - j * BKV;
     float alpha;
     const float m_new = block_offset<BKV>(s, sl2, valid, m, &alpha);
@@ -251,14 +273,12 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
         ok = false;
         break;
       }
+      ptx::tc_fence_after();
     }
-    // P row -> shared memory: keys 0-63 and 64-127 in two 128-byte-swizzled
-    // chunks (16-byte group g of row r at position g ^ (r mod 8)).
-    const uint32_t p_row = base + OFF_P + pb * P_BYTES + row * 128u;
-#pragma unroll
-    for (uint32_t g = 0; g < 16; ++g)
-      ptx::st_shared_v4(p_row + (g >> 3) * P_CHUNK + (((g & 7u) ^ sw) << 4), pk[4 * g],
-                        pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+    // P row -> tensor memory: column c of the buffer holds keys 2c, 2c+1.
+    const uint32_t p_tmem = tmem_base + t_lane + P_COL + pb * (BKV / 2);
+    ptx::tmem_st_32x32b_x32(p_tmem, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+    ptx::tmem_st_32x32b_x32(p_tmem + 32u, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
     if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
       // Compensation: O *= alpha once O += P V of block j-1 has landed.
       const uint32_t ob = (uint32_t)(j - 1) & 1u;
@@ -278,18 +298,10 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
         ptx::tmem_st_32x32b_x32(ta, o);
       }
-      ptx::tmem_st_wait();
     }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncwarp();
+    ptx::tmem_st_wait();
     // The split barrier's ARRIVE (one per warp, on the leader's barrier) ...
-    if (lane == 0) {
-      if (rank == 0)
-        ptx::mbar_arrive_expect_tx(b.p_full + 8 * pb, SIG_BYTES);
-      else
-        ptx::bulk_copy_to_cluster(sig_dst, sig_src, SIG_BYTES, leader_p_full + 8 * pb);
-    }
+    signal(b.p_full + 8 * pb, leader_p_full + 8 * pb, sig_p);
     // ... and the window: the deferred sum update.
     l = l * alpha + lsum;
     m = m_new;
@@ -378,7 +390,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   b.full = b.q_full + 8;
   b.empty = b.full + 8 * RING;
   b.s_full = b.empty + 8 * RING;
-  b.p_full = b.s_full + 16;
+  b.s_free = b.s_full + 8;
+  b.p_full = b.s_free + 8;
   b.o_done = b.p_full + 16;
   b.mma_done = b.o_done + 16;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
@@ -394,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(b.empty + 8 * s, 1);
     }
     ptx::mbar_init(b.s_full, 1);
-    ptx::mbar_init(b.s_full + 8, 1);
+    ptx::mbar_init(b.s_free, SM_WARPS);  // leader warps (+ the peer's bytes)
     for (int k = 0; k < 2; ++k) {
       ptx::mbar_init(b.p_full + 8 * k, SM_WARPS);  // leader warps (+ the peer's bytes)
       ptx::mbar_init(b.o_done + 8 * k, 1);

@@ -367,6 +367,20 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, u
       : "memory");
 }
 
+// Same, with A read from tensor memory: each CTA of the pair supplies its
+// 128 rows of A at `a_tmem` in its own tensor memory (lane = row, a 32-bit
+// column = two consecutive K elements, the lower K index in the low half).
+__device__ __forceinline__ void mma_f16_pair_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
+                                                    uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // One arrive on the barrier at offset `bar` in every CTA of `cta_mask` once
 // the pair MMAs issued so far by this thread have completed.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {

@@ -5,10 +5,14 @@
 //   q_full, full[s]   leader: one arrive.expect_tx (both CTAs' bytes) by the
 //                     leader producer, completed by each CTA's copy;
 //   empty[c][s]       both CTAs: the MMA's multicast commit;
-//   s_full[c][b]      both CTAs: multicast commit after S = Q K^T of a block;
-//   p_full[b]         leader: four arrive.expect_tx(16) by the leader's
+//   s_full[c]         both CTAs: multicast commit after S = Q K^T of a block
+//                     (one S buffer);
+//   s_free, p_full[b] leader: four arrive.expect_tx(16) by the leader's
 //                     softmax warps, 16 bytes from each peer warp's
 //                     signalling copy (which lands at any later time);
+//                     s_free once all eight warps hold S_j in registers
+//                     (not sent for the last block), p_full[b] once they
+//                     wrote their rows of P_j into P buffer b;
 //   o_done[c][b]      both CTAs: multicast commit after O += P V from P
 //                     buffer b.
 // Copies land in any order; tensor-core work and commits complete in issue
@@ -20,9 +24,9 @@
 //   * a ring slot is refilled only after the MMAs reading it completed, and
 //     the MMA reads the tile (K_j or V_j) the schedule says, fully landed,
 //     in both CTAs;
-//   * S = Q K^T of block j overwrites an S buffer only after all eight
-//     softmax warps read the block that used it before; the softmax reads
-//     S_j only after it was written;
+//   * S = Q K^T of block j overwrites the S buffer only after all eight
+//     softmax warps read block j-1 from it; the softmax reads S_j only
+//     after it was written;
 //   * a softmax warp overwrites a P buffer only after O += P V that read it
 //     completed; O += P V of block j runs only after all eight warps wrote
 //     their rows of P_j;
@@ -65,12 +69,12 @@ struct Sim {
   MBar q_full;
   std::vector<MBar> full;
   std::vector<MBar> empty[2];
-  MBar s_full[2][2], p_full[2], o_done[2][2];
+  MBar s_full[2], s_free, p_full[2], o_done[2][2];
   std::vector<SlotState> st[2];
   std::vector<Tile> tag[2];
-  // S buffers (per CTA): block held, warps that read it; P buffers (per CTA):
+  // S buffer (per CTA): block held, warps that read it; P buffers (per CTA):
   // block written, warps done; O: last block accumulated, P V in flight.
-  int s_block[2][2] = {{-1, -1}, {-1, -1}}, s_reads[2][2] = {{0, 0}, {0, 0}};
+  int s_block[2] = {-1, -1}, s_reads[2] = {0, 0};
   int p_block[2][2] = {{-1, -1}, {-1, -1}}, p_writes[2][2] = {{0, 0}, {0, 0}};
   int p_read_done[2][2] = {{-1, -1}, {-1, -1}};  // last block whose P V finished, per buffer
   int o_done_block = -1;                         // last block with O += P V completed
@@ -158,23 +162,27 @@ struct Sim {
     };
     auto issue_qk = [&](int j) {
       const uint32_t s = consume({true, j});
-      const int sb = j & 1;
-      sch.tc_queue.push_back([this, j, sb] {  // S = Q K^T executes: writes S buffer sb
+      sch.tc_queue.push_back([this, j] {  // S = Q K^T executes: writes the S buffer
         for (int c = 0; c < 2; ++c) {
-          if (s_block[c][sb] >= 0 && s_reads[c][sb] != WARPS)
-            fail("S = Q K^T overwrites an S buffer the softmax has not read");
-          s_block[c][sb] = j;
-          s_reads[c][sb] = 0;
+          if (s_block[c] >= 0 && s_reads[c] != WARPS)
+            fail("S = Q K^T overwrites the S buffer before the softmax read it");
+          s_block[c] = j;
+          s_reads[c] = 0;
         }
       });
       release(s);
-      sch.tc_queue.push_back([this, sb] {
-        for (int c = 0; c < 2; ++c) s_full[c][sb].arrive(-1);
+      sch.tc_queue.push_back([this] {
+        for (int c = 0; c < 2; ++c) s_full[c].arrive(-1);
       });
     };
     issue_qk(0);
     for (int j = 0; j < nkv; ++j) {
-      if (j + 1 < nkv) issue_qk(j + 1);
+      if (j + 1 < nkv) {
+#ifndef PLANT_SKIP_S_FREE_WAIT  // defined only by the test that plants this mistake
+        wait_phase(r, s_free, j);
+#endif
+        issue_qk(j + 1);
+      }
       const int pb = j & 1;
       wait_phase(r, p_full[pb], j >> 1);
       const uint32_t s = consume({false, j});
@@ -202,10 +210,16 @@ struct Sim {
     const int r = 3 + cta * WARPS + w;
     sch.start(r);
     for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1, pb = j & 1;
-      wait_phase(r, s_full[cta][sb], j >> 1);
-      if (s_block[cta][sb] != j) fail("softmax reads an S buffer that does not hold its block");
-      s_reads[cta][sb] += 1;
+      const int pb = j & 1;
+      wait_phase(r, s_full[cta], j);
+      if (s_block[cta] != j) fail("softmax reads an S buffer that does not hold its block");
+      s_reads[cta] += 1;
+      if (j + 1 < nkv) {
+        if (cta == 0)
+          s_free.arrive_expect_tx(r, SIG);
+        else
+          sch.copies.push_back({[this] { s_free.complete_tx(SIG); }});
+      }
       sch.role_yield(r);  // exp2, packing
       if (j >= 2) wait_phase(r, o_done[cta][pb], (j - 2) >> 1);
       if (p_block[cta][pb] != j) {  // the first warp to write P_j into this buffer
@@ -264,12 +278,12 @@ int main(int argc, char** argv) {
       for (int c = 0; c < 2; ++c)
         sim->empty[c][s].init("empty[" + std::to_string(c) + "][" + std::to_string(s) + "]", 1);
     }
+    sim->s_free.init("s_free", WARPS, true);
+    for (int c = 0; c < 2; ++c) sim->s_full[c].init("s_full[" + std::to_string(c) + "]", 1);
     for (int b = 0; b < 2; ++b) {
       sim->p_full[b].init("p_full[" + std::to_string(b) + "]", WARPS, true);
-      for (int c = 0; c < 2; ++c) {
-        sim->s_full[c][b].init("s_full[" + std::to_string(c) + "][" + std::to_string(b) + "]", 1);
+      for (int c = 0; c < 2; ++c)
         sim->o_done[c][b].init("o_done[" + std::to_string(c) + "][" + std::to_string(b) + "]", 1);
-      }
     }
     std::vector<std::function<void()>> roles;
     roles.push_back([sim] { sim->producer(0); });
@@ -302,9 +316,11 @@ int main(int argc, char** argv) {
       const int uses = nkv / 2 + (b < nkv % 2 ? 1 : 0);
       if (sim->p_full[b].completions != uses) fail("p_full phase count mismatch");
       for (int c = 0; c < 2; ++c)
-        if (sim->s_full[c][b].completions != uses || sim->o_done[c][b].completions != uses)
-          fail("s_full / o_done phase count mismatch");
+        if (sim->o_done[c][b].completions != uses) fail("o_done phase count mismatch");
     }
+    for (int c = 0; c < 2; ++c)
+      if (sim->s_full[c].completions != nkv) fail("s_full phase count mismatch");
+    if (sim->s_free.completions != nkv - 1) fail("s_free phase count mismatch");
     if (sim->q_full.completions != 1) fail("q_full phase count mismatch");
     if (!sim->sch.copies.empty() || !sim->sch.tc_queue.empty()) fail("work left in flight");
     delete sim;

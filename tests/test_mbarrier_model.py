@@ -29,7 +29,7 @@ PAIR_EXE = os.path.join(BUILD, "pair_model")
 ATTN_EXE = os.path.join(BUILD, "attn_pair_model")
 
 
-def _build(src, exe):
+def _build(src, exe, defines=()):
     if shutil.which("g++") is None:
         pytest.skip("g++ not available")
     os.makedirs(BUILD, exist_ok=True)
@@ -37,8 +37,8 @@ def _build(src, exe):
             os.path.join(HERE, "mbarrier_model", "mbar_model.h")]
     if not os.path.exists(exe) or any(os.path.getmtime(d) > os.path.getmtime(exe) for d in deps):
         tmp = exe + f".tmp{os.getpid()}"
-        subprocess.run(["g++", "-std=c++17", "-O2", "-pthread", "-I", CSRC, src, "-o", tmp],
-                       check=True)
+        subprocess.run(["g++", "-std=c++17", "-O2", "-pthread", *[f"-D{d}" for d in defines],
+                        "-I", CSRC, src, "-o", tmp], check=True)
         os.replace(tmp, exe)
     return exe
 
@@ -141,7 +141,7 @@ def test_pair_fault_on_other_pair_does_not_affect_this_one(pair_model):
 
 # (ring slots, key blocks, seeds): 1 and 2 blocks (no reuse), odd / even
 # counts, the kernel's 3-slot ring and others
-ATTN_CASES = [(3, 1, 100), (3, 2, 100), (3, 5, 100), (3, 8, 60), (2, 6, 100), (4, 7, 60),
+ATTN_CASES = [(5, 1, 100), (5, 2, 100), (5, 5, 100), (5, 8, 60), (2, 6, 100), (3, 7, 60),
               (1, 4, 60)]
 
 
@@ -152,5 +152,13 @@ def test_attention_pair_protocol_interleavings(attn_model, case):
 
 
 def test_attention_pair_fault_blocks_the_mma_on_the_starved_fill(attn_model):
-    rc, out = _run(attn_model, 3, 4, 20, "fault")
+    rc, out = _run(attn_model, 5, 4, 20, "fault")
     assert rc == 0 and out.startswith("DEADLOCK-AS-EXPECTED"), out
+
+
+def test_attention_pair_model_catches_s_overwritten_before_it_is_read():
+    # The same replay with the MMA thread's wait on s_free left out: S of the
+    # next block may then land before every softmax warp has read S.
+    exe = _build(ATTN_SRC, ATTN_EXE + "_planted", defines=("PLANT_SKIP_S_FREE_WAIT",))
+    rc, out = _run(exe, 5, 6, 100)
+    assert rc != 0 and "overwrites the S buffer" in out, out
