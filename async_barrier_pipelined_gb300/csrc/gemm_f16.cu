@@ -739,6 +739,7 @@ struct gemm_f16_plan_s {
   int sm_limit = 0;    // most SMs a launch may use (0: all)
   int attn_kernel = 0; // attention: 0 auto (CTA pair), 1 single CTA, 2 CTA pair
   int max_pairs = 0;   // co-resident clusters of two for the pair kernel
+  int attn_pairs = 0;  // co-resident clusters of two for the pair attention kernel
   void* ws = nullptr;
   size_t ws_bytes = 0;
   std::vector<OrderTable> orders;
@@ -921,7 +922,7 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
             "cudaFuncSetAttribute(pair attention kernel smem)");
   // Co-resident clusters of two for each pair-kernel instance; keep the
   // smaller count (0 if the query fails: the pair kernel is then not used).
-  int max_clusters = 0;
+  int max_clusters = 0, attn_clusters = 0;
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(prop.multiProcessorCount / 2 * 2), 1, 1);
@@ -945,12 +946,20 @@ int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
       n512 = 0;
     }
     max_clusters = std::min(n256, n512);
+    cfg.blockDim = dim3(attnp::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = attnp::SMEM_BYTES;
+    if (cudaOccupancyMaxActiveClusters(&attn_clusters, attnp::attn_f16_fwd_pair_kernel, &cfg) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      attn_clusters = 0;
+    }
   }
   gemm_f16_plan_s* p = new (std::nothrow) gemm_f16_plan_s();
   if (!p) return GEMM_F16_ERR_OOM;
   p->device = device;
   p->num_sms = prop.multiProcessorCount;
   p->max_pairs = max_clusters;
+  p->attn_pairs = attn_clusters;
   cudaError_t e = cudaHostAlloc(&p->status_host, sizeof(int), cudaHostAllocMapped);
   if (e != cudaSuccess) {
     delete p;
@@ -1693,7 +1702,7 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
                              V, v_strides, O, o_strides, scale);
   if (rc) return rc;
   DeviceGuard g(p->device);
-  const bool use_pair = p->attn_kernel != 1;
+  const bool use_pair = p->attn_kernel != 1 && p->attn_pairs > 0;
   CUtensorMap tmQ, tmK, tmV, tmO;
   if ((rc = cached_encode_bhsd(p, &tmQ, Q, batch, heads, seq_q, q_strides, attn::BQ))) return rc;
   if ((rc = cached_encode_bhsd(p, &tmK, K, batch, heads, seq_kv, k_strides, 64))) return rc;
@@ -1705,11 +1714,21 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
     prm.seq_q = seq_q;
     prm.seq_kv = seq_kv;
     prm.nkv = (int)ceil_div(seq_kv, attnp::BKV);
+    prm.n_qt = (int)ceil_div(seq_q, attnp::PQ);
+    prm.heads = heads;
+    const int64_t items = (int64_t)batch * heads * prm.n_qt;
+    if (items > INT32_MAX - 65536) return GEMM_F16_ERR_INVALID_ARG;  // item + clusters fits
+    prm.n_items = (int)items;
     prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     prm.status = p->status_dev;
     prm.timeout_ns = p->timeout_ns;
-    prm.fault_pair = p->fault_unit;
-    const dim3 grid((unsigned)(2 * ceil_div(seq_q, attnp::PQ)), (unsigned)heads, (unsigned)batch);
+    prm.fault_item = p->fault_unit;
+    // Persistent: one cluster per co-resident pair slot (fewer under an SM
+    // limit), never more than there are items.
+    int64_t clusters = p->attn_pairs;
+    if (p->sm_limit > 0) clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, p->sm_limit / 2));
+    clusters = std::min<int64_t>(clusters, items);
+    const dim3 grid((unsigned)(2 * clusters), 1, 1);
     attnp::attn_f16_fwd_pair_kernel<<<grid, attnp::NUM_THREADS, attnp::SMEM_BYTES,
                                       (cudaStream_t)stream>>>(tmQ, tmK, tmV, tmO, prm);
     GF16_CUDA(cudaGetLastError(), "launch attn_f16_fwd_pair_kernel");

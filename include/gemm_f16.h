@@ -88,12 +88,17 @@ typedef enum gemm_f16_option {
     GEMM_F16_OPT_TILE_WIDTH = 5,
     /* Most SMs one launch may occupy (0 = all of them), e.g. to leave SMs
      * to work on other streams.  The tile schedules are planned for the
-     * full device either way. */
+     * full device either way.  Also bounds the persistent CTA-pair
+     * attention kernel (one cluster of two CTAs per two SMs); the
+     * single-CTA attention kernel launches one CTA per 128 query rows and
+     * ignores it. */
     GEMM_F16_OPT_SM_LIMIT = 6,
     /* Attention kernel (attn_f16_fwd in attn_f16.h): 0 = automatic (the
      * CTA-pair kernel), 1 = single-CTA kernel (128 query rows, blocks of 64
      * keys), 2 = CTA-pair kernel (256 query rows over two SMs, blocks of
-     * 128 keys).  Results agree within the usual tolerance. */
+     * 128 keys; persistent: each cluster of two CTAs works through several
+     * (batch, head, 256-row) items).  Results agree within the usual
+     * tolerance and do not depend on the number of clusters. */
     GEMM_F16_OPT_ATTN_KERNEL = 7
 } gemm_f16_option;
 

@@ -1,20 +1,31 @@
-// Host replay of the CTA-pair attention kernel's barrier protocol.
+// Host replay of the CTA-pair attention kernel's barrier protocol, for one
+// cluster that works through several items (256 query rows each).
 //
-// Roles: 0 leader producer, 1 peer producer, 2 MMA issuer (leader), 3..6 the
-// leader's softmax warps, 7..10 the peer's.  Barriers as in the kernel:
+// Roles: 0 leader producer, 1 peer producer, 2 MMA issuer (leader), 3..10
+// the softmax warps (CTA c, warp w: 3 + 4c + w), 11..18 the epilogue warps
+// (11 + 4c + e).  Barriers as in the kernel:
 //   q_full, full[s]   leader: one arrive.expect_tx (both CTAs' bytes) by the
 //                     leader producer, completed by each CTA's copy;
+//   q_empty[c]        both CTAs: the MMA's multicast commit after an item's
+//                     last S = Q K^T;
 //   empty[c][s]       both CTAs: the MMA's multicast commit;
 //   s_full[c]         both CTAs: multicast commit after S = Q K^T of a block
 //                     (one S buffer);
-//   s_free, p_full[b] leader: four arrive.expect_tx(16) by the leader's
-//                     softmax warps, 16 bytes from each peer warp's
-//                     signalling copy (which lands at any later time);
-//                     s_free once all eight warps hold S_j in registers
-//                     (not sent for the last block), p_full[b] once they
-//                     wrote their rows of P_j into P buffer b;
+//   s_free, p_full[b], o_free
+//                     leader: four arrive.expect_tx(16) by the leader's
+//                     softmax (epilogue) warps, 16 bytes from each peer
+//                     warp's signalling copy (which lands at any later time);
+//                     s_free once all eight softmax warps hold S in registers
+//                     (not sent after the cluster's last block), p_full[b]
+//                     once they wrote their rows of P into P buffer b, o_free
+//                     once all eight epilogue warps read O (not sent after
+//                     the last item);
 //   o_done[c][b]      both CTAs: multicast commit after O += P V from P
-//                     buffer b.
+//                     buffer b;
+//   l_ready[c], l_free[c]
+//                     per CTA: four arrivals by the softmax (epilogue) warps
+//                     handing an item's row sums over (l_free not after the
+//                     last item).
 // Copies land in any order; tensor-core work and commits complete in issue
 // order.  Checked on every interleaving:
 //   * no deadlock;
@@ -22,22 +33,26 @@
 //     completed (a parity wait can neither run ahead of the barrier nor be
 //     satisfied by a later phase);
 //   * a ring slot is refilled only after the MMAs reading it completed, and
-//     the MMA reads the tile (K_j or V_j) the schedule says, fully landed,
-//     in both CTAs;
-//   * S = Q K^T of block j overwrites the S buffer only after all eight
-//     softmax warps read block j-1 from it; the softmax reads S_j only
-//     after it was written;
+//     the MMA reads the tile (item, K_j or V_j) the schedule says, fully
+//     landed, in both CTAs; Q of an item is overwritten only after the last
+//     S = Q K^T of the item before ran, and S reads the Q of its own item,
+//     fully landed;
+//   * S = Q K^T overwrites the S buffer only after all eight softmax warps
+//     read the block before; the softmax reads S only after it was written;
 //   * a softmax warp overwrites a P buffer only after O += P V that read it
-//     completed; O += P V of block j runs only after all eight warps wrote
-//     their rows of P_j;
+//     completed; O += P V of a block runs only after all eight warps wrote
+//     their rows of its P;
 //   * the compensation (O *= alpha, done by some warps in some blocks) runs
-//     only after O += P V of block j-1 completed and before that of block j;
-//     the epilogue reads O only after the last O += P V;
+//     only after O += P V of the item's previous block completed and before
+//     that of the current block;
+//   * the epilogue reads O of an item only after its last O += P V and
+//     before the next item's first one, and the row sums of that item;
+//     the softmax overwrites the row sums only after the epilogue read them;
 //   * no role arrives twice on a phase; phase counts balance at the end.
 // With a fault (the leader issues no copy for its first ring fill) the
 // replay must stop with the MMA role blocked on that fill.
 //
-// Usage: attn_pair_model RING NKV SEEDS [fault]
+// Usage: attn_pair_model RING NKV ITEMS SEEDS [fault]
 // Prints "OK <n>" or "FAIL <reason>" / "DEADLOCK <where>".
 
 #include "mbar_model.h"
@@ -50,38 +65,48 @@ using mbmodel::MBar;
 namespace {
 
 constexpr uint32_t Q_BYTES = 65536, SLOT_BYTES = 32768, SIG = 16;
-constexpr int WARPS = 4;                // softmax warps per CTA
-constexpr int NROLES = 3 + 2 * WARPS;
+constexpr int WARPS = 4;                // softmax (and epilogue) warps per CTA
+constexpr int MMA_ROLE = 2;
+constexpr int NROLES = 3 + 4 * WARPS;
 
 enum SlotState { FREE, FILLING, FULL, READING };
 
 struct Tile {
+  int item;
   bool is_k;
   int j;
-  bool operator!=(const Tile& o) const { return is_k != o.is_k || j != o.j; }
+  bool operator!=(const Tile& o) const { return item != o.item || is_k != o.is_k || j != o.j; }
 };
 
 struct Sim {
-  int ring = 3, nkv = 1;
+  int ring = 4, nkv = 1, items = 1;
   bool fault = false;
   uint64_t seed = 1;
   mbmodel::Scheduler sch{NROLES};
-  MBar q_full;
+  MBar q_full, q_empty[2], s_full[2], s_free, p_full[2], o_free, l_ready[2], l_free[2];
   std::vector<MBar> full;
   std::vector<MBar> empty[2];
-  MBar s_full[2], s_free, p_full[2], o_done[2][2];
+  MBar o_done[2][2];
   std::vector<SlotState> st[2];
   std::vector<Tile> tag[2];
-  // S buffer (per CTA): block held, warps that read it; P buffers (per CTA):
-  // block written, warps done; O: last block accumulated, P V in flight.
+  // Q buffer (per CTA): item held, copy landed; the item whose last S ran.
+  int q_item[2] = {-1, -1};
+  bool q_landed[2] = {false, false};
+  int last_s_item_done = -1;
+  // S buffer (per CTA): global block held, warps that read it.  P buffers
+  // (per CTA): global block written, warps done, last global block whose
+  // P V finished reading it.
   int s_block[2] = {-1, -1}, s_reads[2] = {0, 0};
   int p_block[2][2] = {{-1, -1}, {-1, -1}}, p_writes[2][2] = {{0, 0}, {0, 0}};
-  int p_read_done[2][2] = {{-1, -1}, {-1, -1}};  // last block whose P V finished, per buffer
-  int o_done_block = -1;                         // last block with O += P V completed
-  int pv_started = -1;                           // last block whose P V began executing
+  int p_read_done[2][2] = {{-1, -1}, {-1, -1}};
+  // O: item and block of the last O += P V that completed / began.
+  int o_done_item = -1, o_done_j = -1, pv_started_item = -1, pv_started_j = -1;
+  int o_read_item[2][WARPS] = {{-1, -1, -1, -1}, {-1, -1, -1, -1}};  // epilogue reads of O
+  int l_item[2][WARPS] = {{-1, -1, -1, -1}, {-1, -1, -1, -1}};       // row sums written (softmax)
+  int l_read_item[2][WARPS] = {{-1, -1, -1, -1}, {-1, -1, -1, -1}};  // row sums read (epilogue)
 
-  static bool rescale(uint64_t seed, int j, int warp) {
-    const uint64_t h = (seed * 0x9E3779B97F4A7C15ull) ^ ((uint64_t)j * 0xBF58476D1CE4E5B9ull) ^
+  static bool rescale(uint64_t seed, int g, int warp) {
+    const uint64_t h = (seed * 0x9E3779B97F4A7C15ull) ^ ((uint64_t)g * 0xBF58476D1CE4E5B9ull) ^
                        ((uint64_t)warp * 0x94D049BB133111EBull);
     return ((h >> 29) % 3) == 0;
   }
@@ -94,12 +119,25 @@ struct Sim {
            std::to_string(bar.completions) + " phases completed");
   }
 
-  // The consumption order of the ring: K_0, then per block j: K_{j+1}, V_j.
+  // A leader barrier counted in warps: the leader's warp arrives expecting
+  // 16 bytes, the peer's sends them.
+  void signal(int r, int cta, MBar& bar) {
+    if (cta == 0)
+      bar.arrive_expect_tx(r, SIG);
+    else
+      sch.copies.push_back({[&bar] { bar.complete_tx(SIG); }});
+  }
+
+  // The consumption order of the ring: per item K_0, then per block j:
+  // K_{j+1}, V_j.
   std::vector<Tile> order() const {
-    std::vector<Tile> o{{true, 0}};
-    for (int j = 0; j < nkv; ++j) {
-      if (j + 1 < nkv) o.push_back({true, j + 1});
-      o.push_back({false, j});
+    std::vector<Tile> o;
+    for (int k = 0; k < items; ++k) {
+      o.push_back({k, true, 0});
+      for (int j = 0; j < nkv; ++j) {
+        if (j + 1 < nkv) o.push_back({k, true, j + 1});
+        o.push_back({k, false, j});
+      }
     }
     return o;
   }
@@ -107,35 +145,49 @@ struct Sim {
   void producer(int cta) {
     const int r = cta;
     sch.start(r);
-    if (cta == 0) q_full.arrive_expect_tx(r, 2 * Q_BYTES);
-    sch.copies.push_back({[this] { q_full.complete_tx(Q_BYTES); }});
     RingPos pos{0, 0};
     int fill = 0;
-    for (const Tile& t : order()) {
-      const uint32_t s = pos.stage;
-      const int k = (int)(fill / ring);  // this slot's use index
-      if (k > 0) wait_phase(r, empty[cta][s], k - 1);
-      if (st[cta][s] != FREE) fail("producer refills a slot still in use");
-      if (cta == 0) full[s].arrive_expect_tx(r, 2 * SLOT_BYTES);
-      st[cta][s] = FILLING;
-      tag[cta][s] = t;
-      if (!(fault && fill == 0 && cta == 0)) {
-        sch.copies.push_back({[this, cta, s] {
-          st[cta][s] = FULL;
-          full[s].complete_tx(SLOT_BYTES);
-        }});
+    const std::vector<Tile> ord = order();
+    size_t next = 0;
+    for (int k = 0; k < items; ++k) {
+      if (k > 0) {
+        wait_phase(r, q_empty[cta], k - 1);
+        if (last_s_item_done != k - 1) fail("Q overwritten before the last S of its item ran");
       }
-      ++fill;
-      gf16::ring_advance(pos, (uint32_t)ring);
+      if (cta == 0) q_full.arrive_expect_tx(r, 2 * Q_BYTES);
+      q_item[cta] = k;
+      q_landed[cta] = false;
+      sch.copies.push_back({[this, cta] {
+        q_landed[cta] = true;
+        q_full.complete_tx(Q_BYTES);
+      }});
       sch.role_yield(r);
+      for (; next < ord.size() && ord[next].item == k; ++next) {
+        const Tile t = ord[next];
+        const uint32_t s = pos.stage;
+        const int use = fill / ring;  // this slot's use index
+        if (use > 0) wait_phase(r, empty[cta][s], use - 1);
+        if (st[cta][s] != FREE) fail("producer refills a slot still in use");
+        if (cta == 0) full[s].arrive_expect_tx(r, 2 * SLOT_BYTES);
+        st[cta][s] = FILLING;
+        tag[cta][s] = t;
+        if (!(fault && fill == 0 && cta == 0)) {
+          sch.copies.push_back({[this, cta, s] {
+            st[cta][s] = FULL;
+            full[s].complete_tx(SLOT_BYTES);
+          }});
+        }
+        ++fill;
+        gf16::ring_advance(pos, (uint32_t)ring);
+        sch.role_yield(r);
+      }
     }
     sch.finish(r);
   }
 
   void mma() {
-    const int r = 2;
+    const int r = MMA_ROLE;
     sch.start(r);
-    wait_phase(r, q_full, 0);
     RingPos pos{0, 0};
     int fill = 0;
     const std::vector<Tile> ord = order();
@@ -160,48 +212,70 @@ struct Sim {
         }
       });
     };
-    auto issue_qk = [&](int j) {
-      const uint32_t s = consume({true, j});
-      sch.tc_queue.push_back([this, j] {  // S = Q K^T executes: writes the S buffer
+    // S of global block gs (item k, block j) into the S buffer.
+    auto issue_qk = [&](int gs, int k, int j) {
+#ifndef PLANT_SKIP_S_FREE_WAIT  // the PLANT_* switches are set only by tests planting a mistake
+      if (gs > 0) wait_phase(r, s_free, gs - 1);
+#endif
+      const uint32_t s = consume({k, true, j});
+      const bool last = j == nkv - 1;
+      sch.tc_queue.push_back([this, gs, k, last] {  // S = Q K^T executes
         for (int c = 0; c < 2; ++c) {
+          if (q_item[c] != k || !q_landed[c]) fail("S = Q K^T reads a Q tile not of its item");
           if (s_block[c] >= 0 && s_reads[c] != WARPS)
             fail("S = Q K^T overwrites the S buffer before the softmax read it");
-          s_block[c] = j;
+          s_block[c] = gs;
           s_reads[c] = 0;
         }
+        if (last) last_s_item_done = k;
       });
       release(s);
-      sch.tc_queue.push_back([this] {
-        for (int c = 0; c < 2; ++c) s_full[c].arrive(-1);
+      sch.tc_queue.push_back([this, last] {
+        for (int c = 0; c < 2; ++c) {
+          s_full[c].arrive(-1);
+          if (last) q_empty[c].arrive(-1);
+        }
       });
     };
-    issue_qk(0);
-    for (int j = 0; j < nkv; ++j) {
-      if (j + 1 < nkv) {
-#ifndef PLANT_SKIP_S_FREE_WAIT  // defined only by the test that plants this mistake
-        wait_phase(r, s_free, j);
+    for (int k = 0; k < items; ++k) {
+      const int g0 = k * nkv;
+      wait_phase(r, q_full, k);
+      issue_qk(g0, k, 0);
+      for (int j = 0; j < nkv; ++j) {
+        const int g = g0 + j;
+        if (j + 1 < nkv) issue_qk(g + 1, k, j + 1);
+        const int pb = g & 1;
+        wait_phase(r, p_full[pb], g >> 1);
+        const uint32_t s = consume({k, false, j});
+#ifndef PLANT_SKIP_O_FREE_WAIT
+        if (j == 0 && k > 0) wait_phase(r, o_free, k - 1);
 #endif
-        issue_qk(j + 1);
+        sch.tc_queue.push_back([this, g, k, j, pb] {  // O += P V begins
+          for (int c = 0; c < 2; ++c) {
+            if (p_block[c][pb] != g || p_writes[c][pb] != WARPS)
+              fail("O += P V reads a P buffer not fully written for its block");
+            if (j == 0)
+              for (int e = 0; e < WARPS; ++e)
+                if (k > 0 && o_read_item[c][e] != k - 1)
+                  fail("O += P V overwrites O before the epilogue read it");
+          }
+          if (j == 0 ? (o_done_item != k - 1 || (k > 0 && o_done_j != nkv - 1))
+                     : (o_done_item != k || o_done_j != j - 1))
+            fail("O += P V out of order");
+          pv_started_item = k;
+          pv_started_j = j;
+        });
+        sch.tc_queue.push_back([this, k, j, pb, g] {  // ... and ends
+          o_done_item = k;
+          o_done_j = j;
+          for (int c = 0; c < 2; ++c) p_read_done[c][pb] = g;
+        });
+        release(s);
+        sch.tc_queue.push_back([this, pb] {
+          for (int c = 0; c < 2; ++c) o_done[c][pb].arrive(-1);
+        });
+        sch.role_yield(r);
       }
-      const int pb = j & 1;
-      wait_phase(r, p_full[pb], j >> 1);
-      const uint32_t s = consume({false, j});
-      sch.tc_queue.push_back([this, j, pb] {  // O += P V begins
-        for (int c = 0; c < 2; ++c)
-          if (p_block[c][pb] != j || p_writes[c][pb] != WARPS)
-            fail("O += P V reads a P buffer not fully written for its block");
-        if (o_done_block != j - 1) fail("O += P V out of order");
-        pv_started = j;
-      });
-      sch.tc_queue.push_back([this, j, pb] {  // ... and ends
-        o_done_block = j;
-        for (int c = 0; c < 2; ++c) p_read_done[c][pb] = j;
-      });
-      release(s);
-      sch.tc_queue.push_back([this, pb] {
-        for (int c = 0; c < 2; ++c) o_done[c][pb].arrive(-1);
-      });
-      sch.role_yield(r);
     }
     sch.finish(r);
   }
@@ -209,43 +283,65 @@ struct Sim {
   void softmax(int cta, int w) {
     const int r = 3 + cta * WARPS + w;
     sch.start(r);
-    for (int j = 0; j < nkv; ++j) {
-      const int pb = j & 1;
-      wait_phase(r, s_full[cta], j);
-      if (s_block[cta] != j) fail("softmax reads an S buffer that does not hold its block");
-      s_reads[cta] += 1;
-      if (j + 1 < nkv) {
-        if (cta == 0)
-          s_free.arrive_expect_tx(r, SIG);
-        else
-          sch.copies.push_back({[this] { s_free.complete_tx(SIG); }});
+    for (int k = 0; k < items; ++k) {
+      for (int j = 0; j < nkv; ++j) {
+        const int g = k * nkv + j, pb = g & 1;
+        wait_phase(r, s_full[cta], g);
+        if (s_block[cta] != g) fail("softmax reads an S buffer that does not hold its block");
+        s_reads[cta] += 1;
+        if (j + 1 < nkv || k + 1 < items) signal(r, cta, s_free);
+        sch.role_yield(r);  // exp2, packing
+        if (g >= 2) wait_phase(r, o_done[cta][pb], (g - 2) >> 1);
+        if (p_block[cta][pb] != g) {  // the first warp to write this block's P here
+          if (p_block[cta][pb] >= 0 && p_read_done[cta][pb] != p_block[cta][pb])
+            fail("softmax overwrites a P buffer that O += P V still reads");
+          p_block[cta][pb] = g;
+          p_writes[cta][pb] = 0;
+        } else if (p_read_done[cta][pb] == g) {
+          fail("softmax writes P rows after O += P V of their block ran");
+        }
+        p_writes[cta][pb] += 1;
+        if (j > 0 && rescale(seed, g, cta * WARPS + w)) {
+          wait_phase(r, o_done[cta][(g - 1) & 1], (g - 1) >> 1);
+          if (o_done_item != k || o_done_j != j - 1 ||
+              (pv_started_item == k && pv_started_j >= j))
+            fail("compensation while O += P V is not at the item's previous block");
+          sch.role_yield(r);  // O *= alpha
+        }
+        signal(r, cta, p_full[pb]);
+        sch.role_yield(r);  // the window: the sum update
       }
-      sch.role_yield(r);  // exp2, packing
-      if (j >= 2) wait_phase(r, o_done[cta][pb], (j - 2) >> 1);
-      if (p_block[cta][pb] != j) {  // the first warp to write P_j into this buffer
-        if (p_block[cta][pb] >= 0 && p_read_done[cta][pb] != p_block[cta][pb])
-          fail("softmax overwrites a P buffer that O += P V still reads");
-        p_block[cta][pb] = j;
-        p_writes[cta][pb] = 0;
-      } else if (p_read_done[cta][pb] == j) {
-        fail("softmax writes P rows after O += P V of their block ran");
+      // Row sums to the epilogue warps, once they took the previous ones.
+      if (k > 0) {
+#ifndef PLANT_SKIP_L_FREE_WAIT
+        wait_phase(r, l_free[cta], k - 1);
+#endif
+        for (int e = 0; e < WARPS; ++e)
+          if (l_read_item[cta][e] != k - 1) fail("row sums overwritten before the epilogue read them");
       }
-      p_writes[cta][pb] += 1;
-      if (j > 0 && rescale(seed, j, cta * WARPS + w)) {
-        wait_phase(r, o_done[cta][(j - 1) & 1], (j - 1) >> 1);
-        if (o_done_block != j - 1 || pv_started >= j)
-          fail("compensation while O += P V is not at block j-1");
-        sch.role_yield(r);  // O *= alpha
-      }
-      if (cta == 0) {
-        p_full[pb].arrive_expect_tx(r, SIG);
-      } else {
-        sch.copies.push_back({[this, pb] { p_full[pb].complete_tx(SIG); }});
-      }
-      sch.role_yield(r);  // the window: the sum update
+      l_item[cta][w] = k;
+      l_ready[cta].arrive(r);
     }
-    wait_phase(r, o_done[cta][(nkv - 1) & 1], (nkv - 1) >> 1);
-    if (o_done_block != nkv - 1) fail("epilogue reads O before the last O += P V");
+    sch.finish(r);
+  }
+
+  void epilogue(int cta, int e) {
+    const int r = 3 + 2 * WARPS + cta * WARPS + e;
+    sch.start(r);
+    for (int k = 0; k < items; ++k) {
+      const int g_last = (k + 1) * nkv - 1;
+      wait_phase(r, l_ready[cta], k);
+      for (int w = 0; w < WARPS; ++w)
+        if (l_item[cta][w] != k) fail("epilogue reads row sums not of its item");
+      l_read_item[cta][e] = k;
+      if (k + 1 < items) l_free[cta].arrive(r);
+      wait_phase(r, o_done[cta][g_last & 1], g_last >> 1);
+      if (o_done_item != k || o_done_j != nkv - 1 || pv_started_item != k)
+        fail("epilogue reads O that is not the finished O of its item");
+      o_read_item[cta][e] = k;
+      if (k + 1 < items) signal(r, cta, o_free);
+      sch.role_yield(r);  // scale, stage, store
+    }
     sch.finish(r);
   }
 };
@@ -253,33 +349,40 @@ struct Sim {
 }  // namespace
 
 int main(int argc, char** argv) {
-  if (argc < 4) {
-    std::fprintf(stderr, "usage: attn_pair_model RING NKV SEEDS [fault]\n");
+  if (argc < 5) {
+    std::fprintf(stderr, "usage: attn_pair_model RING NKV ITEMS SEEDS [fault]\n");
     return 2;
   }
-  const int ring = std::atoi(argv[1]), nkv = std::atoi(argv[2]), seeds = std::atoi(argv[3]);
-  const bool fault = argc > 4 && std::string(argv[4]) == "fault";
+  const int ring = std::atoi(argv[1]), nkv = std::atoi(argv[2]), items = std::atoi(argv[3]);
+  const int seeds = std::atoi(argv[4]);
+  const bool fault = argc > 5 && std::string(argv[5]) == "fault";
   for (int seed = 0; seed < seeds; ++seed) {
     Sim* sim = new Sim();  // leaked on deadlock (threads detached)
     sim->ring = ring;
     sim->nkv = nkv;
+    sim->items = items;
     sim->fault = fault;
     sim->seed = (uint64_t)seed + 1;
     sim->sch.seed(0x9E3779B97F4A7C15ull * (uint64_t)(seed + 1));
     sim->q_full.init("q_full", 1, true);
+    sim->s_free.init("s_free", WARPS, true);
+    sim->o_free.init("o_free", WARPS, true);
     sim->full.resize(ring);
     for (int c = 0; c < 2; ++c) {
+      const std::string cs = "[" + std::to_string(c) + "]";
+      sim->q_empty[c].init("q_empty" + cs, 1);
+      sim->s_full[c].init("s_full" + cs, 1);
+      sim->l_ready[c].init("l_ready" + cs, WARPS);
+      sim->l_free[c].init("l_free" + cs, WARPS);
       sim->empty[c].resize(ring);
       sim->st[c].assign(ring, FREE);
-      sim->tag[c].assign(ring, {false, -1});
+      sim->tag[c].assign(ring, {-1, false, -1});
     }
     for (int s = 0; s < ring; ++s) {
       sim->full[s].init("full[" + std::to_string(s) + "]", 1, true);
       for (int c = 0; c < 2; ++c)
         sim->empty[c][s].init("empty[" + std::to_string(c) + "][" + std::to_string(s) + "]", 1);
     }
-    sim->s_free.init("s_free", WARPS, true);
-    for (int c = 0; c < 2; ++c) sim->s_full[c].init("s_full[" + std::to_string(c) + "]", 1);
     for (int b = 0; b < 2; ++b) {
       sim->p_full[b].init("p_full[" + std::to_string(b) + "]", WARPS, true);
       for (int c = 0; c < 2; ++c)
@@ -291,11 +394,13 @@ int main(int argc, char** argv) {
     roles.push_back([sim] { sim->mma(); });
     for (int c = 0; c < 2; ++c)
       for (int w = 0; w < WARPS; ++w) roles.push_back([sim, c, w] { sim->softmax(c, w); });
+    for (int c = 0; c < 2; ++c)
+      for (int e = 0; e < WARPS; ++e) roles.push_back([sim, c, e] { sim->epilogue(c, e); });
     std::string where;
     const int rc = sim->sch.run(roles, &where);
     if (fault) {
       if (rc != 1) fail("fault injected but the replay finished");
-      if (!sim->sch.blocked(2)) fail("fault injected but the MMA role is not blocked");
+      if (!sim->sch.blocked(MMA_ROLE)) fail("fault injected but the MMA role is not blocked");
       std::printf("DEADLOCK-AS-EXPECTED%s\n", where.c_str());
       std::fflush(stdout);
       std::_Exit(0);
@@ -305,23 +410,29 @@ int main(int argc, char** argv) {
       std::fflush(stdout);
       std::_Exit(1);
     }
-    const int fills = 2 * nkv;
+    const int fills = 2 * nkv * items;
     for (int s = 0; s < ring; ++s) {
       const int uses = fills / ring + (s < fills % ring ? 1 : 0);
       if (sim->full[s].completions != uses) fail("full phase count mismatch");
       for (int c = 0; c < 2; ++c)
         if (sim->empty[c][s].completions != uses) fail("empty phase count mismatch");
     }
+    const int blocks = nkv * items;
     for (int b = 0; b < 2; ++b) {
-      const int uses = nkv / 2 + (b < nkv % 2 ? 1 : 0);
+      const int uses = blocks / 2 + (b < blocks % 2 ? 1 : 0);
       if (sim->p_full[b].completions != uses) fail("p_full phase count mismatch");
       for (int c = 0; c < 2; ++c)
         if (sim->o_done[c][b].completions != uses) fail("o_done phase count mismatch");
     }
-    for (int c = 0; c < 2; ++c)
-      if (sim->s_full[c].completions != nkv) fail("s_full phase count mismatch");
-    if (sim->s_free.completions != nkv - 1) fail("s_free phase count mismatch");
-    if (sim->q_full.completions != 1) fail("q_full phase count mismatch");
+    for (int c = 0; c < 2; ++c) {
+      if (sim->s_full[c].completions != blocks) fail("s_full phase count mismatch");
+      if (sim->q_empty[c].completions != items) fail("q_empty phase count mismatch");
+      if (sim->l_ready[c].completions != items || sim->l_free[c].completions != items - 1)
+        fail("l_ready / l_free phase count mismatch");
+    }
+    if (sim->s_free.completions != blocks - 1) fail("s_free phase count mismatch");
+    if (sim->o_free.completions != items - 1) fail("o_free phase count mismatch");
+    if (sim->q_full.completions != items) fail("q_full phase count mismatch");
     if (!sim->sch.copies.empty() || !sim->sch.tc_queue.empty()) fail("work left in flight");
     delete sim;
   }

@@ -249,3 +249,27 @@ def test_invalid_arguments_enqueue_nothing(plan):
         assert e.value.code == code
     torch.cuda.synchronize()
     assert plan.status() == g.OK
+
+
+@pytest.mark.parametrize("skv", [100, 200, 333])
+def test_many_items_per_cluster(plan, skv):
+    """The pair kernel is persistent: under an SM limit a few clusters walk
+    many work items (256 query rows of one batch and head), reloading Q and
+    handing O to the epilogue warps between items.  One to three key blocks
+    per item make the item boundaries come fast.  The output must match the
+    oracle and be bitwise the same for every number of clusters (the
+    single-CTA kernel ignores the limit)."""
+    import async_barrier_pipelined_gb300 as g
+    w = si.attn_custom(2, 3, 600, skv, seed=skv + 7)   # 18 items, ragged last query tile
+    Qb, Kb, Vb = w.bits()
+    want = oracle.attention_f16(Qb, Kb, Vb, w.scale)
+    outs = []
+    try:
+        for limit in (0, 6, 4, 2):
+            plan.set_option(g.OPT_SM_LIMIT, limit)
+            outs.append(_run(plan, Qb, Kb, Vb))
+    finally:
+        plan.set_option(g.OPT_SM_LIMIT, 0)
+    parity.check(outs[0], want, f"skv {skv}")
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint64), outs[0].view(np.uint64))

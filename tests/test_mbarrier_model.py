@@ -5,10 +5,12 @@ Operations" page defines them and drives the producer / MMA / epilogue role
 loops with the kernel's own index and parity helpers (schedule.h) under
 seeded random interleavings of roles, copy completions and tensor-core
 completions.  See model.cpp for the invariants checked.  attn_pair_model.cpp
-replays the CTA-pair attention kernel's protocol (copy ring, S / P / O
-hand-over between the MMA thread and the softmax warps of both CTAs, the
-peer's P signalling copies) and also checks that every parity wait returns
-with exactly the phase it waited for.
+replays the persistent CTA-pair attention kernel's protocol for one cluster
+over several items (copy ring, Q reloads, S / P / O hand-over between the
+MMA thread, the softmax warps and the epilogue warps of both CTAs, the
+peer's signalling copies) and also checks that every parity wait returns
+with exactly the phase it waited for; planted mistakes (a wait left out)
+must make it fail.
 """
 from __future__ import annotations
 
@@ -141,8 +143,9 @@ def test_pair_fault_on_other_pair_does_not_affect_this_one(pair_model):
 
 # (ring slots, key blocks, seeds): 1 and 2 blocks (no reuse), odd / even
 # counts, the kernel's 3-slot ring and others
-ATTN_CASES = [(5, 1, 100), (5, 2, 100), (5, 5, 100), (5, 8, 60), (2, 6, 100), (3, 7, 60),
-              (1, 4, 60)]
+# (ring, key blocks per item, items per cluster, seeds)
+ATTN_CASES = [(4, 1, 1, 100), (4, 2, 3, 60), (4, 5, 2, 40), (4, 1, 5, 60), (2, 3, 4, 40),
+              (3, 2, 3, 60), (1, 2, 3, 40)]
 
 
 @pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: "-".join(map(str, c)))
@@ -152,13 +155,23 @@ def test_attention_pair_protocol_interleavings(attn_model, case):
 
 
 def test_attention_pair_fault_blocks_the_mma_on_the_starved_fill(attn_model):
-    rc, out = _run(attn_model, 5, 4, 20, "fault")
+    rc, out = _run(attn_model, 4, 3, 2, 20, "fault")
     assert rc == 0 and out.startswith("DEADLOCK-AS-EXPECTED"), out
 
 
-def test_attention_pair_model_catches_s_overwritten_before_it_is_read():
-    # The same replay with the MMA thread's wait on s_free left out: S of the
-    # next block may then land before every softmax warp has read S.
-    exe = _build(ATTN_SRC, ATTN_EXE + "_planted", defines=("PLANT_SKIP_S_FREE_WAIT",))
-    rc, out = _run(exe, 5, 6, 100)
-    assert rc != 0 and "overwrites the S buffer" in out, out
+@pytest.mark.parametrize("plant,case,expect", [
+    # the MMA thread does not wait for s_free: S of the next block may land
+    # before every softmax warp has read S (needs two blocks per item; with
+    # one, the wait for P of the block orders it anyway)
+    ("PLANT_SKIP_S_FREE_WAIT", (4, 2, 4, 200), "overwrites the S buffer"),
+    # the item's first O += P V does not wait for o_free: it may overwrite O
+    # before the epilogue warps read the previous item's O
+    ("PLANT_SKIP_O_FREE_WAIT", (4, 1, 6, 300), "overwrites O before the epilogue"),
+    # the softmax does not wait for l_free: it may overwrite the row sums
+    # before the epilogue warps read them
+    ("PLANT_SKIP_L_FREE_WAIT", (4, 1, 6, 300), "row sums overwritten"),
+])
+def test_attention_pair_model_catches_planted_mistakes(plant, case, expect):
+    exe = _build(ATTN_SRC, ATTN_EXE + "_" + plant.lower(), defines=(plant,))
+    rc, out = _run(exe, *case)
+    assert rc != 0 and expect in out, out
