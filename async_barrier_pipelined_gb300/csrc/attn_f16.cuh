@@ -471,6 +471,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
+  // The next kernel in the stream may be scheduled now (it waits for this
+  // grid before touching memory); and this one, launched as a programmatic
+  // dependent, touches no global memory before the previous kernel has
+  // completed.  Only the set-up above overlaps that kernel's tail.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   RingPos prod_pos{0, 0};
   uint32_t prod_issued = 0;

@@ -569,6 +569,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + OFF_TMEM_SLOT);
+  // The next kernel in the stream may be scheduled now (it waits for this
+  // grid before touching memory); and this one, launched as a programmatic
+  // dependent, touches no global memory before the previous kernel has
+  // completed.  Only the set-up above overlaps that kernel's tail.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   Issued issued{0, 0};
   if (warp == 0) {

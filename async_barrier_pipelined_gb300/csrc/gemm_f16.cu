@@ -1728,10 +1728,18 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
     int64_t clusters = p->attn_pairs;
     if (p->sm_limit > 0) clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, p->sm_limit / 2));
     clusters = std::min<int64_t>(clusters, items);
-    const dim3 grid((unsigned)(2 * clusters), 1, 1);
-    attnp::attn_f16_fwd_pair_kernel<<<grid, attnp::NUM_THREADS, attnp::SMEM_BYTES,
-                                      (cudaStream_t)stream>>>(tmQ, tmK, tmV, tmO, prm);
-    GF16_CUDA(cudaGetLastError(), "launch attn_f16_fwd_pair_kernel");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(attnp::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = attnp::SMEM_BYTES;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    GF16_CUDA(cudaLaunchKernelEx(&cfg, attnp::attn_f16_fwd_pair_kernel, tmQ, tmK, tmV, tmO, prm),
+              "launch attn_f16_fwd_pair_kernel");
     return GEMM_F16_OK;
   }
   attn::Params prm;
@@ -1742,10 +1750,18 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
   prm.status = p->status_dev;
   prm.timeout_ns = p->timeout_ns;
   prm.fault_cta = p->fault_unit;
-  const dim3 grid((unsigned)ceil_div(seq_q, attn::BQ), (unsigned)heads, (unsigned)batch);
-  attn::attn_f16_fwd_kernel<<<grid, attn::NUM_THREADS, attn::SMEM_BYTES, (cudaStream_t)stream>>>(
-      tmQ, tmK, tmV, tmO, prm);
-  GF16_CUDA(cudaGetLastError(), "launch attn_f16_fwd_kernel");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ceil_div(seq_q, attn::BQ), (unsigned)heads, (unsigned)batch);
+  cfg.blockDim = dim3(attn::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = attn::SMEM_BYTES;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  GF16_CUDA(cudaLaunchKernelEx(&cfg, attn::attn_f16_fwd_kernel, tmQ, tmK, tmV, tmO, prm),
+            "launch attn_f16_fwd_kernel");
   return GEMM_F16_OK;
 }
 
