@@ -314,6 +314,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
     ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + S_COL + sb * BKV + 32,
                             *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
     ptx::tmem_ld_wait();
+    ptx::reg_fence(s);
     const int valid = p.seq_kv - j * BKV;  // keys of this block inside the sequence
     float alpha;
     const float m_new = block_offset<BKV>(s, sl2, valid, m, &alpha);
@@ -350,6 +351,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
         const uint32_t ta = tmem_base + t_lane + O_COL + (uint32_t)c * 32u;
         ptx::tmem_ld_32x32b_x32(ta, o);
         ptx::tmem_ld_wait();
+        ptx::reg_fence(o);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
         ptx::tmem_st_32x32b_x32(ta, o);
@@ -381,6 +383,7 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tmO, const Param
       uint32_t o[32];
       ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + O_COL + (uint32_t)c * 32u, o);
       ptx::tmem_ld_wait();
+      ptx::reg_fence(o);
       const uint32_t box = stage + (uint32_t)(c >> 1) * 4096u + lane * 128u;
 #pragma unroll
       for (uint32_t i = 0; i < 4; ++i) {

@@ -355,6 +355,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
         ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + S_COL + 32u * c,
                                 *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
       ptx::tmem_ld_wait();
+      ptx::reg_fence(s);
       // S is in registers: the next S may overwrite it.
       if (j + 1 < p.nkv || more_items)
         signal_leader(rank, lane, b.s_free, leader_s_free, sig_s, sig_src);
@@ -392,6 +393,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
           const uint32_t ta = tmem_base + t_lane + O_COL + (uint32_t)c * 32u;
           ptx::tmem_ld_32x32b_x32(ta, o);
           ptx::tmem_ld_wait();
+          ptx::reg_fence(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           ptx::tmem_st_32x32b_x32(ta, o);
@@ -448,6 +450,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmO, const Para
       ptx::tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
       ptx::tmem_ld_32x32b_x32(ta + 32u, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
       ptx::tmem_ld_wait();
+      ptx::reg_fence(o);
       // O is in registers: the next item's first O += P V may overwrite it.
       if (c == HD / 64 - 1 && more_items)
         signal_leader(rank, lane, b.o_free, leader_o_free, sig_o, sig_src);

@@ -343,6 +343,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c * 32u, r);
         ptx::tmem_ld_wait();
+        ptx::reg_fence(r);
         if (p.split_k == 1 && col0 + 32 > p.N && (p.N & 7) != 0) {
           // The chunk straddles a column bound that is not 16-byte aligned.
           // A tensor store would write on up to the next 16-byte boundary

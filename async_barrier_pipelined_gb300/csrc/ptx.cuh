@@ -239,6 +239,16 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
 }
 
 // Until this thread's earlier tcgen05.st have completed.
+// Makes every register of `r` look rewritten here, so no use of them can be
+// scheduled before this point.  Placed after tcgen05.wait::ld: the values
+// a tcgen05.ld returns are valid only from there, which the compiler cannot
+// see from the two asm statements.  Emits no instruction.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i])::"memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
