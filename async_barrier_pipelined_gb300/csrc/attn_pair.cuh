@@ -82,8 +82,8 @@ constexpr uint32_t O_BOX = 32 * 128;                   // 32 rows x 64 d of O: 4
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = OFF_Q + Q_BYTES;
 constexpr uint32_t OFF_STAGE = OFF_RING + RING * SLOT_BYTES;  // two O boxes per epilogue warp
-constexpr uint32_t OFF_L = OFF_STAGE + EP_WARPS * 2 * O_BOX;  // row sums, softmax -> epilogue
-constexpr uint32_t OFF_BAR = OFF_L + CQ * 4;
+constexpr uint32_t OFF_L = OFF_STAGE + EP_WARPS * 2 * O_BOX;  // row sums and offsets, softmax -> epilogue
+constexpr uint32_t OFF_BAR = OFF_L + 2 * CQ * 4;
 // q_full, q_empty, full[RING], empty[RING], s_full, s_free, p_full[2],
 // o_done[2], o_free, l_ready, l_free, mma_done
 constexpr uint32_t NUM_BARS = 2 + 2 * RING + 2 + 2 + 2 + 3 + 1;
@@ -123,10 +123,14 @@ struct Params {
   int n_qt;                     // query tiles of 256 rows: ceil(seq_q / 256)
   int heads;
   int n_items;                  // batch * heads * n_qt
+  int n_split;                  // key ranges per item (1: O is written directly)
+  int bps;                      // key blocks per range (the last range may have fewer)
+  int n_units;                  // n_items * n_split
+  float* part_ml;               // n_split > 1: per unit and row, the offset m and the sum l
   float scale_log2;
   int* status;
   unsigned long long timeout_ns;
-  int fault_item;               // test only: item whose first ring fill gets no leader copy
+  int fault_unit;               // test only: unit whose first ring fill gets no leader copy
 };
 
 struct Bars {
@@ -134,13 +138,18 @@ struct Bars {
       mma_done;
 };
 
-// Work item -> first query row, head, batch (query tiles vary fastest).
+// Work unit -> first query row, head, batch (query tiles vary fastest) and
+// the unit's key blocks j0 .. j0 + nb - 1 (a unit is one key range of an
+// item; without a split, the whole item).
 struct Item {
-  int q0, h, bz;
+  int q0, h, bz, j0, nb;
 };
-__device__ __forceinline__ Item decode_item(int it, const Params& p) {
+__device__ __forceinline__ Item decode_unit(int u, const Params& p) {
+  const int it = u / p.n_split;
+  const int j0 = (u - it * p.n_split) * p.bps;
   const int bh = it / p.n_qt;
-  return Item{(it - bh * p.n_qt) * PQ, bh % p.heads, bh / p.heads};
+  const int nb = p.nkv - j0 < p.bps ? p.nkv - j0 : p.bps;
+  return Item{(it - bh * p.n_qt) * PQ, bh % p.heads, bh / p.heads, j0, nb};
 }
 
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
@@ -207,8 +216,8 @@ __device__ __forceinline__ Issued producer_role(const CUtensorMap* tmQ, const CU
   RingPos pos{0, 0};
   Issued n{0, 0};
   bool ok = true;
-  for (int it = cluster; it < p.n_items && ok; it += nclusters) {
-    const Item w = decode_item(it, p);
+  for (int u = cluster; u < p.n_units && ok; u += nclusters) {
+    const Item w = decode_unit(u, p);
     if (n.qloads > 0 && !wait_phase(b.q_empty, (n.qloads - 1) & 1u, p, abort_flag)) break;
     if (rank == 0) ptx::mbar_arrive_expect_tx_relaxed(b.q_full, 2 * Q_BYTES);
 #pragma unroll
@@ -221,19 +230,19 @@ __device__ __forceinline__ Issued producer_role(const CUtensorMap* tmQ, const CU
       if (!wait_phase(b.empty + 8 * pos.stage, producer_wait_parity(pos), p, abort_flag))
         return false;
       if (rank == 0) ptx::mbar_arrive_expect_tx_relaxed(b.full + 8 * pos.stage, 2 * SLOT_BYTES);
-      if (!(first && it == p.fault_item && rank == 0)) {
+      if (!(first && u == p.fault_unit && rank == 0)) {
         const uint32_t dst = base + OFF_RING + pos.stage * SLOT_BYTES;
         const uint32_t fb = leader_full + 8 * pos.stage;
         if (is_k) {
 #pragma unroll
           for (int c = 0; c < HD / 64; ++c)
             ptx::tma_load_4d_pair(dst + c * K_CHUNK, tmK, fb, 64 * c,
-                                  j * BKV + (int)rank * (BKV / 2), w.h, w.bz);
+                                  (w.j0 + j) * BKV + (int)rank * (BKV / 2), w.h, w.bz);
         } else {
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            ptx::tma_load_4d_pair(dst + c * V_CHUNK, tmV, fb, (int)rank * 128 + 64 * c, j * BKV,
-                                  w.h, w.bz);
+            ptx::tma_load_4d_pair(dst + c * V_CHUNK, tmV, fb, (int)rank * 128 + 64 * c,
+                                  (w.j0 + j) * BKV, w.h, w.bz);
         }
       }
       first = false;
@@ -242,8 +251,8 @@ __device__ __forceinline__ Issued producer_role(const CUtensorMap* tmQ, const CU
       return true;
     };
     ok = fill(true, 0);
-    for (int j = 0; j < p.nkv && ok; ++j) {
-      if (j + 1 < p.nkv) ok = fill(true, j + 1);
+    for (int j = 0; j < w.nb && ok; ++j) {
+      if (j + 1 < w.nb) ok = fill(true, j + 1);
       if (ok) ok = fill(false, j);
     }
   }
@@ -282,16 +291,17 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
     return true;
   };
 
-  uint32_t g0 = 0;   // global index of the item's first key block
-  uint32_t ki = 0;   // items done
+  uint32_t g0 = 0;   // global index of the unit's first key block
+  uint32_t ki = 0;   // units done
   bool ok = true;
-  for (int it = cluster; it < p.n_items && ok; it += nclusters, ++ki, g0 += (uint32_t)p.nkv) {
+  for (int u = cluster; u < p.n_units && ok; u += nclusters, ++ki) {
+    const int nb = decode_unit(u, p).nb;
     if (!wait_phase(b.q_full, ki & 1u, p, abort_flag)) break;
     ptx::tc_fence_after();
-    ok = issue_qk(g0, p.nkv == 1);
-    for (int j = 0; j < p.nkv && ok; ++j) {
+    ok = issue_qk(g0, nb == 1);
+    for (int j = 0; j < nb && ok; ++j) {
       const uint32_t gj = g0 + (uint32_t)j;
-      if (j + 1 < p.nkv && !issue_qk(gj + 1, j + 2 == p.nkv)) {
+      if (j + 1 < nb && !issue_qk(gj + 1, j + 2 == nb)) {
         ok = false;
         break;
       }
@@ -302,8 +312,8 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
         ok = false;
         break;
       }
-      // The item's first O += P V overwrites O: both CTAs' epilogue warps
-      // must have read the previous item's O.
+      // The unit's first O += P V overwrites O: both CTAs' epilogue warps
+      // must have read the previous unit's O.
       if (j == 0 && ki > 0 && !wait_phase(b.o_free, (ki - 1) & 1u, p, abort_flag)) {
         ok = false;
         break;
@@ -320,6 +330,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
       ptx::mma_commit_pair(b.o_done + 8 * pb, 0x3);
       ring_advance(pos, RING);
     }
+    g0 += (uint32_t)nb;
   }
 }
 
@@ -337,13 +348,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
   const uint32_t sig_src = base + OFF_SIG + SIG_SRC + (warp - 2) * SIG_BYTES;
   const float sl2 = p.scale_log2;
   uint32_t g = 0;    // global key block
-  uint32_t ki = 0;   // items done
+  uint32_t ki = 0;   // units done
   bool ok = true;
-  for (int it = cluster; it < p.n_items && ok; it += nclusters, ++ki) {
-    const bool more_items = it + nclusters < p.n_items;
+  for (int u = cluster; u < p.n_units && ok; u += nclusters, ++ki) {
+    const bool more_units = u + nclusters < p.n_units;
+    const Item w = decode_unit(u, p);
     float m = -INFINITY;
     float l = 0.f;
-    for (int j = 0; j < p.nkv; ++j, ++g) {
+    for (int j = 0; j < w.nb; ++j, ++g) {
       if (!warp_wait(b.s_full, g & 1u, p, abort_flag)) {
         ok = false;
         break;
@@ -357,9 +369,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       ptx::tmem_ld_wait();
       ptx::reg_fence(s);
       // S is in registers: the next S may overwrite it.
-      if (j + 1 < p.nkv || more_items)
+      if (j + 1 < w.nb || more_units)
         signal_leader(rank, lane, b.s_free, leader_s_free, sig_s, sig_src);
-      const int valid = p.seq_kv - j * BKV;
+      const int valid = p.seq_kv - (w.j0 + j) * BKV;
       float alpha;
       const float m_new = block_offset<BKV>(s, sl2, valid, m, &alpha);
       uint32_t pk[BKV / 2];
@@ -407,22 +419,28 @@ __device__ __forceinline__ void softmax_role(const Params& p, uint32_t base, uin
       m = m_new;
     }
     if (!ok) break;
-    // Hand the row sums to the epilogue warps (once they took the last ones).
+    // Hand the row's sum and offset to the epilogue warps (once they took
+    // the last ones).
     if (ki > 0 && !warp_wait(b.l_free, (ki - 1) & 1u, p, abort_flag)) break;
     l_rows[quarter * 32u + lane] = l;
+    l_rows[CQ + quarter * 32u + lane] = m;
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(b.l_ready);
   }
 }
 
 // ------------------------------------------------------------------ epilogue
-// Per item: O (FP32, tensor memory) * 1/l -> FP16, staged per warp in two
-// 32-row x 64-column boxes (128-byte swizzle) and stored with tensor copies.
-__device__ __forceinline__ void epilogue_role(const CUtensorMap* tmO, const Params& p,
-                                              uint32_t base, uint32_t tmem_base, const Bars& b,
-                                              const float* l_rows, uint32_t rank, uint32_t warp,
-                                              uint32_t lane, int cluster, int nclusters,
-                                              volatile int* abort_flag) {
+// Per unit, once its last O += P V has landed: O (FP32, tensor memory) * 1/l.
+// Without a key split -> FP16, staged per warp in two 32-row x 64-column
+// boxes (128-byte swizzle) and stored into O with tensor copies.  With a
+// split -> FP32 partial, staged in 32-row x 32-column boxes and stored into
+// the workspace (row u * 256 + r of the partial tensor), with the row's
+// offset m and sum l beside it; the combine kernel merges the ranges.
+__device__ __forceinline__ void epilogue_role(const CUtensorMap* tmO, const CUtensorMap* tmP,
+                                              const Params& p, uint32_t base, uint32_t tmem_base,
+                                              const Bars& b, const float* l_rows, uint32_t rank,
+                                              uint32_t warp, uint32_t lane, int cluster,
+                                              int nclusters, volatile int* abort_flag) {
   const uint32_t quarter = warp & 3u;
   const uint32_t t_lane = (quarter * 32u) << 16;
   const uint32_t e = warp - (2 + SM_WARPS);
@@ -431,49 +449,87 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmO, const Para
   const uint32_t sig_src = base + OFF_SIG + SIG_SRC + (SM_WARPS + e) * SIG_BYTES;
   const uint32_t stage = base + OFF_STAGE + e * 2u * O_BOX;
   const uint32_t lsw = lane & 7u;
+  const uint32_t row = quarter * 32u + lane;   // row within this CTA's 128
+  const bool split = p.n_split > 1;
   uint32_t ki = 0;
-  for (int it = cluster; it < p.n_items; it += nclusters, ++ki) {
-    const Item w = decode_item(it, p);
-    const bool more_items = it + nclusters < p.n_items;
-    const uint32_t g_last = (ki + 1) * (uint32_t)p.nkv - 1;
+  uint32_t g_end = 0;  // global key blocks up to and including this unit's
+  for (int u = cluster; u < p.n_units; u += nclusters, ++ki) {
+    const Item w = decode_unit(u, p);
+    const bool more_units = u + nclusters < p.n_units;
+    g_end += (uint32_t)w.nb;
+    const uint32_t g_last = g_end - 1;
     if (!__all_sync(0xffffffffu, wait_sleepy(b.l_ready, ki & 1u, p, abort_flag))) break;
-    const float inv_l = 1.f / l_rows[quarter * 32u + lane];
+    const float l = l_rows[row];
+    const float m = l_rows[CQ + row];
     __syncwarp();
-    if (more_items && lane == 0) ptx::mbar_arrive(b.l_free);
+    if (more_units && lane == 0) ptx::mbar_arrive(b.l_free);
     if (!warp_wait(b.o_done + 8 * (g_last & 1u), (g_last >> 1) & 1u, p, abort_flag)) break;
     ptx::tc_fence_after();
-    const int r0 = w.q0 + (int)rank * CQ + (int)quarter * 32;
+    const float inv_l = 1.f / l;
+    if (!split) {
+      const int r0 = w.q0 + (int)rank * CQ + (int)quarter * 32;
 #pragma unroll 1
-    for (int c = 0; c < HD / 64; ++c) {
-      uint32_t o[64];
-      const uint32_t ta = tmem_base + t_lane + O_COL + (uint32_t)c * 64u;
-      ptx::tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-      ptx::tmem_ld_32x32b_x32(ta + 32u, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-      ptx::tmem_ld_wait();
-      ptx::reg_fence(o);
-      // O is in registers: the next item's first O += P V may overwrite it.
-      if (c == HD / 64 - 1 && more_items)
-        signal_leader(rank, lane, b.o_free, leader_o_free, sig_o, sig_src);
-      // Box c & 1 is free once the store that used it two boxes ago read it.
-      if (lane == 0) ptx::bulk_wait_group_read<1>();
-      __syncwarp();
-      const uint32_t box = stage + (uint32_t)(c & 1) * O_BOX;
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t o[64];
+        const uint32_t ta = tmem_base + t_lane + O_COL + (uint32_t)c * 64u;
+        ptx::tmem_ld_32x32b_x32(ta, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        ptx::tmem_ld_32x32b_x32(ta + 32u, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        ptx::tmem_ld_wait();
+        ptx::reg_fence(o);
+        // O is in registers: the next unit's first O += P V may overwrite it.
+        if (c == HD / 64 - 1 && more_units)
+          signal_leader(rank, lane, b.o_free, leader_o_free, sig_o, sig_src);
+        // Box c & 1 is free once the store that used it two boxes ago read it.
+        if (lane == 0) ptx::bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t box = stage + (uint32_t)(c & 1) * O_BOX;
 #pragma unroll
-      for (uint32_t i = 0; i < 8; ++i) {
-        const float* f = reinterpret_cast<const float*>(&o[8 * i]);
-        ptx::st_shared_v4(box + lane * 128u + ((i ^ lsw) << 4),
-                          pack_half2(f[0] * inv_l, f[1] * inv_l),
-                          pack_half2(f[2] * inv_l, f[3] * inv_l),
-                          pack_half2(f[4] * inv_l, f[5] * inv_l),
-                          pack_half2(f[6] * inv_l, f[7] * inv_l));
+        for (uint32_t i = 0; i < 8; ++i) {
+          const float* f = reinterpret_cast<const float*>(&o[8 * i]);
+          ptx::st_shared_v4(box + lane * 128u + ((i ^ lsw) << 4),
+                            pack_half2(f[0] * inv_l, f[1] * inv_l),
+                            pack_half2(f[2] * inv_l, f[3] * inv_l),
+                            pack_half2(f[4] * inv_l, f[5] * inv_l),
+                            pack_half2(f[6] * inv_l, f[7] * inv_l));
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && r0 < p.seq_q) {
+          ptx::tma_store_4d(tmO, box, 64 * c, r0, w.h, w.bz);
+          ptx::bulk_commit_group();
+        }
+        __syncwarp();
       }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && r0 < p.seq_q) {
-        ptx::tma_store_4d(tmO, box, 64 * c, r0, w.h, w.bz);
-        ptx::bulk_commit_group();
+    } else {
+      const int prow = u * PQ + (int)rank * CQ + (int)quarter * 32;  // first partial row
+      float2* ml = reinterpret_cast<float2*>(p.part_ml) + (size_t)prow + lane;
+      *ml = make_float2(m, l);
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld_32x32b_x32(tmem_base + t_lane + O_COL + (uint32_t)c * 32u, o);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence(o);
+        if (c == HD / 32 - 1 && more_units)
+          signal_leader(rank, lane, b.o_free, leader_o_free, sig_o, sig_src);
+        if (lane == 0) ptx::bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t box = stage + (uint32_t)(c & 1) * O_BOX;
+#pragma unroll
+        for (uint32_t i = 0; i < 8; ++i)
+          ptx::st_shared_v4(box + lane * 128u + ((i ^ lsw) << 4),
+                            __float_as_uint(__uint_as_float(o[4 * i]) * inv_l),
+                            __float_as_uint(__uint_as_float(o[4 * i + 1]) * inv_l),
+                            __float_as_uint(__uint_as_float(o[4 * i + 2]) * inv_l),
+                            __float_as_uint(__uint_as_float(o[4 * i + 3]) * inv_l));
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(tmP, box, 32 * c, prow);
+          ptx::bulk_commit_group();
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
   }
   if (lane == 0) ptx::bulk_wait_group<0>();
@@ -510,7 +566,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     attn_f16_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                              const __grid_constant__ CUtensorMap tmK,
                              const __grid_constant__ CUtensorMap tmV,
-                             const __grid_constant__ CUtensorMap tmO, const Params p) {
+                             const __grid_constant__ CUtensorMap tmO,
+                             const __grid_constant__ CUtensorMap tmP, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -541,7 +598,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
     ptx::prefetch_tmap(&tmV);
-    ptx::prefetch_tmap(&tmO);
+    ptx::prefetch_tmap(p.n_split > 1 ? &tmP : &tmO);
     ptx::mbar_init(b.q_full, 1);
     ptx::mbar_init(b.q_empty, 1);
     for (int s = 0; s < RING; ++s) {
@@ -595,8 +652,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else if (warp < 2 + SM_WARPS) {
     softmax_role(p, base, tmem_base, b, l_rows, rank, warp, lane, cluster, nclusters, abort_flag);
   } else {
-    epilogue_role(&tmO, p, base, tmem_base, b, l_rows, rank, warp, lane, cluster, nclusters,
-                  abort_flag);
+    epilogue_role(&tmO, &tmP, p, base, tmem_base, b, l_rows, rank, warp, lane, cluster,
+                  nclusters, abort_flag);
   }
 
   if (warp == 0 && lane == 0 && rank == 1) {
@@ -616,6 +673,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
+}
+
+// Merges the key ranges of a split run.  Per query row, with M the largest
+// range offset: O = sum_s w_s O_s / sum_s w_s, w_s = l_s 2^(m_s - M), O_s the
+// range's normalised partial (FP32), ranges in order, one RN rounding to
+// FP16.  One warp per row, eight columns per lane; launched as a
+// programmatic dependent of the attention kernel.
+__global__ void __launch_bounds__(256)
+    attn_combine_kernel(const float* __restrict__ part, const float2* __restrict__ ml,
+                        const Params p, __half* __restrict__ O, int64_t os_b, int64_t os_h,
+                        int64_t os_r) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = (int)(threadIdx.x & 31u);
+  if (gw >= (int64_t)p.n_items * PQ) return;
+  const int it = (int)(gw / PQ);
+  const int r = (int)(gw - (int64_t)it * PQ);
+  const int bh = it / p.n_qt;
+  const int q = (it - bh * p.n_qt) * PQ + r;
+  if (q >= p.seq_q) return;
+  const int64_t u0 = (int64_t)it * p.n_split;
+  float mmax = -INFINITY;
+  for (int s = 0; s < p.n_split; ++s) mmax = fmaxf(mmax, ml[(u0 + s) * PQ + r].x);
+  float wsum = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < p.n_split; ++s) {
+    const float2 v = ml[(u0 + s) * PQ + r];
+    const float wgt = v.y * exp2f(v.x - mmax);
+    wsum += wgt;
+    const float4* src =
+        reinterpret_cast<const float4*>(part + ((u0 + s) * PQ + r) * HD + lane * 8);
+    const float4 a0 = src[0], a1 = src[1];
+    acc[0] = fmaf(wgt, a0.x, acc[0]);
+    acc[1] = fmaf(wgt, a0.y, acc[1]);
+    acc[2] = fmaf(wgt, a0.z, acc[2]);
+    acc[3] = fmaf(wgt, a0.w, acc[3]);
+    acc[4] = fmaf(wgt, a1.x, acc[4]);
+    acc[5] = fmaf(wgt, a1.y, acc[5]);
+    acc[6] = fmaf(wgt, a1.z, acc[6]);
+    acc[7] = fmaf(wgt, a1.w, acc[7]);
+  }
+  const float inv = 1.f / wsum;
+  uint4 out;
+  out.x = pack_half2(acc[0] * inv, acc[1] * inv);
+  out.y = pack_half2(acc[2] * inv, acc[3] * inv);
+  out.z = pack_half2(acc[4] * inv, acc[5] * inv);
+  out.w = pack_half2(acc[6] * inv, acc[7] * inv);
+  __half* dst = O + (int64_t)(bh / p.heads) * os_b + (int64_t)(bh % p.heads) * os_h +
+                (int64_t)q * os_r + lane * 8;
+  *reinterpret_cast<uint4*>(dst) = out;
 }
 
 }  // namespace attnp

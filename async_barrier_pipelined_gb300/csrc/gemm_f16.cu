@@ -739,6 +739,7 @@ struct gemm_f16_plan_s {
   int tile_width = 0;  // single-CTA tile width: 0 auto, else 256 / 128 / 64
   int sm_limit = 0;    // most SMs a launch may use (0: all)
   int attn_kernel = 0; // attention: 0 auto (CTA pair), 1 single CTA, 2 CTA pair
+  int attn_split = 0;  // pair attention key ranges: 0 auto, n >= 1 forced
   int max_pairs = 0;   // co-resident clusters of two for the pair kernel
   int attn_pairs = 0;  // co-resident clusters of two for the pair attention kernel
   void* ws = nullptr;
@@ -1029,6 +1030,10 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
       if (value < 0 || value > 2) return GEMM_F16_ERR_INVALID_ARG;
       p->attn_kernel = (int)value;
       return GEMM_F16_OK;
+    case GEMM_F16_OPT_ATTN_SPLIT:
+      if (value < 0 || value > 65536) return GEMM_F16_ERR_INVALID_ARG;
+      p->attn_split = (int)value;
+      return GEMM_F16_OK;
     case GEMM_F16_OPT_TILE_WIDTH:
       if (value != 0 && value != 64 && value != 128 && value != 256) return GEMM_F16_ERR_INVALID_ARG;
       p->tile_width = (int)value;
@@ -1067,6 +1072,7 @@ int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
     case GEMM_F16_OPT_TILE_WIDTH: *value = p->tile_width; return GEMM_F16_OK;
     case GEMM_F16_OPT_SM_LIMIT: *value = p->sm_limit; return GEMM_F16_OK;
     case GEMM_F16_OPT_ATTN_KERNEL: *value = p->attn_kernel; return GEMM_F16_OK;
+    case GEMM_F16_OPT_ATTN_SPLIT: *value = p->attn_split; return GEMM_F16_OK;
     case GEMM_F16_INFO_NUM_SMS: *value = p->num_sms; return GEMM_F16_OK;
     case GEMM_F16_INFO_MAX_PAIRS: *value = p->max_pairs; return GEMM_F16_OK;
     default: return GEMM_F16_ERR_INVALID_ARG;
@@ -1718,17 +1724,45 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
     prm.n_qt = (int)ceil_div(seq_q, attnp::PQ);
     prm.heads = heads;
     const int64_t items = (int64_t)batch * heads * prm.n_qt;
-    if (items > INT32_MAX - 65536) return GEMM_F16_ERR_INVALID_ARG;  // item + clusters fits
+    if (items > INT32_MAX - 65536) return GEMM_F16_ERR_INVALID_ARG;  // unit + clusters fits
     prm.n_items = (int)items;
     prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     prm.status = p->status_dev;
     prm.timeout_ns = p->timeout_ns;
-    prm.fault_item = p->fault_unit;
+    prm.fault_unit = p->fault_unit;
     // Persistent: one cluster per co-resident pair slot (fewer under an SM
-    // limit), never more than there are items.
-    int64_t clusters = p->attn_pairs;
-    if (p->sm_limit > 0) clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, p->sm_limit / 2));
-    clusters = std::min<int64_t>(clusters, items);
+    // limit), never more than there are units.
+    int64_t slots = p->attn_pairs;
+    if (p->sm_limit > 0) slots = std::max<int64_t>(1, std::min<int64_t>(slots, p->sm_limit / 2));
+    // Key split: ranges of bps blocks, none empty.
+    int64_t n_split = 1;
+    if (p->attn_split > 0)
+      n_split = std::min<int64_t>(p->attn_split, prm.nkv);
+    else if (2 * items <= slots && prm.nkv >= 4)
+      n_split = std::min<int64_t>(slots / items, prm.nkv / 2);
+    n_split = std::max<int64_t>(n_split, 1);
+    prm.bps = (int)ceil_div(prm.nkv, n_split);
+    n_split = ceil_div(prm.nkv, prm.bps);
+    const int64_t units = items * n_split;
+    if (units > INT32_MAX - 65536) return GEMM_F16_ERR_INVALID_ARG;
+    prm.n_split = (int)n_split;
+    prm.n_units = (int)units;
+    prm.part_ml = nullptr;
+    CUtensorMap tmP = tmO;
+    const size_t part_bytes = (size_t)units * attnp::PQ * attn::HD * sizeof(float);
+    if (n_split > 1) {
+      const size_t bytes = part_bytes + (size_t)units * attnp::PQ * 2 * sizeof(float);
+      if ((rc = ensure_buffer(&p->ws, &p->ws_bytes, bytes, (cudaStream_t)stream,
+                              "attention workspace allocation")))
+        return rc;
+      prm.part_ml = reinterpret_cast<float*>(static_cast<char*>(p->ws) + part_bytes);
+      // The partial O: units * 256 rows of 256 FP32, stored in 32 x 32 boxes.
+      if ((rc = cached_encode_2d(p, &tmP, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p->ws, attn::HD,
+                                 (uint64_t)units * attnp::PQ, attn::HD * sizeof(float), 32, 32,
+                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
+        return rc;
+    }
+    const int64_t clusters = std::min<int64_t>(slots, units);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.blockDim = dim3(attnp::NUM_THREADS, 1, 1);
@@ -1739,8 +1773,24 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
     pdl.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    GF16_CUDA(cudaLaunchKernelEx(&cfg, attnp::attn_f16_fwd_pair_kernel, tmQ, tmK, tmV, tmO, prm),
+    GF16_CUDA(cudaLaunchKernelEx(&cfg, attnp::attn_f16_fwd_pair_kernel, tmQ, tmK, tmV, tmO, tmP,
+                                 prm),
               "launch attn_f16_fwd_pair_kernel");
+    if (n_split > 1) {
+      // One warp per query row of every item.
+      cudaLaunchConfig_t ccfg = {};
+      ccfg.gridDim = dim3((unsigned)(items * attnp::PQ / 8), 1, 1);
+      ccfg.blockDim = dim3(256, 1, 1);
+      ccfg.stream = (cudaStream_t)stream;
+      ccfg.attrs = &pdl;
+      ccfg.numAttrs = 1;
+      GF16_CUDA(cudaLaunchKernelEx(&ccfg, attnp::attn_combine_kernel,
+                                   static_cast<const float*>(p->ws),
+                                   static_cast<const float2*>(static_cast<const void*>(prm.part_ml)),
+                                   prm, static_cast<__half*>(O), o_strides[0], o_strides[1],
+                                   o_strides[2]),
+                "launch attn_combine_kernel");
+    }
     return GEMM_F16_OK;
   }
   attn::Params prm;

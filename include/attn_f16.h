@@ -17,8 +17,10 @@
  *
  * Uses a gemm_f16 plan (include/gemm_f16.h) for its device, status word
  * and the options GEMM_F16_OPT_TIMEOUT_NS and GEMM_F16_OPT_FAULT_UNIT (here:
- * the linear index x + gx*(y + gy*z) of the CTA whose first key tile gets
- * no copy, for the timeout test).  Errors found on the device are reported
+ * for the single-CTA kernel the linear index x + gx*(y + gy*z) of the CTA
+ * whose first key tile gets no copy, for the CTA-pair kernel the work unit
+ * (item * ranges + range) whose first key tile gets no copy from the
+ * leader; for the timeout test).  Errors found on the device are reported
  * later by gemm_f16_status.
  */
 #ifndef ATTN_F16_H
@@ -51,8 +53,14 @@ extern "C" {
  *   scale             finite; usually 1/sqrt(256) = 0.0625.
  * Returns GEMM_F16_OK, GEMM_F16_ERR_INVALID_ARG (sizes, strides, scale,
  * null pointers), GEMM_F16_ERR_MISALIGNED (pointer or stride alignment) or
- * GEMM_F16_ERR_CUDA (encode or launch failure); nothing is enqueued on an
- * error.  The call allocates nothing.
+ * GEMM_F16_ERR_CUDA (encode or launch failure) or GEMM_F16_ERR_OOM;
+ * nothing is enqueued on an error.  Without a key split the call allocates
+ * nothing; with one (GEMM_F16_OPT_ATTN_SPLIT, automatic when the
+ * (batch, head, 256-row) items are too few to fill the GPU) the CTA-pair
+ * kernel writes each key range's normalised FP32 partial of O (256 KB per
+ * 256 rows and range) and its row offsets and sums into the plan's
+ * workspace, which grows on the stream as needed (as for split GEMM runs),
+ * and a second kernel merges the ranges into O.
  */
 int attn_f16_fwd(gemm_f16_plan_t plan, int batch, int heads, int seq_q, int seq_kv,
                  int head_dim, const void *Q, const int64_t q_strides[3],

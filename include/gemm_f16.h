@@ -99,7 +99,17 @@ typedef enum gemm_f16_option {
      * 128 keys; persistent: each cluster of two CTAs works through several
      * (batch, head, 256-row) items).  Results agree within the usual
      * tolerance and do not depend on the number of clusters. */
-    GEMM_F16_OPT_ATTN_KERNEL = 7
+    GEMM_F16_OPT_ATTN_KERNEL = 7,
+    /* Key split of the CTA-pair attention kernel: 0 = automatic (when the
+     * (batch, head, 256-row) items fill less than half of the co-resident
+     * CTA pairs and there are at least four 128-key blocks, each item's
+     * keys are cut into up to min(pairs / items, blocks / 2) ranges), n >= 1 =
+     * n ranges (capped at the number of key blocks; 1 = no split).  Each
+     * range writes a normalised FP32 partial of O with its row offsets and
+     * sums to the plan's workspace, and a second kernel merges the ranges
+     * in order (bitwise reproducible for a fixed n).  The single-CTA
+     * attention kernel ignores it. */
+    GEMM_F16_OPT_ATTN_SPLIT = 8
 } gemm_f16_option;
 
 /*

@@ -1,5 +1,8 @@
 // Host replay of the CTA-pair attention kernel's barrier protocol, for one
-// cluster that works through several items (256 query rows each).
+// cluster that works through several units (a unit: 256 query rows and one
+// range of their key blocks; with SPLITS ranges per item of NKV blocks, the
+// ranges have ceil(NKV / SPLITS') blocks and the last one the rest, as in the
+// kernel).  "Item" below means unit.
 //
 // Roles: 0 leader producer, 1 peer producer, 2 MMA issuer (leader), 3..10
 // the softmax warps (CTA c, warp w: 3 + 4c + w), 11..18 the epilogue warps
@@ -52,7 +55,7 @@
 // With a fault (the leader issues no copy for its first ring fill) the
 // replay must stop with the MMA role blocked on that fill.
 //
-// Usage: attn_pair_model RING NKV ITEMS SEEDS [fault]
+// Usage: attn_pair_model RING NKV ITEMS SPLITS SEEDS [fault]
 // Prints "OK <n>" or "FAIL <reason>" / "DEADLOCK <where>".
 
 #include "mbar_model.h"
@@ -80,6 +83,7 @@ struct Tile {
 
 struct Sim {
   int ring = 4, nkv = 1, items = 1;
+  std::vector<int> nbs, g0s;  // per unit: key blocks, global index of the first
   bool fault = false;
   uint64_t seed = 1;
   mbmodel::Scheduler sch{NROLES};
@@ -134,8 +138,8 @@ struct Sim {
     std::vector<Tile> o;
     for (int k = 0; k < items; ++k) {
       o.push_back({k, true, 0});
-      for (int j = 0; j < nkv; ++j) {
-        if (j + 1 < nkv) o.push_back({k, true, j + 1});
+      for (int j = 0; j < nbs[k]; ++j) {
+        if (j + 1 < nbs[k]) o.push_back({k, true, j + 1});
         o.push_back({k, false, j});
       }
     }
@@ -218,7 +222,7 @@ struct Sim {
       if (gs > 0) wait_phase(r, s_free, gs - 1);
 #endif
       const uint32_t s = consume({k, true, j});
-      const bool last = j == nkv - 1;
+      const bool last = j == nbs[k] - 1;
       sch.tc_queue.push_back([this, gs, k, last] {  // S = Q K^T executes
         for (int c = 0; c < 2; ++c) {
           if (q_item[c] != k || !q_landed[c]) fail("S = Q K^T reads a Q tile not of its item");
@@ -238,12 +242,12 @@ struct Sim {
       });
     };
     for (int k = 0; k < items; ++k) {
-      const int g0 = k * nkv;
+      const int g0 = g0s[k], nb = nbs[k];
       wait_phase(r, q_full, k);
       issue_qk(g0, k, 0);
-      for (int j = 0; j < nkv; ++j) {
+      for (int j = 0; j < nb; ++j) {
         const int g = g0 + j;
-        if (j + 1 < nkv) issue_qk(g + 1, k, j + 1);
+        if (j + 1 < nb) issue_qk(g + 1, k, j + 1);
         const int pb = g & 1;
         wait_phase(r, p_full[pb], g >> 1);
         const uint32_t s = consume({k, false, j});
@@ -259,7 +263,7 @@ struct Sim {
                 if (k > 0 && o_read_item[c][e] != k - 1)
                   fail("O += P V overwrites O before the epilogue read it");
           }
-          if (j == 0 ? (o_done_item != k - 1 || (k > 0 && o_done_j != nkv - 1))
+          if (j == 0 ? (o_done_item != k - 1 || (k > 0 && o_done_j != nbs[k - 1] - 1))
                      : (o_done_item != k || o_done_j != j - 1))
             fail("O += P V out of order");
           pv_started_item = k;
@@ -284,12 +288,12 @@ struct Sim {
     const int r = 3 + cta * WARPS + w;
     sch.start(r);
     for (int k = 0; k < items; ++k) {
-      for (int j = 0; j < nkv; ++j) {
-        const int g = k * nkv + j, pb = g & 1;
+      for (int j = 0; j < nbs[k]; ++j) {
+        const int g = g0s[k] + j, pb = g & 1;
         wait_phase(r, s_full[cta], g);
         if (s_block[cta] != g) fail("softmax reads an S buffer that does not hold its block");
         s_reads[cta] += 1;
-        if (j + 1 < nkv || k + 1 < items) signal(r, cta, s_free);
+        if (j + 1 < nbs[k] || k + 1 < items) signal(r, cta, s_free);
         sch.role_yield(r);  // exp2, packing
         if (g >= 2) wait_phase(r, o_done[cta][pb], (g - 2) >> 1);
         if (p_block[cta][pb] != g) {  // the first warp to write this block's P here
@@ -329,14 +333,14 @@ struct Sim {
     const int r = 3 + 2 * WARPS + cta * WARPS + e;
     sch.start(r);
     for (int k = 0; k < items; ++k) {
-      const int g_last = (k + 1) * nkv - 1;
+      const int g_last = g0s[k] + nbs[k] - 1;
       wait_phase(r, l_ready[cta], k);
       for (int w = 0; w < WARPS; ++w)
         if (l_item[cta][w] != k) fail("epilogue reads row sums not of its item");
       l_read_item[cta][e] = k;
       if (k + 1 < items) l_free[cta].arrive(r);
       wait_phase(r, o_done[cta][g_last & 1], g_last >> 1);
-      if (o_done_item != k || o_done_j != nkv - 1 || pv_started_item != k)
+      if (o_done_item != k || o_done_j != nbs[k] - 1 || pv_started_item != k)
         fail("epilogue reads O that is not the finished O of its item");
       o_read_item[cta][e] = k;
       if (k + 1 < items) signal(r, cta, o_free);
@@ -349,18 +353,33 @@ struct Sim {
 }  // namespace
 
 int main(int argc, char** argv) {
-  if (argc < 5) {
-    std::fprintf(stderr, "usage: attn_pair_model RING NKV ITEMS SEEDS [fault]\n");
+  if (argc < 6) {
+    std::fprintf(stderr, "usage: attn_pair_model RING NKV ITEMS SPLITS SEEDS [fault]\n");
     return 2;
   }
-  const int ring = std::atoi(argv[1]), nkv = std::atoi(argv[2]), items = std::atoi(argv[3]);
-  const int seeds = std::atoi(argv[4]);
-  const bool fault = argc > 5 && std::string(argv[5]) == "fault";
+  const int ring = std::atoi(argv[1]), nkv = std::atoi(argv[2]), n_items = std::atoi(argv[3]);
+  const int splits_req = std::atoi(argv[4]), seeds = std::atoi(argv[5]);
+  const bool fault = argc > 6 && std::string(argv[6]) == "fault";
+  // Key ranges as the kernel's host code makes them: bps blocks each, none empty.
+  int splits = splits_req < 1 ? 1 : (splits_req > nkv ? nkv : splits_req);
+  const int bps = (nkv + splits - 1) / splits;
+  splits = (nkv + bps - 1) / bps;
+  std::vector<int> nbs, g0s;
+  for (int it = 0, g = 0; it < n_items; ++it)
+    for (int sp = 0; sp < splits; ++sp) {
+      const int nb = nkv - sp * bps < bps ? nkv - sp * bps : bps;
+      nbs.push_back(nb);
+      g0s.push_back(g);
+      g += nb;
+    }
+  const int items = (int)nbs.size();  // units
   for (int seed = 0; seed < seeds; ++seed) {
     Sim* sim = new Sim();  // leaked on deadlock (threads detached)
     sim->ring = ring;
     sim->nkv = nkv;
     sim->items = items;
+    sim->nbs = nbs;
+    sim->g0s = g0s;
     sim->fault = fault;
     sim->seed = (uint64_t)seed + 1;
     sim->sch.seed(0x9E3779B97F4A7C15ull * (uint64_t)(seed + 1));
@@ -410,14 +429,15 @@ int main(int argc, char** argv) {
       std::fflush(stdout);
       std::_Exit(1);
     }
-    const int fills = 2 * nkv * items;
+    int blocks = 0;
+    for (int nb : nbs) blocks += nb;
+    const int fills = 2 * blocks;
     for (int s = 0; s < ring; ++s) {
       const int uses = fills / ring + (s < fills % ring ? 1 : 0);
       if (sim->full[s].completions != uses) fail("full phase count mismatch");
       for (int c = 0; c < 2; ++c)
         if (sim->empty[c][s].completions != uses) fail("empty phase count mismatch");
     }
-    const int blocks = nkv * items;
     for (int b = 0; b < 2; ++b) {
       const int uses = blocks / 2 + (b < blocks % 2 ? 1 : 0);
       if (sim->p_full[b].completions != uses) fail("p_full phase count mismatch");

@@ -273,3 +273,39 @@ def test_many_items_per_cluster(plan, skv):
     parity.check(outs[0], want, f"skv {skv}")
     for o in outs[1:]:
         assert np.array_equal(o.view(np.uint64), outs[0].view(np.uint64))
+
+
+@pytest.mark.parametrize("splits", [2, 3, 8, 64])
+def test_key_split_matches_oracle(plan, splits):
+    """The pair kernel cuts each item's keys into ranges, writes normalised
+    FP32 partials with their row offsets and sums, and a second kernel merges
+    them.  1000 keys are 8 blocks, the last one ragged (104 keys): 2 and 3
+    ranges leave a short last range, 8 ranges are one block each, 64 is
+    capped at 8.  The single-CTA kernel ignores the option."""
+    import async_barrier_pipelined_gb300 as g
+    w = si.attn_custom(1, 3, 300, 1000, seed=splits + 40)
+    Qb, Kb, Vb = w.bits()
+    try:
+        plan.set_option(g.OPT_ATTN_SPLIT, splits)
+        o = _run(plan, Qb, Kb, Vb)
+    finally:
+        plan.set_option(g.OPT_ATTN_SPLIT, 0)
+    parity.check(o, oracle.attention_f16(Qb, Kb, Vb, w.scale), f"{splits} key ranges")
+
+
+def test_key_split_bitwise_repeatable_and_strided(plan):
+    """A split run with [B, S, H, D] storage and padded rows matches the
+    oracle and repeats bit for bit."""
+    import torch
+    import async_barrier_pipelined_gb300 as g
+    w = si.attn_custom(2, 2, 260, 700, seed=77)
+    Qb, Kb, Vb = w.bits()
+    want = oracle.attention_f16(Qb, Kb, Vb, w.scale)
+    try:
+        plan.set_option(g.OPT_ATTN_SPLIT, 3)
+        outs = [_run(plan, Qb, Kb, Vb, layout="bshd", pad=8) for _ in range(3)]
+    finally:
+        plan.set_option(g.OPT_ATTN_SPLIT, 0)
+    parity.check(outs[0], want, "split, bshd")
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint64), outs[0].view(np.uint64))

@@ -143,9 +143,11 @@ def test_pair_fault_on_other_pair_does_not_affect_this_one(pair_model):
 
 # (ring slots, key blocks, seeds): 1 and 2 blocks (no reuse), odd / even
 # counts, the kernel's 3-slot ring and others
-# (ring, key blocks per item, items per cluster, seeds)
-ATTN_CASES = [(4, 1, 1, 100), (4, 2, 3, 60), (4, 5, 2, 40), (4, 1, 5, 60), (2, 3, 4, 40),
-              (3, 2, 3, 60), (1, 2, 3, 40)]
+# (ring, key blocks per item, items per cluster, key ranges per item, seeds);
+# with ranges the units have ceil(blocks / ranges) blocks and the last fewer
+ATTN_CASES = [(4, 1, 1, 1, 100), (4, 2, 3, 1, 60), (4, 5, 2, 1, 40), (4, 1, 5, 1, 60),
+              (2, 3, 4, 1, 40), (3, 2, 3, 1, 60), (1, 2, 3, 1, 40),
+              (4, 5, 2, 3, 40), (4, 8, 1, 8, 40), (3, 7, 2, 2, 40)]
 
 
 @pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: "-".join(map(str, c)))
@@ -155,7 +157,7 @@ def test_attention_pair_protocol_interleavings(attn_model, case):
 
 
 def test_attention_pair_fault_blocks_the_mma_on_the_starved_fill(attn_model):
-    rc, out = _run(attn_model, 4, 3, 2, 20, "fault")
+    rc, out = _run(attn_model, 4, 3, 2, 1, 20, "fault")
     assert rc == 0 and out.startswith("DEADLOCK-AS-EXPECTED"), out
 
 
@@ -163,13 +165,13 @@ def test_attention_pair_fault_blocks_the_mma_on_the_starved_fill(attn_model):
     # the MMA thread does not wait for s_free: S of the next block may land
     # before every softmax warp has read S (needs two blocks per item; with
     # one, the wait for P of the block orders it anyway)
-    ("PLANT_SKIP_S_FREE_WAIT", (4, 2, 4, 200), "overwrites the S buffer"),
+    ("PLANT_SKIP_S_FREE_WAIT", (4, 2, 4, 1, 200), "overwrites the S buffer"),
     # the item's first O += P V does not wait for o_free: it may overwrite O
     # before the epilogue warps read the previous item's O
-    ("PLANT_SKIP_O_FREE_WAIT", (4, 1, 6, 300), "overwrites O before the epilogue"),
+    ("PLANT_SKIP_O_FREE_WAIT", (4, 1, 6, 1, 300), "overwrites O before the epilogue"),
     # the softmax does not wait for l_free: it may overwrite the row sums
     # before the epilogue warps read them
-    ("PLANT_SKIP_L_FREE_WAIT", (4, 1, 6, 300), "row sums overwritten"),
+    ("PLANT_SKIP_L_FREE_WAIT", (4, 1, 6, 1, 300), "row sums overwritten"),
 ])
 def test_attention_pair_model_catches_planted_mistakes(plant, case, expect):
     exe = _build(ATTN_SRC, ATTN_EXE + "_" + plant.lower(), defines=(plant,))
