@@ -27,6 +27,7 @@ __all__ = [
     "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "OPT_ATTN_KERNEL", "OPT_ATTN_SPLIT", "INFO_NUM_SMS", "INFO_MAX_PAIRS",
     "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
     "gemm_f16_run_ex", "gemm_f16_validate_ex", "attn_f16_fwd", "attn_f16_validate",
+    "attn_f16_key_ranges",
     "attention", "ATTN_HEAD_DIM",
     "LAYOUT_NN", "LAYOUT_TN", "LAYOUT_NT", "LAYOUT_TT",
 ]
@@ -94,6 +95,8 @@ _SIGNATURES = {
                                    _vp, ctypes.POINTER(_c_i64), _vp, ctypes.POINTER(_c_i64),
                                    _vp, ctypes.POINTER(_c_i64), _vp, ctypes.POINTER(_c_i64),
                                    ctypes.c_float]),
+    "attn_f16_key_ranges": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int,
+                                     ctypes.POINTER(_c_int)]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -237,6 +240,14 @@ def attn_f16_validate(batch, heads, seq_q, seq_kv, head_dim, Q, q_strides, K, k_
                                     Q, _strides3(q_strides), K, _strides3(k_strides),
                                     V, _strides3(v_strides), O, _strides3(o_strides),
                                     float(scale))
+
+
+def attn_f16_key_ranges(plan: int, batch: int, heads: int, seq_q: int, seq_kv: int) -> int:
+    """Key ranges attn_f16_fwd would use for these sizes (1: no split)."""
+    n = _c_int(0)
+    _check(load().attn_f16_key_ranges(plan, batch, heads, seq_q, seq_kv, ctypes.byref(n)),
+           "attn_f16_key_ranges")
+    return n.value
 
 
 def gemm_f16_tile_order(tiles_m: int, tiles_n: int, order: int = 0) -> list:

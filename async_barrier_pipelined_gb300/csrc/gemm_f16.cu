@@ -1678,6 +1678,30 @@ bool strides_ok(const int64_t* st) {
 
 }  // namespace
 
+// Co-resident CTA pairs the pair attention kernel may use (SM limit applied).
+static int64_t attn_pair_slots(const gemm_f16_plan_s* p) {
+  int64_t slots = p->attn_pairs;
+  if (p->sm_limit > 0) slots = std::max<int64_t>(1, std::min<int64_t>(slots, p->sm_limit / 2));
+  return slots;
+}
+
+// Key ranges per item of the pair attention kernel and the blocks per range
+// (none empty): the option if set (capped at the block count), else a split
+// when the items fill less than half of the pair slots and there are at
+// least four key blocks.
+static int64_t attn_key_ranges(const gemm_f16_plan_s* p, int64_t items, int64_t nkv,
+                               int* bps) {
+  const int64_t slots = attn_pair_slots(p);
+  int64_t n = 1;
+  if (p->attn_split > 0)
+    n = std::min<int64_t>(p->attn_split, nkv);
+  else if (2 * items <= slots && nkv >= 4)
+    n = std::min<int64_t>(slots / items, nkv / 2);
+  n = std::max<int64_t>(n, 1);
+  *bps = (int)ceil_div(nkv, n);
+  return ceil_div(nkv, *bps);
+}
+
 extern "C" {
 
 int attn_f16_validate(int batch, int heads, int seq_q, int seq_kv, int head_dim, const void* Q,
@@ -1697,6 +1721,18 @@ int attn_f16_validate(int batch, int heads, int seq_q, int seq_kv, int head_dim,
     if ((uintptr_t)ptr & 15) return GEMM_F16_ERR_MISALIGNED;
   for (const int64_t* st : sts)
     if ((st[0] | st[1] | st[2]) & 7) return GEMM_F16_ERR_MISALIGNED;
+  return GEMM_F16_OK;
+}
+
+int attn_f16_key_ranges(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
+                        int* ranges) {
+  if (!p || !ranges || batch < 1 || heads < 1 || seq_q < 1 || seq_kv < 1)
+    return GEMM_F16_ERR_INVALID_ARG;
+  *ranges = 1;
+  if (p->attn_kernel == 1 || p->attn_pairs <= 0) return GEMM_F16_OK;
+  const int64_t items = (int64_t)batch * heads * ceil_div(seq_q, attnp::PQ);
+  int bps = 0;
+  *ranges = (int)attn_key_ranges(p, items, ceil_div(seq_kv, attnp::BKV), &bps);
   return GEMM_F16_OK;
 }
 
@@ -1732,17 +1768,8 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
     prm.fault_unit = p->fault_unit;
     // Persistent: one cluster per co-resident pair slot (fewer under an SM
     // limit), never more than there are units.
-    int64_t slots = p->attn_pairs;
-    if (p->sm_limit > 0) slots = std::max<int64_t>(1, std::min<int64_t>(slots, p->sm_limit / 2));
-    // Key split: ranges of bps blocks, none empty.
-    int64_t n_split = 1;
-    if (p->attn_split > 0)
-      n_split = std::min<int64_t>(p->attn_split, prm.nkv);
-    else if (2 * items <= slots && prm.nkv >= 4)
-      n_split = std::min<int64_t>(slots / items, prm.nkv / 2);
-    n_split = std::max<int64_t>(n_split, 1);
-    prm.bps = (int)ceil_div(prm.nkv, n_split);
-    n_split = ceil_div(prm.nkv, prm.bps);
+    const int64_t slots = attn_pair_slots(p);
+    int64_t n_split = attn_key_ranges(p, items, prm.nkv, &prm.bps);
     const int64_t units = items * n_split;
     if (units > INT32_MAX - 65536) return GEMM_F16_ERR_INVALID_ARG;
     prm.n_split = (int)n_split;

@@ -414,6 +414,9 @@ def run_attention(args):
     plan = g.Plan(dev.index)
     plan.set_option(g.OPT_ATTN_KERNEL, min(args.kernel, 2))
     use_pair = args.kernel != 1
+    # key ranges the library picks for this shape: > 1 adds the merging kernel
+    ranges = g.attn_f16_key_ranges(plan.handle, w.B, w.H, w.Sq, w.Skv)
+    launches_per_step = 1 if ranges == 1 else 2
 
     # the C entry point with its arguments marshalled once (as the GEMM steps
     # call gemm_f16_run directly), so host overhead does not pace small cases
@@ -472,7 +475,8 @@ def run_attention(args):
                 "traffic": load_traffic(w.name) if use_pair else None,
                 "flop_per_byte": float(w.flops) / cbytes,
                 "kernel": ("gf16::attnp::attn_f16_fwd_pair_kernel" if use_pair
-                           else "gf16::attn::attn_f16_fwd_kernel")}
+                           else "gf16::attn::attn_f16_fwd_kernel")
+                + ("" if ranges == 1 else " + gf16::attnp::attn_combine_kernel")}
 
     e2e = None
     if not args.no_e2e:
@@ -518,9 +522,10 @@ def run_attention(args):
             "dtype": "f16", "data": "synthetic",
             "config": dict(attn_config(w), kernel=("CTA pair (tcgen05 cta_group::2, 256 query "
                                                    "rows, 128-key blocks)" if use_pair else
-                                                   "single CTA (128 query rows, 64-key blocks)")),
+                                                   "single CTA (128 query rows, 64-key blocks)"),
+                           key_ranges=ranges),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "gpu_launches": args.steps, "pct_of_peak": 100.0 * achieved / peak,
+            "gpu_launches": args.steps * launches_per_step, "pct_of_peak": 100.0 * achieved / peak,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

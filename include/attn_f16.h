@@ -68,6 +68,16 @@ int attn_f16_fwd(gemm_f16_plan_t plan, int batch, int heads, int seq_q, int seq_
                  const int64_t v_strides[3], void *O, const int64_t o_strides[3],
                  float scale, gemm_f16_stream_t stream);
 
+/*
+ * The number of key ranges attn_f16_fwd would cut each item's keys into for
+ * these sizes with this plan's current options (1: no split, one kernel
+ * launch; n > 1: the CTA-pair kernel plus the merging kernel).  Enqueues
+ * nothing.  Returns GEMM_F16_OK or GEMM_F16_ERR_INVALID_ARG (null pointers,
+ * sizes < 1).
+ */
+int attn_f16_key_ranges(gemm_f16_plan_t plan, int batch, int heads, int seq_q, int seq_kv,
+                        int *ranges);
+
 /* Host-only argument check used by attn_f16_fwd (no device needed). */
 int attn_f16_validate(int batch, int heads, int seq_q, int seq_kv, int head_dim,
                       const void *Q, const int64_t q_strides[3], const void *K,

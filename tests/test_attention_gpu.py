@@ -309,3 +309,26 @@ def test_key_split_bitwise_repeatable_and_strided(plan):
     parity.check(outs[0], want, "split, bshd")
     for o in outs[1:]:
         assert np.array_equal(o.view(np.uint64), outs[0].view(np.uint64))
+
+
+def test_key_ranges_query(plan):
+    """attn_f16_key_ranges reports the split attn_f16_fwd uses: for the pair
+    kernel the option capped at the block count and rounded to non-empty
+    ranges, no split when the items fill the GPU and a split when they fill
+    less than half of it; always 1 for the single-CTA kernel."""
+    import async_barrier_pipelined_gb300 as g
+    h = plan.handle
+    single = plan.get_option(g.OPT_ATTN_KERNEL) == 1
+    try:
+        # 1000 keys = 8 blocks of 128; 5 ranges of 2 blocks would leave one empty
+        for opt, want in ((3, 3), (64, 8), (5, 4)):
+            plan.set_option(g.OPT_ATTN_SPLIT, opt)
+            assert g.attn_f16_key_ranges(h, 1, 3, 300, 1000) == (1 if single else want)
+        plan.set_option(g.OPT_ATTN_SPLIT, 0)
+        assert g.attn_f16_key_ranges(h, 4, 16, 4096, 4096) == 1
+        n = g.attn_f16_key_ranges(h, 1, 2, 256, 16384)   # 2 items, 128 blocks
+        assert n == 1 if single else 2 <= n <= 64
+    finally:
+        plan.set_option(g.OPT_ATTN_SPLIT, 0)
+    with pytest.raises(g.GemmError):
+        g.attn_f16_key_ranges(h, 0, 1, 1, 1)
