@@ -486,6 +486,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// Row repack of an operand whose row pitch is not a multiple of 128 bytes:
+// dst[r, c] = src[r, c] for r < rows, c < cols, with dst rows at a pitch of
+// whole 128-byte lines.  A 128-byte copy-box row of such an operand spans two
+// cache lines, which makes the operand copies of the GEMM kernels much
+// slower than the lines they bring; the repacked copy is read instead.  Each
+// thread moves 16-byte chunks (both pitches are multiples of 8 elements and
+// both bases 16-byte aligned); a row's last chunk, if it ends past `cols`,
+// is moved element by element so that nothing beyond the row is read.  The
+// columns of dst past `cols` are never read (the tensor map's extent is
+// `cols`).  Launched in stream order after whatever wrote src.
+__global__ void __launch_bounds__(256)
+    pack_rows_kernel(const __half* __restrict__ src, int64_t ld_src, __half* __restrict__ dst,
+                     int64_t ld_dst, int64_t rows, int64_t cols) {
+  const int64_t chunks = (cols + 7) / 8;
+  const int64_t total = rows * chunks;
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += 4 * step) {
+    uint4 v[4];
+    int64_t r[4], c[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t gi = g + u * step;
+      r[u] = gi / chunks;
+      c[u] = (gi - r[u] * chunks) * 8;
+      if (gi < total && c[u] + 8 <= cols)
+        v[u] = __ldcs(reinterpret_cast<const uint4*>(src + r[u] * ld_src + c[u]));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t gi = g + u * step;
+      if (gi >= total) continue;
+      if (c[u] + 8 <= cols) {
+        *reinterpret_cast<uint4*>(dst + r[u] * ld_dst + c[u]) = v[u];
+      } else {
+        for (int64_t t = c[u]; t < cols; ++t) dst[r[u] * ld_dst + t] = src[r[u] * ld_src + t];
+      }
+    }
+  }
+}
+
 // Fixed-order split reduction: C[i,j] = fp16_rn(P_0 + P_1 + ... + P_{S-1}),
 // summed left to right in FP32.  Each thread owns 4 consecutive columns;
 // the partial loads are issued four splits at a time (independent loads),
@@ -740,10 +780,13 @@ struct gemm_f16_plan_s {
   int sm_limit = 0;    // most SMs a launch may use (0: all)
   int attn_kernel = 0; // attention: 0 auto (CTA pair), 1 single CTA, 2 CTA pair
   int attn_split = 0;  // pair attention key ranges: 0 auto, n >= 1 forced
+  int a_repack = 0;    // repack A with a pitch off 128-byte lines: 0 auto, 1 never, 2 always
   int max_pairs = 0;   // co-resident clusters of two for the pair kernel
   int attn_pairs = 0;  // co-resident clusters of two for the pair attention kernel
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  void* apack = nullptr;  // repacked copy of A (see pack_rows_kernel)
+  size_t apack_bytes = 0;
   std::vector<OrderTable> orders;
   // run_host: two slots of device staging (A, B, C) used by alternate calls,
   // a stream for the input copies and the events that order the slots.
@@ -985,6 +1028,7 @@ int gemm_f16_destroy(gemm_f16_plan_t p) {
     cudaDeviceSynchronize();
     for (auto& t : p->orders) cudaFree(t.dev);
     if (p->ws) cudaFree(p->ws);
+    if (p->apack) cudaFree(p->apack);
     for (int sl = 0; sl < 2; ++sl)
       for (int i = 0; i < 3; ++i)
         if (p->hbuf[sl][i]) cudaFree(p->hbuf[sl][i]);
@@ -1034,6 +1078,10 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
       if (value < 0 || value > 65536) return GEMM_F16_ERR_INVALID_ARG;
       p->attn_split = (int)value;
       return GEMM_F16_OK;
+    case GEMM_F16_OPT_A_REPACK:
+      if (value < 0 || value > 2) return GEMM_F16_ERR_INVALID_ARG;
+      p->a_repack = (int)value;
+      return GEMM_F16_OK;
     case GEMM_F16_OPT_TILE_WIDTH:
       if (value != 0 && value != 64 && value != 128 && value != 256) return GEMM_F16_ERR_INVALID_ARG;
       p->tile_width = (int)value;
@@ -1073,6 +1121,7 @@ int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
     case GEMM_F16_OPT_SM_LIMIT: *value = p->sm_limit; return GEMM_F16_OK;
     case GEMM_F16_OPT_ATTN_KERNEL: *value = p->attn_kernel; return GEMM_F16_OK;
     case GEMM_F16_OPT_ATTN_SPLIT: *value = p->attn_split; return GEMM_F16_OK;
+    case GEMM_F16_OPT_A_REPACK: *value = p->a_repack; return GEMM_F16_OK;
     case GEMM_F16_INFO_NUM_SMS: *value = p->num_sms; return GEMM_F16_OK;
     case GEMM_F16_INFO_MAX_PAIRS: *value = p->max_pairs; return GEMM_F16_OK;
     default: return GEMM_F16_ERR_INVALID_ARG;
@@ -1210,6 +1259,28 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
   int rc = use_pair ? get_pair_table(p, M, N, split_k, pair_tn, &order, &pair_tiles)
                     : get_order_table(p, tiles_m, tiles_n, &order);
   if (rc) return rc;
+
+  // A whose row pitch is not a multiple of 128 bytes: copy it to rows of
+  // whole lines first (see pack_rows_kernel), when asked to or, by default,
+  // for products large enough that the copy costs less than it saves.
+  const int64_t a_rows = (layout & LAYOUT_AT) ? K : M, a_cols = (layout & LAYOUT_AT) ? M : K;
+  if ((lda * 2) % 128 != 0 &&
+      (p->a_repack == 2 ||
+       (p->a_repack == 0 && use_pair && N >= 2048 && a_rows * a_cols >= ((int64_t)1 << 22)))) {
+    const int64_t ldp = (a_cols + 63) / 64 * 64;
+    rc = ensure_buffer(&p->apack, &p->apack_bytes, (size_t)(a_rows * ldp * 2), stream,
+                       "A repack allocation");
+    if (rc) return rc;
+    const int64_t total = a_rows * ((a_cols + 7) / 8);
+    const int pgrid = (int)std::max<int64_t>(
+        1, std::min<int64_t>(ceil_div(total, 256 * 4), (int64_t)p->num_sms * 8));
+    pack_rows_kernel<<<pgrid, 256, 0, stream>>>(static_cast<const __half*>(A), lda,
+                                                static_cast<__half*>(p->apack), ldp, a_rows,
+                                                a_cols);
+    GF16_CUDA(cudaGetLastError(), "launch pack_rows_kernel");
+    A = p->apack;
+    lda = ldp;
+  }
 
   alignas(64) CUtensorMap tmA, tmB, tmC, tmW;
   std::memset(&tmW, 0, sizeof(tmW));
@@ -1396,6 +1467,9 @@ int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, in
   if (!p) return GEMM_F16_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0 || !hA || !hB || !hC) return GEMM_F16_ERR_INVALID_ARG;
   if (lda < K || ldb < N || ldc < N) return GEMM_F16_ERR_INVALID_ARG;
+  // Staging rows at the 16-byte minimum pitch: a contiguous host matrix then
+  // moves in one plain copy (a pitched copy is several times slower); an A
+  // whose pitch is then off 128-byte lines is repacked on the device.
   const int64_t dlda = (K + 7) / 8 * 8, dldb = (N + 7) / 8 * 8, dldc = dldb;
   int rc = gemm_f16_validate(M, N, K, (const void*)16, dlda, (const void*)16, dldb, (const void*)16,
                              dldc, split_k);

@@ -109,7 +109,17 @@ typedef enum gemm_f16_option {
      * sums to the plan's workspace, and a second kernel merges the ranges
      * in order (bitwise reproducible for a fixed n).  The single-CTA
      * attention kernel ignores it. */
-    GEMM_F16_OPT_ATTN_SPLIT = 8
+    GEMM_F16_OPT_ATTN_SPLIT = 8,
+    /* Repack of A when its row pitch (lda * 2 bytes) is not a multiple of
+     * 128 bytes: 0 = automatic (for the CTA-pair kernel when N >= 2048 and
+     * A has at least 2^22 elements), 1 = never, 2 = whenever the pitch is
+     * off.  A 128-byte row of an operand copy from such a matrix touches two
+     * cache lines, which slows the copies that feed the MMAs (4000 x 4104 x
+     * 3000 with lda = 3000: ~20 % longer than with lda = 3008); the repack
+     * copies A once into plan-owned rows of whole lines (grown on the
+     * stream like the split workspace, kept for later runs) and the product
+     * reads that copy.  Results are bit-identical either way. */
+    GEMM_F16_OPT_A_REPACK = 9
 } gemm_f16_option;
 
 /*

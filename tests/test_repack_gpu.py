@@ -1,0 +1,119 @@
+"""GPU tests of the A repack (option GEMM_F16_OPT_A_REPACK).
+
+When A's row pitch is not a multiple of 128 bytes, the library may first
+copy A into rows of whole 128-byte lines and run the product on that copy.
+The copy moves binary16 values unchanged, so the product must be bit for bit
+the one computed from the original A (same kernel, same tiles, same order),
+and it must meet the parity criteria of the "Xe2 ESIMD GEMM" page
+("Correctness testing") against the FP64 oracle.  The source rows are padded
+with a NaN sentinel past K (past M for A stored K x M): a repack that read or
+kept anything beyond a row would turn the product into NaN.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic_inputs as si
+from tests import gpu_util, parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", params=[1, 2], ids=["cta1", "pair256"])
+def plan(request):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import async_barrier_pipelined_gb300 as g
+    from async_barrier_pipelined_gb300 import build
+    build.build()
+    p = g.Plan(0)
+    p.set_option(g.OPT_KERNEL, request.param)
+    yield p
+    p.set_option(g.OPT_A_REPACK, 0)
+    p.close()
+
+
+def _both(plan, A, B, layout, lda, split_k=1):
+    """(product with the repack forced off, product with it forced on, twice)."""
+    import async_barrier_pipelined_gb300 as g
+    out = []
+    for opt in (1, 2, 2):
+        plan.set_option(g.OPT_A_REPACK, opt)
+        c, full = gpu_util.run_layout(plan, A, B, layout, split_k=split_k, lda=lda,
+                                      guard_rows=1)
+        gpu_util.assert_untouched_outside(full, A.shape[0], B.shape[1])
+        out.append(c)
+    plan.set_option(g.OPT_A_REPACK, 0)
+    return out
+
+
+# (M, N, K, split_k); lda is the stored row length rounded up to 8, plus 8 when
+# that happens to land on a whole line, so that every pitch is off by 16-112 bytes.
+CASES = [(300, 520, 200, 1), (385, 513, 1000, 1), (256, 256, 72, 1), (129, 300, 13, 1),
+         (700, 1100, 520, 1), (200, 300, 1000, 3)]
+
+
+def _off_line_ld(cols):
+    ld = (cols + 7) // 8 * 8
+    return ld + 8 if (ld * 2) % 128 == 0 else ld
+
+
+@pytest.mark.parametrize("layout", [0, 1], ids=["NN", "TN"])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
+def test_repack_bit_identical_and_correct(plan, layout, case):
+    M, N, K, split = case
+    w = si.custom(M, N, K, seed=M + 3 * N + 7 * K + layout)
+    A, B = w.pair_bits(0)
+    lda = _off_line_ld(M if layout else K)
+    assert (lda * 2) % 128 != 0
+    never, once, again = _both(plan, A, B, layout, lda, split)
+    parity.check(once, oracle.gemm_f16(A, B), f"repacked A {M}x{N}x{K} layout {layout}")
+    assert np.array_equal(never.view(np.uint64), once.view(np.uint64))
+    assert np.array_equal(once.view(np.uint64), again.view(np.uint64))
+
+
+def test_repack_grows_and_shrinks_between_shapes(plan):
+    """The plan keeps one repack buffer: a larger A grows it, a smaller one
+    reuses it; each product is still exact on small-integer inputs."""
+    import async_barrier_pipelined_gb300 as g
+    rng = np.random.default_rng(5)
+    plan.set_option(g.OPT_A_REPACK, 2)
+    try:
+        for M, N, K in [(130, 140, 60), (520, 300, 1000), (130, 140, 60)]:
+            a = rng.integers(-1, 2, size=(M, K)).astype(np.float16)
+            b = rng.integers(-1, 2, size=(K, N)).astype(np.float16)
+            want = a.astype(np.float64) @ b.astype(np.float64)   # |entries| <= K < 2048: exact
+            c, _ = gpu_util.run(plan, a.view(np.uint16), b.view(np.uint16),
+                                lda=_off_line_ld(K))
+            assert np.array_equal(c, want), (M, N, K)
+    finally:
+        plan.set_option(g.OPT_A_REPACK, 0)
+
+
+def test_repack_option_values(plan):
+    import async_barrier_pipelined_gb300 as g
+    for v in (0, 1, 2):
+        plan.set_option(g.OPT_A_REPACK, v)
+        assert plan.get_option(g.OPT_A_REPACK) == v
+    plan.set_option(g.OPT_A_REPACK, 0)
+    with pytest.raises(g.GemmError):
+        plan.set_option(g.OPT_A_REPACK, 3)
+
+
+def test_ragged_workload_auto_repack_matches_plain(plan):
+    """4000 x 4104 x 3000 with lda = 3000 (6000-byte rows): on the pair
+    kernel the automatic setting repacks A.  Same bits as without the
+    repack, and correct on sampled rows against the oracle."""
+    import async_barrier_pipelined_gb300 as g
+    w = si.WORKLOADS["gemm_ragged"]
+    A, B = w.pair_bits(0)
+    plan.set_option(g.OPT_A_REPACK, 1)
+    plain, _ = gpu_util.run(plan, A, B, lda=w.K)
+    plan.set_option(g.OPT_A_REPACK, 0)
+    auto, _ = gpu_util.run(plan, A, B, lda=w.K)
+    assert np.array_equal(plain.view(np.uint64), auto.view(np.uint64))
+    rows = np.array([0, 1, 127, 128, 255, 256, 2047, 3839, 3968, 3999])
+    parity.check(auto[rows], oracle.gemm_f16(A[rows], B), "ragged workload, sampled rows")
