@@ -27,7 +27,7 @@ __all__ = [
     "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "OPT_ATTN_KERNEL", "OPT_ATTN_SPLIT", "OPT_A_REPACK", "INFO_NUM_SMS", "INFO_MAX_PAIRS",
     "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
     "gemm_f16_run_ex", "gemm_f16_validate_ex", "attn_f16_fwd", "attn_f16_validate",
-    "attn_f16_key_ranges",
+    "attn_f16_key_ranges", "gemm_f16_run_info",
     "attention", "ATTN_HEAD_DIM",
     "LAYOUT_NN", "LAYOUT_TN", "LAYOUT_NT", "LAYOUT_TT",
 ]
@@ -98,6 +98,8 @@ _SIGNATURES = {
                                    ctypes.c_float]),
     "attn_f16_key_ranges": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int,
                                      ctypes.POINTER(_c_int)]),
+    "gemm_f16_run_info": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int,
+                                   ctypes.POINTER(_c_int)]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -241,6 +243,16 @@ def attn_f16_validate(batch, heads, seq_q, seq_kv, head_dim, Q, q_strides, K, k_
                                     Q, _strides3(q_strides), K, _strides3(k_strides),
                                     V, _strides3(v_strides), O, _strides3(o_strides),
                                     float(scale))
+
+
+def gemm_f16_run_info(plan: int, layout: int, M: int, N: int, K: int, lda: int,
+                      split_k: int = 1) -> dict:
+    """What gemm_f16_run_ex would enqueue for these sizes (nothing is run)."""
+    info = (_c_int * 4)()
+    _check(load().gemm_f16_run_info(plan, layout, M, N, K, lda, split_k, info),
+           "gemm_f16_run_info")
+    return {"kernel": info[0], "launches": info[1], "repack_a": bool(info[2]),
+            "tile_width": info[3]}
 
 
 def attn_f16_key_ranges(plan: int, batch: int, heads: int, seq_q: int, seq_kv: int) -> int:

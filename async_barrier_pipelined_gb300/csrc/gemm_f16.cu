@@ -1231,42 +1231,63 @@ inline void* pick_instance(int layout, F0 f0, F1 f1, F2 f2, F3 f3) {
   }
 }
 
-int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* A, int64_t lda,
-               const void* B, int64_t ldb, void* C, int64_t ldc, int split_k,
-               cudaStream_t stream) {
-  const int tiles_m = (int)ceil_div(M, BM);
-  const int kblocks = (int)ceil_div(K, BK);
-  const int bn = (p->tile_width != 0 && ceil_div(N, p->tile_width) <= 65535)
-                     ? p->tile_width
-                     : pick_tile_width(M, N, kblocks, split_k, p->num_sms);
-  const int tiles_n = (int)ceil_div(N, bn);
-  const int64_t units = (int64_t)tiles_m * tiles_n * split_k;
-  if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
+// What a run of this shape does with the plan's current options: which
+// kernel, the single-CTA tile width, and whether A is repacked first.
+struct RunChoice {
+  bool use_pair;  // CTA-pair kernel (else single-CTA kernel)
+  int pair_tn;    // pair tile width: 256 or 512
+  int bn;         // single-CTA tile width: 256, 128 or 64
+  bool pack_a;    // A copied to whole-line rows before the product
+};
 
+RunChoice choose_run(const gemm_f16_plan_s* p, int layout, int M, int N, int K, int64_t lda,
+                     int split_k) {
+  RunChoice c;
+  const int kblocks = (int)ceil_div(K, BK);
+  c.bn = (p->tile_width != 0 && ceil_div(N, p->tile_width) <= 65535)
+             ? p->tile_width
+             : pick_tile_width(M, N, kblocks, split_k, p->num_sms);
   // Automatic choice: the pair kernel once its 256 x 256 tiles (times the
   // splits) fill at least half a wave of pairs; below that the single-CTA
   // kernel's smaller tiles spread the work over more SMs.
   const bool pair_fits = (N + 127) / 128 < 0x3FFF && p->max_pairs > 0;
   const int64_t pair_work = ceil_div(M, 256) * ceil_div(N, 256) * (int64_t)split_k;
-  const bool use_pair = pair_fits && (p->kernel == 2 || p->kernel == 3 ||
-                                      (p->kernel == 0 && M > BM && 2 * pair_work >= p->max_pairs));
+  c.use_pair = pair_fits && (p->kernel == 2 || p->kernel == 3 ||
+                             (p->kernel == 0 && M > BM && 2 * pair_work >= p->max_pairs));
   // 512-wide tiles (less load traffic per MMA, but one accumulator and so
   // no epilogue overlap) only on request: measured slower than 256-wide
   // tiles from 2048^3 to 8192^3.
-  const int pair_tn = (p->kernel == 3 && layout == 0) ? 512 : 256;
+  c.pair_tn = (p->kernel == 3 && layout == 0) ? 512 : 256;
+  // A whose row pitch is not a multiple of 128 bytes: copy it to rows of
+  // whole lines first (see pack_rows_kernel), when asked to or, by default,
+  // for products large enough that the copy costs less than it saves.
+  const int64_t a_elems = (int64_t)M * K;
+  c.pack_a = (lda * 2) % 128 != 0 &&
+             (p->a_repack == 2 ||
+              (p->a_repack == 0 && c.use_pair && N >= 2048 && a_elems >= ((int64_t)1 << 22)));
+  return c;
+}
+
+int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* A, int64_t lda,
+               const void* B, int64_t ldb, void* C, int64_t ldc, int split_k,
+               cudaStream_t stream) {
+  const RunChoice choice = choose_run(p, layout, M, N, K, lda, split_k);
+  const int tiles_m = (int)ceil_div(M, BM);
+  const int kblocks = (int)ceil_div(K, BK);
+  const int bn = choice.bn;
+  const int tiles_n = (int)ceil_div(N, bn);
+  const int64_t units = (int64_t)tiles_m * tiles_n * split_k;
+  if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
+  const bool use_pair = choice.use_pair;
+  const int pair_tn = choice.pair_tn;
   const uint32_t* order = nullptr;
   int64_t pair_tiles = 0;
   int rc = use_pair ? get_pair_table(p, M, N, split_k, pair_tn, &order, &pair_tiles)
                     : get_order_table(p, tiles_m, tiles_n, &order);
   if (rc) return rc;
 
-  // A whose row pitch is not a multiple of 128 bytes: copy it to rows of
-  // whole lines first (see pack_rows_kernel), when asked to or, by default,
-  // for products large enough that the copy costs less than it saves.
   const int64_t a_rows = (layout & LAYOUT_AT) ? K : M, a_cols = (layout & LAYOUT_AT) ? M : K;
-  if ((lda * 2) % 128 != 0 &&
-      (p->a_repack == 2 ||
-       (p->a_repack == 0 && use_pair && N >= 2048 && a_rows * a_cols >= ((int64_t)1 << 22)))) {
+  if (choice.pack_a) {
     const int64_t ldp = (a_cols + 63) / 64 * 64;
     rc = ensure_buffer(&p->apack, &p->apack_bytes, (size_t)(a_rows * ldp * 2), stream,
                        "A repack allocation");
@@ -1459,6 +1480,19 @@ int gemm_f16_run_ex(gemm_f16_plan_t p, int layout, int M, int N, int K, const vo
   if (rc) return rc;
   DeviceGuard g(p->device);
   return run_device(p, layout, M, N, K, A, lda, B, ldb, C, ldc, split_k, (cudaStream_t)stream);
+}
+
+int gemm_f16_run_info(gemm_f16_plan_t p, int layout, int M, int N, int K, int64_t lda,
+                      int split_k, int info[4]) {
+  if (!p || !info || M <= 0 || N <= 0 || K <= 0 || split_k < 1 || layout < 0 || layout > 3 ||
+      lda < ((layout & LAYOUT_AT) ? M : K))
+    return GEMM_F16_ERR_INVALID_ARG;
+  const RunChoice c = choose_run(p, layout, M, N, K, lda, split_k);
+  info[0] = c.use_pair ? (c.pair_tn == 512 ? 3 : 2) : 1;
+  info[1] = 1 + (split_k > 1 ? 1 : 0) + (c.pack_a ? 1 : 0);
+  info[2] = c.pack_a ? 1 : 0;
+  info[3] = c.use_pair ? c.pair_tn : c.bn;
+  return GEMM_F16_OK;
 }
 
 int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, int64_t lda,

@@ -561,7 +561,10 @@ def run_ours(args):
     sh = int(stream.cuda_stream)
     plan = g.Plan(dev.index)
     plan.set_option(g.OPT_KERNEL, args.kernel)
-    launches_per_step = 1 if w.split_k == 1 else 2
+    # what one call enqueues: kernel choice, launches (product, split
+    # reduction, repack of an A whose rows are off 128-byte lines)
+    info = g.gemm_f16_run_info(plan.handle, 0, w.M, w.N, w.K, w.K, w.split_k)
+    launches_per_step = info["launches"]
 
     def step(i):
         p = i % npairs
@@ -668,16 +671,16 @@ def run_ours(args):
 
     plan_sms = plan.get_option(g.INFO_NUM_SMS)
     plan_pairs = plan.get_option(g.INFO_MAX_PAIRS)
-    pair_work = -(-w.M // 256) * -(-w.N // 256) * w.split_k
-    use_pair = plan_pairs > 0 and (args.kernel == 2 or (
-        args.kernel == 0 and w.M > 128 and 2 * pair_work >= plan_pairs))
-    use_wide = use_pair and args.kernel == 3
+    use_pair, use_wide = info["kernel"] in (2, 3), info["kernel"] == 3
     kernel_desc = ("CTA pair (tcgen05 cta_group::2, 256x512 tiles)" if use_wide else
                    "CTA pair (tcgen05 cta_group::2, 256x256 tiles)" if use_pair
-                   else "single CTA (tcgen05 cta_group::1, 128-row tiles)")
+                   else f"single CTA (tcgen05 cta_group::1, 128x{info['tile_width']} tiles)")
+    if info["repack_a"]:
+        kernel_desc += "; A repacked to 128-byte-aligned rows first"
     roofline["kernel"] = ("gf16::pairw::gemm_f16_pair_kernel<512>" if use_wide else
                           "gf16::pair::gemm_f16_pair_kernel" if use_pair
                           else "gf16::gemm_f16_kernel")
+    roofline["launches_per_step"] = launches_per_step
     plan.close()
     if rank == 0:
         line = {

@@ -191,6 +191,22 @@ int gemm_f16_run_ex(gemm_f16_plan_t plan, int layout, int M, int N, int K,
                     void *C, int64_t ldc, int split_k, gemm_f16_stream_t stream);
 
 /*
+ * What gemm_f16_run_ex would enqueue for these sizes with the plan's current
+ * options, without enqueuing anything (host only):
+ *   info[0]  kernel: 1 single-CTA, 2 CTA pair with 256-wide tiles, 3 CTA
+ *            pair with 512-wide tiles;
+ *   info[1]  kernel launches per call: the product, plus one for the split
+ *            reduction when split_k > 1, plus one for the repack of A;
+ *   info[2]  1 if A is repacked first (GEMM_F16_OPT_A_REPACK), else 0;
+ *   info[3]  output tile width of the chosen kernel (single-CTA: 256 / 128 /
+ *            64 columns; pair: 256 or 512).
+ * Returns GEMM_F16_OK or GEMM_F16_ERR_INVALID_ARG (null plan or info, sizes
+ * or split_k < 1, layout outside 0..3, lda below the stored row length).
+ */
+int gemm_f16_run_info(gemm_f16_plan_t plan, int layout, int M, int N, int K, int64_t lda,
+                      int split_k, int info[4]);
+
+/*
  * Same product with HOST operands: copies hA and hB into plan-owned device
  * buffers, runs gemm_f16_run on them and copies the result into hC.
  * Consecutive calls overlap: the input copies run on a plan-internal stream

@@ -117,3 +117,29 @@ def test_ragged_workload_auto_repack_matches_plain(plan):
     assert np.array_equal(plain.view(np.uint64), auto.view(np.uint64))
     rows = np.array([0, 1, 127, 128, 255, 256, 2047, 3839, 3968, 3999])
     parity.check(auto[rows], oracle.gemm_f16(A[rows], B), "ragged workload, sampled rows")
+
+
+def test_run_info_reports_the_launches(plan):
+    """gemm_f16_run_info names the kernel and counts the launches one call
+    enqueues: the product, the split reduction and the repack of A."""
+    import async_barrier_pipelined_gb300 as g
+    h = plan.handle
+    kernel = plan.get_option(g.OPT_KERNEL)
+    info = g.gemm_f16_run_info(h, 0, 4000, 4104, 3000, 3000)
+    assert info["kernel"] == kernel
+    assert info["repack_a"] == (kernel == 2) and info["launches"] == 1 + (kernel == 2)
+    assert g.gemm_f16_run_info(h, 0, 4000, 4104, 3000, 3008)["launches"] == 1
+    assert g.gemm_f16_run_info(h, 0, 512, 512, 32768, 32768, 16)["launches"] == 2
+    plan.set_option(g.OPT_A_REPACK, 2)
+    try:
+        i2 = g.gemm_f16_run_info(h, 1, 300, 520, 200, 304, 3)   # A stored 200 x 300
+        assert i2["repack_a"] and i2["launches"] == 3
+        plan.set_option(g.OPT_A_REPACK, 1)
+        assert not g.gemm_f16_run_info(h, 0, 4000, 4104, 3000, 3000)["repack_a"]
+    finally:
+        plan.set_option(g.OPT_A_REPACK, 0)
+    assert g.gemm_f16_run_info(h, 0, 128, 128, 128, 128)["tile_width"] in (64, 128, 256)
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_run_info(h, 0, 128, 128, 128, 100)   # lda < K
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_run_info(h, 4, 128, 128, 128, 128)
