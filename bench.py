@@ -9,7 +9,9 @@ fixed-order reduction).  The 4096^3 workload rotates through eight seeded A/B
 pairs (8 x 64 MiB = 512 MiB, well above the 129 MB L2), so consecutive
 steps never find their inputs in L2.  Protocol from the "Xe2 ESIMD GEMM"
 page, "Performance testing": random non-zero inputs, rotating buffers, a 5 s
-pause, >= 20 warm-up and 1000 timed iterations by default.
+pause, >= 20 warm-up and 1000 timed iterations by default (more when a
+step is short, so that the timed region lasts at least 0.3 s and the clock
+samples fall inside it).
 
 Timing: CUDA events on the launching stream around exactly K steps, with a
 barrier and a device synchronise on both sides; max over ranks.  With
@@ -64,7 +66,9 @@ KERNEL_SOURCES = [os.path.join(ROOT, "async_barrier_pipelined_gb300", "csrc", f)
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 1000, or more when a step is short, so that "
+                         "the timed region lasts at least 0.3 s and the clock samples cover it)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gemm_4096",
@@ -214,6 +218,28 @@ def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms_total: fl
     """Work of all ranks (each runs `steps` steps of its own replica) over
     the slowest rank's time."""
     return flops_per_step * steps * world / (ms_total * 1e-3) / 1e12
+
+
+MIN_TIMED_S = 0.3
+
+
+def auto_steps(step, barrier, stream, world, dev, start, n=50):
+    """Timed-step count when none is given: 1000, or as many as fill
+    MIN_TIMED_S (at most 200000), from the time of n more untimed steps
+    (the slowest rank's, so that every rank runs the same count).
+    Returns (steps, n)."""
+    import math
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        step(start + i)
+    e1.record(stream)
+    e1.synchronize()
+    barrier()
+    per_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / n
+    return int(min(200000, max(1000, math.ceil(MIN_TIMED_S * 1e3 / max(per_ms, 1e-6))))), n
 
 
 def dist_setup(args):
@@ -448,6 +474,9 @@ def run_attention(args):
     for i in range(args.warmup):
         step(i)
     barrier()
+    probe = 0
+    if args.steps is None:
+        args.steps, probe = auto_steps(step, barrier, stream, world, dev, args.warmup)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -517,7 +546,7 @@ def run_attention(args):
     if rank == 0:
         line = {
             "metric": ATTN_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "steps": args.steps, "warmup": args.warmup + probe, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
             "config": dict(attn_config(w), kernel=("CTA pair (tcgen05 cta_group::2, 256 query "
@@ -590,6 +619,9 @@ def run_ours(args):
     for i in range(args.warmup):
         step(i)
     barrier()
+    probe = 0
+    if args.steps is None:
+        args.steps, probe = auto_steps(step, barrier, stream, world, dev, args.warmup)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -685,7 +717,7 @@ def run_ours(args):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "steps": args.steps, "warmup": args.warmup + probe, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
             "config": dict(workload_config(w), kernel=kernel_desc,
@@ -703,6 +735,8 @@ def run_ours(args):
 def main():
     args = parse_args()
     if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 1000   # each a bounded CPU sample
         return run_reference(args)
     return run_ours(args)
 
