@@ -925,7 +925,7 @@ int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order, uint32_t* out, 
   std::vector<uint32_t> v;
   build_tile_order(tiles_m, tiles_n, order, v);
   const int64_t n = (int64_t)v.size();
-  std::memcpy(out, v.data(), sizeof(uint32_t) * (size_t)std::min<int64_t>(n, cap));
+  if (cap > 0) std::memcpy(out, v.data(), sizeof(uint32_t) * (size_t)std::min<int64_t>(n, cap));
   return n;
 }
 
@@ -1106,7 +1106,7 @@ int64_t gemm_f16_pair_tiles(int M, int N, int pairs, int split_k, int order, int
   std::vector<uint32_t> v;
   build_pair_tiles(M, N, pairs, split_k, order, tile_width, v);
   const int64_t n = (int64_t)v.size();
-  std::memcpy(out, v.data(), sizeof(uint32_t) * (size_t)std::min<int64_t>(n, cap));
+  if (cap > 0) std::memcpy(out, v.data(), sizeof(uint32_t) * (size_t)std::min<int64_t>(n, cap));
   return n;
 }
 

@@ -135,6 +135,12 @@ def test_gemm_splitk_full_and_reproducible(plan):
     for _ in range(10):
         _, full = gpu_util.run(plan, A, B, split_k=w.split_k)
         assert np.array_equal(full, full0)
+    # and on a freshly created plan (new workspace, new tile tables)
+    import async_barrier_pipelined_gb300 as g
+    with g.Plan(0) as fresh:
+        fresh.set_option(g.OPT_KERNEL, plan.get_option(g.OPT_KERNEL))
+        _, full = gpu_util.run(fresh, A, B, split_k=w.split_k)
+    assert np.array_equal(full, full0)
 
 
 # ---------------------------------------------------------------- shape sweep
