@@ -10,7 +10,7 @@ pairs (8 x 64 MiB = 512 MiB, well above the 129 MB L2), so consecutive
 steps never find their inputs in L2.  Protocol from the "Xe2 ESIMD GEMM"
 page, "Performance testing": random non-zero inputs, rotating buffers, a 5 s
 pause, >= 20 warm-up and 1000 timed iterations by default (more when a
-step is short, so that the timed region lasts at least 0.3 s and the clock
+step is short, so that the timed region lasts at least 50 ms and the clock
 samples fall inside it).
 
 Timing: CUDA events on the launching stream around exactly K steps, with a
@@ -68,7 +68,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default: 1000, or more when a step is short, so that "
-                         "the timed region lasts at least 0.3 s and the clock samples cover it)")
+                         "the timed region lasts at least 50 ms and the clock samples cover it)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gemm_4096",
@@ -220,7 +220,7 @@ def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms_total: fl
     return flops_per_step * steps * world / (ms_total * 1e-3) / 1e12
 
 
-MIN_TIMED_S = 0.3
+MIN_TIMED_S = 0.05
 
 
 def auto_steps(step, barrier, stream, world, dev, start, n=50):
