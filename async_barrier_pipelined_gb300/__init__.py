@@ -84,8 +84,9 @@ _SIGNATURES = {
     "gemm_f16_tile_order": (_c_i64, [_c_int, _c_int, _c_int,
                                      ctypes.POINTER(ctypes.c_uint32), _c_i64]),
     "gemm_f16_tile_shape": (_c_int, [ctypes.POINTER(_c_int)] * 4),
-    "gemm_f16_pair_tiles": (_c_i64, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
-                                     ctypes.POINTER(ctypes.c_uint32), _c_i64]),
+    "gemm_f16_pair_tiles": (_c_i64, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                     ctypes.POINTER(ctypes.c_uint32), _c_i64,
+                                     ctypes.POINTER(_c_int)]),
     "gemm_f16_run_noalloc": (_c_int, [_c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
                                       _vp, _c_i64, _c_int, _vp, _vp]),
     "attn_f16_fwd": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
@@ -273,14 +274,17 @@ def gemm_f16_tile_order(tiles_m: int, tiles_n: int, order: int = 0) -> list:
 
 
 def gemm_f16_pair_tiles(M: int, N: int, pairs: int, split_k: int = 1, order: int = 0,
-                        tile_width: int = 256) -> list:
-    """CTA-pair work list as (row0, col0, width) tuples."""
-    n = _check(load().gemm_f16_pair_tiles(M, N, pairs, split_k, order, tile_width, None, 0),
-               "gemm_f16_pair_tiles")
+                        tile_width: int = 256, K: int = 4096, with_parts: bool = False):
+    """CTA-pair work list as (row0, col0, width) tuples; with ``with_parts``
+    also the K parts of the last (len % pairs) tiles: (tiles, parts)."""
+    parts = _c_int(1)
+    n = _check(load().gemm_f16_pair_tiles(M, N, K, pairs, split_k, order, tile_width, None, 0,
+                                          ctypes.byref(parts)), "gemm_f16_pair_tiles")
     buf = (ctypes.c_uint32 * n)()
-    _check(load().gemm_f16_pair_tiles(M, N, pairs, split_k, order, tile_width, buf, n),
+    _check(load().gemm_f16_pair_tiles(M, N, K, pairs, split_k, order, tile_width, buf, n, None),
            "gemm_f16_pair_tiles")
-    return [((v & 0xFFFF) * 256, ((v >> 16) & 0x3FFF) * 128, 128 << (v >> 30)) for v in buf]
+    tiles = [((v & 0xFFFF) * 256, ((v >> 16) & 0x3FFF) * 128, 128 << (v >> 30)) for v in buf]
+    return (tiles, parts.value) if with_parts else tiles
 
 
 def gemm_f16_tile_shape() -> tuple:

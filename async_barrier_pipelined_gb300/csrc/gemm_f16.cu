@@ -580,6 +580,46 @@ __global__ void __launch_bounds__(256)
 }  // namespace gf16
 
 #include "gemm_pair.cuh"
+
+namespace gf16 {
+// C of the pair kernel's tail tiles: C[i, j] = fp16_rn(P0[i, j] + P1[i, j]),
+// P_q the FP32 values of K half q, stored as [2 t + q][256][256] for tail
+// tile t = tiles[t] (pair-kernel table entries).  One thread per 4 columns;
+// rows past M and columns past N are skipped.  Launched as a programmatic
+// dependent of the pair kernel: waits for its completion first.
+__global__ void __launch_bounds__(256)
+    tail_reduce_kernel(const float* __restrict__ ws, const uint32_t* __restrict__ tiles,
+                       int ntiles, int M, int N, __half* __restrict__ C, int64_t ldc) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t total = (int64_t)ntiles * 256 * 64;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(g / (256 * 64));
+    const int rem = (int)(g - (int64_t)t * 256 * 64);
+    const int row = rem >> 6, col = (rem & 63) * 4;
+    const uint32_t e = tiles[t];
+    const int width = pair::narrow_of(e) ? pair::NARROW : pair::WIDE;
+    const int i = (int)pair::tpm_of(e) * pair::PM + row;
+    const int j = (int)pair::n128_of(e) * 128 + col;
+    if (col >= width || i >= M || j >= N) continue;
+    const float* p0 = ws + ((int64_t)(2 * t) * 256 + row) * 256 + col;
+    const float4 a = *reinterpret_cast<const float4*>(p0);
+    const float4 b = *reinterpret_cast<const float4*>(p0 + 256 * 256);
+    const __half2 h0 = __floats2half2_rn(a.x + b.x, a.y + b.y);
+    const __half2 h1 = __floats2half2_rn(a.z + b.z, a.w + b.w);
+    __half* dst = C + (int64_t)i * ldc + j;
+    if (j + 4 <= N && (ldc & 3) == 0) {
+      uint2 v;
+      v.x = *reinterpret_cast<const uint32_t*>(&h0);
+      v.y = *reinterpret_cast<const uint32_t*>(&h1);
+      *reinterpret_cast<uint2*>(dst) = v;
+    } else {
+      const __half vals[4] = {__low2half(h0), __high2half(h0), __low2half(h1), __high2half(h1)};
+      for (int k = 0; k < 4 && j + k < N; ++k) dst[k] = vals[k];
+    }
+  }
+}
+}  // namespace gf16
 #include "gemm_pair_wide.cuh"
 #include "attn_f16.cuh"
 #include "attn_pair.cuh"
@@ -702,6 +742,7 @@ struct OrderTable {
   int64_t key[6];
   uint32_t* dev;
   int64_t count;
+  int parts;  // pair tables: K parts of the last (count % pairs) tiles (1: none)
 };
 
 double pair_makespan(const std::vector<uint32_t>& tiles, int pairs, int tn) {
@@ -711,13 +752,31 @@ double pair_makespan(const std::vector<uint32_t>& tiles, int pairs, int tn) {
   return *std::max_element(load.begin(), load.end());
 }
 
+// K halves for the tiles of a partial last wave of 256-wide pair tiles (one
+// split only).  A pair tile's k-blocks take about the same time whatever its
+// width (measured at 4096^3: a 256 x 128 tile of the last wave 19 us, a
+// 256 x 256 tile 18.8 us), so a half-width tile does not shorten the wave;
+// two units of half the k-blocks each do.  Each half stores its FP32 values
+// and a small kernel adds the two (in half order) and writes C.  Used when
+// the 2 r halves of the r tiles of the partial wave fit in one wave and the
+// tiles have at least 32 k-blocks (shorter ones gain less than the partial
+// stores and the extra launch cost).  Returns 2, or 1 for no split.
+int tail_parts_for(int64_t tiles, int pairs, int split_k, int kblocks) {
+  if (split_k != 1 || pairs <= 0 || kblocks < 32) return 1;
+  const int64_t r = tiles % pairs;
+  return (r > 0 && 2 * r <= pairs) ? 2 : 1;
+}
+
 // Pair-kernel tile list for tiles TN (256 or 512) columns wide: full tiles
 // over the output in Morton order (pair-row on the even bits), then the
 // column remainder as tiles of TN/2 or TN/4 (never under 128).  With one
-// split, if the full tiles leave a partial last wave, those tiles are cut
-// into halves or quarters when that shortens the busiest pair's work.
-void build_pair_tiles(int M, int N, int pairs, int split_k, int order, int tn,
-                      std::vector<uint32_t>& out) {
+// split, if the tiles leave a partial last wave: 256-wide tiles get K halves
+// (`*parts` = 2, see tail_parts_for) for the last (count % pairs) tiles;
+// otherwise the full tiles of that wave are cut into halves or quarters when
+// that shortens the busiest pair's work.
+void build_pair_tiles(int M, int N, int kblocks, int pairs, int split_k, int order, int tn,
+                      std::vector<uint32_t>& out, int* parts) {
+  *parts = 1;
   const int tpms = (int)ceil_div(M, pairw::PM);
   const int min_w = 128;
   // full-width column tiles while more than TN/2 columns remain
@@ -737,6 +796,10 @@ void build_pair_tiles(int M, int N, int pairs, int split_k, int order, int tn,
   out = full;
   out.insert(out.end(), rest.begin(), rest.end());
   if (split_k != 1 || pairs <= 0 || full.empty()) return;
+  if (tn == 256) {
+    *parts = tail_parts_for((int64_t)out.size(), pairs, split_k, kblocks);
+    if (*parts > 1) return;
+  }
   const size_t r = full.size() % (size_t)pairs;
   if (r == 0) return;
   double best = pair_makespan(out, pairs, tn);
@@ -787,6 +850,9 @@ struct gemm_f16_plan_s {
   size_t ws_bytes = 0;
   void* apack = nullptr;  // repacked copy of A (see pack_rows_kernel)
   size_t apack_bytes = 0;
+  // FP32 values of the K halves of the pair kernel's last-wave tiles.
+  void* tail_ws = nullptr;
+  size_t tail_ws_bytes = 0;
   std::vector<OrderTable> orders;
   // run_host: two slots of device staging (A, B, C) used by alternate calls,
   // a stream for the input copies and the events that order the slots.
@@ -1029,6 +1095,7 @@ int gemm_f16_destroy(gemm_f16_plan_t p) {
     for (auto& t : p->orders) cudaFree(t.dev);
     if (p->ws) cudaFree(p->ws);
     if (p->apack) cudaFree(p->apack);
+    if (p->tail_ws) cudaFree(p->tail_ws);
     for (int sl = 0; sl < 2; ++sl)
       for (int i = 0; i < 3; ++i)
         if (p->hbuf[sl][i]) cudaFree(p->hbuf[sl][i]);
@@ -1096,17 +1163,19 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
   }
 }
 
-int64_t gemm_f16_pair_tiles(int M, int N, int pairs, int split_k, int order, int tile_width,
-                            uint32_t* out, int64_t cap) {
-  if (M <= 0 || N <= 0 || pairs < 1 || split_k < 1 || (order != 0 && order != 1))
+int64_t gemm_f16_pair_tiles(int M, int N, int K, int pairs, int split_k, int order,
+                            int tile_width, uint32_t* out, int64_t cap, int* tail_parts) {
+  if (M <= 0 || N <= 0 || K <= 0 || pairs < 1 || split_k < 1 || (order != 0 && order != 1))
     return GEMM_F16_ERR_INVALID_ARG;
   if (tile_width != 256 && tile_width != 512) return GEMM_F16_ERR_INVALID_ARG;
   if (ceil_div(M, pairw::PM) > 65535 || (N + 127) / 128 >= 0x3FFF) return GEMM_F16_ERR_INVALID_ARG;
   if (cap < 0 || (cap > 0 && !out)) return GEMM_F16_ERR_INVALID_ARG;
   std::vector<uint32_t> v;
-  build_pair_tiles(M, N, pairs, split_k, order, tile_width, v);
+  int parts = 1;
+  build_pair_tiles(M, N, (int)ceil_div(K, BK), pairs, split_k, order, tile_width, v, &parts);
   const int64_t n = (int64_t)v.size();
   if (cap > 0) std::memcpy(out, v.data(), sizeof(uint32_t) * (size_t)std::min<int64_t>(n, cap));
+  if (tail_parts) *tail_parts = parts;
   return n;
 }
 
@@ -1133,7 +1202,7 @@ int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
 namespace {
 
 int upload_table(gemm_f16_plan_s* p, const int64_t (&key)[6], const std::vector<uint32_t>& host,
-                 const uint32_t** out) {
+                 const uint32_t** out, int parts = 1) {
   uint32_t* dev = nullptr;
   GF16_CUDA(cudaMalloc(&dev, host.size() * sizeof(uint32_t)), "cudaMalloc(tile order)");
   cudaError_t e = cudaMemcpy(dev, host.data(), host.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
@@ -1145,6 +1214,7 @@ int upload_table(gemm_f16_plan_s* p, const int64_t (&key)[6], const std::vector<
   std::memcpy(t.key, key, sizeof(key));
   t.dev = dev;
   t.count = (int64_t)host.size();
+  t.parts = parts;
   p->orders.push_back(t);
   *out = dev;
   return GEMM_F16_OK;
@@ -1167,21 +1237,23 @@ int get_order_table(gemm_f16_plan_s* p, int tiles_m, int tiles_n, const uint32_t
   return upload_table(p, key, host, out);
 }
 
-int get_pair_table(gemm_f16_plan_s* p, int M, int N, int split_k, int tn, const uint32_t** out,
-                   int64_t* count) {
-  const int64_t key[6] = {tn, M, N, p->max_pairs, split_k, p->tile_order};
+int get_pair_table(gemm_f16_plan_s* p, int M, int N, int kblocks, int split_k, int tn,
+                   const uint32_t** out, int64_t* count, int* parts) {
+  const int64_t key[6] = {tn, M, N, p->max_pairs,
+                          (int64_t)split_k | ((int64_t)kblocks << 32), p->tile_order};
   if (const OrderTable* t = find_table(p, key)) {
     *out = t->dev;
     *count = t->count;
+    *parts = t->parts;
     return GEMM_F16_OK;
   }
   std::vector<uint32_t> host;
-  build_pair_tiles(M, N, p->max_pairs, split_k, p->tile_order, tn, host);
+  build_pair_tiles(M, N, kblocks, p->max_pairs, split_k, p->tile_order, tn, host, parts);
   if (tn == 256)  // the 256-wide kernel's entry format: narrow flag in bit 31
     for (uint32_t& e : host)
       e = pair::pack(pairw::tpm_of(e), pairw::n128_of(e), pairw::width_of(e) == 128);
   *count = (int64_t)host.size();
-  return upload_table(p, key, host, out);
+  return upload_table(p, key, host, out, *parts);
 }
 
 int ensure_buffer(void** buf, size_t* cap, size_t bytes, cudaStream_t stream, const char* what) {
@@ -1282,7 +1354,9 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
   const int pair_tn = choice.pair_tn;
   const uint32_t* order = nullptr;
   int64_t pair_tiles = 0;
-  int rc = use_pair ? get_pair_table(p, M, N, split_k, pair_tn, &order, &pair_tiles)
+  int tail_parts = 1;
+  int rc = use_pair ? get_pair_table(p, M, N, kblocks, split_k, pair_tn, &order, &pair_tiles,
+                                     &tail_parts)
                     : get_order_table(p, tiles_m, tiles_n, &order);
   if (rc) return rc;
 
@@ -1347,9 +1421,28 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
   }
 
   if (use_pair) {
-    const int64_t punits = pair_tiles * split_k;
+    int64_t pair_cap = std::max(p->max_pairs, 1);
+    if (p->sm_limit > 0) pair_cap = std::max<int64_t>(1, std::min<int64_t>(pair_cap, p->sm_limit / 2));
+    // The last (pair_tiles % pairs) tiles run as two K halves each (one
+    // split, 256-wide tiles; see tail_parts_for), planned for all pairs.
+    const int64_t tail_tiles = tail_parts > 1 ? pair_tiles % std::max(p->max_pairs, 1) : 0;
+    const int64_t full_units = (pair_tiles - tail_tiles) * split_k;
+    const int64_t punits = full_units + tail_tiles * tail_parts;
     if (punits > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
     pair::Params pp;
+    pp.full_units = (int)full_units;
+    pp.tail_parts = tail_tiles > 0 ? tail_parts : 1;
+    if (tail_tiles > 0) {
+      // [2 t + q][256][256] FP32 values of the halves; tmW maps it instead
+      // of the split workspace (one split, so that is unused).
+      const int64_t planes = tail_tiles * 2;
+      rc = ensure_buffer(&p->tail_ws, &p->tail_ws_bytes, (size_t)planes * 256 * 256 * sizeof(float),
+                         stream, "tail partial allocation");
+      if (rc) return rc;
+      rc = encode_3d_f32(&tmW, p->tail_ws, 256, 256, (uint64_t)planes, 256 * sizeof(float),
+                         256 * 256 * sizeof(float));
+      if (rc) return rc;
+    }
     pp.M = M;
     pp.N = N;
     pp.K = K;
@@ -1363,8 +1456,6 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
     pp.timeout_ns = p->timeout_ns;
     pp.fault_unit = p->fault_unit;
     pp.b3d = b3d ? 1 : 0;
-    int64_t pair_cap = std::max(p->max_pairs, 1);
-    if (p->sm_limit > 0) pair_cap = std::max<int64_t>(1, std::min<int64_t>(pair_cap, p->sm_limit / 2));
     const int64_t npairs = std::min<int64_t>(punits, pair_cap);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * npairs), 1, 1);
@@ -1398,6 +1489,21 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
                                pair::gemm_f16_pair_kernel<2>, pair::gemm_f16_pair_kernel<3>);
       void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmC, (void*)&tmW, (void*)&pp};
       GF16_CUDA(cudaLaunchKernelExC(&cfg, fn, args), "launch gemm_f16_pair_kernel");
+    }
+    if (tail_tiles > 0) {
+      // P0 + P1 of each tail tile into C (a programmatic dependent launch).
+      const int64_t groups = tail_tiles * 256 * 64;
+      cudaLaunchConfig_t tcfg = {};
+      tcfg.gridDim = dim3((unsigned)std::min<int64_t>(ceil_div(groups, 256), (int64_t)p->num_sms * 8),
+                          1, 1);
+      tcfg.blockDim = dim3(256, 1, 1);
+      tcfg.stream = stream;
+      tcfg.attrs = &pdl;
+      tcfg.numAttrs = 1;
+      GF16_CUDA(cudaLaunchKernelEx(&tcfg, tail_reduce_kernel, (const float*)p->tail_ws,
+                                   order + full_units, (int)tail_tiles, M, N,
+                                   static_cast<__half*>(C), (int64_t)ldc),
+                "launch tail_reduce_kernel");
     }
   } else {
   Params prm;
@@ -1488,8 +1594,15 @@ int gemm_f16_run_info(gemm_f16_plan_t p, int layout, int M, int N, int K, int64_
       lda < ((layout & LAYOUT_AT) ? M : K))
     return GEMM_F16_ERR_INVALID_ARG;
   const RunChoice c = choose_run(p, layout, M, N, K, lda, split_k);
+  // a partial last wave of 256-wide pair tiles in K halves adds their merge
+  int parts = 1;
+  if (c.use_pair && c.pair_tn == 256 && split_k == 1) {
+    std::vector<uint32_t> tiles;
+    build_pair_tiles(M, N, (int)ceil_div(K, BK), p->max_pairs, split_k, p->tile_order, 256, tiles,
+                     &parts);
+  }
   info[0] = c.use_pair ? (c.pair_tn == 512 ? 3 : 2) : 1;
-  info[1] = 1 + (split_k > 1 ? 1 : 0) + (c.pack_a ? 1 : 0);
+  info[1] = 1 + (split_k > 1 ? 1 : 0) + (c.pack_a ? 1 : 0) + (parts > 1 ? 1 : 0);
   info[2] = c.pack_a ? 1 : 0;
   info[3] = c.use_pair ? c.pair_tn : c.bn;
   return GEMM_F16_OK;

@@ -96,6 +96,13 @@ struct Params {
   unsigned long long timeout_ns;
   int fault_unit;
   int b3d;       // row-major B seen as 3-D (64 columns, K, column groups): one copy per stage
+  // Units [0, full_units) are whole tiles (times the splits); units past it
+  // are K halves (one split only): unit full_units + 2 t + q covers half q
+  // of the k-blocks of tile order[full_units + t] ("tail" tile t) and stores
+  // its FP32 values through tmW, which then maps a [2 t + q][256][256]
+  // buffer; a second kernel adds the two halves (P0 + P1) and writes C.
+  int full_units;
+  int tail_parts;          // 2 with tail units, else 1
 };
 
 struct Bars {
@@ -108,13 +115,26 @@ struct UnitGeom {
   int width;     // 256 or 128
   int split;
   int kb0, kb1;
+  int tail;      // tail tile index, or -1 for a whole tile
+  int part;      // K part of a tail tile
 };
 
 __device__ __forceinline__ UnitGeom unit_geom(const Params& p, int u, uint32_t rank) {
   UnitGeom g;
   int tpos;
-  decode_unit(u, p.split_k, &tpos, &g.split);
-  split_range(p.kblocks, p.split_k, g.split, &g.kb0, &g.kb1);
+  if (u < p.full_units) {
+    decode_unit(u, p.split_k, &tpos, &g.split);
+    split_range(p.kblocks, p.split_k, g.split, &g.kb0, &g.kb1);
+    g.tail = -1;
+    g.part = 0;
+  } else {
+    const int v = u - p.full_units;
+    g.tail = v / p.tail_parts;
+    g.part = v - g.tail * p.tail_parts;
+    g.split = 0;
+    split_range(p.kblocks, p.tail_parts, g.part, &g.kb0, &g.kb1);
+    tpos = p.full_units + g.tail;
+  }
   const uint32_t e = p.order[tpos];
   g.m0 = (int)tpm_of(e) * PM + (int)rank * CM;
   g.n0 = (int)n128_of(e) * 128;
@@ -247,17 +267,85 @@ __device__ __forceinline__ uint32_t pack_h2(uint32_t lo, uint32_t hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Per-warp state of the epilogue's FP16 (or split FP32) stores.
+struct EpiStore {
+  uint32_t stage0;   // this warp's two shared staging buffers
+  uint32_t row_off;  // this lane's row in a staging buffer
+  uint32_t sw;       // 16-byte-unit swizzle of that row
+  uint32_t nstore;   // stores issued so far (selects the buffer)
+};
+
+// One 32-column chunk of accumulator values (lane = row) to C, or, with
+// `fp32`, as FP32 values to tmW at (wx, wy, wz) (a split partial, or a tail
+// tile's K half): rows past M and columns past N are clipped by the copy,
+// except a ragged last chunk of an N that is not 16-byte aligned, which goes
+// out to C with masked stores.
+__device__ __forceinline__ void store_chunk(const CUtensorMap* tmC, const CUtensorMap* tmW,
+                                            const Params& p, const uint32_t (&r)[32], int row0,
+                                            int col0, bool fp32, int wx, int wy, int wz,
+                                            uint32_t lane, EpiStore& st) {
+  if (!fp32 && col0 + 32 > p.N && (p.N & 7) != 0) {
+    const int row = row0 + (int)lane;
+    if (row < p.M) {
+      __half* dst = p.C + (int64_t)row * p.ldc + col0;
+      const int nvalid = p.N - col0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nvalid) dst[j] = __float2half_rn(__uint_as_float(r[j]));
+    }
+  } else if (!fp32) {
+    const uint32_t buf = st.stage0 + (st.nstore & 1u) * EPI_BUF;
+    if (lane == 0) ptx::bulk_wait_group_read<1>();
+    __syncwarp();
+#pragma unroll
+    for (uint32_t j = 0; j < 4; ++j) {
+      ptx::st_shared_v4(buf + st.row_off + ((j ^ st.sw) << 4), pack_h2(r[8 * j + 0], r[8 * j + 1]),
+                        pack_h2(r[8 * j + 2], r[8 * j + 3]), pack_h2(r[8 * j + 4], r[8 * j + 5]),
+                        pack_h2(r[8 * j + 6], r[8 * j + 7]));
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(tmC, buf, col0, row0);
+      ptx::bulk_commit_group();
+    }
+    ++st.nstore;
+  } else {
+#pragma unroll
+    for (uint32_t h = 0; h < 2; ++h) {
+      if (col0 + 16 * (int)h >= p.N) break;
+      const uint32_t buf = st.stage0 + (st.nstore & 1u) * EPI_BUF;
+      if (lane == 0) ptx::bulk_wait_group_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (uint32_t j = 0; j < 4; ++j) {
+        const uint32_t* v = &r[16 * h + 4 * j];
+        ptx::st_shared_v4(buf + st.row_off + ((j ^ st.sw) << 4), v[0], v[1], v[2], v[3]);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_3d(tmW, buf, wx + 16 * (int)h, wy, wz);
+        ptx::bulk_commit_group();
+      }
+      ++st.nstore;
+    }
+  }
+}
+
 __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUtensorMap* tmW,
                                               const Params& p, uint32_t base, uint32_t tmem_base,
                                               uint32_t rank, uint32_t pair, uint32_t npairs,
                                               const Bars& b, uint32_t warp, uint32_t lane,
                                               volatile int* abort_flag) {
   const uint32_t quarter = warp & 3u;
-  const uint32_t stage0 = base + OFF_EPI + (warp - EPI_WARP0) * 2 * EPI_BUF;
-  const uint32_t row_off = lane * 64u;
-  const uint32_t sw = (lane >> 1) & 3u;
+  EpiStore st;
+  st.stage0 = base + OFF_EPI + (warp - EPI_WARP0) * 2 * EPI_BUF;
+  st.row_off = lane * 64u;
+  st.sw = (lane >> 1) & 3u;
+  st.nstore = 0;
   const uint32_t leader_tempty = ptx::map_to_cta(b.tempty, 0);
-  uint32_t local = 0, nstore = 0;
+  uint32_t local = 0;
   for (int u = (int)pair; u < p.num_units; u += (int)npairs) {
     const UnitGeom g = unit_geom(p, u, rank);
     const uint32_t acc = local & 1u;
@@ -267,6 +355,11 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
     ptx::tc_fence_after();
     const int row0 = g.m0 + (int)quarter * 32;
     const uint32_t t_row = tmem_base + acc * ACC_COLS + ((quarter * 32u) << 16);
+    // FP32 values for split partials ([split][M][ldw]) and tail halves
+    // ([2 t + q][256][256], tile-relative coordinates).
+    const bool fp32 = p.split_k > 1 || g.tail >= 0;
+    const int wy = g.tail >= 0 ? (int)(rank * 128u + quarter * 32u) : row0;
+    const int wz = g.tail >= 0 ? 2 * g.tail + g.part : g.split;
     if (row0 < p.M) {
       for (int c = 0; c < g.width / 32; ++c) {
         const int col0 = g.n0 + c * 32;
@@ -275,54 +368,8 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
         ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c * 32u, r);
         ptx::tmem_ld_wait();
         ptx::reg_fence(r);
-        if (p.split_k == 1 && col0 + 32 > p.N && (p.N & 7) != 0) {
-          const int row = row0 + (int)lane;
-          if (row < p.M) {
-            __half* dst = p.C + (int64_t)row * p.ldc + col0;
-            const int nvalid = p.N - col0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nvalid) dst[j] = __float2half_rn(__uint_as_float(r[j]));
-          }
-        } else if (p.split_k == 1) {
-          const uint32_t buf = stage0 + (nstore & 1u) * EPI_BUF;
-          if (lane == 0) ptx::bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (uint32_t j = 0; j < 4; ++j) {
-            ptx::st_shared_v4(buf + row_off + ((j ^ sw) << 4), pack_h2(r[8 * j + 0], r[8 * j + 1]),
-                              pack_h2(r[8 * j + 2], r[8 * j + 3]),
-                              pack_h2(r[8 * j + 4], r[8 * j + 5]),
-                              pack_h2(r[8 * j + 6], r[8 * j + 7]));
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_2d(tmC, buf, col0, row0);
-            ptx::bulk_commit_group();
-          }
-          ++nstore;
-        } else {
-#pragma unroll
-          for (uint32_t h = 0; h < 2; ++h) {
-            if (col0 + 16 * (int)h >= p.N) break;
-            const uint32_t buf = stage0 + (nstore & 1u) * EPI_BUF;
-            if (lane == 0) ptx::bulk_wait_group_read<1>();
-            __syncwarp();
-#pragma unroll
-            for (uint32_t j = 0; j < 4; ++j) {
-              const uint32_t* v = &r[16 * h + 4 * j];
-              ptx::st_shared_v4(buf + row_off + ((j ^ sw) << 4), v[0], v[1], v[2], v[3]);
-            }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              ptx::tma_store_3d(tmW, buf, col0 + 16 * (int)h, row0, g.split);
-              ptx::bulk_commit_group();
-            }
-            ++nstore;
-          }
-        }
+        store_chunk(tmC, tmW, p, r, row0, col0, fp32, g.tail >= 0 ? c * 32 : col0, wy, wz, lane,
+                    st);
       }
     }
     ptx::tc_fence_before();
@@ -382,7 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
     ptx::prefetch_tmap(&tmC);
-    if (p.split_k > 1) ptx::prefetch_tmap(&tmW);
+    if (p.split_k > 1 || p.tail_parts > 1) ptx::prefetch_tmap(&tmW);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(b.full + 8 * s, 1);
       ptx::mbar_init(b.empty + 8 * s, 1);

@@ -709,6 +709,8 @@ def run_ours(args):
                    else f"single CTA (tcgen05 cta_group::1, 128x{info['tile_width']} tiles)")
     if info["repack_a"]:
         kernel_desc += "; A repacked to 128-byte-aligned rows first"
+    if info["launches"] > 1 + (w.split_k > 1) + info["repack_a"]:
+        kernel_desc += "; partial last wave in K halves, merged by a second kernel"
     roofline["kernel"] = ("gf16::pairw::gemm_f16_pair_kernel<512>" if use_wide else
                           "gf16::pair::gemm_f16_pair_kernel" if use_pair
                           else "gf16::gemm_f16_kernel")

@@ -196,7 +196,9 @@ int gemm_f16_run_ex(gemm_f16_plan_t plan, int layout, int M, int N, int K,
  *   info[0]  kernel: 1 single-CTA, 2 CTA pair with 256-wide tiles, 3 CTA
  *            pair with 512-wide tiles;
  *   info[1]  kernel launches per call: the product, plus one for the split
- *            reduction when split_k > 1, plus one for the repack of A;
+ *            reduction when split_k > 1, plus one for the repack of A, plus
+ *            one for merging the K halves of a partial last wave of pair
+ *            tiles (see gemm_f16_pair_tiles);
  *   info[2]  1 if A is repacked first (GEMM_F16_OPT_A_REPACK), else 0;
  *   info[3]  output tile width of the chosen kernel (single-CTA: 256 / 128 /
  *            64 columns; pair: 256 or 512).
@@ -278,14 +280,22 @@ int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order,
 
 /*
  * Host-only: the work list of the CTA-pair kernel with full tiles
- * `tile_width` (256 or 512) columns wide, for an M x N output with `pairs`
- * co-resident CTA pairs (see GEMM_F16_INFO_MAX_PAIRS).  Each entry is
- * (pair_row | col128 << 16 | log2(width/128) << 30): rows 256*pair_row ..
- * +255, columns 128*col128 .. +width-1.  Writes up to `cap` entries and
- * returns the count, or a negative error code.
+ * `tile_width` (256 or 512) columns wide, for an M x N x K product with
+ * `pairs` co-resident CTA pairs (see GEMM_F16_INFO_MAX_PAIRS).  Each entry
+ * is (pair_row | col128 << 16 | log2(width/128) << 30): rows 256*pair_row ..
+ * +255, columns 128*col128 .. +width-1.  Writes up to `cap` entries (`out`
+ * may be NULL when cap is 0) and returns the count, or a negative error
+ * code.  If `tail_parts` is not NULL it receives 2 when the last
+ * (count % pairs) tiles run as two K halves each, else 1.  That happens with
+ * split_k 1, 256-wide tiles, at least 32 k-blocks and a partial last wave
+ * whose halves fit in one wave (a pair tile of half the width takes about as
+ * long as a full one, a tile of half the k-blocks half as long): each half
+ * covers a contiguous half of the k-blocks and stores FP32 values in the
+ * plan's workspace, and a second kernel writes C = fp16_rn(P0 + P1), so the
+ * result is deterministic (not bit-identical to a single pass).
  */
-int64_t gemm_f16_pair_tiles(int M, int N, int pairs, int split_k, int order,
-                            int tile_width, uint32_t *out, int64_t cap);
+int64_t gemm_f16_pair_tiles(int M, int N, int K, int pairs, int split_k, int order,
+                            int tile_width, uint32_t *out, int64_t cap, int *tail_parts);
 
 /* Compile-time tile shape of the kernel: BM x BN output tile, BK k-block. */
 int gemm_f16_tile_shape(int *bm, int *bn, int *bk, int *stages);

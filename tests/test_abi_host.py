@@ -176,18 +176,45 @@ def _makespan(tiles, pairs, tw=256):
     return max(load)
 
 
+def _tail_makespan(tiles, parts, pairs, tw=256):
+    """Busiest pair's work in tile times when the last len % pairs tiles run
+    as `parts` K parts each (units handed out round-robin)."""
+    r = len(tiles) % pairs if parts > 1 else 0
+    units = [w / tw for *_, w in tiles[:len(tiles) - r]]
+    for *_, w in tiles[len(tiles) - r:]:
+        units += [w / tw / parts] * parts
+    load = [0.0] * pairs
+    for i, x in enumerate(units):
+        load[i % pairs] += x
+    return max(load)
+
+
 def test_pair_tiles_balance_the_last_wave(lib):
-    # 4096^2: 256 wide tiles on 76 pairs = 3 full waves + 28; the 28 become
-    # 56 narrow tiles, so the busiest pair does 3.5 tiles' work instead of 4
-    t = g.gemm_f16_pair_tiles(4096, 4096, 76, 1)
+    # 4096^3: 256 wide tiles on 76 pairs = 3 full waves + 28; the 28 run as
+    # two K halves each (56 units), so the busiest pair does 3.5 tiles' work
+    t, parts = g.gemm_f16_pair_tiles(4096, 4096, 76, 1, K=4096, with_parts=True)
+    assert len(t) == 256 and all(w == 256 for *_, w in t) and parts == 2
+    assert _tail_makespan(t, parts, 76) == 3.5
+    # ragged 4000 x 4104 x 3000: 256 tiles + 16 narrow remainder tiles = 3
+    # waves + 44; 88 halves would not fit in one wave, so the 44 are cut
+    # into narrow tiles instead (3.5 tiles' work for the busiest pair)
+    t, parts = g.gemm_f16_pair_tiles(4000, 4104, 76, 1, K=3000, with_parts=True)
+    assert parts == 1 and _makespan(t, 76) == 3.5
+    # 1024 x 1024 x 4096: 16 tiles on 76 pairs, 32 halves; with K = 1024
+    # (16 k-blocks) the halves would save less than their merge costs
+    t, parts = g.gemm_f16_pair_tiles(1024, 1024, 76, 1, K=4096, with_parts=True)
+    assert len(t) == 16 and parts == 2 and _tail_makespan(t, parts, 76) == 0.5
+    assert g.gemm_f16_pair_tiles(1024, 1024, 76, 1, K=1024, with_parts=True)[1] == 1
+    # a whole last wave: no parts
+    assert g.gemm_f16_pair_tiles(4864, 4096, 76, 1, K=4096, with_parts=True)[1] == 1
+    # too few k-blocks for parts of two: the 28 tiles become 56 narrow ones
+    t, parts = g.gemm_f16_pair_tiles(4096, 4096, 76, 1, K=64, with_parts=True)
+    assert parts == 1
     assert sum(w == 256 for *_, w in t) == 228 and sum(w == 128 for *_, w in t) == 56
     assert _makespan(t, 76) == 3.5
-    # ragged 4000 x 4104: a 128-wide column remainder plus the same balancing
-    t = g.gemm_f16_pair_tiles(4000, 4104, 76, 1)
-    assert _makespan(t, 76) == 3.5
     # splits keep whole tiles (the split units are the parallelism)
-    t = g.gemm_f16_pair_tiles(512, 512, 76, 16)
-    assert len(t) == 4 and all(w == 256 for *_, w in t)
+    t, parts = g.gemm_f16_pair_tiles(512, 512, 76, 16, K=32768, with_parts=True)
+    assert len(t) == 4 and all(w == 256 for *_, w in t) and parts == 1
     # 512-wide tiles: 128 tiles on 76 pairs; the second wave is cut into
     # quarters (3 per pair at most), 1.75 instead of 2 tiles' work
     t = g.gemm_f16_pair_tiles(4096, 4096, 76, 1, 0, 512)
@@ -195,10 +222,12 @@ def test_pair_tiles_balance_the_last_wave(lib):
 
 
 def test_pair_tiles_reject_bad_arguments(lib):
-    assert lib.gemm_f16_pair_tiles(0, 8, 76, 1, 0, 256, None, 0) == g.ERR_INVALID_ARG
-    assert lib.gemm_f16_pair_tiles(8, 8, 0, 1, 0, 256, None, 0) == g.ERR_INVALID_ARG
-    assert lib.gemm_f16_pair_tiles(8, 8, 76, 0, 0, 256, None, 0) == g.ERR_INVALID_ARG
-    assert lib.gemm_f16_pair_tiles(8, 8, 76, 1, 0, 384, None, 0) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(0, 8, 8, 76, 1, 0, 256, None, 0, None) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 0, 76, 1, 0, 256, None, 0, None) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 8, 0, 1, 0, 256, None, 0, None) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 8, 76, 0, 0, 256, None, 0, None) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 8, 76, 1, 0, 384, None, 0, None) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 8, 76, 1, 0, 256, None, 0, None) == 1
 
 
 @pytest.mark.parametrize("layout,args,code", [

@@ -291,3 +291,38 @@ def test_run_host_back_to_back_calls(plan):
     assert plan.status() == 0
     for A, B, _, _, hC in jobs:
         parity.check(hC.numpy().astype(np.float64), oracle.gemm_f16(A, B), "run_host chain")
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 2048), (300, 600, 2048), (1300, 1024, 2048),
+                                   (256, 256, 2048)])
+def test_tail_k_halves_exact_and_repeatable(plan, shape):
+    """With one split, the pair kernel runs the tiles of a partial last wave
+    as two K halves whose FP32 values a second kernel adds (P0 + P1).
+    Small-integer products stay exact; random inputs meet the parity bounds
+    and repeat bit for bit, also on fewer SMs (the halves are planned for
+    the device, not for the launch).  The other kernels run the same checks."""
+    import async_barrier_pipelined_gb300 as g
+    M, N, K = shape
+    if plan.get_option(g.OPT_KERNEL) == 2:
+        _, parts = g.gemm_f16_pair_tiles(M, N, plan.get_option(g.INFO_MAX_PAIRS), 1, K=K,
+                                         with_parts=True)
+        assert parts == 2
+        assert g.gemm_f16_run_info(plan.handle, 0, M, N, K, K)["launches"] == 2
+    rng = np.random.default_rng(M + N + K)
+    A = _small_int_bits(rng, (M, K), -1, 2)
+    B = _small_int_bits(rng, (K, N), -1, 2)
+    c, full = gpu_util.run(plan, A, B, guard_rows=1, ldc=(N + 7) // 8 * 8 + 8)
+    assert np.array_equal(c, oracle.gemm_f16(A, B))      # |entries| <= K < 2^24, |C| < 2048
+    gpu_util.assert_untouched_outside(full, M, N)
+    w = si.custom(M, N, K, seed=K + 5)
+    A, B = w.pair_bits(0)
+    outs = []
+    try:
+        for limit in (0, 0, 24, 8):
+            plan.set_option(g.OPT_SM_LIMIT, limit)
+            outs.append(gpu_util.run(plan, A, B)[0])
+    finally:
+        plan.set_option(g.OPT_SM_LIMIT, 0)
+    parity.check(outs[0], oracle.gemm_f16(A, B), f"tail halves {shape}")
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint64), outs[0].view(np.uint64))
