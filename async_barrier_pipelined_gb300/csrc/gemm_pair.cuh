@@ -8,7 +8,10 @@
 // CTA a k-block stage is 16 KB of A plus W/2 x 64 halves of B, so the ring
 // is six stages deep and each SM pulls a third less data per MMA cycle than
 // the single-CTA kernel.  Tiles are W = 256 columns wide, or 128 ("narrow")
-// where that balances the last wave or covers a thin column remainder.
+// for a thin column remainder or, when K halves do not apply, to balance the
+// last wave.  With one split, the tiles of a partial last wave may run as two
+// K halves each (see Params::full_units) whose FP32 values a second kernel
+// adds.
 //
 // Operand layouts are a template parameter (bit 0: A stored K x M, bit 1: B
 // stored N x K): only the copies' boxes and the MMA descriptors differ.

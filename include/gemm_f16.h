@@ -74,7 +74,9 @@ typedef enum gemm_f16_option {
      * number of co-resident pairs, else the single-CTA kernel),
      * 1 = single-CTA kernel (128-row tiles, tcgen05 cta_group::1),
      * 2 = CTA-pair kernel with 256-row x 256-column tiles (two TMEM
-     * accumulators, epilogue overlapped; 128-wide tiles in the last wave),
+     * accumulators, epilogue overlapped; with one split a partial last wave
+     * runs as K halves merged by a second kernel, see gemm_f16_pair_tiles,
+     * or as 128-wide tiles),
      * 3 = CTA-pair kernel with 256 x 512 tiles (less load traffic per MMA,
      * one accumulator; 256- and 128-wide tiles in the last wave).  Results
      * agree within the usual tolerance; split results are bitwise
