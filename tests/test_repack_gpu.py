@@ -53,7 +53,8 @@ def _both(plan, A, B, layout, lda, split_k=1):
 # (M, N, K, split_k); lda is the stored row length rounded up to 8, plus 8 when
 # that happens to land on a whole line, so that every pitch is off by 16-112 bytes.
 CASES = [(300, 520, 200, 1), (385, 513, 1000, 1), (256, 256, 72, 1), (129, 300, 13, 1),
-         (700, 1100, 520, 1), (200, 300, 1000, 3)]
+         (700, 1100, 520, 1), (200, 300, 1000, 3),
+         (1000, 1104, 2048, 1)]   # on the pair kernel: a last wave in K halves
 
 
 def _off_line_ld(cols):
