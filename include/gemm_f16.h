@@ -140,16 +140,20 @@ int gemm_f16_plan(gemm_f16_plan_t *out, int device);
  *   B        device, K x N row-major, row stride ldb >= N.
  *   C        device, M x N row-major, row stride ldc >= N.  Overwritten
  *            (no alpha/beta).  Must not overlap A or B.
- *   split_k  1 = one pass over K per output tile.  s > 1 = the K range of
+ *   split_k  1 = no split requested: one pass over K per output tile, except
+ *            that the CTA-pair kernel may run the tiles of a partial last
+ *            wave as two K halves whose FP32 sums a second kernel adds
+ *            (see gemm_f16_pair_tiles; deterministic).  s > 1 = the K range of
  *            every tile is cut into s contiguous, non-empty ranges of
  *            64-wide k-blocks (range t covers k-blocks
  *            [floor(t*KB/s), floor((t+1)*KB/s)), KB = ceil(K/64)); each
  *            range's FP32 partial tile goes to the plan's workspace and a
  *            second kernel sums the s partials in order t = 0..s-1 in FP32
  *            and rounds once to binary16.  Requires s <= KB.
- * The first run with a new tile grid uploads that grid's tile-order table
- * and a split run may grow the workspace; both are stream-ordered on
- * `stream`, so make one such run before capturing the stream in a graph.
+ * The first run with a new tile grid uploads that grid's tile-order table,
+ * and a split run, a run with K halves or a repack of A may grow a plan
+ * buffer; all of that is stream-ordered on `stream`, so make one such run
+ * before capturing the stream in a graph.
  * Errors found on the device (a wait that timed out) are reported later by
  * gemm_f16_status.
  */
