@@ -279,3 +279,21 @@ _ST = (64 * 256, 64 * 256, 256)
 ])
 def test_attn_validate(lib, args, code):
     assert g.attn_f16_validate(*args) == code
+
+
+@pytest.mark.parametrize("tiles,kblocks,want", [
+    (76 + 38, 32, 2),    # 38 tiles left over: 76 halves fill one wave exactly
+    (76 + 39, 32, 1),    # 39 left: 78 halves would need a second wave
+    (76 + 38, 31, 1),    # fewer than 32 k-blocks: the halves would not pay
+    (76, 64, 1),         # whole waves only
+    (1, 32, 2),          # a single tile on 76 pairs
+])
+def test_pair_tail_halves_rule(lib, tiles, kblocks, want):
+    """K halves for the tiles of a partial last wave: only with one split,
+    256-wide tiles, at least 32 k-blocks, and all halves in one wave."""
+    M, N = 256 * tiles, 256          # one pair-tile column: `tiles` tiles
+    _, parts = g.gemm_f16_pair_tiles(M, N, 76, 1, K=64 * kblocks, with_parts=True)
+    assert parts == want
+    # never with a split, never for 512-wide tiles
+    assert g.gemm_f16_pair_tiles(M, N, 76, 2, K=64 * kblocks, with_parts=True)[1] == 1
+    assert g.gemm_f16_pair_tiles(M, 512, 76, 1, 0, 512, K=64 * kblocks, with_parts=True)[1] == 1
