@@ -27,7 +27,7 @@ __all__ = [
     "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "OPT_ATTN_KERNEL", "OPT_ATTN_SPLIT", "OPT_A_REPACK", "INFO_NUM_SMS", "INFO_MAX_PAIRS",
     "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
     "gemm_f16_run_ex", "gemm_f16_validate_ex", "attn_f16_fwd", "attn_f16_validate",
-    "attn_f16_key_ranges", "gemm_f16_run_info",
+    "attn_f16_key_ranges", "gemm_f16_run_info", "attn_f16_fwd_host", "attention_host",
     "attention", "ATTN_HEAD_DIM",
     "LAYOUT_NN", "LAYOUT_TN", "LAYOUT_NT", "LAYOUT_TT",
 ]
@@ -101,6 +101,8 @@ _SIGNATURES = {
                                      ctypes.POINTER(_c_int)]),
     "gemm_f16_run_info": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int,
                                    ctypes.POINTER(_c_int)]),
+    "attn_f16_fwd_host": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,
+                                   _vp, ctypes.c_float, _vp]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -393,3 +395,30 @@ def attention(plan: Plan, Q, K, V, O=None, scale=None, stream=None):
     attn_f16_fwd(plan.handle, B, H, Sq, Skv, D, Q.data_ptr(), st(Q), K.data_ptr(), st(K),
                  V.data_ptr(), st(V), O.data_ptr(), st(O), scale, _stream_handle(stream))
     return O
+
+
+def attn_f16_fwd_host(plan: int, batch: int, heads: int, seq_q: int, seq_kv: int, head_dim: int,
+                      hQ: int, hK: int, hV: int, hO: int, scale: float, stream: int = 0) -> None:
+    """The forward pass on contiguous host buffers (see attn_f16.h)."""
+    _check(load().attn_f16_fwd_host(plan, batch, heads, seq_q, seq_kv, head_dim, hQ, hK, hV, hO,
+                                    float(scale), stream), "attn_f16_fwd_host")
+
+
+def attention_host(plan: Plan, hQ, hK, hV, hO, scale=None, stream=None):
+    """attention() for contiguous float16 CPU tensors (pinned for asynchronous
+    copies): Q, K, V are copied in and O out by the library, overlapping
+    consecutive calls.  Synchronise the stream before reading hO."""
+    import torch
+    for name, X in (("Q", hQ), ("K", hK), ("V", hV), ("O", hO)):
+        if X.dtype != torch.float16 or X.dim() != 4 or X.is_cuda or not X.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float16 CPU tensor [B, H, S, D]")
+    B, H, Sq, D = hQ.shape
+    Skv = hK.shape[2]
+    if (tuple(hK.shape) != (B, H, Skv, D) or tuple(hV.shape) != (B, H, Skv, D)
+            or tuple(hO.shape) != (B, H, Sq, D)):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    attn_f16_fwd_host(plan.handle, B, H, Sq, Skv, D, hQ.data_ptr(), hK.data_ptr(), hV.data_ptr(),
+                      hO.data_ptr(), scale, _stream_handle(stream))
+    return hO

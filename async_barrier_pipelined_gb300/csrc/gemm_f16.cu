@@ -862,6 +862,12 @@ struct gemm_f16_plan_s {
   cudaEvent_t in_done[2] = {nullptr, nullptr};
   cudaEvent_t gemm_done[2] = {nullptr, nullptr};
   int host_slot = 0;
+  // attn_f16_fwd_host: two slots of device Q, K, V, O and their events.
+  void* abuf[2][4] = {{nullptr, nullptr, nullptr, nullptr}, {nullptr, nullptr, nullptr, nullptr}};
+  size_t acap[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+  cudaEvent_t attn_in_done[2] = {nullptr, nullptr};
+  cudaEvent_t attn_done[2] = {nullptr, nullptr};
+  int attn_slot = 0;
   TmapEntry tmaps[TMAP_CACHE];
   int tmap_used = 0, tmap_next = 0;
 };
@@ -1102,6 +1108,10 @@ int gemm_f16_destroy(gemm_f16_plan_t p) {
     for (int sl = 0; sl < 2; ++sl) {
       if (p->in_done[sl]) cudaEventDestroy(p->in_done[sl]);
       if (p->gemm_done[sl]) cudaEventDestroy(p->gemm_done[sl]);
+      if (p->attn_in_done[sl]) cudaEventDestroy(p->attn_in_done[sl]);
+      if (p->attn_done[sl]) cudaEventDestroy(p->attn_done[sl]);
+      for (int i = 0; i < 4; ++i)
+        if (p->abuf[sl][i]) cudaFree(p->abuf[sl][i]);
     }
     if (p->in_stream) cudaStreamDestroy(p->in_stream);
     if (p->status_host) cudaFreeHost(p->status_host);
@@ -2061,6 +2071,68 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
   cfg.numAttrs = 1;
   GF16_CUDA(cudaLaunchKernelEx(&cfg, attn::attn_f16_fwd_kernel, tmQ, tmK, tmV, tmO, prm),
             "launch attn_f16_fwd_kernel");
+  return GEMM_F16_OK;
+}
+
+int attn_f16_fwd_host(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
+                      int head_dim, const void* hQ, const void* hK, const void* hV, void* hO,
+                      float scale, gemm_f16_stream_t stream_) {
+  if (!p || !hQ || !hK || !hV || !hO) return GEMM_F16_ERR_INVALID_ARG;
+  // device copies are contiguous [batch, head, row, 256]
+  const int64_t qs[3] = {(int64_t)heads * seq_q * 256, (int64_t)seq_q * 256, 256};
+  const int64_t ks[3] = {(int64_t)heads * seq_kv * 256, (int64_t)seq_kv * 256, 256};
+  const void* probe = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  int rc = attn_f16_validate(batch, heads, seq_q, seq_kv, head_dim, probe, qs, probe, ks, probe, ks,
+                             probe, qs, scale);
+  if (rc) return rc;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  DeviceGuard g(p->device);
+  if (!p->in_stream)
+    GF16_CUDA(cudaStreamCreateWithFlags(&p->in_stream, cudaStreamNonBlocking),
+              "create input-copy stream");
+  if (!p->attn_in_done[0]) {
+    for (int sl = 0; sl < 2; ++sl) {
+      GF16_CUDA(cudaEventCreateWithFlags(&p->attn_in_done[sl], cudaEventDisableTiming),
+                "create event");
+      GF16_CUDA(cudaEventCreateWithFlags(&p->attn_done[sl], cudaEventDisableTiming),
+                "create event");
+    }
+  }
+  const int slot = p->attn_slot;
+  p->attn_slot ^= 1;
+  void** buf = p->abuf[slot];
+  const size_t qbytes = (size_t)batch * heads * seq_q * 256 * 2;
+  const size_t kbytes = (size_t)batch * heads * seq_kv * 256 * 2;
+  const size_t bytes[4] = {qbytes, kbytes, kbytes, qbytes};
+  bool grow = false;
+  for (int i = 0; i < 4; ++i) grow = grow || p->acap[slot][i] < bytes[i];
+  if (grow) {
+    // Growing a slot: let everything that may still use it finish first.
+    GF16_CUDA(cudaDeviceSynchronize(), "synchronise before growing attention staging");
+    for (int i = 0; i < 4; ++i) {
+      if (p->acap[slot][i] >= bytes[i]) continue;
+      if (buf[i]) cudaFree(buf[i]);
+      buf[i] = nullptr;
+      p->acap[slot][i] = 0;
+      GF16_CUDA(cudaMalloc(&buf[i], bytes[i]), "attention staging allocation");
+      p->acap[slot][i] = bytes[i];
+    }
+  }
+  // Q, K, V go in on the plan's input stream once the call that last used
+  // this slot (two calls ago) has finished its pass and its output copy; the
+  // pass on `stream` waits for them; O comes back on `stream` after the pass.
+  GF16_CUDA(cudaStreamWaitEvent(p->in_stream, p->attn_done[slot], 0), "order input copies");
+  GF16_CUDA(cudaMemcpyAsync(buf[0], hQ, qbytes, cudaMemcpyHostToDevice, p->in_stream), "copy Q");
+  GF16_CUDA(cudaMemcpyAsync(buf[1], hK, kbytes, cudaMemcpyHostToDevice, p->in_stream), "copy K");
+  GF16_CUDA(cudaMemcpyAsync(buf[2], hV, kbytes, cudaMemcpyHostToDevice, p->in_stream), "copy V");
+  GF16_CUDA(cudaEventRecord(p->attn_in_done[slot], p->in_stream), "record input copies");
+  GF16_CUDA(cudaStreamWaitEvent(stream, p->attn_in_done[slot], 0), "order pass after inputs");
+  rc = attn_f16_fwd(p, batch, heads, seq_q, seq_kv, head_dim, buf[0], qs, buf[1], ks, buf[2], ks,
+                    buf[3], qs, scale, stream_);
+  if (rc) return rc;
+  GF16_CUDA(cudaMemcpyAsync(hO, buf[3], qbytes, cudaMemcpyDeviceToHost, stream), "copy O to host");
+  // The slot is free again once O has left it, whatever stream the next call uses.
+  GF16_CUDA(cudaEventRecord(p->attn_done[slot], stream), "record pass and output copy");
   return GEMM_F16_OK;
 }
 

@@ -69,6 +69,25 @@ int attn_f16_fwd(gemm_f16_plan_t plan, int batch, int heads, int seq_q, int seq_
                  float scale, gemm_f16_stream_t stream);
 
 /*
+ * The same forward pass with HOST operands: hQ [batch, heads, seq_q, 256],
+ * hK and hV [batch, heads, seq_kv, 256], hO [batch, heads, seq_q, 256], all
+ * contiguous binary16 in host memory (pinned memory gives asynchronous
+ * copies).  Q, K, V are copied into one of two plan-owned sets of device
+ * buffers on a plan-internal stream, the pass runs on `stream` once they
+ * have arrived, and O is copied back on `stream`; consecutive calls
+ * alternate the two sets, so one call's input copies overlap the previous
+ * call's pass and output copy.  hQ, hK, hV must therefore be ready when the
+ * call is made; synchronise `stream` before reading hO or reusing the
+ * inputs.  A set grows (after a device synchronisation) when a call needs
+ * more room than it has.  Returns the codes of attn_f16_fwd (the sizes and
+ * scale are checked as there; null host pointers give
+ * GEMM_F16_ERR_INVALID_ARG).
+ */
+int attn_f16_fwd_host(gemm_f16_plan_t plan, int batch, int heads, int seq_q, int seq_kv,
+                      int head_dim, const void *hQ, const void *hK, const void *hV, void *hO,
+                      float scale, gemm_f16_stream_t stream);
+
+/*
  * The number of key ranges attn_f16_fwd would cut each item's keys into for
  * these sizes with this plan's current options (1: no split, one kernel
  * launch; n > 1: the CTA-pair kernel plus the merging kernel).  Enqueues

@@ -332,3 +332,31 @@ def test_key_ranges_query(plan):
         plan.set_option(g.OPT_ATTN_SPLIT, 0)
     with pytest.raises(g.GemmError):
         g.attn_f16_key_ranges(h, 0, 1, 1, 1)
+
+
+def test_host_entry_matches_device_path(plan):
+    """attn_f16_fwd_host with pinned host Q, K, V, O: three calls in a row
+    with different inputs and sizes (the two device sets alternate, the
+    second call grows its set) give the device path's bits and meet the
+    oracle's bounds."""
+    import torch
+    import async_barrier_pipelined_gb300 as g
+    shapes = [(1, 2, 300, 500), (2, 1, 256, 256), (1, 3, 520, 700)]
+    calls = []
+    for i, (B, H, Sq, Skv) in enumerate(shapes):
+        w = si.attn_custom(B, H, Sq, Skv, seed=100 + i)
+        qb, kb, vb = w.bits()
+        hQ, hK, hV = (torch.from_numpy(x.view(np.float16).copy()).pin_memory()
+                      for x in (qb, kb, vb))
+        hO = torch.empty((B, H, Sq, D), dtype=torch.float16).pin_memory()
+        g.attention_host(plan, hQ, hK, hV, hO, scale=w.scale)
+        calls.append((hO, hQ, hK, hV, qb, kb, vb, w))
+    torch.cuda.current_stream().synchronize()
+    assert plan.status() == g.OK
+    for hO, hQ, hK, hV, qb, kb, vb, w in calls:
+        got = hO.numpy().astype(np.float64)
+        want_dev = _run(plan, qb, kb, vb, scale=w.scale)
+        assert np.array_equal(got.view(np.uint64), want_dev.view(np.uint64))
+        parity.check(got, oracle.attention_f16(qb, kb, vb, w.scale), f"host entry {qb.shape}")
+    with pytest.raises(g.GemmError):
+        g.attn_f16_fwd_host(plan.handle, 1, 1, 1, 1, 128, 1, 1, 1, 1, 0.0625, 0)
