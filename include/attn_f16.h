@@ -79,9 +79,12 @@ int attn_f16_fwd(gemm_f16_plan_t plan, int batch, int heads, int seq_q, int seq_
  * call's pass and output copy.  hQ, hK, hV must therefore be ready when the
  * call is made; synchronise `stream` before reading hO or reusing the
  * inputs.  A set grows (after a device synchronisation) when a call needs
- * more room than it has.  Returns the codes of attn_f16_fwd (the sizes and
- * scale are checked as there; null host pointers give
- * GEMM_F16_ERR_INVALID_ARG).
+ * more room than it has.  Calls on different streams must be ordered by
+ * the caller, as for every use of a plan (one pass at a time); the plan
+ * orders its own input copies after the output copy of the call that last
+ * used the same set, whatever stream that call ran on.  Returns the codes
+ * of attn_f16_fwd (the sizes and scale are checked as there; null host
+ * pointers give GEMM_F16_ERR_INVALID_ARG).
  */
 int attn_f16_fwd_host(gemm_f16_plan_t plan, int batch, int heads, int seq_q, int seq_kv,
                       int head_dim, const void *hQ, const void *hK, const void *hV, void *hO,

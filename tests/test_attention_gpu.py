@@ -335,13 +335,15 @@ def test_key_ranges_query(plan):
 
 
 def test_host_entry_matches_device_path(plan):
-    """attn_f16_fwd_host with pinned host Q, K, V, O: three calls in a row
-    with different inputs and sizes (the two device sets alternate, the
-    second call grows its set) give the device path's bits and meet the
-    oracle's bounds."""
+    """attn_f16_fwd_host with pinned host Q, K, V, O: five calls in a row
+    with different inputs and sizes, one of them on another stream (the two
+    device sets alternate, the second and third calls grow theirs) give the
+    device path's bits and meet the oracle's bounds."""
     import torch
     import async_barrier_pipelined_gb300 as g
-    shapes = [(1, 2, 300, 500), (2, 1, 256, 256), (1, 3, 520, 700)]
+    shapes = [(1, 2, 300, 500), (2, 1, 256, 256), (1, 3, 520, 700), (1, 2, 300, 500),
+              (1, 1, 400, 600)]
+    side = torch.cuda.Stream()
     calls = []
     for i, (B, H, Sq, Skv) in enumerate(shapes):
         w = si.attn_custom(B, H, Sq, Skv, seed=100 + i)
@@ -349,9 +351,17 @@ def test_host_entry_matches_device_path(plan):
         hQ, hK, hV = (torch.from_numpy(x.view(np.float16).copy()).pin_memory()
                       for x in (qb, kb, vb))
         hO = torch.empty((B, H, Sq, D), dtype=torch.float16).pin_memory()
-        g.attention_host(plan, hQ, hK, hV, hO, scale=w.scale)
+        # The third call runs on another stream, ordered between its
+        # neighbours (a plan's workspace serves one pass at a time); the
+        # plan's input copies for the fifth call reuse its set (without
+        # growing it) only once its pass and output copy there are done.
+        if i == 2:
+            side.wait_stream(torch.cuda.current_stream())
+        g.attention_host(plan, hQ, hK, hV, hO, scale=w.scale, stream=side if i == 2 else None)
+        if i == 2:
+            torch.cuda.current_stream().wait_stream(side)
         calls.append((hO, hQ, hK, hV, qb, kb, vb, w))
-    torch.cuda.current_stream().synchronize()
+    torch.cuda.synchronize()
     assert plan.status() == g.OK
     for hO, hQ, hK, hV, qb, kb, vb, w in calls:
         got = hO.numpy().astype(np.float64)
