@@ -684,6 +684,9 @@ __global__ void __launch_bounds__(256)
     attn_combine_kernel(const float* __restrict__ part, const float2* __restrict__ ml,
                         const Params p, __half* __restrict__ O, int64_t os_b, int64_t os_h,
                         int64_t os_r) {
+  // The next kernel of the stream may start its set-up at once; it waits
+  // for this grid before it touches memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = (int)(threadIdx.x & 31u);

@@ -499,6 +499,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 __global__ void __launch_bounds__(256)
     pack_rows_kernel(const __half* __restrict__ src, int64_t ld_src, __half* __restrict__ dst,
                      int64_t ld_dst, int64_t rows, int64_t cols) {
+  // The product kernel that follows may start its set-up now; it waits for
+  // this grid's completion (griddepcontrol.wait) before it reads dst.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t chunks = (cols + 7) / 8;
   const int64_t total = rows * chunks;
   const int64_t step = (int64_t)gridDim.x * blockDim.x;
@@ -528,8 +531,9 @@ __global__ void __launch_bounds__(256)
 
 // Fixed-order split reduction: C[i,j] = fp16_rn(P_0 + P_1 + ... + P_{S-1}),
 // summed left to right in FP32.  Each thread owns 4 consecutive columns;
-// the partial loads are issued four splits at a time (independent loads),
-// but the additions keep the order t = 0, 1, ..., S-1.
+// the partial loads are issued eight splits at a time (independent loads,
+// so a 16-way split waits for two rounds of loads, not sixteen), but the
+// additions keep the order t = 0, 1, ..., S-1.
 __device__ __forceinline__ void add4(float4& acc, const float4& v) {
   acc.x += v.x;
   acc.y += v.y;
@@ -541,7 +545,9 @@ __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ ws, int M, int N, int64_t ldw, int split_k,
                          int64_t split_stride, __half* __restrict__ C, int64_t ldc) {
   // Launched as a programmatic dependent of the GEMM kernel: wait here until
-  // that grid has finished and its partials are visible.
+  // that grid has finished and its partials are visible.  (No early signal
+  // to the next kernel: letting the next product start its set-up here made
+  // 512 x 512 x 32768 in 16 splits 2 us slower per call.)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t groups = (N + 3) / 4;
   const int64_t total = (int64_t)M * groups;
@@ -552,17 +558,25 @@ __global__ void __launch_bounds__(256)
     const float* src = ws + i * ldw + j;
     float4 acc = *reinterpret_cast<const float4*>(src);
     int s = 1;
-    for (; s + 4 <= split_k; s += 4) {
-      const float4 v0 = *reinterpret_cast<const float4*>(src + (int64_t)s * split_stride);
-      const float4 v1 = *reinterpret_cast<const float4*>(src + (int64_t)(s + 1) * split_stride);
-      const float4 v2 = *reinterpret_cast<const float4*>(src + (int64_t)(s + 2) * split_stride);
-      const float4 v3 = *reinterpret_cast<const float4*>(src + (int64_t)(s + 3) * split_stride);
-      add4(acc, v0);
-      add4(acc, v1);
-      add4(acc, v2);
-      add4(acc, v3);
+    for (; s + 8 <= split_k; s += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[q] = *reinterpret_cast<const float4*>(src + (int64_t)(s + q) * split_stride);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) add4(acc, v[q]);
     }
-    for (; s < split_k; ++s) add4(acc, *reinterpret_cast<const float4*>(src + (int64_t)s * split_stride));
+    if (s < split_k) {
+      // the last 1..7 splits, also loaded together before they are added
+      float4 v[7];
+#pragma unroll
+      for (int q = 0; q < 7; ++q)
+        if (s + q < split_k)
+          v[q] = *reinterpret_cast<const float4*>(src + (int64_t)(s + q) * split_stride);
+#pragma unroll
+      for (int q = 0; q < 7; ++q)
+        if (s + q < split_k) add4(acc, v[q]);
+    }
     const __half2 h0 = __floats2half2_rn(acc.x, acc.y), h1 = __floats2half2_rn(acc.z, acc.w);
     __half* dst = C + i * ldc + j;
     if (j + 4 <= N) {

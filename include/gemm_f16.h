@@ -28,6 +28,14 @@
  *     an error no work has been enqueued.
  *   - A plan may be used from one host thread / one stream at a time (it
  *     owns a workspace and a status word that concurrent runs would share).
+ *   - Every kernel of a call is launched with programmatic stream
+ *     serialisation, and some let the next kernel of the stream start
+ *     early: a
+ *     kernel the caller launches next on the same stream WITH that launch
+ *     attribute must execute griddepcontrol.wait
+ *     (cudaGridDependencySynchronize) before it touches the call's results
+ *     or operands; kernels, copies and events enqueued without it are
+ *     ordered as usual.
  */
 #ifndef GEMM_F16_H
 #define GEMM_F16_H
