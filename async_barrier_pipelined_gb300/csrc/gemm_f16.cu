@@ -1671,9 +1671,10 @@ int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, in
       p->hcap[slot][i] = bytes[i];
     }
   }
-  // Input copies on the plan's own stream, once the product that last read
-  // this slot (two calls ago) has finished; the product on `stream` waits
-  // for them; the result copy follows the product on `stream`.
+  // Input copies on the plan's own stream, once the call that last used
+  // this slot (two calls ago) has finished its product and its result copy;
+  // the product on `stream` waits for them; the result copy follows the
+  // product on `stream`.
   GF16_CUDA(cudaStreamWaitEvent(p->in_stream, p->gemm_done[slot], 0), "order input copies");
   GF16_CUDA(copy_rows(buf[0], dlda * 2, hA, lda * 2, (int64_t)K * 2, M, cudaMemcpyHostToDevice,
                       p->in_stream),
@@ -1685,10 +1686,12 @@ int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, in
   GF16_CUDA(cudaStreamWaitEvent(stream, p->in_done[slot], 0), "order product after inputs");
   rc = run_device(p, 0, M, N, K, buf[0], dlda, buf[1], dldb, buf[2], dldc, split_k, stream);
   if (rc) return rc;
-  GF16_CUDA(cudaEventRecord(p->gemm_done[slot], stream), "record product");
   GF16_CUDA(copy_rows(hC, ldc * 2, buf[2], dldc * 2, (int64_t)N * 2, M, cudaMemcpyDeviceToHost,
                       stream),
             "copy C to host");
+  // The slot is free again once C has left it, whatever stream the next
+  // call that uses it runs on.
+  GF16_CUDA(cudaEventRecord(p->gemm_done[slot], stream), "record product and result copy");
   return GEMM_F16_OK;
 }
 

@@ -233,7 +233,10 @@ int gemm_f16_run_info(gemm_f16_plan_t plan, int layout, int M, int N, int K, int
  * read); synchronise `stream` before reading hC or reusing hA / hB.
  * Pinned host memory gives asynchronous copies.  Host buffers need no
  * alignment; lda/ldb/ldc >= K/N/N (any value).  The device slots grow on
- * demand (growing synchronises the device) and stay with the plan.
+ * demand (growing synchronises the device) and stay with the plan.  Calls
+ * on different streams must be ordered by the caller (one product at a
+ * time per plan); a slot's next input copies wait for the result copy of
+ * the call that last used it, whatever stream that call ran on.
  */
 int gemm_f16_run_host(gemm_f16_plan_t plan, int M, int N, int K,
                       const void *hA, int64_t lda, const void *hB, int64_t ldb,

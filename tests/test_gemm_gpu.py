@@ -277,6 +277,7 @@ def test_run_host_back_to_back_calls(plan):
     shapes = [(300, 260, 200), (300, 260, 200), (520, 300, 330), (300, 260, 200),
               (129, 64, 1000), (520, 300, 330)]
     s = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
     jobs = []
     for t, (M, N, K) in enumerate(shapes):
         w = si.custom(M, N, K, seed=100 + t)
@@ -284,10 +285,18 @@ def test_run_host_back_to_back_calls(plan):
         hA = torch.from_numpy(A.view(np.float16)).pin_memory()
         hB = torch.from_numpy(B.view(np.float16)).pin_memory()
         hC = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+        # Call 2 runs on another stream, ordered between its neighbours; call
+        # 4 reuses its slot (without growing it) and must not overwrite that
+        # slot's C before call 2's result copy there has finished.
+        st = side if t == 2 else s
+        if t == 2:
+            side.wait_stream(s)
         g.gemm_f16_run_host(plan.handle, M, N, K, hA.data_ptr(), K, hB.data_ptr(), N,
-                            hC.data_ptr(), N, 1, int(s.cuda_stream))
+                            hC.data_ptr(), N, 1, int(st.cuda_stream))
+        if t == 2:
+            s.wait_stream(side)
         jobs.append((A, B, hA, hB, hC))
-    s.synchronize()
+    torch.cuda.synchronize()
     assert plan.status() == 0
     for A, B, _, _, hC in jobs:
         parity.check(hC.numpy().astype(np.float64), oracle.gemm_f16(A, B), "run_host chain")
