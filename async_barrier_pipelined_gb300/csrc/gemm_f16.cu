@@ -1647,13 +1647,17 @@ int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, in
   if (rc) return rc;
   cudaStream_t stream = (cudaStream_t)stream_;
   DeviceGuard g(p->device);
-  if (!p->in_stream) {
+  // The input-copy stream is shared with attn_f16_fwd_host; each entry point
+  // creates its own events, each one once.
+  if (!p->in_stream)
     GF16_CUDA(cudaStreamCreateWithFlags(&p->in_stream, cudaStreamNonBlocking),
               "create input-copy stream");
-    for (int sl = 0; sl < 2; ++sl) {
+  for (int sl = 0; sl < 2; ++sl) {
+    if (!p->in_done[sl])
       GF16_CUDA(cudaEventCreateWithFlags(&p->in_done[sl], cudaEventDisableTiming), "create event");
-      GF16_CUDA(cudaEventCreateWithFlags(&p->gemm_done[sl], cudaEventDisableTiming), "create event");
-    }
+    if (!p->gemm_done[sl])
+      GF16_CUDA(cudaEventCreateWithFlags(&p->gemm_done[sl], cudaEventDisableTiming),
+                "create event");
   }
   const int slot = p->host_slot;
   p->host_slot ^= 1;
@@ -2107,13 +2111,13 @@ int attn_f16_fwd_host(gemm_f16_plan_t p, int batch, int heads, int seq_q, int se
   if (!p->in_stream)
     GF16_CUDA(cudaStreamCreateWithFlags(&p->in_stream, cudaStreamNonBlocking),
               "create input-copy stream");
-  if (!p->attn_in_done[0]) {
-    for (int sl = 0; sl < 2; ++sl) {
+  for (int sl = 0; sl < 2; ++sl) {
+    if (!p->attn_in_done[sl])
       GF16_CUDA(cudaEventCreateWithFlags(&p->attn_in_done[sl], cudaEventDisableTiming),
                 "create event");
+    if (!p->attn_done[sl])
       GF16_CUDA(cudaEventCreateWithFlags(&p->attn_done[sl], cudaEventDisableTiming),
                 "create event");
-    }
   }
   const int slot = p->attn_slot;
   p->attn_slot ^= 1;

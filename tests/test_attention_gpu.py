@@ -370,3 +370,38 @@ def test_host_entry_matches_device_path(plan):
         parity.check(got, oracle.attention_f16(qb, kb, vb, w.scale), f"host entry {qb.shape}")
     with pytest.raises(g.GemmError):
         g.attn_f16_fwd_host(plan.handle, 1, 1, 1, 1, 128, 1, 1, 1, 1, 0.0625, 0)
+
+
+def test_host_entries_share_a_plan():
+    """attn_f16_fwd_host and gemm_f16_run_host on one fresh plan, attention
+    first: both entry points share the plan's input-copy stream and each
+    keeps its own events and device sets."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import async_barrier_pipelined_gb300 as g
+    from async_barrier_pipelined_gb300 import build
+    build.build()
+    with g.Plan(0) as p:
+        w = si.attn_custom(1, 2, 300, 500, seed=7)
+        qb, kb, vb = w.bits()
+        hQ, hK, hV = (torch.from_numpy(x.view(np.float16).copy()).pin_memory()
+                      for x in (qb, kb, vb))
+        hO = torch.empty((1, 2, 300, D), dtype=torch.float16).pin_memory()
+        g.attention_host(p, hQ, hK, hV, hO, scale=w.scale)
+        gw = si.custom(300, 260, 200, seed=8)
+        A, B = gw.pair_bits(0)
+        hA = torch.from_numpy(A.view(np.float16)).pin_memory()
+        hB = torch.from_numpy(B.view(np.float16)).pin_memory()
+        hC = torch.full((300, 260), float("nan"), dtype=torch.float16).pin_memory()
+        s = torch.cuda.current_stream()
+        g.gemm_f16_run_host(p.handle, 300, 260, 200, hA.data_ptr(), 200, hB.data_ptr(), 260,
+                            hC.data_ptr(), 260, 1, int(s.cuda_stream))
+        hO2 = torch.empty_like(hO).pin_memory()
+        g.attention_host(p, hQ, hK, hV, hO2, scale=w.scale)
+        s.synchronize()
+        assert p.status() == g.OK
+        parity.check(hC.numpy().astype(np.float64), oracle.gemm_f16(A, B), "gemm host after attention")
+        ref = oracle.attention_f16(qb, kb, vb, w.scale)
+        parity.check(hO.numpy().astype(np.float64), ref, "attention host, first")
+        assert np.array_equal(hO.numpy().view(np.uint16), hO2.numpy().view(np.uint16))
