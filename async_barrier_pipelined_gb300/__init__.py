@@ -23,7 +23,7 @@ __all__ = [
     "gemm_f16_strerror", "gemm_f16_last_cuda_error", "gemm_f16_validate",
     "gemm_f16_tile_order", "gemm_f16_tile_shape", "Plan", "matmul",
     "OK", "ERR_INVALID_ARG", "ERR_MISALIGNED", "ERR_UNSUPPORTED_DEVICE",
-    "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT", "ERR_SCRATCH_TOO_SMALL", "gemm_f16_run_noalloc",
+    "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT", "ERR_SCRATCH_TOO_SMALL", "gemm_f16_run_noalloc", "gemm_f16_noalloc_status",
     "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "OPT_ATTN_KERNEL", "OPT_ATTN_SPLIT", "OPT_A_REPACK", "INFO_NUM_SMS", "INFO_MAX_PAIRS",
     "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
     "gemm_f16_run_ex", "gemm_f16_validate_ex", "attn_f16_fwd", "attn_f16_validate",
@@ -89,6 +89,7 @@ _SIGNATURES = {
                                      ctypes.POINTER(_c_int)]),
     "gemm_f16_run_noalloc": (_c_int, [_c_int, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64,
                                       _vp, _c_i64, _c_int, _vp, _vp]),
+    "gemm_f16_noalloc_status": (_c_int, []),
     "attn_f16_fwd": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                               _vp, ctypes.POINTER(_c_i64), _vp, ctypes.POINTER(_c_i64),
                               _vp, ctypes.POINTER(_c_i64), _vp, ctypes.POINTER(_c_i64),
@@ -214,6 +215,16 @@ def gemm_f16_run_noalloc(M: int, N: int, K: int, A: int, lda: int, B: int, ldb: 
     """
     _check(load().gemm_f16_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, split_k, status,
                                        stream), "gemm_f16_run_noalloc")
+
+
+def gemm_f16_noalloc_status() -> int:
+    """Read and clear the status word of no-alloc calls made with status 0
+    on the current device (0, or ERR_TIMEOUT).  Call after their stream has
+    been synchronised."""
+    rc = int(load().gemm_f16_noalloc_status())
+    if rc not in (0, ERR_TIMEOUT):
+        _check(rc, "gemm_f16_noalloc_status")
+    return rc
 
 
 def gemm_f16_validate(M, N, K, A, lda, B, ldb, C, ldc, split_k) -> int:

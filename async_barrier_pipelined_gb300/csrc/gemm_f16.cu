@@ -48,10 +48,10 @@
 #include <utility>
 #include <vector>
 
-#include "attn_f16.h"
-#include "gemm_f16.h"
+#include "host.h"
 #include "ptx.cuh"
 #include "schedule.h"
+#include "common.cuh"
 
 namespace gf16 {
 
@@ -97,15 +97,6 @@ __host__ __device__ constexpr int stages_for(int w) {
 static_assert(stages_for(256) == 4 && stages_for(128) == 6 && stages_for(64) == 8, "ring sizes");
 static_assert(2 * ACC_COLS <= TMEM_COLS, "two accumulators must fit in TMEM");
 
-// Instruction descriptor of tcgen05.mma kind::f16: D FP32 (bits 4-5 = 1),
-// A and B FP16 (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B MN-major
-// (bit 16 = 1, row-major B is N-contiguous), N >> 3 at bits 17-22,
-// M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
 // Operand layouts (the `layout` of gemm_f16_run_ex): bit 0 = A is stored
 // K x M (M contiguous), bit 1 = B is stored N x K (K contiguous).  Row-major
 // A is K-major for the MMA and row-major B is MN-major; a stored-transposed
@@ -116,13 +107,6 @@ __host__ __device__ constexpr uint32_t idesc_for_layout(uint32_t idesc, int layo
          ((layout & LAYOUT_BT) ? 0u : (1u << 16));
 }
 
-// Shared-memory matrix descriptor (tcgen05): start address >> 4 (bits 0-13),
-// leading byte offset >> 4 (16-29), stride byte offset >> 4 (32-45), fixed
-// 0b001 at bits 46-48, base offset 0, swizzle mode 2 = 128-byte (bits 61-63).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
 // A tile (K-major, 128-byte swizzle): 8-row groups 1024 B apart (SBO); the
 // leading offset is unused for swizzled K-major operands.  One MMA K-slice
 // of 16 halves is 32 bytes, so slice k starts 32*k bytes into the rows.
@@ -153,7 +137,7 @@ struct Params {
   int stages;              // ring depth for that width (stages_for(bn))
   uint32_t stage_bytes;    // A_STAGE + bn * BK * 2
   int tiles_m, tiles_n, split_k, kblocks, num_units;
-  const uint32_t* order;   // tile order: tiles_m*tiles_n packed (tm | tn<<16)
+  int row_major;           // tile order: 1 row-major, 0 Morton (morton_tile_of_rank)
   __half* C;               // output, for the masked stores of a ragged last chunk
   int64_t ldc;
   int* status;             // device-visible status word
@@ -164,6 +148,12 @@ struct Params {
 struct Bars {
   uint32_t full, empty, tfull, tempty, mma_done;  // shared addresses of the arrays
 };
+
+// Packed (tm, tn) of the tile at position `tpos` of the launch's tile order.
+__device__ __forceinline__ uint32_t tile_at(const Params& p, int tpos) {
+  return p.row_major ? pack_tile((uint32_t)tpos / (uint32_t)p.tiles_n, (uint32_t)tpos % (uint32_t)p.tiles_n)
+                     : morton_tile_of_rank((uint32_t)tpos, (uint32_t)p.tiles_m, (uint32_t)p.tiles_n);
+}
 
 // ------------------------------------------------------------------ waits
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Params& p,
@@ -188,15 +178,6 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   return wait_slow(bar, parity, p, abort_flag);
 }
 
-// Bounded wait used while draining after an abort (ignores the abort flag).
-__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer() - t0 > limit_ns) return false;
-  }
-  return true;
-}
-
 // ------------------------------------------------------------------ roles
 // Returns, through pos_out / issued_out, where the ring stands when the role
 // stops, so that an aborted CTA can drain its copies in flight.
@@ -214,7 +195,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tmA, const CUte
     int tpos, s, kb0, kb1;
     decode_unit(u, p.split_k, &tpos, &s);
     split_range(p.kblocks, p.split_k, s, &kb0, &kb1);
-    const uint32_t packed = p.order[tpos];
+    const uint32_t packed = tile_at(p, tpos);
     const int m0 = (int)tile_m_of(packed) * BM;
     const int n0 = (int)tile_n_of(packed) * p.bn;
     const int skip_kb = (u == p.fault_unit) ? kb0 : -1;
@@ -326,7 +307,7 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     int tpos, s;
     decode_unit(u, p.split_k, &tpos, &s);
-    const uint32_t packed = p.order[tpos];
+    const uint32_t packed = tile_at(p, tpos);
     const int m0 = (int)tile_m_of(packed) * BM;
     const int n0 = (int)tile_n_of(packed) * p.bn;
     const uint32_t acc = local & 1u;
@@ -634,135 +615,39 @@ __global__ void __launch_bounds__(256)
   }
 }
 }  // namespace gf16
-#include "gemm_pair_wide.cuh"
-#include "attn_f16.cuh"
-#include "attn_pair.cuh"
 
 // ====================================================================== host
 using namespace gf16;
+using namespace gf16::host;
 
 namespace {
 
-thread_local char g_last_cuda_error[512] = "no CUDA error recorded";
-
-int cuda_fail(cudaError_t e, const char* what) {
-  std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%s)", what,
-                cudaGetErrorName(e), cudaGetErrorString(e));
-  return (e == cudaErrorMemoryAllocation) ? GEMM_F16_ERR_OOM : GEMM_F16_ERR_CUDA;
-}
-
-#define GF16_CUDA(call, what)                          \
-  do {                                                 \
-    cudaError_t e_ = (call);                           \
-    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
-  } while (0)
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
-              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-              CUtensorMapSwizzle swz, CUtensorMapL2promotion promo) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) {
-    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
-                  "cuTensorMapEncodeTiled entry point not available");
-    return GEMM_F16_ERR_CUDA;
-  }
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
-                  "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
-    return GEMM_F16_ERR_CUDA;
-  }
-  return GEMM_F16_OK;
-}
-
-int encode_3d_f32(CUtensorMap* map, const void* ptr, uint64_t n, uint64_t m, uint64_t s,
-                  uint64_t row_bytes, uint64_t plane_bytes) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return GEMM_F16_ERR_CUDA;
-  const cuuint64_t dims[3] = {n, m, s};
-  const cuuint64_t strides[2] = {row_bytes, plane_bytes};
-  const cuuint32_t box[3] = {16, 32, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
-                  "cuTensorMapEncodeTiled (workspace) failed (CUresult %d)", (int)r);
-    return GEMM_F16_ERR_CUDA;
-  }
-  return GEMM_F16_OK;
-}
-
-struct DeviceGuard {
-  int prev = -1;
-  bool switched = false;
-  explicit DeviceGuard(int dev) {
-    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
-      switched = (cudaSetDevice(dev) == cudaSuccess);
-    }
-  }
-  ~DeviceGuard() {
-    if (switched) cudaSetDevice(prev);
-  }
-};
-
-int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
+// Tile order of a tiles_m x tiles_n grid: row-major (order 1) or Morton
+// (order 0, by increasing morton_code; the kernels derive the same order
+// from a tile's rank with morton_tile_of_rank).
 void build_tile_order(int tiles_m, int tiles_n, int order, std::vector<uint32_t>& out) {
   out.clear();
   out.reserve((size_t)tiles_m * tiles_n);
-  if (order == 1) {
-    for (int tm = 0; tm < tiles_m; ++tm)
-      for (int tn = 0; tn < tiles_n; ++tn) out.push_back(pack_tile(tm, tn));
-    return;
-  }
-  std::vector<std::pair<uint32_t, uint32_t>> coded;
-  coded.reserve(out.capacity());
-  for (int tm = 0; tm < tiles_m; ++tm)
-    for (int tn = 0; tn < tiles_n; ++tn)
-      coded.emplace_back(morton_code((uint32_t)tm, (uint32_t)tn), pack_tile(tm, tn));
-  std::sort(coded.begin(), coded.end());
-  for (auto& c : coded) out.push_back(c.second);
+  const uint32_t n = (uint32_t)tiles_m * (uint32_t)tiles_n;
+  for (uint32_t r = 0; r < n; ++r)
+    out.push_back(order == 1 ? pack_tile(r / (uint32_t)tiles_n, r % (uint32_t)tiles_n)
+                             : morton_tile_of_rank(r, (uint32_t)tiles_m, (uint32_t)tiles_n));
 }
 
-// Device tile tables cached per plan.  kind 0: single-CTA grid
-// (tiles_m, tiles_n, order); kind 1: pair tiles (M, N, pairs, split, order).
-struct OrderTable {
-  int64_t key[6];
-  uint32_t* dev;
-  int64_t count;
-  int parts;  // pair tables: K parts of the last (count % pairs) tiles (1: none)
-};
+// Pair-kernel work-list entries as the host planner and gemm_f16_pair_tiles
+// see them: pair row (256 rows) in bits 0-15, column offset in units of 128
+// in bits 16-29, log2(width / 128) in bits 30-31 (width 128 or 256).
+uint32_t ptile(uint32_t tpm, uint32_t n128, int width) {
+  return tpm | (n128 << 16) | ((width == 256 ? 1u : 0u) << 30);
+}
+uint32_t ptile_tpm(uint32_t e) { return e & 0xFFFFu; }
+uint32_t ptile_n128(uint32_t e) { return (e >> 16) & 0x3FFFu; }
+int ptile_width(uint32_t e) { return 128 << (e >> 30); }
 
-double pair_makespan(const std::vector<uint32_t>& tiles, int pairs, int tn) {
+double pair_makespan(const std::vector<uint32_t>& tiles, int pairs) {
   std::vector<double> load((size_t)pairs, 0.0);
   for (size_t i = 0; i < tiles.size(); ++i)
-    load[i % (size_t)pairs] += (double)pairw::width_of(tiles[i]) / tn;
+    load[i % (size_t)pairs] += (double)ptile_width(tiles[i]) / pair::WIDE;
   return *std::max_element(load.begin(), load.end());
 }
 
@@ -781,135 +666,45 @@ int tail_parts_for(int64_t tiles, int pairs, int split_k, int kblocks) {
   return (r > 0 && 2 * r <= pairs) ? 2 : 1;
 }
 
-// Pair-kernel tile list for tiles TN (256 or 512) columns wide: full tiles
-// over the output in Morton order (pair-row on the even bits), then the
-// column remainder as tiles of TN/2 or TN/4 (never under 128).  With one
-// split, if the tiles leave a partial last wave: 256-wide tiles get K halves
-// (`*parts` = 2, see tail_parts_for) for the last (count % pairs) tiles;
-// otherwise the full tiles of that wave are cut into halves or quarters when
-// that shortens the busiest pair's work.
-void build_pair_tiles(int M, int N, int kblocks, int pairs, int split_k, int order, int tn,
+// Pair-kernel tile list: 256-wide tiles over the output in Morton order
+// (pair-row on the even bits) while more than 128 columns remain, then the
+// column remainder as 128-wide tiles.  With one split, if the tiles leave a
+// partial last wave, the last (count % pairs) tiles get K halves (`*parts`
+// = 2, see tail_parts_for); otherwise the full tiles of that wave are cut
+// into 128-wide halves when that shortens the busiest pair's work.
+void build_pair_tiles(int M, int N, int kblocks, int pairs, int split_k, int order,
                       std::vector<uint32_t>& out, int* parts) {
   *parts = 1;
-  const int tpms = (int)ceil_div(M, pairw::PM);
-  const int min_w = 128;
-  // full-width column tiles while more than TN/2 columns remain
+  const int tn = pair::WIDE, w_half = pair::NARROW;
+  const int tpms = (int)ceil_div(M, pair::PM);
   int full_cols = 0;
-  while (N - full_cols * tn > tn / 2) ++full_cols;
+  while (N - full_cols * tn > w_half) ++full_cols;
   std::vector<uint32_t> grid;
   build_tile_order(tpms, std::max(full_cols, 1), order, grid);
   std::vector<uint32_t> full, rest;
   if (full_cols > 0)
-    for (uint32_t e : grid)
-      full.push_back(pairw::pack(tile_m_of(e), tile_n_of(e) * (tn / 128), tn));
-  const int rem = N - full_cols * tn;  // <= tn/2
-  if (rem > 0) {
-    const int w = (rem > tn / 4 || tn / 4 < min_w) ? tn / 2 : tn / 4;
-    for (int t = 0; t < tpms; ++t) rest.push_back(pairw::pack(t, full_cols * (tn / 128), w));
-  }
+    for (uint32_t e : grid) full.push_back(ptile(tile_m_of(e), tile_n_of(e) * 2, tn));
+  if (N - full_cols * tn > 0)
+    for (int t = 0; t < tpms; ++t) rest.push_back(ptile(t, full_cols * 2, w_half));
   out = full;
   out.insert(out.end(), rest.begin(), rest.end());
   if (split_k != 1 || pairs <= 0 || full.empty()) return;
-  if (tn == 256) {
-    *parts = tail_parts_for((int64_t)out.size(), pairs, split_k, kblocks);
-    if (*parts > 1) return;
-  }
+  *parts = tail_parts_for((int64_t)out.size(), pairs, split_k, kblocks);
+  if (*parts > 1) return;
   const size_t r = full.size() % (size_t)pairs;
   if (r == 0) return;
-  double best = pair_makespan(out, pairs, tn);
-  for (int parts : {2, 4}) {
-    const int w = tn / parts;
-    if (w < min_w) continue;
-    std::vector<uint32_t> alt(full.begin(), full.end() - r);
-    for (size_t i = full.size() - r; i < full.size(); ++i)
-      for (int k = 0; k < parts; ++k) {
-        const uint32_t n128 = pairw::n128_of(full[i]) + k * (w / 128);
-        if ((int64_t)n128 * 128 < N) alt.push_back(pairw::pack(pairw::tpm_of(full[i]), n128, w));
-      }
-    alt.insert(alt.end(), rest.begin(), rest.end());
-    const double m = pair_makespan(alt, pairs, tn);
-    if (m < best) {
-      best = m;
-      out.swap(alt);
+  std::vector<uint32_t> alt(full.begin(), full.end() - r);
+  for (size_t i = full.size() - r; i < full.size(); ++i)
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t n128 = ptile_n128(full[i]) + k;
+      if ((int64_t)n128 * 128 < N) alt.push_back(ptile(ptile_tpm(full[i]), n128, w_half));
     }
-  }
+  alt.insert(alt.end(), rest.begin(), rest.end());
+  if (pair_makespan(alt, pairs) < pair_makespan(out, pairs)) out.swap(alt);
 }
 }  // namespace
 
-// Recently encoded tensor maps, keyed by everything the encoding depends on,
-// so that repeated runs on the same buffers skip cuTensorMapEncodeTiled.
-struct TmapEntry {
-  uint64_t key[8];
-  CUtensorMap map;
-};
-constexpr int TMAP_CACHE = 32;
-
-struct gemm_f16_plan_s {
-  int device = 0;
-  int num_sms = 0;
-  int* status_host = nullptr;  // mapped pinned host memory
-  int* status_dev = nullptr;
-  unsigned long long timeout_ns = 1000000000ull;
-  int tile_order = 0;
-  int fault_unit = -1;
-  int kernel = 0;      // 0 auto, 1 single CTA, 2 CTA pair
-  int tile_width = 0;  // single-CTA tile width: 0 auto, else 256 / 128 / 64
-  int sm_limit = 0;    // most SMs a launch may use (0: all)
-  int attn_kernel = 0; // attention: 0 auto (CTA pair), 1 single CTA, 2 CTA pair
-  int attn_split = 0;  // pair attention key ranges: 0 auto, n >= 1 forced
-  int a_repack = 0;    // repack A with a pitch off 128-byte lines: 0 auto, 1 never, 2 always
-  int max_pairs = 0;   // co-resident clusters of two for the pair kernel
-  int attn_pairs = 0;  // co-resident clusters of two for the pair attention kernel
-  void* ws = nullptr;
-  size_t ws_bytes = 0;
-  void* apack = nullptr;  // repacked copy of A (see pack_rows_kernel)
-  size_t apack_bytes = 0;
-  // FP32 values of the K halves of the pair kernel's last-wave tiles.
-  void* tail_ws = nullptr;
-  size_t tail_ws_bytes = 0;
-  std::vector<OrderTable> orders;
-  // run_host: two slots of device staging (A, B, C) used by alternate calls,
-  // a stream for the input copies and the events that order the slots.
-  void* hbuf[2][3] = {{nullptr, nullptr, nullptr}, {nullptr, nullptr, nullptr}};
-  size_t hcap[2][3] = {{0, 0, 0}, {0, 0, 0}};
-  cudaStream_t in_stream = nullptr;
-  cudaEvent_t in_done[2] = {nullptr, nullptr};
-  cudaEvent_t gemm_done[2] = {nullptr, nullptr};
-  int host_slot = 0;
-  // attn_f16_fwd_host: two slots of device Q, K, V, O and their events.
-  void* abuf[2][4] = {{nullptr, nullptr, nullptr, nullptr}, {nullptr, nullptr, nullptr, nullptr}};
-  size_t acap[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-  cudaEvent_t attn_in_done[2] = {nullptr, nullptr};
-  cudaEvent_t attn_done[2] = {nullptr, nullptr};
-  int attn_slot = 0;
-  TmapEntry tmaps[TMAP_CACHE];
-  int tmap_used = 0, tmap_next = 0;
-};
-
 namespace {
-
-// encode_2d through the plan's cache.
-int cached_encode_2d(gemm_f16_plan_s* p, CUtensorMap* map, CUtensorMapDataType dt, const void* ptr,
-                     uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
-                     uint32_t box_outer, CUtensorMapSwizzle swz, CUtensorMapL2promotion promo) {
-  const uint64_t key[8] = {(uint64_t)(uintptr_t)ptr, inner, outer, row_bytes,
-                           ((uint64_t)box_inner << 32) | box_outer,
-                           ((uint64_t)dt << 32) | (uint64_t)swz, (uint64_t)promo, 0};
-  for (int i = 0; i < p->tmap_used; ++i) {
-    if (std::memcmp(p->tmaps[i].key, key, sizeof(key)) == 0) {
-      *map = p->tmaps[i].map;
-      return GEMM_F16_OK;
-    }
-  }
-  const int rc = encode_2d(map, dt, ptr, inner, outer, row_bytes, box_inner, box_outer, swz, promo);
-  if (rc) return rc;
-  TmapEntry& e = p->tmaps[p->tmap_next];
-  std::memcpy(e.key, key, sizeof(key));
-  e.map = *map;
-  p->tmap_next = (p->tmap_next + 1) % TMAP_CACHE;
-  if (p->tmap_used < TMAP_CACHE) ++p->tmap_used;
-  return GEMM_F16_OK;
-}
 
 // Row-major B (K x N, N a multiple of 64) as a 3-D tensor (64 columns, K
 // rows, N / 64 column groups; strides: row, 128 bytes), boxes of 64 x 64 x 2:
@@ -918,12 +713,7 @@ int cached_encode_2d(gemm_f16_plan_s* p, CUtensorMap* map, CUtensorMapDataType d
 int cached_encode_b3d(gemm_f16_plan_s* p, CUtensorMap* map, const void* ptr, uint64_t K,
                       uint64_t N, uint64_t ldb) {
   const uint64_t key[8] = {(uint64_t)(uintptr_t)ptr, K, N, ldb, 0, 0, 0, 0x3D00000000000000ull};
-  for (int i = 0; i < p->tmap_used; ++i) {
-    if (std::memcmp(p->tmaps[i].key, key, sizeof(key)) == 0) {
-      *map = p->tmaps[i].map;
-      return GEMM_F16_OK;
-    }
-  }
+  if (tmap_lookup(p, key, map)) return GEMM_F16_OK;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return GEMM_F16_ERR_CUDA;
   const cuuint64_t dims[3] = {64, K, N / 64};
@@ -938,11 +728,7 @@ int cached_encode_b3d(gemm_f16_plan_s* p, CUtensorMap* map, const void* ptr, uin
                   "cuTensorMapEncodeTiled (3-D B) failed (CUresult %d)", (int)r);
     return GEMM_F16_ERR_CUDA;
   }
-  TmapEntry& e = p->tmaps[p->tmap_next];
-  std::memcpy(e.key, key, sizeof(key));
-  e.map = *map;
-  p->tmap_next = (p->tmap_next + 1) % TMAP_CACHE;
-  if (p->tmap_used < TMAP_CACHE) ++p->tmap_used;
+  tmap_remember(p, key, *map);
   return GEMM_F16_OK;
 }
 
@@ -958,23 +744,61 @@ cudaError_t copy_rows(void* dst, int64_t dpitch, const void* src, int64_t spitch
 
 }  // namespace
 
-extern "C" {
+namespace gf16 {
+namespace host {
 
-const char* gemm_f16_strerror(int code) {
-  switch (code) {
-    case GEMM_F16_OK: return "ok";
-    case GEMM_F16_ERR_INVALID_ARG: return "invalid argument";
-    case GEMM_F16_ERR_MISALIGNED: return "pointer not 16-byte aligned or leading dimension not a multiple of 8";
-    case GEMM_F16_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
-    case GEMM_F16_ERR_OOM: return "out of memory";
-    case GEMM_F16_ERR_CUDA: return "CUDA call failed";
-    case GEMM_F16_ERR_TIMEOUT: return "an in-kernel barrier wait timed out";
-    case GEMM_F16_ERR_SCRATCH_TOO_SMALL: return "problem too large for the fixed no-alloc scratch";
-    default: return "unknown error code";
+int gemm_plan_init(gemm_f16_plan_s* p, const cudaDeviceProp& prop) {
+  void* const single[4] = {(void*)gemm_f16_kernel<0>, (void*)gemm_f16_kernel<1>,
+                           (void*)gemm_f16_kernel<2>, (void*)gemm_f16_kernel<3>};
+  void* const pairs[4] = {(void*)pair::gemm_f16_pair_kernel<0>, (void*)pair::gemm_f16_pair_kernel<1>,
+                          (void*)pair::gemm_f16_pair_kernel<2>, (void*)pair::gemm_f16_pair_kernel<3>};
+  for (int l = 0; l < 4; ++l) {
+    GF16_CUDA(cudaFuncSetAttribute(single[l], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)SMEM_BYTES),
+              "cudaFuncSetAttribute(max dynamic smem)");
+    GF16_CUDA(cudaFuncSetAttribute(pairs[l], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)pair::SMEM_BYTES),
+              "cudaFuncSetAttribute(pair kernel smem)");
+  }
+  // Co-resident clusters of two for the pair kernel (0 if the query fails:
+  // the pair kernel is then not used).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(prop.multiProcessorCount / 2 * 2), 1, 1);
+  cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, pair::gemm_f16_pair_kernel<0>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    clusters = 0;
+  }
+  p->max_pairs = clusters;
+  return GEMM_F16_OK;
+}
+
+void gemm_plan_release(gemm_f16_plan_s* p) {
+  for (auto& t : p->orders) cudaFree(t.dev);
+  p->orders.clear();
+  if (p->apack) cudaFree(p->apack);
+  if (p->tail_ws) cudaFree(p->tail_ws);
+  for (int sl = 0; sl < 2; ++sl) {
+    for (int i = 0; i < 3; ++i)
+      if (p->hbuf[sl][i]) cudaFree(p->hbuf[sl][i]);
+    if (p->in_done[sl]) cudaEventDestroy(p->in_done[sl]);
+    if (p->gemm_done[sl]) cudaEventDestroy(p->gemm_done[sl]);
   }
 }
 
-const char* gemm_f16_last_cuda_error(void) { return g_last_cuda_error; }
+}  // namespace host
+}  // namespace gf16
+
+extern "C" {
 
 int gemm_f16_tile_shape(int* bm, int* bn, int* bk, int* stages) {
   if (bm) *bm = BM;
@@ -1015,210 +839,20 @@ int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order, uint32_t* out, 
   return n;
 }
 
-int gemm_f16_plan(gemm_f16_plan_t* out, int device) {
-  if (!out) return GEMM_F16_ERR_INVALID_ARG;
-  *out = nullptr;
-  int ndev = 0;
-  GF16_CUDA(cudaGetDeviceCount(&ndev), "cudaGetDeviceCount");
-  if (device < 0 || device >= ndev) return GEMM_F16_ERR_INVALID_ARG;
-  cudaDeviceProp prop;
-  GF16_CUDA(cudaGetDeviceProperties(&prop, device), "cudaGetDeviceProperties");
-  if (prop.major != 10 || prop.minor != 3) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
-  DeviceGuard g(device);
-  {
-    void* const single[4] = {(void*)gemm_f16_kernel<0>, (void*)gemm_f16_kernel<1>,
-                             (void*)gemm_f16_kernel<2>, (void*)gemm_f16_kernel<3>};
-    void* const pairs[4] = {(void*)pair::gemm_f16_pair_kernel<0>, (void*)pair::gemm_f16_pair_kernel<1>,
-                            (void*)pair::gemm_f16_pair_kernel<2>, (void*)pair::gemm_f16_pair_kernel<3>};
-    for (int l = 0; l < 4; ++l) {
-      GF16_CUDA(cudaFuncSetAttribute(single[l], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)SMEM_BYTES),
-                "cudaFuncSetAttribute(max dynamic smem)");
-      GF16_CUDA(cudaFuncSetAttribute(pairs[l], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)pair::SMEM_BYTES),
-                "cudaFuncSetAttribute(pair kernel smem)");
-    }
-  }
-  GF16_CUDA(cudaFuncSetAttribute(pairw::gemm_f16_pair_kernel<512>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)pairw::Cfg<512>::SMEM_BYTES),
-            "cudaFuncSetAttribute(wide pair kernel smem)");
-  GF16_CUDA(cudaFuncSetAttribute(attn::attn_f16_fwd_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)attn::SMEM_BYTES),
-            "cudaFuncSetAttribute(attention kernel smem)");
-  GF16_CUDA(cudaFuncSetAttribute(attnp::attn_f16_fwd_pair_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)attnp::SMEM_BYTES),
-            "cudaFuncSetAttribute(pair attention kernel smem)");
-  // Co-resident clusters of two for each pair-kernel instance; keep the
-  // smaller count (0 if the query fails: the pair kernel is then not used).
-  int max_clusters = 0, attn_clusters = 0;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(prop.multiProcessorCount / 2 * 2), 1, 1);
-    cfg.blockDim = dim3(pair::NUM_THREADS, 1, 1);
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n256 = 0, n512 = 0;
-    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
-    if (cudaOccupancyMaxActiveClusters(&n256, pair::gemm_f16_pair_kernel<0>, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n256 = 0;
-    }
-    cfg.dynamicSmemBytes = pairw::Cfg<512>::SMEM_BYTES;
-    if (cudaOccupancyMaxActiveClusters(&n512, pairw::gemm_f16_pair_kernel<512>, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n512 = 0;
-    }
-    max_clusters = std::min(n256, n512);
-    cfg.blockDim = dim3(attnp::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = attnp::SMEM_BYTES;
-    if (cudaOccupancyMaxActiveClusters(&attn_clusters, attnp::attn_f16_fwd_pair_kernel, &cfg) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      attn_clusters = 0;
-    }
-  }
-  gemm_f16_plan_s* p = new (std::nothrow) gemm_f16_plan_s();
-  if (!p) return GEMM_F16_ERR_OOM;
-  p->device = device;
-  p->num_sms = prop.multiProcessorCount;
-  p->max_pairs = max_clusters;
-  p->attn_pairs = attn_clusters;
-  cudaError_t e = cudaHostAlloc(&p->status_host, sizeof(int), cudaHostAllocMapped);
-  if (e != cudaSuccess) {
-    delete p;
-    return cuda_fail(e, "cudaHostAlloc(status)");
-  }
-  *p->status_host = 0;
-  e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&p->status_dev), p->status_host, 0);
-  if (e != cudaSuccess) {
-    cudaFreeHost(p->status_host);
-    delete p;
-    return cuda_fail(e, "cudaHostGetDevicePointer(status)");
-  }
-  *out = p;
-  return GEMM_F16_OK;
-}
-
-int gemm_f16_destroy(gemm_f16_plan_t p) {
-  if (!p) return GEMM_F16_OK;
-  {
-    DeviceGuard g(p->device);
-    cudaDeviceSynchronize();
-    for (auto& t : p->orders) cudaFree(t.dev);
-    if (p->ws) cudaFree(p->ws);
-    if (p->apack) cudaFree(p->apack);
-    if (p->tail_ws) cudaFree(p->tail_ws);
-    for (int sl = 0; sl < 2; ++sl)
-      for (int i = 0; i < 3; ++i)
-        if (p->hbuf[sl][i]) cudaFree(p->hbuf[sl][i]);
-    for (int sl = 0; sl < 2; ++sl) {
-      if (p->in_done[sl]) cudaEventDestroy(p->in_done[sl]);
-      if (p->gemm_done[sl]) cudaEventDestroy(p->gemm_done[sl]);
-      if (p->attn_in_done[sl]) cudaEventDestroy(p->attn_in_done[sl]);
-      if (p->attn_done[sl]) cudaEventDestroy(p->attn_done[sl]);
-      for (int i = 0; i < 4; ++i)
-        if (p->abuf[sl][i]) cudaFree(p->abuf[sl][i]);
-    }
-    if (p->in_stream) cudaStreamDestroy(p->in_stream);
-    if (p->status_host) cudaFreeHost(p->status_host);
-  }
-  delete p;
-  return GEMM_F16_OK;
-}
-
-int gemm_f16_status(gemm_f16_plan_t p) {
-  if (!p) return GEMM_F16_ERR_INVALID_ARG;
-  volatile int* s = p->status_host;
-  const int v = *s;
-  *s = 0;
-  return v;
-}
-
-int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
-  if (!p) return GEMM_F16_ERR_INVALID_ARG;
-  switch (option) {
-    case GEMM_F16_OPT_TIMEOUT_NS:
-      if (value <= 0) return GEMM_F16_ERR_INVALID_ARG;
-      p->timeout_ns = (unsigned long long)value;
-      return GEMM_F16_OK;
-    case GEMM_F16_OPT_TILE_ORDER:
-      if (value != 0 && value != 1) return GEMM_F16_ERR_INVALID_ARG;
-      p->tile_order = (int)value;
-      return GEMM_F16_OK;
-    case GEMM_F16_OPT_FAULT_UNIT:
-      if (value < -1 || value > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
-      p->fault_unit = (int)value;
-      return GEMM_F16_OK;
-    case GEMM_F16_OPT_SM_LIMIT:
-      if (value < 0 || value > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
-      p->sm_limit = (int)value;
-      return GEMM_F16_OK;
-    case GEMM_F16_OPT_ATTN_KERNEL:
-      if (value < 0 || value > 2) return GEMM_F16_ERR_INVALID_ARG;
-      p->attn_kernel = (int)value;
-      return GEMM_F16_OK;
-    case GEMM_F16_OPT_ATTN_SPLIT:
-      if (value < 0 || value > 65536) return GEMM_F16_ERR_INVALID_ARG;
-      p->attn_split = (int)value;
-      return GEMM_F16_OK;
-    case GEMM_F16_OPT_A_REPACK:
-      if (value < 0 || value > 2) return GEMM_F16_ERR_INVALID_ARG;
-      p->a_repack = (int)value;
-      return GEMM_F16_OK;
-    case GEMM_F16_OPT_TILE_WIDTH:
-      if (value != 0 && value != 64 && value != 128 && value != 256) return GEMM_F16_ERR_INVALID_ARG;
-      p->tile_width = (int)value;
-      return GEMM_F16_OK;
-    case GEMM_F16_OPT_KERNEL:
-      if (value < 0 || value > 3) return GEMM_F16_ERR_INVALID_ARG;
-      if (value >= 2 && p->max_pairs <= 0) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
-      p->kernel = (int)value;
-      return GEMM_F16_OK;
-    default:
-      return GEMM_F16_ERR_INVALID_ARG;
-  }
-}
-
 int64_t gemm_f16_pair_tiles(int M, int N, int K, int pairs, int split_k, int order,
                             int tile_width, uint32_t* out, int64_t cap, int* tail_parts) {
   if (M <= 0 || N <= 0 || K <= 0 || pairs < 1 || split_k < 1 || (order != 0 && order != 1))
     return GEMM_F16_ERR_INVALID_ARG;
-  if (tile_width != 256 && tile_width != 512) return GEMM_F16_ERR_INVALID_ARG;
-  if (ceil_div(M, pairw::PM) > 65535 || (N + 127) / 128 >= 0x3FFF) return GEMM_F16_ERR_INVALID_ARG;
+  if (tile_width != 256) return GEMM_F16_ERR_INVALID_ARG;
+  if (ceil_div(M, pair::PM) > 65535 || (N + 127) / 128 >= 0x3FFF) return GEMM_F16_ERR_INVALID_ARG;
   if (cap < 0 || (cap > 0 && !out)) return GEMM_F16_ERR_INVALID_ARG;
   std::vector<uint32_t> v;
   int parts = 1;
-  build_pair_tiles(M, N, (int)ceil_div(K, BK), pairs, split_k, order, tile_width, v, &parts);
+  build_pair_tiles(M, N, (int)ceil_div(K, BK), pairs, split_k, order, v, &parts);
   const int64_t n = (int64_t)v.size();
   if (cap > 0) std::memcpy(out, v.data(), sizeof(uint32_t) * (size_t)std::min<int64_t>(n, cap));
   if (tail_parts) *tail_parts = parts;
   return n;
-}
-
-int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
-  if (!p || !value) return GEMM_F16_ERR_INVALID_ARG;
-  switch (option) {
-    case GEMM_F16_OPT_TIMEOUT_NS: *value = (int64_t)p->timeout_ns; return GEMM_F16_OK;
-    case GEMM_F16_OPT_TILE_ORDER: *value = p->tile_order; return GEMM_F16_OK;
-    case GEMM_F16_OPT_FAULT_UNIT: *value = p->fault_unit; return GEMM_F16_OK;
-    case GEMM_F16_OPT_KERNEL: *value = p->kernel; return GEMM_F16_OK;
-    case GEMM_F16_OPT_TILE_WIDTH: *value = p->tile_width; return GEMM_F16_OK;
-    case GEMM_F16_OPT_SM_LIMIT: *value = p->sm_limit; return GEMM_F16_OK;
-    case GEMM_F16_OPT_ATTN_KERNEL: *value = p->attn_kernel; return GEMM_F16_OK;
-    case GEMM_F16_OPT_ATTN_SPLIT: *value = p->attn_split; return GEMM_F16_OK;
-    case GEMM_F16_OPT_A_REPACK: *value = p->a_repack; return GEMM_F16_OK;
-    case GEMM_F16_INFO_NUM_SMS: *value = p->num_sms; return GEMM_F16_OK;
-    case GEMM_F16_INFO_MAX_PAIRS: *value = p->max_pairs; return GEMM_F16_OK;
-    default: return GEMM_F16_ERR_INVALID_ARG;
-  }
 }
 
 }  // extern "C"
@@ -1250,20 +884,9 @@ const OrderTable* find_table(gemm_f16_plan_s* p, const int64_t (&key)[6]) {
   return nullptr;
 }
 
-int get_order_table(gemm_f16_plan_s* p, int tiles_m, int tiles_n, const uint32_t** out) {
-  const int64_t key[6] = {0, tiles_m, tiles_n, p->tile_order, 0, 0};
-  if (const OrderTable* t = find_table(p, key)) {
-    *out = t->dev;
-    return GEMM_F16_OK;
-  }
-  std::vector<uint32_t> host;
-  build_tile_order(tiles_m, tiles_n, p->tile_order, host);
-  return upload_table(p, key, host, out);
-}
-
-int get_pair_table(gemm_f16_plan_s* p, int M, int N, int kblocks, int split_k, int tn,
+int get_pair_table(gemm_f16_plan_s* p, int M, int N, int kblocks, int split_k,
                    const uint32_t** out, int64_t* count, int* parts) {
-  const int64_t key[6] = {tn, M, N, p->max_pairs,
+  const int64_t key[6] = {1, M, N, p->max_pairs,
                           (int64_t)split_k | ((int64_t)kblocks << 32), p->tile_order};
   if (const OrderTable* t = find_table(p, key)) {
     *out = t->dev;
@@ -1272,24 +895,11 @@ int get_pair_table(gemm_f16_plan_s* p, int M, int N, int kblocks, int split_k, i
     return GEMM_F16_OK;
   }
   std::vector<uint32_t> host;
-  build_pair_tiles(M, N, kblocks, p->max_pairs, split_k, p->tile_order, tn, host, parts);
-  if (tn == 256)  // the 256-wide kernel's entry format: narrow flag in bit 31
-    for (uint32_t& e : host)
-      e = pair::pack(pairw::tpm_of(e), pairw::n128_of(e), pairw::width_of(e) == 128);
+  build_pair_tiles(M, N, kblocks, p->max_pairs, split_k, p->tile_order, host, parts);
+  for (uint32_t& e : host)  // the kernel's entry format: narrow flag in bit 31
+    e = pair::pack(ptile_tpm(e), ptile_n128(e), ptile_width(e) == pair::NARROW);
   *count = (int64_t)host.size();
   return upload_table(p, key, host, out, *parts);
-}
-
-int ensure_buffer(void** buf, size_t* cap, size_t bytes, cudaStream_t stream, const char* what) {
-  if (*cap >= bytes) return GEMM_F16_OK;
-  if (*buf) {
-    GF16_CUDA(cudaFreeAsync(*buf, stream), what);
-    *buf = nullptr;
-    *cap = 0;
-  }
-  GF16_CUDA(cudaMallocAsync(buf, bytes, stream), what);
-  *cap = bytes;
-  return GEMM_F16_OK;
 }
 
 // Tile width of the single-CTA kernel: 256, 128 or 64 columns.  Estimated
@@ -1331,7 +941,6 @@ inline void* pick_instance(int layout, F0 f0, F1 f1, F2 f2, F3 f3) {
 // kernel, the single-CTA tile width, and whether A is repacked first.
 struct RunChoice {
   bool use_pair;  // CTA-pair kernel (else single-CTA kernel)
-  int pair_tn;    // pair tile width: 256 or 512
   int bn;         // single-CTA tile width: 256, 128 or 64
   bool pack_a;    // A copied to whole-line rows before the product
 };
@@ -1348,12 +957,8 @@ RunChoice choose_run(const gemm_f16_plan_s* p, int layout, int M, int N, int K, 
   // kernel's smaller tiles spread the work over more SMs.
   const bool pair_fits = (N + 127) / 128 < 0x3FFF && p->max_pairs > 0;
   const int64_t pair_work = ceil_div(M, 256) * ceil_div(N, 256) * (int64_t)split_k;
-  c.use_pair = pair_fits && (p->kernel == 2 || p->kernel == 3 ||
+  c.use_pair = pair_fits && (p->kernel == 2 ||
                              (p->kernel == 0 && M > BM && 2 * pair_work >= p->max_pairs));
-  // 512-wide tiles (less load traffic per MMA, but one accumulator and so
-  // no epilogue overlap) only on request: measured slower than 256-wide
-  // tiles from 2048^3 to 8192^3.
-  c.pair_tn = (p->kernel == 3 && layout == 0) ? 512 : 256;
   // A whose row pitch is not a multiple of 128 bytes: copy it to rows of
   // whole lines first (see pack_rows_kernel), when asked to or, by default,
   // for products large enough that the copy costs less than it saves.
@@ -1375,14 +980,14 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
   const int64_t units = (int64_t)tiles_m * tiles_n * split_k;
   if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
   const bool use_pair = choice.use_pair;
-  const int pair_tn = choice.pair_tn;
   const uint32_t* order = nullptr;
   int64_t pair_tiles = 0;
   int tail_parts = 1;
-  int rc = use_pair ? get_pair_table(p, M, N, kblocks, split_k, pair_tn, &order, &pair_tiles,
-                                     &tail_parts)
-                    : get_order_table(p, tiles_m, tiles_n, &order);
-  if (rc) return rc;
+  int rc = GEMM_F16_OK;
+  if (use_pair) {
+    rc = get_pair_table(p, M, N, kblocks, split_k, &order, &pair_tiles, &tail_parts);
+    if (rc) return rc;
+  }
 
   const int64_t a_rows = (layout & LAYOUT_AT) ? K : M, a_cols = (layout & LAYOUT_AT) ? M : K;
   if (choice.pack_a) {
@@ -1416,7 +1021,7 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
                           (uint64_t)lda * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc) return rc;
-  const bool b3d = use_pair && pair_tn == 256 && !(layout & LAYOUT_BT) && (N % 64) == 0;
+  const bool b3d = use_pair && !(layout & LAYOUT_BT) && (N % 64) == 0;
   if (layout & LAYOUT_BT)
     rc = cached_encode_2d(p, &tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, (uint64_t)K, (uint64_t)N,
                           (uint64_t)ldb * 2, BK, use_pair ? 128u : (uint32_t)bn,
@@ -1490,30 +1095,11 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
     pdl.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    if (pair_tn == 512) {
-      pairw::Params pw;
-      pw.M = pp.M;
-      pw.N = pp.N;
-      pw.K = pp.K;
-      pw.split_k = pp.split_k;
-      pw.kblocks = pp.kblocks;
-      pw.num_units = pp.num_units;
-      pw.order = pp.order;
-      pw.C = pp.C;
-      pw.ldc = pp.ldc;
-      pw.status = pp.status;
-      pw.timeout_ns = pp.timeout_ns;
-      pw.fault_unit = pp.fault_unit;
-      cfg.dynamicSmemBytes = pairw::Cfg<512>::SMEM_BYTES;
-      GF16_CUDA(cudaLaunchKernelEx(&cfg, pairw::gemm_f16_pair_kernel<512>, tmA, tmB, tmC, tmW, pw),
-                "launch wide gemm_f16_pair_kernel<512>");
-    } else {
-      cfg.dynamicSmemBytes = pair::SMEM_BYTES;
-      void* fn = pick_instance(layout, pair::gemm_f16_pair_kernel<0>, pair::gemm_f16_pair_kernel<1>,
-                               pair::gemm_f16_pair_kernel<2>, pair::gemm_f16_pair_kernel<3>);
-      void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmC, (void*)&tmW, (void*)&pp};
-      GF16_CUDA(cudaLaunchKernelExC(&cfg, fn, args), "launch gemm_f16_pair_kernel");
-    }
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    void* fn = pick_instance(layout, pair::gemm_f16_pair_kernel<0>, pair::gemm_f16_pair_kernel<1>,
+                             pair::gemm_f16_pair_kernel<2>, pair::gemm_f16_pair_kernel<3>);
+    void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmC, (void*)&tmW, (void*)&pp};
+    GF16_CUDA(cudaLaunchKernelExC(&cfg, fn, args), "launch gemm_f16_pair_kernel");
     if (tail_tiles > 0) {
       // P0 + P1 of each tail tile into C (a programmatic dependent launch).
       const int64_t groups = tail_tiles * 256 * 64;
@@ -1542,7 +1128,7 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
   prm.split_k = split_k;
   prm.kblocks = kblocks;
   prm.num_units = (int)units;
-  prm.order = order;
+  prm.row_major = p->tile_order;
   prm.C = static_cast<__half*>(C);
   prm.ldc = ldc;
   prm.status = p->status_dev;
@@ -1620,15 +1206,14 @@ int gemm_f16_run_info(gemm_f16_plan_t p, int layout, int M, int N, int K, int64_
   const RunChoice c = choose_run(p, layout, M, N, K, lda, split_k);
   // a partial last wave of 256-wide pair tiles in K halves adds their merge
   int parts = 1;
-  if (c.use_pair && c.pair_tn == 256 && split_k == 1) {
+  if (c.use_pair && split_k == 1) {
     std::vector<uint32_t> tiles;
-    build_pair_tiles(M, N, (int)ceil_div(K, BK), p->max_pairs, split_k, p->tile_order, 256, tiles,
-                     &parts);
+    build_pair_tiles(M, N, (int)ceil_div(K, BK), p->max_pairs, split_k, p->tile_order, tiles, &parts);
   }
-  info[0] = c.use_pair ? (c.pair_tn == 512 ? 3 : 2) : 1;
+  info[0] = c.use_pair ? 2 : 1;
   info[1] = 1 + (split_k > 1 ? 1 : 0) + (c.pack_a ? 1 : 0) + (parts > 1 ? 1 : 0);
   info[2] = c.pack_a ? 1 : 0;
-  info[3] = c.use_pair ? c.pair_tn : c.bn;
+  info[3] = c.use_pair ? pair::WIDE : c.bn;
   return GEMM_F16_OK;
 }
 
@@ -1705,34 +1290,29 @@ int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, in
 // gemm_f16_run_noalloc: the plan-free variant for callers that must not
 // allocate device memory (see gemm_f16.h).  Its scratch is one file-scope
 // device array, laid out as
-//   [0, 4*MAX_TILES)            tile-order table (uint32 per tile)
-//   [4*MAX_TILES, +256)         status word used when the caller passes none
-//   [4*MAX_TILES + 256, +32 MiB) FP32 split partials [split][M][ldw]
-// Host code must not use the array's name as an address: the per-device
-// set-up below asks the runtime for its device address.
+//   [0, 256)              status word used when the caller passes none
+//   [256, 256 + 32 MiB)   FP32 split partials [split][M][ldw]
+// The kernel derives its tiles from the unit index (morton_tile_of_rank),
+// so no tile table is kept between calls.  Host code must not use the
+// array's name as an address: the per-device set-up below asks the runtime
+// for its device address.
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_F16_NOALLOC_SCRATCH_BYTES];
 
-constexpr size_t NOALLOC_ORDER_OFF = 0;
-constexpr size_t NOALLOC_STATUS_OFF = (size_t)GEMM_F16_NOALLOC_MAX_TILES * 4u;
-constexpr size_t NOALLOC_WS_OFF = NOALLOC_STATUS_OFF + 256u;
+constexpr size_t NOALLOC_STATUS_OFF = 0;
+constexpr size_t NOALLOC_WS_OFF = 256;
 static_assert(NOALLOC_WS_OFF + GEMM_F16_NOALLOC_WS_BYTES == GEMM_F16_NOALLOC_SCRATCH_BYTES,
               "scratch layout");
-static_assert(NOALLOC_WS_OFF % 256 == 0, "workspace alignment");
 
 constexpr int NOALLOC_MAX_DEVICES = 64;
 struct NoallocDevice {
   bool ready = false;
   unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   int num_sms = 0;
-  int order_tm = -1, order_tn = -1;  // grid whose order the device table holds
 };
 NoallocDevice g_noalloc_devices[NOALLOC_MAX_DEVICES];
 std::mutex g_noalloc_mutex;
-// Host staging for the tile order, static so that building it allocates nothing.
-uint64_t g_noalloc_keys[GEMM_F16_NOALLOC_MAX_TILES];
-uint32_t g_noalloc_order[GEMM_F16_NOALLOC_MAX_TILES];
 
 // One-time set-up on the current device `dev` (that device is current).
 int noalloc_setup(int dev, NoallocDevice* d) {
@@ -1751,8 +1331,21 @@ int noalloc_setup(int dev, NoallocDevice* d) {
   GF16_CUDA(cudaGetSymbolAddress(&ptr, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)");
   d->scratch = static_cast<unsigned char*>(ptr);
   d->num_sms = sms;
-  d->order_tm = d->order_tn = -1;
   d->ready = true;
+  return GEMM_F16_OK;
+}
+
+// The current device's entry, set up on first use (mutex held by the caller).
+int noalloc_device(NoallocDevice** out) {
+  int dev = 0;
+  GF16_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+  NoallocDevice* d = &g_noalloc_devices[dev];
+  if (!d->ready) {
+    const int rc = noalloc_setup(dev, d);
+    if (rc) return rc;
+  }
+  *out = d;
   return GEMM_F16_OK;
 }
 
@@ -1768,39 +1361,17 @@ extern "C" int gemm_f16_run_noalloc(int M, int N, int K, const void* A, int64_t 
   const int64_t tiles = (int64_t)tiles_m * tiles_n;
   const int64_t ldw = (N + 7) / 8 * 8;
   const int64_t split_stride = (int64_t)M * ldw;
-  if (tiles > GEMM_F16_NOALLOC_MAX_TILES) return GEMM_F16_ERR_SCRATCH_TOO_SMALL;
   if (split_k > 1 &&
       (uint64_t)split_k * (uint64_t)split_stride * sizeof(float) > GEMM_F16_NOALLOC_WS_BYTES)
     return GEMM_F16_ERR_SCRATCH_TOO_SMALL;
+  const int64_t units = tiles * split_k;
+  if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
   cudaStream_t stream = (cudaStream_t)stream_;
 
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  int dev = 0;
-  GF16_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
-  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
-  NoallocDevice* d = &g_noalloc_devices[dev];
-  if (!d->ready) {
-    rc = noalloc_setup(dev, d);
-    if (rc) return rc;
-  }
-
-  uint32_t* order = reinterpret_cast<uint32_t*>(d->scratch + NOALLOC_ORDER_OFF);
-  if (d->order_tm != tiles_m || d->order_tn != tiles_n) {
-    int64_t n = 0;
-    for (int tm = 0; tm < tiles_m; ++tm)
-      for (int tn = 0; tn < tiles_n; ++tn)
-        g_noalloc_keys[n++] = ((uint64_t)morton_code((uint32_t)tm, (uint32_t)tn) << 32) |
-                              pack_tile((uint32_t)tm, (uint32_t)tn);
-    std::sort(g_noalloc_keys, g_noalloc_keys + n);  // in place, no allocation
-    for (int64_t t = 0; t < n; ++t) g_noalloc_order[t] = (uint32_t)g_noalloc_keys[t];
-    // Pageable source: the call returns once the bytes are staged, so the
-    // static host buffer may be rebuilt by the next call.
-    GF16_CUDA(cudaMemcpyAsync(order, g_noalloc_order, (size_t)n * sizeof(uint32_t),
-                              cudaMemcpyHostToDevice, stream),
-              "upload tile order (no-alloc)");
-    d->order_tm = tiles_m;
-    d->order_tn = tiles_n;
-  }
+  NoallocDevice* d = nullptr;
+  rc = noalloc_device(&d);
+  if (rc) return rc;
 
   alignas(64) CUtensorMap tmA, tmB, tmC, tmW;
   std::memset(&tmW, 0, sizeof(tmW));
@@ -1823,8 +1394,6 @@ extern "C" int gemm_f16_run_noalloc(int M, int N, int K, const void* A, int64_t 
     if (rc) return rc;
   }
 
-  const int64_t units = tiles * split_k;
-  if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
   Params prm;
   prm.M = M;
   prm.N = N;
@@ -1837,7 +1406,7 @@ extern "C" int gemm_f16_run_noalloc(int M, int N, int K, const void* A, int64_t 
   prm.split_k = split_k;
   prm.kblocks = (int)ceil_div(K, BK);
   prm.num_units = (int)units;
-  prm.order = order;
+  prm.row_major = 0;
   prm.C = static_cast<__half*>(C);
   prm.ldc = ldc;
   prm.status = status ? status : reinterpret_cast<int*>(d->scratch + NOALLOC_STATUS_OFF);
@@ -1864,297 +1433,20 @@ extern "C" int gemm_f16_run_noalloc(int M, int N, int K, const void* A, int64_t 
   return GEMM_F16_OK;
 }
 
-// ====================================================================== attention
-namespace {
-
-// [batch, head, row, 256] binary16 view as a 4-D tensor map: dims (d, row,
-// head, batch), box (64, box_rows, 1, 1), 128-byte swizzle.
-int encode_bhsd(CUtensorMap* map, const void* ptr, int batch, int heads, int rows,
-                const int64_t st[3], uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) {
-    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
-                  "cuTensorMapEncodeTiled entry point not available");
-    return GEMM_F16_ERR_CUDA;
-  }
-  // A stride of an extent-1 dimension is never used; give the map a valid one.
-  const int64_t row_st = st[2];
-  const int64_t head_st = heads > 1 ? st[1] : row_st * rows;
-  const int64_t batch_st = batch > 1 ? st[0] : head_st * heads;
-  const cuuint64_t dims[4] = {(cuuint64_t)attn::HD, (cuuint64_t)rows, (cuuint64_t)heads,
-                              (cuuint64_t)batch};
-  const cuuint64_t strides[3] = {(cuuint64_t)row_st * 2, (cuuint64_t)head_st * 2,
-                                 (cuuint64_t)batch_st * 2};
-  const cuuint32_t box[4] = {64, box_rows, 1, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
-                  "cuTensorMapEncodeTiled (attention operand) failed (CUresult %d)", (int)r);
-    return GEMM_F16_ERR_CUDA;
-  }
-  return GEMM_F16_OK;
-}
-
-// encode_bhsd through the plan's tensor-map cache (keys tagged apart from
-// the 2-D GEMM maps).
-int cached_encode_bhsd(gemm_f16_plan_s* p, CUtensorMap* map, const void* ptr, int batch,
-                       int heads, int rows, const int64_t st[3], uint32_t box_rows) {
-  const uint64_t key[8] = {(uint64_t)(uintptr_t)ptr, ((uint64_t)(uint32_t)batch << 32) | (uint32_t)heads,
-                           (uint64_t)(uint32_t)rows, (uint64_t)st[0], (uint64_t)st[1],
-                           (uint64_t)st[2], (uint64_t)box_rows, 0x4D00000000000000ull};
-  for (int i = 0; i < p->tmap_used; ++i) {
-    if (std::memcmp(p->tmaps[i].key, key, sizeof(key)) == 0) {
-      *map = p->tmaps[i].map;
-      return GEMM_F16_OK;
-    }
-  }
-  const int rc = encode_bhsd(map, ptr, batch, heads, rows, st, box_rows);
+extern "C" int gemm_f16_noalloc_status(void) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoallocDevice* d = nullptr;
+  int rc = noalloc_device(&d);
   if (rc) return rc;
-  TmapEntry& e = p->tmaps[p->tmap_next];
-  std::memcpy(e.key, key, sizeof(key));
-  e.map = *map;
-  p->tmap_next = (p->tmap_next + 1) % TMAP_CACHE;
-  if (p->tmap_used < TMAP_CACHE) ++p->tmap_used;
-  return GEMM_F16_OK;
-}
-
-bool strides_ok(const int64_t* st) {
-  if (!st) return false;
-  for (int i = 0; i < 3; ++i)
-    if (st[i] <= 0 || st[i] >= ((int64_t)1 << 38)) return false;
-  return st[2] >= attn::HD;
-}
-
-}  // namespace
-
-// Co-resident CTA pairs the pair attention kernel may use (SM limit applied).
-static int64_t attn_pair_slots(const gemm_f16_plan_s* p) {
-  int64_t slots = p->attn_pairs;
-  if (p->sm_limit > 0) slots = std::max<int64_t>(1, std::min<int64_t>(slots, p->sm_limit / 2));
-  return slots;
-}
-
-// Key ranges per item of the pair attention kernel and the blocks per range
-// (none empty): the option if set (capped at the block count), else a split
-// when the items fill less than half of the pair slots and there are at
-// least four key blocks.
-static int64_t attn_key_ranges(const gemm_f16_plan_s* p, int64_t items, int64_t nkv,
-                               int* bps) {
-  const int64_t slots = attn_pair_slots(p);
-  int64_t n = 1;
-  if (p->attn_split > 0)
-    n = std::min<int64_t>(p->attn_split, nkv);
-  else if (2 * items <= slots && nkv >= 4)
-    n = std::min<int64_t>(slots / items, nkv / 2);
-  n = std::max<int64_t>(n, 1);
-  *bps = (int)ceil_div(nkv, n);
-  return ceil_div(nkv, *bps);
-}
-
-extern "C" {
-
-int attn_f16_validate(int batch, int heads, int seq_q, int seq_kv, int head_dim, const void* Q,
-                      const int64_t q_strides[3], const void* K, const int64_t k_strides[3],
-                      const void* V, const int64_t v_strides[3], const void* O,
-                      const int64_t o_strides[3], float scale) {
-  if (batch < 1 || heads < 1 || batch > 65535 || heads > 65535) return GEMM_F16_ERR_INVALID_ARG;
-  if (seq_q < 1 || seq_kv < 1) return GEMM_F16_ERR_INVALID_ARG;
-  if (head_dim != attn::HD) return GEMM_F16_ERR_INVALID_ARG;
-  if (!Q || !K || !V || !O) return GEMM_F16_ERR_INVALID_ARG;
-  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return GEMM_F16_ERR_INVALID_ARG;
-  const int64_t* sts[4] = {q_strides, k_strides, v_strides, o_strides};
-  for (const int64_t* st : sts)
-    if (!strides_ok(st)) return GEMM_F16_ERR_INVALID_ARG;
-  const void* ptrs[4] = {Q, K, V, O};
-  for (const void* ptr : ptrs)
-    if ((uintptr_t)ptr & 15) return GEMM_F16_ERR_MISALIGNED;
-  for (const int64_t* st : sts)
-    if ((st[0] | st[1] | st[2]) & 7) return GEMM_F16_ERR_MISALIGNED;
-  return GEMM_F16_OK;
-}
-
-int attn_f16_key_ranges(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
-                        int* ranges) {
-  if (!p || !ranges || batch < 1 || heads < 1 || seq_q < 1 || seq_kv < 1)
-    return GEMM_F16_ERR_INVALID_ARG;
-  *ranges = 1;
-  if (p->attn_kernel == 1 || p->attn_pairs <= 0) return GEMM_F16_OK;
-  const int64_t items = (int64_t)batch * heads * ceil_div(seq_q, attnp::PQ);
-  int bps = 0;
-  *ranges = (int)attn_key_ranges(p, items, ceil_div(seq_kv, attnp::BKV), &bps);
-  return GEMM_F16_OK;
-}
-
-int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv, int head_dim,
-                 const void* Q, const int64_t q_strides[3], const void* K,
-                 const int64_t k_strides[3], const void* V, const int64_t v_strides[3], void* O,
-                 const int64_t o_strides[3], float scale, gemm_f16_stream_t stream) {
-  if (!p) return GEMM_F16_ERR_INVALID_ARG;
-  int rc = attn_f16_validate(batch, heads, seq_q, seq_kv, head_dim, Q, q_strides, K, k_strides,
-                             V, v_strides, O, o_strides, scale);
-  if (rc) return rc;
-  DeviceGuard g(p->device);
-  const bool use_pair = p->attn_kernel != 1 && p->attn_pairs > 0;
-  CUtensorMap tmQ, tmK, tmV, tmO;
-  if ((rc = cached_encode_bhsd(p, &tmQ, Q, batch, heads, seq_q, q_strides, attn::BQ))) return rc;
-  if ((rc = cached_encode_bhsd(p, &tmK, K, batch, heads, seq_kv, k_strides, 64))) return rc;
-  if ((rc = cached_encode_bhsd(p, &tmV, V, batch, heads, seq_kv, v_strides, use_pair ? 128u : 64u)))
-    return rc;
-  if ((rc = cached_encode_bhsd(p, &tmO, O, batch, heads, seq_q, o_strides, 32))) return rc;
-  if (use_pair) {
-    attnp::Params prm;
-    prm.seq_q = seq_q;
-    prm.seq_kv = seq_kv;
-    prm.nkv = (int)ceil_div(seq_kv, attnp::BKV);
-    prm.n_qt = (int)ceil_div(seq_q, attnp::PQ);
-    prm.heads = heads;
-    const int64_t items = (int64_t)batch * heads * prm.n_qt;
-    if (items > INT32_MAX - 65536) return GEMM_F16_ERR_INVALID_ARG;  // unit + clusters fits
-    prm.n_items = (int)items;
-    prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-    prm.status = p->status_dev;
-    prm.timeout_ns = p->timeout_ns;
-    prm.fault_unit = p->fault_unit;
-    // Persistent: one cluster per co-resident pair slot (fewer under an SM
-    // limit), never more than there are units.
-    const int64_t slots = attn_pair_slots(p);
-    int64_t n_split = attn_key_ranges(p, items, prm.nkv, &prm.bps);
-    const int64_t units = items * n_split;
-    if (units > INT32_MAX - 65536) return GEMM_F16_ERR_INVALID_ARG;
-    prm.n_split = (int)n_split;
-    prm.n_units = (int)units;
-    prm.part_ml = nullptr;
-    CUtensorMap tmP = tmO;
-    const size_t part_bytes = (size_t)units * attnp::PQ * attn::HD * sizeof(float);
-    if (n_split > 1) {
-      const size_t bytes = part_bytes + (size_t)units * attnp::PQ * 2 * sizeof(float);
-      if ((rc = ensure_buffer(&p->ws, &p->ws_bytes, bytes, (cudaStream_t)stream,
-                              "attention workspace allocation")))
-        return rc;
-      prm.part_ml = reinterpret_cast<float*>(static_cast<char*>(p->ws) + part_bytes);
-      // The partial O: units * 256 rows of 256 FP32, stored in 32 x 32 boxes.
-      if ((rc = cached_encode_2d(p, &tmP, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p->ws, attn::HD,
-                                 (uint64_t)units * attnp::PQ, attn::HD * sizeof(float), 32, 32,
-                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
-        return rc;
-    }
-    const int64_t clusters = std::min<int64_t>(slots, units);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-    cfg.blockDim = dim3(attnp::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = attnp::SMEM_BYTES;
-    cfg.stream = (cudaStream_t)stream;
-    cudaLaunchAttribute pdl;
-    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pdl.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &pdl;
-    cfg.numAttrs = 1;
-    GF16_CUDA(cudaLaunchKernelEx(&cfg, attnp::attn_f16_fwd_pair_kernel, tmQ, tmK, tmV, tmO, tmP,
-                                 prm),
-              "launch attn_f16_fwd_pair_kernel");
-    if (n_split > 1) {
-      // One warp per query row of every item.
-      cudaLaunchConfig_t ccfg = {};
-      ccfg.gridDim = dim3((unsigned)(items * attnp::PQ / 8), 1, 1);
-      ccfg.blockDim = dim3(256, 1, 1);
-      ccfg.stream = (cudaStream_t)stream;
-      ccfg.attrs = &pdl;
-      ccfg.numAttrs = 1;
-      GF16_CUDA(cudaLaunchKernelEx(&ccfg, attnp::attn_combine_kernel,
-                                   static_cast<const float*>(p->ws),
-                                   static_cast<const float2*>(static_cast<const void*>(prm.part_ml)),
-                                   prm, static_cast<__half*>(O), o_strides[0], o_strides[1],
-                                   o_strides[2]),
-                "launch attn_combine_kernel");
-    }
-    return GEMM_F16_OK;
+  int v = 0;
+  GF16_CUDA(cudaMemcpyFromSymbol(&v, g_noalloc_scratch, sizeof(int), NOALLOC_STATUS_OFF,
+                                 cudaMemcpyDeviceToHost),
+            "read no-alloc status word");
+  if (v != 0) {
+    const int zero = 0;
+    GF16_CUDA(cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof(int), NOALLOC_STATUS_OFF,
+                                 cudaMemcpyHostToDevice),
+              "clear no-alloc status word");
   }
-  attn::Params prm;
-  prm.seq_q = seq_q;
-  prm.seq_kv = seq_kv;
-  prm.nkv = (int)ceil_div(seq_kv, attn::BKV);
-  prm.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-  prm.status = p->status_dev;
-  prm.timeout_ns = p->timeout_ns;
-  prm.fault_cta = p->fault_unit;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ceil_div(seq_q, attn::BQ), (unsigned)heads, (unsigned)batch);
-  cfg.blockDim = dim3(attn::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = attn::SMEM_BYTES;
-  cfg.stream = (cudaStream_t)stream;
-  cudaLaunchAttribute pdl;
-  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &pdl;
-  cfg.numAttrs = 1;
-  GF16_CUDA(cudaLaunchKernelEx(&cfg, attn::attn_f16_fwd_kernel, tmQ, tmK, tmV, tmO, prm),
-            "launch attn_f16_fwd_kernel");
-  return GEMM_F16_OK;
+  return v;
 }
-
-int attn_f16_fwd_host(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
-                      int head_dim, const void* hQ, const void* hK, const void* hV, void* hO,
-                      float scale, gemm_f16_stream_t stream_) {
-  if (!p || !hQ || !hK || !hV || !hO) return GEMM_F16_ERR_INVALID_ARG;
-  // device copies are contiguous [batch, head, row, 256]
-  const int64_t qs[3] = {(int64_t)heads * seq_q * 256, (int64_t)seq_q * 256, 256};
-  const int64_t ks[3] = {(int64_t)heads * seq_kv * 256, (int64_t)seq_kv * 256, 256};
-  const void* probe = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
-  int rc = attn_f16_validate(batch, heads, seq_q, seq_kv, head_dim, probe, qs, probe, ks, probe, ks,
-                             probe, qs, scale);
-  if (rc) return rc;
-  cudaStream_t stream = (cudaStream_t)stream_;
-  DeviceGuard g(p->device);
-  if (!p->in_stream)
-    GF16_CUDA(cudaStreamCreateWithFlags(&p->in_stream, cudaStreamNonBlocking),
-              "create input-copy stream");
-  for (int sl = 0; sl < 2; ++sl) {
-    if (!p->attn_in_done[sl])
-      GF16_CUDA(cudaEventCreateWithFlags(&p->attn_in_done[sl], cudaEventDisableTiming),
-                "create event");
-    if (!p->attn_done[sl])
-      GF16_CUDA(cudaEventCreateWithFlags(&p->attn_done[sl], cudaEventDisableTiming),
-                "create event");
-  }
-  const int slot = p->attn_slot;
-  p->attn_slot ^= 1;
-  void** buf = p->abuf[slot];
-  const size_t qbytes = (size_t)batch * heads * seq_q * 256 * 2;
-  const size_t kbytes = (size_t)batch * heads * seq_kv * 256 * 2;
-  const size_t bytes[4] = {qbytes, kbytes, kbytes, qbytes};
-  bool grow = false;
-  for (int i = 0; i < 4; ++i) grow = grow || p->acap[slot][i] < bytes[i];
-  if (grow) {
-    // Growing a slot: let everything that may still use it finish first.
-    GF16_CUDA(cudaDeviceSynchronize(), "synchronise before growing attention staging");
-    for (int i = 0; i < 4; ++i) {
-      if (p->acap[slot][i] >= bytes[i]) continue;
-      if (buf[i]) cudaFree(buf[i]);
-      buf[i] = nullptr;
-      p->acap[slot][i] = 0;
-      GF16_CUDA(cudaMalloc(&buf[i], bytes[i]), "attention staging allocation");
-      p->acap[slot][i] = bytes[i];
-    }
-  }
-  // Q, K, V go in on the plan's input stream once the call that last used
-  // this slot (two calls ago) has finished its pass and its output copy; the
-  // pass on `stream` waits for them; O comes back on `stream` after the pass.
-  GF16_CUDA(cudaStreamWaitEvent(p->in_stream, p->attn_done[slot], 0), "order input copies");
-  GF16_CUDA(cudaMemcpyAsync(buf[0], hQ, qbytes, cudaMemcpyHostToDevice, p->in_stream), "copy Q");
-  GF16_CUDA(cudaMemcpyAsync(buf[1], hK, kbytes, cudaMemcpyHostToDevice, p->in_stream), "copy K");
-  GF16_CUDA(cudaMemcpyAsync(buf[2], hV, kbytes, cudaMemcpyHostToDevice, p->in_stream), "copy V");
-  GF16_CUDA(cudaEventRecord(p->attn_in_done[slot], p->in_stream), "record input copies");
-  GF16_CUDA(cudaStreamWaitEvent(stream, p->attn_in_done[slot], 0), "order pass after inputs");
-  rc = attn_f16_fwd(p, batch, heads, seq_q, seq_kv, head_dim, buf[0], qs, buf[1], ks, buf[2], ks,
-                    buf[3], qs, scale, stream_);
-  if (rc) return rc;
-  GF16_CUDA(cudaMemcpyAsync(hO, buf[3], qbytes, cudaMemcpyDeviceToHost, stream), "copy O to host");
-  // The slot is free again once O has left it, whatever stream the next call uses.
-  GF16_CUDA(cudaEventRecord(p->attn_done[slot], stream), "record pass and output copy");
-  return GEMM_F16_OK;
-}
-
-}  // extern "C"

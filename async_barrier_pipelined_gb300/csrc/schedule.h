@@ -92,4 +92,34 @@ GF16_HD uint32_t pack_tile(uint32_t tm, uint32_t tn) { return tm | (tn << 16); }
 GF16_HD uint32_t tile_m_of(uint32_t packed) { return packed & 0xFFFFu; }
 GF16_HD uint32_t tile_n_of(uint32_t packed) { return packed >> 16; }
 
+// The tile at position `rank` when the tiles of a tiles_m x tiles_n grid are
+// listed by increasing morton_code, returned packed (pack_tile).  Z-order
+// is the depth-first walk of the quadtree over the enclosing 2^L x 2^L
+// square whose child digit is (tn bit, tm bit); descending it, and skipping
+// each child by its number of in-grid tiles (the product of its clipped row
+// and column extents), reaches the rank-th in-grid tile in 2 L steps with
+// no table.  Requires rank < tiles_m * tiles_n and both sizes <= 65536.
+GF16_HD uint32_t morton_tile_of_rank(uint32_t rank, uint32_t tiles_m, uint32_t tiles_n) {
+  uint32_t side = 1;
+  while (side < tiles_m || side < tiles_n) side <<= 1;
+  uint32_t m0 = 0, n0 = 0;
+  while (side > 1) {
+    const uint32_t h = side >> 1;
+    for (uint32_t digit = 0; digit < 4; ++digit) {
+      const uint32_t cm = m0 + (digit & 1u) * h, cn = n0 + (digit >> 1) * h;
+      const uint32_t rows = cm < tiles_m ? (tiles_m - cm < h ? tiles_m - cm : h) : 0u;
+      const uint32_t cols = cn < tiles_n ? (tiles_n - cn < h ? tiles_n - cn : h) : 0u;
+      const uint32_t count = rows * cols;
+      if (rank < count || digit == 3) {
+        m0 = cm;
+        n0 = cn;
+        break;
+      }
+      rank -= count;
+    }
+    side = h;
+  }
+  return pack_tile(m0, n0);
+}
+
 }  // namespace gf16

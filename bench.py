@@ -19,10 +19,12 @@ torchrun each rank runs an independent replica on its own GPU (the GEMM has
 no exchange step, so there is no collective on the data path).
 
 Extra keys: roofline (dominant kernel vs the measured dense 16-bit tensor
-peak), cpu_baseline (the FP64 oracle on a bounded row sample, host cores),
-e2e (same metric through gemm_f16_run_host with pinned host buffers, copies
-inside the timed region), clocks (nvidia-smi sampled under load),
-gpu_launches (kernels launched in the timed region).
+peak), cpu_baseline (the FP64 oracle on a bounded row sample, host cores,
+with the host's machine type and CPU model), e2e (same metric through
+gemm_f16_run_host with pinned host buffers, copies inside the timed region),
+clocks (nvidia-smi sampled under load), sustained (the same step re-timed
+back to back over >= 0.3 s with its own clock samples, against the measured
+sustained tensor peak), gpu_launches (kernels launched in the timed region).
 
 --impl reference times the FP64 CPU oracle on the same workload instead
 (bounded row samples per step).
@@ -59,8 +61,10 @@ ATTN_METRIC = "FP16 attention forward TFLOPS, head dim 256, on 1 GB300"
 FALLBACK_TENSOR_TFLOPS = 1900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "async_barrier_pipelined_gb300", "csrc", f)
-                  for f in ("gemm_f16.cu", "gemm_pair.cuh", "gemm_pair_wide.cuh", "ptx.cuh", "schedule.h",
-                            "attn_f16.cuh", "attn_pair.cuh")]
+                  for f in ("plan.cu", "gemm_f16.cu", "attn_f16.cu", "host.h", "common.cuh",
+                            "gemm_pair.cuh", "ptx.cuh", "schedule.h", "attn_f16.cuh",
+                            "attn_pair.cuh")]
+SUSTAINED_S = 0.3
 
 
 def parse_args():
@@ -77,9 +81,11 @@ def parse_args():
                     help="idle seconds before the warm-up (page protocol: 5)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
-                    help="GEMM: 0 automatic, 1 single-CTA kernel, 2 CTA pair 256x256, "
-                         "3 CTA pair 256x512; attention: 0 automatic, 1 single CTA, 2 CTA pair")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="GEMM: 0 automatic, 1 single-CTA kernel, 2 CTA pair 256x256; "
+                         "attention: 0 automatic, 1 single CTA, 2 CTA pair")
+    ap.add_argument("--no-sustained", action="store_true",
+                    help="skip the sustained (>= 0.3 s) re-timing of the step")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU seconds for the oracle baseline sample")
     return ap.parse_args()
@@ -196,7 +202,10 @@ class ClockSampler:
                     reasons.add(name)
         if not under:
             return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                    "samples": 0}
+                    "samples": 0,
+                    "note": (f"region of {1e3 * (t1 - t0):.1f} ms is shorter than the "
+                             f"{self.interval} ms sampling period: no sample fell in it "
+                             "(see the sustained record for clocks under load)")}
         return {"sm_mhz": statistics.median(under), "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(under),
                 "window": "last warm-up steps and the timed region"}
@@ -249,6 +258,62 @@ def dist_setup(args):
     return world, rank, local
 
 
+def sustained_record(step, barrier, stream, dev, world, ms_step, flops_per_step, start,
+                     peak_sustained, peak_burst):
+    """The same step timed again over at least SUSTAINED_S seconds (back to
+    back, so that the GPU settles at its power limit), with its own clock
+    samples: the figure a long run would see, against the measured
+    sustained tensor peak as well as the burst one."""
+    import math
+    import torch
+    n = int(max(1, math.ceil(SUSTAINED_S * 1e3 / max(ms_step, 1e-6))))
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.2)
+    sampler.mark("load_start")
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        step(start + i)
+    e1.record(stream)
+    e1.synchronize()
+    barrier()
+    sampler.mark("timed_end")
+    clocks = sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    value = whole_job_tflops(flops_per_step, n, world, ms)
+    return {"value": value, "unit": "TFLOPS", "steps": n, "ms_per_step": ms / n,
+            "seconds": ms * 1e-3,
+            "frac_of_sustained_peak": value / world / peak_sustained if peak_sustained else None,
+            "frac_of_burst_peak": value / world / peak_burst, "clocks": clocks}
+
+
+def host_record() -> dict:
+    """Machine and CPU model of the host the CPU baseline ran on."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for ln in fh:
+                    if ln.lower().startswith(("model name", "cpu part")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"machine": platform.machine(), "cpu_model": model,
+            "logical_cpus": os.cpu_count()}
+
+
 # ------------------------------------------------------------------ CPU oracle
 def cpu_oracle_sample(w: si.Workload, rows: np.ndarray, A_bits, B_bits):
     import oracle
@@ -287,7 +352,7 @@ def cpu_baseline(w: si.Workload, target_s: float, pairs_bits):
         sample = (f"{products} full products over {min(products, len(pairs_bits))} "
                   f"pair(s): {flops / 1e9:.1f} GFLOP in {t:.1f} s, FP64 triple loop")
     return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-            "sample": sample}
+            "sample": sample, "host": host_record()}
 
 
 # ------------------------------------------------------------------ arms
@@ -318,7 +383,8 @@ def attn_cpu_baseline(w, target_s: float):
     flops = 4.0 * done * w.Skv * w.D
     return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
             "sample": f"{n} of {w.Sq} query rows (evenly spaced) of {heads} head(s): "
-                      f"{flops / 1e9:.1f} GFLOP in {t:.1f} s, FP64 plain softmax"}
+                      f"{flops / 1e9:.1f} GFLOP in {t:.1f} s, FP64 plain softmax",
+            "host": host_record()}
 
 
 def attn_config(w):
@@ -356,7 +422,8 @@ def run_reference_attention(args):
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": attn_config(w),
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-                         "sample": f"{n} query rows of one head per step, FP64 plain softmax"},
+                         "sample": f"{n} query rows of one head per step, FP64 plain softmax",
+                         "host": host_record()},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -401,7 +468,7 @@ def run_reference(args):
         "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                          "sample": f"{n} rows of C per step ({n}x{w.N} outputs, "
-                                   f"K={w.K}), FP64 triple loop"},
+                                   f"K={w.K}), FP64 triple loop", "host": host_record()},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -495,6 +562,12 @@ def run_attention(args):
     value = whole_job_tflops(float(w.flops), args.steps, world, ms_total)
 
     peak, peak_sus, peak_hbm, peak_kind = load_peaks()
+    sustained = None
+    if not args.no_sustained:
+        sustained = sustained_record(step, barrier, stream, dev, world, ms_step, float(w.flops),
+                                     args.steps, peak_sus, peak)
+        if plan.status() != 0:
+            raise RuntimeError("device status error in the sustained region")
     achieved = float(w.flops) / (ms_step * 1e-3) / 1e12
     cbytes = 2.0 * w.D * w.B * w.H * (2 * w.Sq + 2 * w.Skv)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -551,6 +624,7 @@ def run_attention(args):
                                                    "single CTA (128 query rows, 64-key blocks)"),
                            key_ranges=ranges),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "sustained": sustained,
             "gpu_launches": args.steps * launches_per_step, "pct_of_peak": 100.0 * achieved / peak,
         }
         print(json.dumps(line), flush=True)
@@ -602,7 +676,7 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # correctness guard on this run's own inputs: one output row vs the oracle
+    # a first call, checked for a device-side timeout before any timing
     step(0)
     torch.cuda.synchronize(dev)
     st = plan.status()
@@ -638,6 +712,12 @@ def run_ours(args):
     value = whole_job_tflops(float(w.flops), args.steps, world, ms_total)
 
     peak, peak_sus, peak_hbm, peak_kind = load_peaks()
+    sustained = None
+    if not args.no_sustained:
+        sustained = sustained_record(step, barrier, stream, dev, world, ms_step, float(w.flops),
+                                     args.steps, peak_sus, peak)
+        if plan.status() != 0:
+            raise RuntimeError("device status error in the sustained region")
     # Dominant kernel: the GEMM kernel.  For split workloads the step also
     # holds the reduce launch; the figure is then the whole step's.  Bound:
     # tensor if the workload's FLOP per compulsory byte is above the ridge
@@ -700,16 +780,14 @@ def run_ours(args):
 
     plan_sms = plan.get_option(g.INFO_NUM_SMS)
     plan_pairs = plan.get_option(g.INFO_MAX_PAIRS)
-    use_pair, use_wide = info["kernel"] in (2, 3), info["kernel"] == 3
-    kernel_desc = ("CTA pair (tcgen05 cta_group::2, 256x512 tiles)" if use_wide else
-                   "CTA pair (tcgen05 cta_group::2, 256x256 tiles)" if use_pair
+    use_pair = info["kernel"] == 2
+    kernel_desc = ("CTA pair (tcgen05 cta_group::2, 256x256 tiles)" if use_pair
                    else f"single CTA (tcgen05 cta_group::1, 128x{info['tile_width']} tiles)")
     if info["repack_a"]:
         kernel_desc += "; A repacked to 128-byte-aligned rows first"
     if info["launches"] > 1 + (w.split_k > 1) + info["repack_a"]:
         kernel_desc += "; partial last wave in K halves, merged by a second kernel"
-    roofline["kernel"] = ("gf16::pairw::gemm_f16_pair_kernel<512>" if use_wide else
-                          "gf16::pair::gemm_f16_pair_kernel" if use_pair
+    roofline["kernel"] = ("gf16::pair::gemm_f16_pair_kernel" if use_pair
                           else "gf16::gemm_f16_kernel")
     roofline["launches_per_step"] = launches_per_step
     plan.close()
@@ -722,7 +800,8 @@ def run_ours(args):
             "config": dict(workload_config(w), kernel=kernel_desc,
                            sms=plan_sms, max_pairs=plan_pairs),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "clocks": clocks, "gpu_launches": args.steps * launches_per_step,
+            "clocks": clocks, "sustained": sustained,
+            "gpu_launches": args.steps * launches_per_step,
             "pct_of_peak": 100.0 * (float(w.flops) / (ms_step * 1e-3) / 1e12) / peak,
         }
         print(json.dumps(line), flush=True)

@@ -84,10 +84,8 @@ typedef enum gemm_f16_option {
      * 2 = CTA-pair kernel with 256-row x 256-column tiles (two TMEM
      * accumulators, epilogue overlapped; with one split a partial last wave
      * runs as K halves merged by a second kernel, see gemm_f16_pair_tiles,
-     * or as 128-wide tiles),
-     * 3 = CTA-pair kernel with 256 x 512 tiles (less load traffic per MMA,
-     * one accumulator; 256- and 128-wide tiles in the last wave).  Results
-     * agree within the usual tolerance; split results are bitwise
+     * or as 128-wide tiles).  Any other value is GEMM_F16_ERR_INVALID_ARG.
+     * Results agree within the usual tolerance; split results are bitwise
      * reproducible for a fixed choice. */
     GEMM_F16_OPT_KERNEL = 4,
     /* Output tile width of the single-CTA kernel: 0 = automatic (a cost
@@ -197,8 +195,7 @@ enum {
  * gemm_f16_run with an operand layout (above).  gemm_f16_run is
  * gemm_f16_run_ex with GEMM_F16_LAYOUT_NN.  Same semantics, workspace,
  * split-K order and errors; GEMM_F16_ERR_INVALID_ARG also for a layout
- * outside 0..3.  Option GEMM_F16_OPT_KERNEL 3 (512-wide pair tiles) is
- * honoured for layout NN only; other layouts then use 256-wide pair tiles.
+ * outside 0..3.
  */
 int gemm_f16_run_ex(gemm_f16_plan_t plan, int layout, int M, int N, int K,
                     const void *A, int64_t lda, const void *B, int64_t ldb,
@@ -207,15 +204,14 @@ int gemm_f16_run_ex(gemm_f16_plan_t plan, int layout, int M, int N, int K,
 /*
  * What gemm_f16_run_ex would enqueue for these sizes with the plan's current
  * options, without enqueuing anything (host only):
- *   info[0]  kernel: 1 single-CTA, 2 CTA pair with 256-wide tiles, 3 CTA
- *            pair with 512-wide tiles;
+ *   info[0]  kernel: 1 single-CTA, 2 CTA pair;
  *   info[1]  kernel launches per call: the product, plus one for the split
  *            reduction when split_k > 1, plus one for the repack of A, plus
  *            one for merging the K halves of a partial last wave of pair
  *            tiles (see gemm_f16_pair_tiles);
  *   info[2]  1 if A is repacked first (GEMM_F16_OPT_A_REPACK), else 0;
  *   info[3]  output tile width of the chosen kernel (single-CTA: 256 / 128 /
- *            64 columns; pair: 256 or 512).
+ *            64 columns; pair: 256).
  * Returns GEMM_F16_OK or GEMM_F16_ERR_INVALID_ARG (null plan or info, sizes
  * or split_k < 1, layout outside 0..3, lda below the stored row length).
  */
@@ -297,7 +293,7 @@ int64_t gemm_f16_tile_order(int tiles_m, int tiles_n, int order,
 
 /*
  * Host-only: the work list of the CTA-pair kernel with full tiles
- * `tile_width` (256 or 512) columns wide, for an M x N x K product with
+ * `tile_width` columns wide (must be 256), for an M x N x K product with
  * `pairs` co-resident CTA pairs (see GEMM_F16_INFO_MAX_PAIRS).  Each entry
  * is (pair_row | col128 << 16 | log2(width/128) << 30): rows 256*pair_row ..
  * +255, columns 128*col128 .. +width-1.  Writes up to `cap` entries (`out`
@@ -333,38 +329,50 @@ int gemm_f16_tile_shape(int *bm, int *bn, int *bk, int *stages);
  * Instead of plan-owned buffers this entry point uses one fixed scratch
  * array compiled into the library (a file-scope __device__ array), which
  * every GPU that loads the library holds until the process exits:
- *   GEMM_F16_NOALLOC_SCRATCH_BYTES bytes = a tile-order table of up to
- *   GEMM_F16_NOALLOC_MAX_TILES entries plus GEMM_F16_NOALLOC_WS_BYTES of
- *   FP32 split partials.
- * Limits: ceil(M/128) * ceil(N/256) <= GEMM_F16_NOALLOC_MAX_TILES, and for
- * split_k > 1, split_k * M * (N rounded up to 8) * 4 bytes <=
+ *   GEMM_F16_NOALLOC_SCRATCH_BYTES bytes = a 256-byte status area plus
+ *   GEMM_F16_NOALLOC_WS_BYTES of FP32 split partials.
+ * The kernel computes each tile's position from its index, so nothing but
+ * split partials is kept in the scratch between calls.
+ * Limit: for split_k > 1, split_k * M * (N rounded up to 8) * 4 bytes <=
  * GEMM_F16_NOALLOC_WS_BYTES (32 MiB; e.g. 512 x 512 with 16 splits uses 16
  * MiB).  Larger problems return GEMM_F16_ERR_SCRATCH_TOO_SMALL and enqueue
- * nothing.
+ * nothing.  split_k = 1 uses no scratch beyond the status area.
  *
  * Arguments are those of gemm_f16_run (same validation and error codes),
- * plus `status`: NULL, or a device-visible int the caller owns, into which
- * the kernel writes GEMM_F16_ERR_TIMEOUT if one of its bounded waits runs
- * out (it is never cleared by this call).  The device is the current CUDA
- * device.
+ * plus `status`: a device-visible int the caller owns, into which the
+ * kernel writes GEMM_F16_ERR_TIMEOUT if one of its bounded waits runs out
+ * (it is never cleared by this call), or NULL.  With NULL the timeout goes
+ * to the scratch's own status word, which only gemm_f16_noalloc_status
+ * (below) reads: a caller that passes NULL and never calls it cannot learn
+ * of a timeout, after which C is incomplete.  The device is the current
+ * CUDA device.
  *
- * The first call on a device does a one-time set-up with that device
- * current (shared-memory limit of the kernel, the scratch array's device
- * address via cudaGetSymbolAddress, SM count); make that first call before
- * any stream capture.  Every call shares the one scratch array and it keeps
- * the last call's contents: calls that overlap on the GPU (different
- * streams, or different host threads) race on it and must not be issued
- * concurrently.  A call whose tile grid differs from the previous call's on
- * that device uploads a new tile-order table with a pageable-memory copy on
- * `stream`, which may wait for the stream's earlier work.
+ * The first call on a device (of this function or of
+ * gemm_f16_noalloc_status) does a one-time set-up with that device current
+ * (shared-memory limit of the kernel, the scratch array's device address via
+ * cudaGetSymbolAddress, SM count); make that first call before any stream
+ * capture.  Every call shares the one scratch array and it keeps the last
+ * call's contents: calls that overlap on the GPU (different streams, or
+ * different host threads) race on the split partials and must not be
+ * issued concurrently.
  */
-#define GEMM_F16_NOALLOC_MAX_TILES 65536
 #define GEMM_F16_NOALLOC_WS_BYTES (32u << 20)
-#define GEMM_F16_NOALLOC_SCRATCH_BYTES \
-    (GEMM_F16_NOALLOC_MAX_TILES * 4u + 256u + GEMM_F16_NOALLOC_WS_BYTES)
+#define GEMM_F16_NOALLOC_SCRATCH_BYTES (256u + GEMM_F16_NOALLOC_WS_BYTES)
 int gemm_f16_run_noalloc(int M, int N, int K, const void *A, int64_t lda,
                          const void *B, int64_t ldb, void *C, int64_t ldc,
                          int split_k, int *status, gemm_f16_stream_t stream);
+
+/*
+ * Read and clear the scratch status word that gemm_f16_run_noalloc calls
+ * given status == NULL write on the current device: returns 0 if none of
+ * them timed out since the last read, GEMM_F16_ERR_TIMEOUT if one did, or a
+ * negative error code of its own.  It copies 4 bytes with
+ * cudaMemcpyFromSymbol (and clears them with cudaMemcpyToSymbol), which
+ * allocates nothing but waits for the device's preceding work on the legacy
+ * default stream; call it after the calls it should cover have finished
+ * (e.g. after synchronising their stream).  No counterpart in the paper.
+ */
+int gemm_f16_noalloc_status(void);
 
 #ifdef __cplusplus
 }

@@ -159,30 +159,29 @@ def _covered(tiles, M, N):
                                  (129, 300), (256, 129), (300, 384), (1, 1), (2000, 100),
                                  (777, 5000)])
 @pytest.mark.parametrize("pairs", [76, 7, 1])
-@pytest.mark.parametrize("tw", [256, 512])
-def test_pair_tiles_cover_output_exactly_once(lib, M, N, pairs, tw):
+def test_pair_tiles_cover_output_exactly_once(lib, M, N, pairs):
     import numpy as np
-    tiles = g.gemm_f16_pair_tiles(M, N, pairs, 1, 0, tw)
+    tiles = g.gemm_f16_pair_tiles(M, N, pairs, 1, 0)
     cov = _covered(tiles, M, N)
     assert np.all(cov == 1)
     for r0, c0, w in tiles:            # no tile starts outside the output
-        assert r0 < M and c0 < N and w in ((128, 256) if tw == 256 else (128, 256, 512))
+        assert r0 < M and c0 < N and w in (128, 256)
 
 
-def _makespan(tiles, pairs, tw=256):
+def _makespan(tiles, pairs):
     load = [0.0] * pairs
     for i, (_, _, w) in enumerate(tiles):
-        load[i % pairs] += w / tw
+        load[i % pairs] += w / 256
     return max(load)
 
 
-def _tail_makespan(tiles, parts, pairs, tw=256):
+def _tail_makespan(tiles, parts, pairs):
     """Busiest pair's work in tile times when the last len % pairs tiles run
     as `parts` K parts each (units handed out round-robin)."""
     r = len(tiles) % pairs if parts > 1 else 0
-    units = [w / tw for *_, w in tiles[:len(tiles) - r]]
+    units = [w / 256 for *_, w in tiles[:len(tiles) - r]]
     for *_, w in tiles[len(tiles) - r:]:
-        units += [w / tw / parts] * parts
+        units += [w / 256 / parts] * parts
     load = [0.0] * pairs
     for i, x in enumerate(units):
         load[i % pairs] += x
@@ -215,10 +214,6 @@ def test_pair_tiles_balance_the_last_wave(lib):
     # splits keep whole tiles (the split units are the parallelism)
     t, parts = g.gemm_f16_pair_tiles(512, 512, 76, 16, K=32768, with_parts=True)
     assert len(t) == 4 and all(w == 256 for *_, w in t) and parts == 1
-    # 512-wide tiles: 128 tiles on 76 pairs; the second wave is cut into
-    # quarters (3 per pair at most), 1.75 instead of 2 tiles' work
-    t = g.gemm_f16_pair_tiles(4096, 4096, 76, 1, 0, 512)
-    assert _makespan(t, 76, 512) == 1.75
 
 
 def test_pair_tiles_reject_bad_arguments(lib):
@@ -227,6 +222,7 @@ def test_pair_tiles_reject_bad_arguments(lib):
     assert lib.gemm_f16_pair_tiles(8, 8, 8, 0, 1, 0, 256, None, 0, None) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_pair_tiles(8, 8, 8, 76, 0, 0, 256, None, 0, None) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_pair_tiles(8, 8, 8, 76, 1, 0, 384, None, 0, None) == g.ERR_INVALID_ARG
+    assert lib.gemm_f16_pair_tiles(8, 8, 8, 76, 1, 0, 512, None, 0, None) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_pair_tiles(8, 8, 8, 76, 1, 0, 256, None, 0, None) == 1
 
 
@@ -294,6 +290,5 @@ def test_pair_tail_halves_rule(lib, tiles, kblocks, want):
     M, N = 256 * tiles, 256          # one pair-tile column: `tiles` tiles
     _, parts = g.gemm_f16_pair_tiles(M, N, 76, 1, K=64 * kblocks, with_parts=True)
     assert parts == want
-    # never with a split, never for 512-wide tiles
+    # never with a split
     assert g.gemm_f16_pair_tiles(M, N, 76, 2, K=64 * kblocks, with_parts=True)[1] == 1
-    assert g.gemm_f16_pair_tiles(M, 512, 76, 1, 0, 512, K=64 * kblocks, with_parts=True)[1] == 1

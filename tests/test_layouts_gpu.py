@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 import synthetic_inputs as si
-from tests import gpu_util, parity
+from tests import gpu_util, oracle_cache, parity
 
 pytestmark = pytest.mark.gpu
 
@@ -118,14 +118,12 @@ def test_split_k_layouts_match_nn_bitwise(plan, layout, shape, split):
     assert np.array_equal(c0.view(np.uint64), c1.view(np.uint64))
 
 
-def test_gemm_4096_tt_sampled(plan):
-    """The 4096^3 workload with both operands stored transposed, sampled rows."""
-    w = si.WORKLOADS["gemm_4096"]
-    A, B = w.pair_bits(1)
+def test_gemm_4096_tt_full(plan):
+    """The 4096^3 workload with both operands stored transposed, every
+    element against the oracle."""
+    A, B = oracle_cache.gemm_inputs("gemm_4096", 1)
     c, _ = gpu_util.run_layout(plan, A, B, 3)
-    rows = np.array(sorted({0, 1, 127, 128, 2047, 4095} |
-                           set(np.random.default_rng(8).choice(4096, 24, replace=False).tolist())))
-    parity.check(c[rows], oracle.gemm_f16(A, B, rows=rows), "gemm_4096 TT")
+    parity.check(c, oracle_cache.gemm_ref("gemm_4096", 1), "gemm_4096 TT")
 
 
 def test_matmul_takes_transposed_views(plan):
