@@ -512,8 +512,8 @@ __global__ void __launch_bounds__(256)
 
 // Fixed-order split reduction: C[i,j] = fp16_rn(P_0 + P_1 + ... + P_{S-1}),
 // summed left to right in FP32.  Each thread owns 4 consecutive columns;
-// the partial loads are issued eight splits at a time (independent loads,
-// so a 16-way split waits for two rounds of loads, not sixteen), but the
+// the partial loads are issued sixteen splits at a time (independent loads,
+// so a 16-way split waits for one round of loads, not sixteen), but the
 // additions keep the order t = 0, 1, ..., S-1.
 __device__ __forceinline__ void add4(float4& acc, const float4& v) {
   acc.x += v.x;
@@ -539,23 +539,23 @@ __global__ void __launch_bounds__(256)
     const float* src = ws + i * ldw + j;
     float4 acc = *reinterpret_cast<const float4*>(src);
     int s = 1;
-    for (; s + 8 <= split_k; s += 8) {
-      float4 v[8];
+    for (; s + 16 <= split_k; s += 16) {
+      float4 v[16];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
+      for (int q = 0; q < 16; ++q)
         v[q] = *reinterpret_cast<const float4*>(src + (int64_t)(s + q) * split_stride);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) add4(acc, v[q]);
+      for (int q = 0; q < 16; ++q) add4(acc, v[q]);
     }
     if (s < split_k) {
-      // the last 1..7 splits, also loaded together before they are added
-      float4 v[7];
+      // the last 1..15 splits, also loaded together before they are added
+      float4 v[15];
 #pragma unroll
-      for (int q = 0; q < 7; ++q)
+      for (int q = 0; q < 15; ++q)
         if (s + q < split_k)
           v[q] = *reinterpret_cast<const float4*>(src + (int64_t)(s + q) * split_stride);
 #pragma unroll
-      for (int q = 0; q < 7; ++q)
+      for (int q = 0; q < 15; ++q)
         if (s + q < split_k) add4(acc, v[q]);
     }
     const __half2 h0 = __floats2half2_rn(acc.x, acc.y), h1 = __floats2half2_rn(acc.z, acc.w);
