@@ -120,18 +120,32 @@ def compulsory_bytes(w: si.Workload) -> int:
     return 2 * (w.M * w.K + w.K * w.N + w.M * w.N)
 
 
-def load_traffic(workload: str):
-    """Per-launch DRAM bytes of the GEMM kernel from a committed ncu summary,
-    or None when the kernel source changed since it was captured."""
+def _traffic_entry(workload: str):
+    """The workload's entry of the committed ncu summary, or None when the
+    kernel sources changed since it was captured."""
     try:
         with open(TRAFFIC_FILE) as fh:
-            t = json.load(fh)
-        e = t.get(workload)
+            e = json.load(fh).get(workload)
         if e and e.get("kernel_source_sha") == kernel_source_hash():
-            return float(e["dram_bytes_per_launch"])
+            return e
     except Exception:
         pass
     return None
+
+
+def load_traffic(workload: str):
+    """Per-launch DRAM bytes of the dominant kernel from a committed ncu
+    summary, or None when the kernel source changed since it was captured."""
+    e = _traffic_entry(workload)
+    return float(e["dram_bytes_per_launch"]) if e else None
+
+
+def load_tensor_pipe(workload: str):
+    """The dominant kernel's tensor-pipe activity from a committed `ncu --set
+    full` capture ({"of_active_pct", "of_elapsed_pct", "sm_ghz"}; a clock-
+    independent measure of how busy the tensor cores are), or None."""
+    e = _traffic_entry(workload)
+    return e.get("tensor_pipe") if e else None
 
 
 class ClockSampler:
@@ -575,6 +589,7 @@ def run_attention(args):
                 "peak_source": f"{peak_kind} dense bf16 burst (fp16 runs at the same rate)",
                 "algorithmic_flops_per_launch": float(w.flops),
                 "traffic": load_traffic(w.name) if use_pair else None,
+                "tensor_pipe_ncu": load_tensor_pipe(w.name) if use_pair else None,
                 "flop_per_byte": float(w.flops) / cbytes,
                 "kernel": ("gf16::attnp::attn_f16_fwd_pair_kernel" if use_pair
                            else "gf16::attn::attn_f16_fwd_kernel")
@@ -737,6 +752,7 @@ def run_ours(args):
                     "algorithmic_bytes_per_launch": float(cbytes),
                     "tflops": float(w.flops) / (ms_step * 1e-3) / 1e12}
     roofline["traffic"] = load_traffic(w.name)
+    roofline["tensor_pipe_ncu"] = load_tensor_pipe(w.name)
     roofline["flop_per_byte"] = w.flops / cbytes
     roofline["ridge_flop_per_byte"] = ridge
 
