@@ -134,7 +134,7 @@ typedef enum gemm_f16_option {
  * Create a plan on CUDA device `device`.  Checks the device (compute
  * capability 10.3), sets the kernels' shared-memory limits and allocates the
  * plan's status word (mapped pinned host memory).  The workspace for split
- * runs and the tile-order tables are allocated on first use.
+ * runs and the CTA-pair kernel's work lists are allocated on first use.
  * `*out` receives the plan, or NULL on error.
  */
 int gemm_f16_plan(gemm_f16_plan_t *out, int device);
@@ -156,10 +156,12 @@ int gemm_f16_plan(gemm_f16_plan_t *out, int device);
  *            range's FP32 partial tile goes to the plan's workspace and a
  *            second kernel sums the s partials in order t = 0..s-1 in FP32
  *            and rounds once to binary16.  Requires s <= KB.
- * The first run with a new tile grid uploads that grid's tile-order table,
- * and a split run, a run with K halves or a repack of A may grow a plan
- * buffer; all of that is stream-ordered on `stream`, so make one such run
- * before capturing the stream in a graph.
+ * The first run of the CTA-pair kernel for a new shape builds its work list
+ * and uploads it (cudaMalloc and a synchronous copy; the single-CTA kernel
+ * derives its tile order on the device and needs no list), and a split run,
+ * a run with K halves or a repack of A may grow a plan buffer (stream-ordered
+ * on `stream`); make one run of each shape before capturing the stream in a
+ * graph.
  * Errors found on the device (a wait that timed out) are reported later by
  * gemm_f16_status.
  */
@@ -323,7 +325,7 @@ int gemm_f16_tile_shape(int *bm, int *bn, int *bk, int *stages);
  * caching pool that has reserved the free HBM, so a direct cudaMalloc can
  * fail), or latency-critical loops where the implicit device-wide
  * synchronisation of cudaMalloc/cudaFree would stall every other stream.
- * gemm_f16_plan allocates (status word, tile tables, the split workspace),
+ * gemm_f16_plan allocates (status word, work lists, the split workspace),
  * so such callers cannot use it.
  *
  * Instead of plan-owned buffers this entry point uses one fixed scratch
