@@ -29,6 +29,9 @@ sustained tensor peak), gpu_launches (kernels launched in the timed region).
 --impl reference times the FP64 CPU oracle on the same workload instead
 (bounded row samples per step).
 
+--graph submits the timed steps as replays of a CUDA graph of consecutive
+steps captured after the warm-up (the same kernels, no host call per step).
+
 --workload attn_256 / attn_ragged / attn_4096 measures the attention
 forward kernel (attn_f16_fwd, head dimension 256) instead: one step = one
 O = softmax(Q K^T / 16) V over all batches and heads, TFLOPS counted as
@@ -86,6 +89,10 @@ def parse_args():
                          "attention: 0 automatic, 1 single CTA, 2 CTA pair")
     ap.add_argument("--no-sustained", action="store_true",
                     help="skip the sustained (>= 0.3 s) re-timing of the step")
+    ap.add_argument("--graph", action="store_true",
+                    help="submit the timed steps as replays of a CUDA graph of consecutive "
+                         "steps (captured after the warm-up) instead of one host call each: "
+                         "the launch-bound small workloads then show the GPU's time")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU seconds for the oracle baseline sample")
     return ap.parse_args()
@@ -263,6 +270,33 @@ def auto_steps(step, barrier, stream, world, dev, start, n=50):
     barrier()
     per_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / n
     return int(min(200000, max(1000, math.ceil(MIN_TIMED_S * 1e3 / max(per_ms, 1e-6))))), n
+
+
+GRAPH_STEPS = 32
+
+
+def capture_steps(step, stream, first: int, n: int):
+    """A CUDA graph of n consecutive steps (first .. first + n - 1), captured
+    on `stream` after the warm-up has built every buffer the steps use."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(n):
+            step(first + i)
+    return graph
+
+
+def issue_steps(step, stream, steps: int, graph, gsteps: int):
+    """The timed region's work: `steps` host calls, or steps / gsteps
+    replays of the captured graph (steps is then a multiple of gsteps)."""
+    import torch
+    if graph is None:
+        for i in range(steps):
+            step(i)
+        return
+    with torch.cuda.stream(stream):
+        for _ in range(steps // gsteps):
+            graph.replay()
 
 
 def dist_setup(args):
@@ -525,6 +559,7 @@ def run_attention(args):
     ranges = g.attn_f16_key_ranges(plan.handle, w.B, w.H, w.Sq, w.Skv)
     launches_per_step = 1 if ranges == 1 else 2
 
+    npairs = 1   # one set of inputs (a CUDA graph of --graph covers GRAPH_STEPS steps)
     # the C entry point with its arguments marshalled once (as the GEMM steps
     # call gemm_f16_run directly), so host overhead does not pace small cases
     lib = g.load()
@@ -558,11 +593,17 @@ def run_attention(args):
     probe = 0
     if args.steps is None:
         args.steps, probe = auto_steps(step, barrier, stream, world, dev, args.warmup)
+    graph, gsteps = None, 0
+    if args.graph:
+        gsteps = GRAPH_STEPS * npairs
+        args.steps = (args.steps + gsteps - 1) // gsteps * gsteps
+        graph = capture_steps(step, stream, 0, gsteps)
+        issue_steps(step, stream, gsteps, graph, gsteps)     # one untimed replay
+        barrier()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    issue_steps(step, stream, args.steps, graph, gsteps)
     ev1.record(stream)
     ev1.synchronize()
     barrier()
@@ -637,7 +678,9 @@ def run_attention(args):
             "config": dict(attn_config(w), kernel=("CTA pair (tcgen05 cta_group::2, 256 query "
                                                    "rows, 128-key blocks)" if use_pair else
                                                    "single CTA (128 query rows, 64-key blocks)"),
-                           key_ranges=ranges),
+                           key_ranges=ranges,
+                           submission=(f"CUDA graph of {gsteps} steps, replayed"
+                                       if graph is not None else "one host call per step")),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "sustained": sustained,
             "gpu_launches": args.steps * launches_per_step, "pct_of_peak": 100.0 * achieved / peak,
@@ -708,11 +751,17 @@ def run_ours(args):
     probe = 0
     if args.steps is None:
         args.steps, probe = auto_steps(step, barrier, stream, world, dev, args.warmup)
+    graph, gsteps = None, 0
+    if args.graph:
+        gsteps = GRAPH_STEPS * npairs
+        args.steps = (args.steps + gsteps - 1) // gsteps * gsteps
+        graph = capture_steps(step, stream, 0, gsteps)
+        issue_steps(step, stream, gsteps, graph, gsteps)     # one untimed replay
+        barrier()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    issue_steps(step, stream, args.steps, graph, gsteps)
     ev1.record(stream)
     ev1.synchronize()
     barrier()
@@ -814,7 +863,9 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
             "config": dict(workload_config(w), kernel=kernel_desc,
-                           sms=plan_sms, max_pairs=plan_pairs),
+                           sms=plan_sms, max_pairs=plan_pairs,
+                           submission=(f"CUDA graph of {gsteps} steps, replayed"
+                                       if graph is not None else "one host call per step")),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "sustained": sustained,
             "gpu_launches": args.steps * launches_per_step,
