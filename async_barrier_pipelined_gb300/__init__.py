@@ -24,7 +24,7 @@ __all__ = [
     "gemm_f16_tile_order", "gemm_f16_tile_shape", "Plan", "matmul",
     "OK", "ERR_INVALID_ARG", "ERR_MISALIGNED", "ERR_UNSUPPORTED_DEVICE",
     "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT", "ERR_SCRATCH_TOO_SMALL", "gemm_f16_run_noalloc", "gemm_f16_noalloc_status",
-    "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "OPT_ATTN_KERNEL", "OPT_ATTN_SPLIT", "OPT_A_REPACK", "INFO_NUM_SMS", "INFO_MAX_PAIRS",
+    "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "OPT_ATTN_KERNEL", "OPT_ATTN_SPLIT", "OPT_A_REPACK", "INFO_NUM_SMS", "INFO_MAX_PAIRS", "INFO_MAX_QUADS",
     "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
     "gemm_f16_run_ex", "gemm_f16_validate_ex", "attn_f16_fwd", "attn_f16_validate",
     "attn_f16_key_ranges", "gemm_f16_run_info", "attn_f16_fwd_host", "attention_host",
@@ -52,6 +52,7 @@ OPT_ATTN_SPLIT = 8
 OPT_A_REPACK = 9
 INFO_NUM_SMS = 100
 INFO_MAX_PAIRS = 101
+INFO_MAX_QUADS = 102
 
 ATTN_HEAD_DIM = 256
 

@@ -575,6 +575,7 @@ __global__ void __launch_bounds__(256)
 }  // namespace gf16
 
 #include "gemm_pair.cuh"
+#include "gemm_quad.cuh"
 
 namespace gf16 {
 // C of the pair kernel's tail tiles: C[i, j] = fp16_rn(P0[i, j] + P1[i, j]),
@@ -779,6 +780,21 @@ int gemm_plan_init(gemm_f16_plan_s* p, const cudaDeviceProp& prop) {
     clusters = 0;
   }
   p->max_pairs = clusters;
+  // ... and of four for the cluster-of-four kernel.
+  GF16_CUDA(cudaFuncSetAttribute(quad::gemm_f16_quad_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)quad::SMEM_BYTES),
+            "cudaFuncSetAttribute(cluster-of-four kernel smem)");
+  cfg.gridDim = dim3((unsigned)(prop.multiProcessorCount / 4 * 4), 1, 1);
+  cfg.blockDim = dim3(quad::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = quad::SMEM_BYTES;
+  attr.val.clusterDim.x = 4;
+  int quads = 0;
+  if (cudaOccupancyMaxActiveClusters(&quads, quad::gemm_f16_quad_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    quads = 0;
+  }
+  p->max_quads = clusters > 0 ? quads : 0;
   return GEMM_F16_OK;
 }
 
@@ -902,6 +918,19 @@ int get_pair_table(gemm_f16_plan_s* p, int M, int N, int kblocks, int split_k,
   return upload_table(p, key, host, out, *parts);
 }
 
+// The cluster-of-four kernel's tile order (256 x 512 cluster tiles, packed
+// pack_tile(tm, tn)), built and uploaded on first use.
+int get_quad_table(gemm_f16_plan_s* p, int tiles_m, int tiles_n, const uint32_t** out) {
+  const int64_t key[6] = {2, tiles_m, tiles_n, 0, 0, p->tile_order};
+  if (const OrderTable* t = find_table(p, key)) {
+    *out = t->dev;
+    return GEMM_F16_OK;
+  }
+  std::vector<uint32_t> host;
+  build_tile_order(tiles_m, tiles_n, p->tile_order, host);
+  return upload_table(p, key, host, out);
+}
+
 // Tile width of the single-CTA kernel: 256, 128 or 64 columns.  Estimated
 // time = waves x (k-blocks per unit x cycles per k-block + fixed cost per
 // tile), with cycles per k-block max(W/2, 32 + W/4) for a 128 x W x 64
@@ -940,7 +969,8 @@ inline void* pick_instance(int layout, F0 f0, F1 f1, F2 f2, F3 f3) {
 // What a run of this shape does with the plan's current options: which
 // kernel, the single-CTA tile width, and whether A is repacked first.
 struct RunChoice {
-  bool use_pair;  // CTA-pair kernel (else single-CTA kernel)
+  bool use_quad;  // cluster-of-four kernel (two CTA pairs sharing A)
+  bool use_pair;  // CTA-pair kernel (else single-CTA kernel; also set with use_quad)
   int bn;         // single-CTA tile width: 256, 128 or 64
   bool pack_a;    // A copied to whole-line rows before the product
 };
@@ -957,15 +987,31 @@ RunChoice choose_run(const gemm_f16_plan_s* p, int layout, int M, int N, int K, 
   // kernel's smaller tiles spread the work over more SMs.
   const bool pair_fits = (N + 127) / 128 < 0x3FFF && p->max_pairs > 0;
   const int64_t pair_work = ceil_div(M, 256) * ceil_div(N, 256) * (int64_t)split_k;
-  c.use_pair = pair_fits && (p->kernel == 2 ||
+  c.use_pair = pair_fits && (p->kernel == 2 || p->kernel == 3 ||
                              (p->kernel == 0 && M > BM && 2 * pair_work >= p->max_pairs));
-  // A whose row pitch is not a multiple of 128 bytes: copy it to rows of
-  // whole lines first (see pack_rows_kernel), when asked to or, by default,
-  // for products large enough that the copy costs less than it saves.
+  // A whose row pitch is not a multiple of 128 bytes: every 128-byte row of
+  // an A copy box spans two cache lines.  On large products the automatic
+  // choice either runs the cluster-of-four kernel, which fetches half as
+  // many A rows per SM (so half the extra lines), or copies A to rows of
+  // whole lines first (see pack_rows_kernel) for the pair kernel.  Measured
+  // at 4000 x 4104 x 3000 (lda 3000): clusters of four without the copy
+  // 68-71 us, the pair kernel after the copy 77 us, clusters of four after
+  // the copy 75-77 us.  Clusters of four are taken when their waves (36
+  // clusters of 256 x 512 tiles on 152 SMs) are no more than the pair
+  // kernel's.
   const int64_t a_elems = (int64_t)M * K;
-  c.pack_a = (lda * 2) % 128 != 0 &&
-             (p->a_repack == 2 ||
-              (p->a_repack == 0 && c.use_pair && N >= 2048 && a_elems >= ((int64_t)1 << 22)));
+  const bool a_off_lines = (lda * 2) % 128 != 0;
+  const bool large = N >= 2048 && a_elems >= ((int64_t)1 << 22);
+  const bool quad_fits = c.use_pair && layout == 0 && p->max_quads > 0 &&
+                         ceil_div(N, quad::QN) <= 0xFFFF && ceil_div(M, pair::PM) <= 0xFFFF;
+  const int64_t quad_waves =
+      ceil_div(ceil_div(M, pair::PM) * ceil_div(N, quad::QN) * (int64_t)split_k,
+               std::max(p->max_quads, 1));
+  const int64_t pair_waves = ceil_div(pair_work, std::max(p->max_pairs, 1));
+  c.use_quad = quad_fits && (p->kernel == 3 || (p->kernel == 0 && a_off_lines && large &&
+                                                p->a_repack != 2 && quad_waves <= pair_waves));
+  c.pack_a = a_off_lines && (p->a_repack == 2 ||
+                             (p->a_repack == 0 && c.use_pair && !c.use_quad && large));
   return c;
 }
 
@@ -980,11 +1026,16 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
   const int64_t units = (int64_t)tiles_m * tiles_n * split_k;
   if (units > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
   const bool use_pair = choice.use_pair;
+  const bool use_quad = choice.use_quad;
+  const int quad_tm = (int)ceil_div(M, pair::PM), quad_tn = (int)ceil_div(N, quad::QN);
   const uint32_t* order = nullptr;
   int64_t pair_tiles = 0;
   int tail_parts = 1;
   int rc = GEMM_F16_OK;
-  if (use_pair) {
+  if (use_quad) {
+    rc = get_quad_table(p, quad_tm, quad_tn, &order);
+    if (rc) return rc;
+  } else if (use_pair) {
     rc = get_pair_table(p, M, N, kblocks, split_k, &order, &pair_tiles, &tail_parts);
     if (rc) return rc;
   }
@@ -1018,8 +1069,8 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   else
     rc = cached_encode_2d(p, &tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, (uint64_t)K, (uint64_t)M,
-                          (uint64_t)lda * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                          (uint64_t)lda * 2, BK, use_quad ? BM / 2 : BM,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc) return rc;
   const bool b3d = use_pair && !(layout & LAYOUT_BT) && (N % 64) == 0;
   if (layout & LAYOUT_BT)
@@ -1049,7 +1100,42 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
     if (rc) return rc;
   }
 
-  if (use_pair) {
+  if (use_quad) {
+    const int64_t qunits = (int64_t)quad_tm * quad_tn * split_k;
+    if (qunits > 0x7fffffff) return GEMM_F16_ERR_INVALID_ARG;
+    pair::Params pp;
+    pp.M = M;
+    pp.N = N;
+    pp.K = K;
+    pp.split_k = split_k;
+    pp.kblocks = kblocks;
+    pp.num_units = (int)qunits;
+    pp.order = order;
+    pp.C = static_cast<__half*>(C);
+    pp.ldc = ldc;
+    pp.status = p->status_dev;
+    pp.timeout_ns = p->timeout_ns;
+    pp.fault_unit = p->fault_unit;
+    pp.b3d = b3d ? 1 : 0;
+    pp.full_units = (int)qunits;
+    pp.tail_parts = 1;
+    int64_t cap = std::max(p->max_quads, 1);
+    if (p->sm_limit > 0) cap = std::max<int64_t>(1, std::min<int64_t>(cap, p->sm_limit / 4));
+    const int64_t nquads = std::min<int64_t>(qunits, cap);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(4 * nquads), 1, 1);
+    cfg.blockDim = dim3(quad::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = quad::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmC, (void*)&tmW, (void*)&pp};
+    GF16_CUDA(cudaLaunchKernelExC(&cfg, (void*)quad::gemm_f16_quad_kernel, args),
+              "launch gemm_f16_quad_kernel");
+  } else if (use_pair) {
     int64_t pair_cap = std::max(p->max_pairs, 1);
     if (p->sm_limit > 0) pair_cap = std::max<int64_t>(1, std::min<int64_t>(pair_cap, p->sm_limit / 2));
     // The last (pair_tiles % pairs) tiles run as two K halves each (one
@@ -1206,11 +1292,11 @@ int gemm_f16_run_info(gemm_f16_plan_t p, int layout, int M, int N, int K, int64_
   const RunChoice c = choose_run(p, layout, M, N, K, lda, split_k);
   // a partial last wave of 256-wide pair tiles in K halves adds their merge
   int parts = 1;
-  if (c.use_pair && split_k == 1) {
+  if (c.use_pair && !c.use_quad && split_k == 1) {
     std::vector<uint32_t> tiles;
     build_pair_tiles(M, N, (int)ceil_div(K, BK), p->max_pairs, split_k, p->tile_order, tiles, &parts);
   }
-  info[0] = c.use_pair ? 2 : 1;
+  info[0] = c.use_quad ? 3 : c.use_pair ? 2 : 1;
   info[1] = 1 + (split_k > 1 ? 1 : 0) + (c.pack_a ? 1 : 0) + (parts > 1 ? 1 : 0);
   info[2] = c.pack_a ? 1 : 0;
   info[3] = c.use_pair ? pair::WIDE : c.bn;

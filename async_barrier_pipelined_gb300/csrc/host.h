@@ -107,6 +107,7 @@ struct gemm_f16_plan_s {
   int attn_split = 0;  // pair attention key ranges: 0 auto, n >= 1 forced
   int a_repack = 0;    // repack A with a pitch off 128-byte lines: 0 auto, 1 never, 2 always
   int max_pairs = 0;   // co-resident clusters of two for the pair kernel
+  int max_quads = 0;   // co-resident clusters of four for the cluster-of-four kernel
   int attn_pairs = 0;  // co-resident clusters of two for the pair attention kernel
   void* ws = nullptr;
   size_t ws_bytes = 0;

@@ -239,8 +239,9 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
       p->tile_width = (int)value;
       return GEMM_F16_OK;
     case GEMM_F16_OPT_KERNEL:
-      if (value < 0 || value > 2) return GEMM_F16_ERR_INVALID_ARG;
-      if (value == 2 && p->max_pairs <= 0) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+      if (value < 0 || value > 3) return GEMM_F16_ERR_INVALID_ARG;
+      if (value >= 2 && p->max_pairs <= 0) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+      if (value == 3 && p->max_quads <= 0) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
       p->kernel = (int)value;
       return GEMM_F16_OK;
     default:
@@ -262,6 +263,7 @@ int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
     case GEMM_F16_OPT_A_REPACK: *value = p->a_repack; return GEMM_F16_OK;
     case GEMM_F16_INFO_NUM_SMS: *value = p->num_sms; return GEMM_F16_OK;
     case GEMM_F16_INFO_MAX_PAIRS: *value = p->max_pairs; return GEMM_F16_OK;
+    case GEMM_F16_INFO_MAX_QUADS: *value = p->max_quads; return GEMM_F16_OK;
     default: return GEMM_F16_ERR_INVALID_ARG;
   }
 }

@@ -314,6 +314,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// 2-D tensor load multicast into the CTAs of `cta_mask` (the same
+// shared-memory offset in each); each destination's bytes are credited to
+// the barrier at the offset of `cluster_bar` in that destination's pair
+// leader.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap,
+                                                    uint32_t cluster_bar, int32_t x, int32_t y,
+                                                    uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(cluster_bar), "h"(cta_mask)
+      : "memory");
+}
+
 // 3-D tensor load into this CTA's shared memory crediting a barrier that
 // may live in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,

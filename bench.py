@@ -84,8 +84,9 @@ def parse_args():
                     help="idle seconds before the warm-up (page protocol: 5)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2],
-                    help="GEMM: 0 automatic, 1 single-CTA kernel, 2 CTA pair 256x256; "
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="GEMM: 0 automatic, 1 single-CTA kernel, 2 CTA pair 256x256, "
+                         "3 cluster of four (two pairs sharing A); "
                          "attention: 0 automatic, 1 single CTA, 2 CTA pair")
     ap.add_argument("--no-sustained", action="store_true",
                     help="skip the sustained (>= 0.3 s) re-timing of the step")
@@ -845,15 +846,20 @@ def run_ours(args):
 
     plan_sms = plan.get_option(g.INFO_NUM_SMS)
     plan_pairs = plan.get_option(g.INFO_MAX_PAIRS)
-    use_pair = info["kernel"] == 2
-    kernel_desc = ("CTA pair (tcgen05 cta_group::2, 256x256 tiles)" if use_pair
-                   else f"single CTA (tcgen05 cta_group::1, 128x{info['tile_width']} tiles)")
+    plan_quads = plan.get_option(g.INFO_MAX_QUADS)
+    kernel_id = info["kernel"]
+    kernel_desc = {
+        3: "cluster of four (two tcgen05 cta_group::2 pairs sharing A by multicast, "
+           "256x512 cluster tiles)",
+        2: "CTA pair (tcgen05 cta_group::2, 256x256 tiles)",
+    }.get(kernel_id, f"single CTA (tcgen05 cta_group::1, 128x{info['tile_width']} tiles)")
     if info["repack_a"]:
         kernel_desc += "; A repacked to 128-byte-aligned rows first"
     if info["launches"] > 1 + (w.split_k > 1) + info["repack_a"]:
         kernel_desc += "; partial last wave in K halves, merged by a second kernel"
-    roofline["kernel"] = ("gf16::pair::gemm_f16_pair_kernel" if use_pair
-                          else "gf16::gemm_f16_kernel")
+    roofline["kernel"] = {3: "gf16::quad::gemm_f16_quad_kernel",
+                          2: "gf16::pair::gemm_f16_pair_kernel"}.get(kernel_id,
+                                                                    "gf16::gemm_f16_kernel")
     roofline["launches_per_step"] = launches_per_step
     plan.close()
     if rank == 0:
@@ -864,6 +870,7 @@ def run_ours(args):
             "dtype": "f16", "data": "synthetic",
             "config": dict(workload_config(w), kernel=kernel_desc,
                            sms=plan_sms, max_pairs=plan_pairs,
+                           max_quads=plan_quads,
                            submission=(f"CUDA graph of {gsteps} steps, replayed"
                                        if graph is not None else "one host call per step")),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

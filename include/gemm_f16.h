@@ -79,12 +79,25 @@ typedef enum gemm_f16_option {
     GEMM_F16_OPT_FAULT_UNIT = 3,
     /* Which kernel runs the product: 0 = automatic (the CTA-pair kernel when
      * M > 128 and ceil(M/256) * ceil(N/256) * split_k is at least half the
-     * number of co-resident pairs, else the single-CTA kernel),
+     * number of co-resident pairs, else the single-CTA kernel; in place of
+     * the pair kernel the cluster-of-four kernel, without a repack of A,
+     * when A and B are row-major, A's row pitch is not a multiple of 128
+     * bytes, N >= 2048, A has at least 2^22 elements, GEMM_F16_OPT_A_REPACK
+     * is not 2 and its waves of 36 clusters are no more than the pair
+     * kernel's waves),
      * 1 = single-CTA kernel (128-row tiles, tcgen05 cta_group::1),
      * 2 = CTA-pair kernel with 256-row x 256-column tiles (two TMEM
      * accumulators, epilogue overlapped; with one split a partial last wave
      * runs as K halves merged by a second kernel, see gemm_f16_pair_tiles,
-     * or as 128-wide tiles).  Any other value is GEMM_F16_ERR_INVALID_ARG.
+     * or as 128-wide tiles), 3 = cluster-of-four kernel: two CTA pairs
+     * compute a 256 x 512 cluster tile, each 256 x 256 half as in kernel 2,
+     * and share their A rows through multicast copies (each CTA fetches
+     * half of the A rows it shares with its counterpart in the other
+     * pair), so an SM fetches a quarter fewer bytes per MMA; row-major A
+     * and B only (other layouts run kernel 2), no K-halves tail, 36 clusters
+     * of four on 152 SMs (GEMM_F16_INFO_MAX_QUADS).  Any other value is
+     * GEMM_F16_ERR_INVALID_ARG; 3 without clusters of four (or 2 and 3
+     * without pairs) is GEMM_F16_ERR_UNSUPPORTED_DEVICE.
      * Results agree within the usual tolerance; split results are bitwise
      * reproducible for a fixed choice. */
     GEMM_F16_OPT_KERNEL = 4,
@@ -120,8 +133,9 @@ typedef enum gemm_f16_option {
     GEMM_F16_OPT_ATTN_SPLIT = 8,
     /* Repack of A when its row pitch (lda * 2 bytes) is not a multiple of
      * 128 bytes: 0 = automatic (for the CTA-pair kernel when N >= 2048 and
-     * A has at least 2^22 elements), 1 = never, 2 = whenever the pitch is
-     * off.  A 128-byte row of an operand copy from such a matrix touches two
+     * A has at least 2^22 elements; not for the cluster-of-four kernel,
+     * which fetches half as many A rows per SM), 1 = never, 2 = whenever
+     * the pitch is off.  A 128-byte row of an operand copy from such a matrix touches two
      * cache lines, which slows the copies that feed the MMAs (4000 x 4104 x
      * 3000 with lda = 3000: ~20 % longer than with lda = 3008); the repack
      * copies A once into plan-owned rows of whole lines (grown on the
@@ -206,7 +220,7 @@ int gemm_f16_run_ex(gemm_f16_plan_t plan, int layout, int M, int N, int K,
 /*
  * What gemm_f16_run_ex would enqueue for these sizes with the plan's current
  * options, without enqueuing anything (host only):
- *   info[0]  kernel: 1 single-CTA, 2 CTA pair;
+ *   info[0]  kernel: 1 single-CTA, 2 CTA pair, 3 cluster of four;
  *   info[1]  kernel launches per call: the product, plus one for the split
  *            reduction when split_k > 1, plus one for the repack of A, plus
  *            one for merging the K halves of a partial last wave of pair
@@ -258,7 +272,8 @@ int gemm_f16_set_option(gemm_f16_plan_t plan, int option, int64_t value);
 /* Read-only plan facts for gemm_f16_get_option. */
 enum {
     GEMM_F16_INFO_NUM_SMS = 100,   /* SMs of the plan's device */
-    GEMM_F16_INFO_MAX_PAIRS = 101  /* co-resident CTA pairs of the pair kernel (0: unavailable) */
+    GEMM_F16_INFO_MAX_PAIRS = 101, /* co-resident CTA pairs of the pair kernel (0: unavailable) */
+    GEMM_F16_INFO_MAX_QUADS = 102  /* co-resident clusters of four of kernel 3 (0: unavailable) */
 };
 
 /* Read an option's current value, or one of the GEMM_F16_INFO_* facts. */

@@ -18,10 +18,11 @@ from tests import gpu_util, oracle_cache, parity
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[1, 2], ids=["cta1", "pair256"])
+@pytest.fixture(scope="module", params=[1, 2, 3], ids=["cta1", "pair256", "quad"])
 def plan(request):
     """A plan pinned to one kernel: 1 = single-CTA, 2 = CTA pair with
-    256-wide tiles.  Every test in this file runs once per kernel."""
+    256-wide tiles, 3 = two CTA pairs in a cluster of four sharing A by
+    multicast.  Every test in this file runs once per kernel."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no GPU")

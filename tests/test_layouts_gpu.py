@@ -23,9 +23,10 @@ LAYOUTS = [0, 1, 2, 3]
 LAYOUT_IDS = ["NN", "TN", "NT", "TT"]
 
 
-@pytest.fixture(scope="module", params=[1, 2], ids=["cta1", "pair256"])
+@pytest.fixture(scope="module", params=[1, 2, 3], ids=["cta1", "pair256", "quad"])
 def plan(request):
-    """A plan pinned to the single-CTA kernel (1) or the CTA-pair kernel (2)."""
+    """A plan pinned to the single-CTA kernel (1), the CTA-pair kernel (2) or
+    the cluster-of-four kernel (3; row-major layouts only, others run 2)."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no GPU")

@@ -21,7 +21,7 @@ from tests import gpu_util, oracle_cache, parity
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[1, 2], ids=["cta1", "pair256"])
+@pytest.fixture(scope="module", params=[1, 2, 3], ids=["cta1", "pair256", "quad"])
 def plan(request):
     import torch
     if not torch.cuda.is_available():

@@ -23,7 +23,7 @@ def _f16(x):
     return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
 
 
-@pytest.mark.parametrize("kernel", [1, 2], ids=["cta1", "pair256"])
+@pytest.mark.parametrize("kernel", [1, 2, 3], ids=["cta1", "pair256", "quad"])
 def test_bounded_wait_reports_timeout_and_context_survives(kernel):
     import torch
     if not torch.cuda.is_available():
