@@ -21,7 +21,8 @@ LIB_PATH = os.path.join(LIB_DIR, "libgemm_f16.so")
 
 SOURCES = [os.path.join(CSRC, f) for f in ("plan.cu", "gemm_f16.cu", "attn_f16.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("host.h", "ptx.cuh", "schedule.h", "common.cuh",
-                                            "gemm_pair.cuh", "attn_f16.cuh", "attn_pair.cuh")]
+                                            "gemm_pair.cuh", "gemm_quad.cuh", "attn_f16.cuh",
+                                            "attn_pair.cuh")]
 DEPENDS = SOURCES + HEADERS + [os.path.join(INCLUDE, "gemm_f16.h"),
                                os.path.join(INCLUDE, "attn_f16.h")]
 

@@ -66,7 +66,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "async_barrier_pipelined_gb300", "csrc", f)
                   for f in ("plan.cu", "gemm_f16.cu", "attn_f16.cu", "host.h", "common.cuh",
                             "gemm_pair.cuh", "ptx.cuh", "schedule.h", "attn_f16.cuh",
-                            "attn_pair.cuh")]
+                            "attn_pair.cuh", "gemm_quad.cuh")]
 SUSTAINED_S = 0.3
 
 
