@@ -85,9 +85,10 @@ struct MBar {
 // Runs NROLES role threads one at a time.  A role gives the token back at
 // every yield point and when it blocks in wait_until; the scheduler then
 // picks, with its seeded generator, one runnable role, one pending copy
-// completion (any order) or the oldest pending tensor-core completion (in
-// issue order).  No runnable choice left while roles are unfinished is a
-// deadlock.
+// completion (any order) or the oldest pending completion of a tensor core
+// (in issue order; two independent tensor cores, `tc_queue` and
+// `tc_queue_b`, for kernels with two MMA issuers).  No runnable choice left
+// while roles are unfinished is a deadlock.
 class Scheduler {
  public:
   struct Copy {
@@ -99,6 +100,7 @@ class Scheduler {
   void seed(uint64_t s) { rng_.seed(s); }
   std::vector<Copy> copies;
   std::deque<std::function<void()>> tc_queue;
+  std::deque<std::function<void()>> tc_queue_b;
 
   void role_yield(int r) {
     std::unique_lock<std::mutex> lk(mu_);
@@ -133,11 +135,12 @@ class Scheduler {
     while (true) {
       std::unique_lock<std::mutex> lk(mu_);
       cv_.wait(lk, [&] { return turn_ == -1; });
-      std::vector<int> choices;  // role r, nroles + i = copy i, -2 = tensor core
+      std::vector<int> choices;  // role r, nroles + i = copy i, -2 / -3 = tensor core a / b
       for (int r = 0; r < nroles_; ++r)
         if (!done_[r] && (!waiting_[r] || waiting_[r]())) choices.push_back(r);
       for (size_t i = 0; i < copies.size(); ++i) choices.push_back(nroles_ + (int)i);
       if (!tc_queue.empty()) choices.push_back(-2);
+      if (!tc_queue_b.empty()) choices.push_back(-3);
       bool all_done = true;
       for (int r = 0; r < nroles_; ++r) all_done = all_done && done_[r];
       if (choices.empty()) {
@@ -153,6 +156,10 @@ class Scheduler {
       if (c == -2) {
         auto f = tc_queue.front();
         tc_queue.pop_front();
+        f();
+      } else if (c == -3) {
+        auto f = tc_queue_b.front();
+        tc_queue_b.pop_front();
         f();
       } else if (c >= nroles_) {
         auto f = copies[c - nroles_].land;

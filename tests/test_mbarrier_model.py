@@ -10,7 +10,10 @@ over several items (copy ring, Q reloads, S / P / O hand-over between the
 MMA thread, the softmax warps and the epilogue warps of both CTAs, the
 peer's signalling copies) and also checks that every parity wait returns
 with exactly the phase it waited for; planted mistakes (a wait left out)
-must make it fail.
+must make it fail.  quad_model.cpp replays the cluster-of-four GEMM
+kernel (two CTA pairs multicasting A halves into each other's shared
+memory, stages released by both pairs' commits) with its abort drains;
+planted mistakes there must fail too.
 """
 from __future__ import annotations
 
@@ -24,11 +27,13 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "mbarrier_model", "model.cpp")
 PAIR_SRC = os.path.join(HERE, "mbarrier_model", "pair_model.cpp")
 ATTN_SRC = os.path.join(HERE, "mbarrier_model", "attn_pair_model.cpp")
+QUAD_SRC = os.path.join(HERE, "mbarrier_model", "quad_model.cpp")
 CSRC = os.path.join(os.path.dirname(HERE), "async_barrier_pipelined_gb300", "csrc")
 BUILD = os.path.join(HERE, "mbarrier_model", "_build")
 EXE = os.path.join(BUILD, "model")
 PAIR_EXE = os.path.join(BUILD, "pair_model")
 ATTN_EXE = os.path.join(BUILD, "attn_pair_model")
+QUAD_EXE = os.path.join(BUILD, "quad_model")
 
 
 def _build(src, exe, defines=()):
@@ -58,6 +63,11 @@ def pair_model():
 @pytest.fixture(scope="module")
 def attn_model():
     return _build(ATTN_SRC, ATTN_EXE)
+
+
+@pytest.fixture(scope="module")
+def quad_model():
+    return _build(QUAD_SRC, QUAD_EXE)
 
 
 def _run(exe, *args):
@@ -175,5 +185,62 @@ def test_attention_pair_fault_blocks_the_mma_on_the_starved_fill(attn_model):
 ])
 def test_attention_pair_model_catches_planted_mistakes(plant, case, expect):
     exe = _build(ATTN_SRC, ATTN_EXE + "_" + plant.lower(), defines=(plant,))
+    rc, out = _run(exe, *case)
+    assert rc != 0 and expect in out, out
+
+
+# Cluster-of-four protocol: (stages, units, clusters, cluster, split_k,
+# kblocks, seeds, mode[, args])
+QUAD_CASES = [
+    (6, 144, 36, 0, 1, 47, 10, "normal"),     # ragged 4000 x 4104 x 3000: 16 x 9 cluster tiles
+    (6, 144, 36, 35, 1, 47, 10, "normal"),    # ... last cluster
+    (6, 128, 36, 20, 1, 64, 10, "normal"),    # 4096^3: 16 x 8 cluster tiles
+    (6, 32, 36, 3, 16, 512, 4, "normal"),     # 512 x 512 x 32768, 16 splits
+    (2, 9, 4, 1, 3, 7, 50, "normal"),         # uneven split ranges
+    (1, 5, 2, 0, 1, 3, 50, "normal"),         # one stage
+    (6, 3, 1, 0, 1, 1, 50, "normal"),         # one k-block per unit
+]
+
+
+@pytest.mark.parametrize("case", QUAD_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_quad_protocol_interleavings(quad_model, case):
+    rc, out = _run(quad_model, *case)
+    assert rc == 0 and out.startswith("OK") and "deadlocks=0" in out, out
+
+
+@pytest.mark.parametrize("case", [
+    (6, 8, 2, 0, 1, 4, 50, "fault", 2),           # CTA 0 skips one fill's copies
+    (6, 8, 2, 0, 1, 9, 50, "fault", 0),
+    (6, 8, 2, 0, 1, 20, 50, "stop", 0, 5),        # a pair leader's producer times out
+    (3, 8, 2, 0, 1, 20, 50, "stop", 1, 0),        # a pair peer's
+    (6, 8, 2, 0, 1, 20, 50, "stop", 2, 7),        # the other pair's leader
+    (3, 8, 2, 0, 1, 20, 50, "stop", 3, 4),        # the other pair's peer
+    (4, 8, 1, 0, 2, 20, 50, "stop", 3, 13),
+], ids=lambda c: "-".join(map(str, c)))
+def test_quad_abort_drains_complete_issued_phases(quad_model, case):
+    """Every seed deadlocks (the state the kernel's bounded waits escape);
+    both leaders' drains then complete every phase whose copies were issued,
+    and only the faulted fill (whose bytes never come, in both pairs) stays
+    open."""
+    rc, out = _run(quad_model, *case)
+    seeds = case[6]
+    assert rc == 0 and out.startswith("OK") and f"deadlocks={seeds}" in out, out
+
+
+def test_quad_fault_on_other_cluster_does_not_affect_this_one(quad_model):
+    rc, out = _run(quad_model, 6, 8, 2, 1, 1, 4, 20, "fault", 2)
+    assert rc == 0 and "deadlocks=0" in out, out
+
+
+@pytest.mark.parametrize("plant,case,expect", [
+    # each leader's commit releases only its own pair's stages: the other
+    # pair's producers multicast into a stage still being read
+    ("PLANT_OWN_PAIR_RELEASE", (2, 6, 1, 0, 1, 8, 300, "normal"), "still being read"),
+    # a leader's drain forgets the other pair's A halves
+    ("PLANT_DRAIN_OWN_PAIR_ONLY", (6, 8, 2, 0, 1, 20, 100, "stop", 2, 7), "incomplete"),
+    ("PLANT_DRAIN_OWN_PAIR_ONLY", (6, 8, 2, 0, 1, 20, 100, "stop", 0, 5), "incomplete"),
+])
+def test_quad_model_catches_planted_mistakes(plant, case, expect):
+    exe = _build(QUAD_SRC, QUAD_EXE + "_" + plant.lower(), defines=(plant,))
     rc, out = _run(exe, *case)
     assert rc != 0 and expect in out, out
