@@ -143,3 +143,43 @@ def test_run_info_reports_the_launches(plan):
         g.gemm_f16_run_info(h, 0, 128, 128, 128, 100)   # lda < K
     with pytest.raises(g.GemmError):
         g.gemm_f16_run_info(h, 4, 128, 128, 128, 128)
+
+
+def test_automatic_choice_for_an_off_line_a():
+    """The automatic kernel choice for large products whose A rows are off
+    128-byte lines: the cluster-of-four kernel on A as it lies when its
+    waves of clusters are no more than the pair kernel's waves, else the
+    pair kernel after a repack of A; whole-line A keeps the pair kernel.
+    The expectations follow the documented rule from the plan's own cluster
+    counts, and every product is checked on every element."""
+    import math
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import async_barrier_pipelined_gb300 as g
+    from async_barrier_pipelined_gb300 import build
+    build.build()
+    with g.Plan(0) as plan:
+        pairs = plan.get_option(g.INFO_MAX_PAIRS)
+        quads = plan.get_option(g.INFO_MAX_QUADS)
+        if pairs <= 0 or quads <= 0:
+            pytest.skip("no clusters of two or four on this device")
+        for M, N, K, lda in [(4000, 4104, 3000, 3000), (4864, 2048, 1000, 1000),
+                             (2048, 2048, 2048, 2048)]:
+            tm = math.ceil(M / 256)
+            off_line = (lda * 2) % 128 != 0
+            quad_ok = math.ceil(tm * math.ceil(N / 512) / quads) <= math.ceil(tm * math.ceil(N / 256) / pairs)
+            want_quad = off_line and quad_ok
+            info = g.gemm_f16_run_info(plan.handle, 0, M, N, K, lda)
+            assert info["kernel"] == (3 if want_quad else 2), (M, N, K, info)
+            assert info["repack_a"] == (off_line and not want_quad), (M, N, K, info)
+            if (M, N, K) == (4000, 4104, 3000):
+                A, B = oracle_cache.gemm_inputs("gemm_ragged")
+                want = oracle_cache.gemm_ref("gemm_ragged")
+            else:
+                w = si.custom(M, N, K, seed=M + N + K)
+                A, B = w.pair_bits(0)
+                want = oracle.gemm_f16(A, B)
+            c, full = gpu_util.run(plan, A, B, lda=lda, guard_rows=1)
+            gpu_util.assert_untouched_outside(full, M, N)
+            parity.check(c, want, f"automatic choice {M}x{N}x{K} lda={lda}")
