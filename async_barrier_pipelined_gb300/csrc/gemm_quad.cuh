@@ -197,11 +197,13 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
                                               const Bars& b, uint32_t warp, uint32_t lane,
                                               volatile int* abort_flag) {
   const uint32_t quarter = warp & 3u;
-  const uint32_t stage0 = base + OFF_EPI + (warp - EPI_WARP0) * 2 * EPI_BUF;
-  const uint32_t row_off = lane * 64u;
-  const uint32_t sw = (lane >> 1) & 3u;
+  pair::EpiStore st;
+  st.stage0 = base + OFF_EPI + (warp - EPI_WARP0) * 2 * EPI_BUF;
+  st.row_off = lane * 64u;
+  st.sw = (lane >> 1) & 3u;
+  st.nstore = 0;
   const uint32_t leader_tempty = ptx::map_to_cta(b.tempty, rank & ~1u);
-  uint32_t local = 0, nstore = 0;
+  uint32_t local = 0;
   for (int u = (int)cl; u < p.num_units; u += (int)ncl) {
     const UnitGeom g = quad_geom(p, u, rank);
     const uint32_t acc = local & 1u;
@@ -219,56 +221,9 @@ __device__ __forceinline__ void epilogue_role(const CUtensorMap* tmC, const CUte
         ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)c * 32u, r);
         ptx::tmem_ld_wait();
         ptx::reg_fence(r);
-        if (p.split_k == 1 && col0 + 32 > p.N && (p.N & 7) != 0) {
-          // ragged last chunk of an N that is not 16-byte aligned: masked stores
-          const int row = row0 + (int)lane;
-          if (row < p.M) {
-            __half* dst = p.C + (int64_t)row * p.ldc + col0;
-            const int nvalid = p.N - col0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nvalid) dst[j] = __float2half_rn(__uint_as_float(r[j]));
-          }
-        } else if (p.split_k == 1) {
-          const uint32_t buf = stage0 + (nstore & 1u) * EPI_BUF;
-          if (lane == 0) ptx::bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (uint32_t j = 0; j < 4; ++j) {
-            ptx::st_shared_v4(buf + row_off + ((j ^ sw) << 4),
-                              pair::pack_h2(r[8 * j + 0], r[8 * j + 1]),
-                              pair::pack_h2(r[8 * j + 2], r[8 * j + 3]),
-                              pair::pack_h2(r[8 * j + 4], r[8 * j + 5]),
-                              pair::pack_h2(r[8 * j + 6], r[8 * j + 7]));
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_2d(tmC, buf, col0, row0);
-            ptx::bulk_commit_group();
-          }
-          ++nstore;
-        } else {
-#pragma unroll
-          for (uint32_t h = 0; h < 2; ++h) {
-            if (col0 + 16 * (int)h >= p.N) break;
-            const uint32_t buf = stage0 + (nstore & 1u) * EPI_BUF;
-            if (lane == 0) ptx::bulk_wait_group_read<1>();
-            __syncwarp();
-#pragma unroll
-            for (uint32_t j = 0; j < 4; ++j) {
-              const uint32_t* v = &r[16 * h + 4 * j];
-              ptx::st_shared_v4(buf + row_off + ((j ^ sw) << 4), v[0], v[1], v[2], v[3]);
-            }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              ptx::tma_store_3d(tmW, buf, col0 + 16 * (int)h, row0, g.split);
-              ptx::bulk_commit_group();
-            }
-            ++nstore;
-          }
-        }
+        // C (FP16), or a split's FP32 partial at [split][row][column]
+        pair::store_chunk(tmC, tmW, p, r, row0, col0, p.split_k > 1, col0, row0, g.split, lane,
+                          st);
       }
     }
     ptx::tc_fence_before();
