@@ -142,7 +142,8 @@ def test_attn_4096_full(plan):
     import torch
     import async_barrier_pipelined_gb300 as g
     Qb, Kb, Vb = oracle_cache.attn_inputs("attn_4096")
-    Q, K, V = (torch.from_numpy(x.view(np.float16)).cuda() for x in (Qb, Kb, Vb))
+    # the cached inputs are read-only arrays: copy before handing them to torch
+    Q, K, V = (torch.from_numpy(x.view(np.float16).copy()).cuda() for x in (Qb, Kb, Vb))
     O = g.attention(plan, Q, K, V)
     torch.cuda.synchronize()
     assert plan.status() == g.OK
