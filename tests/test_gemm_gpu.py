@@ -325,3 +325,36 @@ def test_tail_k_halves_exact_and_repeatable(plan, shape):
     parity.check(outs[0], oracle.gemm_f16(A, B), f"tail halves {shape}")
     for o in outs[1:]:
         assert np.array_equal(o.view(np.uint64), outs[0].view(np.uint64))
+
+
+def _random_cases(n, seed):
+    """Seeded random products: sizes from 1 up to ~1300 (several tiles of
+    every kernel, with ragged edges), K up to ~2300, split_k up to 6, and
+    operand / output strides padded by 0-120 elements (multiples of 8)."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        M = int(rng.integers(1, 1300))
+        N = int(rng.integers(1, 1300))
+        K = int(rng.integers(1, 2300))
+        kb = (K + 63) // 64
+        split = int(rng.integers(1, min(6, kb) + 1))
+        pad = [int(rng.integers(0, 16)) * 8 for _ in range(3)]
+        cases.append((M, N, K, split, pad))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(24, 2024),
+                         ids=lambda c: "x".join(map(str, c[:4])) + "-p" + "_".join(map(str, c[4])))
+def test_random_shapes_against_oracle(plan, case):
+    """Random shapes, splits and padded strides, every element against the
+    oracle, with NaN sentinels around C and in the operands' padding."""
+    M, N, K, split, (pa, pb, pc) = case
+    w = si.custom(M, N, K, seed=M * 7 + N * 13 + K)
+    A, B = w.pair_bits(0)
+    lda = (K + 7) // 8 * 8 + pa
+    ldb = (N + 7) // 8 * 8 + pb
+    ldc = (N + 7) // 8 * 8 + pc
+    c, full = gpu_util.run(plan, A, B, split_k=split, lda=lda, ldb=ldb, ldc=ldc, guard_rows=1)
+    gpu_util.assert_untouched_outside(full, M, N)
+    parity.check(c, oracle.gemm_f16(A, B), f"random {case}")
