@@ -108,8 +108,9 @@ typedef enum gemm_f16_option {
      * the usual tolerance. */
     GEMM_F16_OPT_TILE_WIDTH = 5,
     /* Most SMs one launch may occupy (0 = all of them), e.g. to leave SMs
-     * to work on other streams.  The tile schedules are planned for the
-     * full device either way.  Also bounds the persistent CTA-pair
+     * to work on other streams; the cluster kernels still run one cluster
+     * (2 or 4 SMs) when the limit is below that.  The tile schedules are
+     * planned for the full device either way.  Also bounds the persistent CTA-pair
      * attention kernel (one cluster of two CTAs per two SMs); the
      * single-CTA attention kernel launches one CTA per 128 query rows and
      * ignores it. */
