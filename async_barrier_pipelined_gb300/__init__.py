@@ -27,7 +27,7 @@ __all__ = [
     "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "OPT_ATTN_KERNEL", "OPT_ATTN_SPLIT", "OPT_A_REPACK", "INFO_NUM_SMS", "INFO_MAX_PAIRS", "INFO_MAX_QUADS",
     "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
     "gemm_f16_run_ex", "gemm_f16_validate_ex", "attn_f16_fwd", "attn_f16_validate",
-    "attn_f16_key_ranges", "gemm_f16_run_info", "attn_f16_fwd_host", "attention_host",
+    "attn_f16_key_ranges", "gemm_f16_run_info", "gemm_f16_run_choice", "attn_f16_fwd_host", "attention_host",
     "attention", "ATTN_HEAD_DIM",
     "LAYOUT_NN", "LAYOUT_TN", "LAYOUT_NT", "LAYOUT_TT",
 ]
@@ -103,6 +103,8 @@ _SIGNATURES = {
                                      ctypes.POINTER(_c_int)]),
     "gemm_f16_run_info": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int,
                                    ctypes.POINTER(_c_int)]),
+    "gemm_f16_run_choice": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int,
+                                     _c_int, _c_int, ctypes.POINTER(_c_int)]),
     "attn_f16_fwd_host": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                    _vp, ctypes.c_float, _vp]),
 }
@@ -266,6 +268,17 @@ def gemm_f16_run_info(plan: int, layout: int, M: int, N: int, K: int, lda: int,
     info = (_c_int * 4)()
     _check(load().gemm_f16_run_info(plan, layout, M, N, K, lda, split_k, info),
            "gemm_f16_run_info")
+    return {"kernel": info[0], "launches": info[1], "repack_a": bool(info[2]),
+            "tile_width": info[3]}
+
+
+def gemm_f16_run_choice(layout: int, M: int, N: int, K: int, lda: int, split_k: int = 1,
+                        num_sms: int = 152, max_pairs: int = 76, max_quads: int = 36) -> dict:
+    """gemm_f16_run_info for default options on a device with these facts
+    (host only; the defaults are a GB300's)."""
+    info = (_c_int * 4)()
+    _check(load().gemm_f16_run_choice(layout, M, N, K, lda, split_k, num_sms, max_pairs,
+                                      max_quads, info), "gemm_f16_run_choice")
     return {"kernel": info[0], "launches": info[1], "repack_a": bool(info[2]),
             "tile_width": info[3]}
 

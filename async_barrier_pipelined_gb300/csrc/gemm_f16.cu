@@ -1260,6 +1260,27 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
   return GEMM_F16_OK;
 }
 
+// What a run of these sizes would enqueue with the plan's options and
+// device facts (gemm_f16_run_info, gemm_f16_run_choice).
+int run_info_impl(const gemm_f16_plan_s* p, int layout, int M, int N, int K, int64_t lda,
+                  int split_k, int info[4]) {
+  if (!info || M <= 0 || N <= 0 || K <= 0 || split_k < 1 || layout < 0 || layout > 3 ||
+      lda < ((layout & LAYOUT_AT) ? M : K))
+    return GEMM_F16_ERR_INVALID_ARG;
+  const RunChoice c = choose_run(p, layout, M, N, K, lda, split_k);
+  // a partial last wave of 256-wide pair tiles in K halves adds their merge
+  int parts = 1;
+  if (c.use_pair && !c.use_quad && split_k == 1) {
+    std::vector<uint32_t> tiles;
+    build_pair_tiles(M, N, (int)ceil_div(K, BK), p->max_pairs, split_k, p->tile_order, tiles, &parts);
+  }
+  info[0] = c.use_quad ? 3 : c.use_pair ? 2 : 1;
+  info[1] = 1 + (split_k > 1 ? 1 : 0) + (c.pack_a ? 1 : 0) + (parts > 1 ? 1 : 0);
+  info[2] = c.pack_a ? 1 : 0;
+  info[3] = c.use_pair ? pair::WIDE : c.bn;
+  return GEMM_F16_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1286,21 +1307,20 @@ int gemm_f16_run_ex(gemm_f16_plan_t p, int layout, int M, int N, int K, const vo
 
 int gemm_f16_run_info(gemm_f16_plan_t p, int layout, int M, int N, int K, int64_t lda,
                       int split_k, int info[4]) {
-  if (!p || !info || M <= 0 || N <= 0 || K <= 0 || split_k < 1 || layout < 0 || layout > 3 ||
-      lda < ((layout & LAYOUT_AT) ? M : K))
+  if (!p) return GEMM_F16_ERR_INVALID_ARG;
+  return run_info_impl(p, layout, M, N, K, lda, split_k, info);
+}
+
+int gemm_f16_run_choice(int layout, int M, int N, int K, int64_t lda, int split_k, int num_sms,
+                        int max_pairs, int max_quads, int info[4]) {
+  if (num_sms < 1 || max_pairs < 0 || max_quads < 0 || 2 * max_pairs > num_sms ||
+      4 * max_quads > num_sms)
     return GEMM_F16_ERR_INVALID_ARG;
-  const RunChoice c = choose_run(p, layout, M, N, K, lda, split_k);
-  // a partial last wave of 256-wide pair tiles in K halves adds their merge
-  int parts = 1;
-  if (c.use_pair && !c.use_quad && split_k == 1) {
-    std::vector<uint32_t> tiles;
-    build_pair_tiles(M, N, (int)ceil_div(K, BK), p->max_pairs, split_k, p->tile_order, tiles, &parts);
-  }
-  info[0] = c.use_quad ? 3 : c.use_pair ? 2 : 1;
-  info[1] = 1 + (split_k > 1 ? 1 : 0) + (c.pack_a ? 1 : 0) + (parts > 1 ? 1 : 0);
-  info[2] = c.pack_a ? 1 : 0;
-  info[3] = c.use_pair ? pair::WIDE : c.bn;
-  return GEMM_F16_OK;
+  gemm_f16_plan_s facts;  // default options; only the device facts are set
+  facts.num_sms = num_sms;
+  facts.max_pairs = max_pairs;
+  facts.max_quads = max_quads;
+  return run_info_impl(&facts, layout, M, N, K, lda, split_k, info);
 }
 
 int gemm_f16_run_host(gemm_f16_plan_t p, int M, int N, int K, const void* hA, int64_t lda,

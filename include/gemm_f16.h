@@ -287,6 +287,19 @@ const char *gemm_f16_strerror(int code);
 const char *gemm_f16_last_cuda_error(void);
 
 /*
+ * Host-only: what gemm_f16_run_info would report for a plan with default
+ * options (automatic kernel, tile width and repack; Morton order) on a device
+ * with `num_sms` SMs, `max_pairs` co-resident clusters of two and
+ * `max_quads` of four (GEMM_F16_INFO_NUM_SMS / _MAX_PAIRS / _MAX_QUADS of a
+ * plan; 152, 76 and 36 on a GB300), so that the automatic choice can be
+ * checked without a GPU.  Returns GEMM_F16_OK, or GEMM_F16_ERR_INVALID_ARG
+ * for the arguments gemm_f16_run_info rejects, num_sms < 1, negative counts
+ * or more clusters than the SMs hold.
+ */
+int gemm_f16_run_choice(int layout, int M, int N, int K, int64_t lda, int split_k,
+                        int num_sms, int max_pairs, int max_quads, int info[4]);
+
+/*
  * Host-only argument check used by gemm_f16_run (no device needed):
  * returns GEMM_F16_OK, GEMM_F16_ERR_INVALID_ARG or GEMM_F16_ERR_MISALIGNED.
  */

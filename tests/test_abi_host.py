@@ -292,3 +292,48 @@ def test_pair_tail_halves_rule(lib, tiles, kblocks, want):
     assert parts == want
     # never with a split
     assert g.gemm_f16_pair_tiles(M, N, 76, 2, K=64 * kblocks, with_parts=True)[1] == 1
+
+
+@pytest.mark.parametrize("args,want", [
+    # the benchmark's workloads on a GB300 (152 SMs, 76 pairs, 36 clusters of four)
+    ((0, 256, 256, 256, 256, 1), (1, 1, False, 64)),         # single CTA, 64-wide tiles
+    ((0, 1024, 1024, 1024, 1024, 1), (1, 1, False, 64)),
+    ((0, 4096, 4096, 4096, 4096, 1), (2, 2, False, 256)),    # pair + K-halves merge
+    ((0, 4000, 4104, 3000, 3000, 1), (3, 1, False, 256)),    # off-line A: cluster of four
+    ((0, 512, 512, 32768, 32768, 16), (2, 2, False, 256)),   # pair + split reduction
+    # the same ragged product with whole-line A rows: the pair kernel
+    ((0, 4000, 4104, 3000, 3008, 1), (2, 1, False, 256)),
+    # off-line A, but clusters of four would take more waves (3 of 36 vs 2 of 76)
+    ((0, 4864, 2048, 1000, 1000, 1), (2, 2, True, 256)),
+    # off-line A stored transposed: only the pair kernel, after a repack
+    ((1, 4000, 4104, 3000, 4000, 1), (2, 2, True, 256)),
+    # off-line A on a product too small for either
+    ((0, 1000, 1000, 1000, 1000, 1), (1, 1, False, 64)),
+])
+def test_automatic_choice_on_a_gb300(lib, args, want):
+    """The automatic kernel choice, pinned for the benchmark's workloads and
+    the boundaries of the off-line-A rule, without a GPU."""
+    info = g.gemm_f16_run_choice(*args)
+    assert (info["kernel"], info["launches"], info["repack_a"], info["tile_width"]) == want
+
+
+def test_automatic_choice_follows_the_device_facts(lib):
+    ragged = (0, 4000, 4104, 3000, 3000, 1)
+    # no clusters of four: the pair kernel after a repack of A
+    info = g.gemm_f16_run_choice(*ragged, num_sms=152, max_pairs=76, max_quads=0)
+    assert info["kernel"] == 2 and info["repack_a"] and info["launches"] == 2
+    # fewer SMs: still 4 waves either way, clusters of four
+    info = g.gemm_f16_run_choice(*ragged, num_sms=148, max_pairs=74, max_quads=36)
+    assert info["kernel"] == 3 and not info["repack_a"]
+    # no pairs at all: the single-CTA kernel
+    info = g.gemm_f16_run_choice(0, 4096, 4096, 4096, 4096, 1, num_sms=152, max_pairs=0,
+                                 max_quads=0)
+    assert info["kernel"] == 1
+
+
+@pytest.mark.parametrize("facts", [(0, 0, 0), (152, 77, 36), (152, 76, 39), (152, -1, 0)])
+def test_automatic_choice_rejects_impossible_device_facts(lib, facts):
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_run_choice(0, 256, 256, 256, 256, 1, *facts)
+    with pytest.raises(g.GemmError):     # lda below K, like gemm_f16_run_info
+        g.gemm_f16_run_choice(0, 256, 256, 256, 100, 1)
