@@ -150,9 +150,14 @@ struct Bars {
 };
 
 // Packed (tm, tn) of the tile at position `tpos` of the launch's tile order.
+// With every unit in the first wave (one per CTA) the walk order cannot
+// change what shares L2 at a time, and the quadtree descent (~1 us on one
+// thread, before the first copy of a CTA's only tile) is not worth it: such
+// launches take the row-major order.
 __device__ __forceinline__ uint32_t tile_at(const Params& p, int tpos) {
-  return p.row_major ? pack_tile((uint32_t)tpos / (uint32_t)p.tiles_n, (uint32_t)tpos % (uint32_t)p.tiles_n)
-                     : morton_tile_of_rank((uint32_t)tpos, (uint32_t)p.tiles_m, (uint32_t)p.tiles_n);
+  return (p.row_major || p.num_units <= (int)gridDim.x)
+             ? pack_tile((uint32_t)tpos / (uint32_t)p.tiles_n, (uint32_t)tpos % (uint32_t)p.tiles_n)
+             : morton_tile_of_rank((uint32_t)tpos, (uint32_t)p.tiles_m, (uint32_t)p.tiles_n);
 }
 
 // ------------------------------------------------------------------ waits

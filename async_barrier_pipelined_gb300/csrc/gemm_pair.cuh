@@ -458,9 +458,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   // A dependent launch (the split reduction) may be scheduled now; it waits
   // for this grid's completion before touching the partials.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The work list was written by the host before any launch of this shape,
+  // not by the kernel this one waits for: its first entry for this pair can
+  // be on its way while the wait lasts.
+  if (warp == 0 && lane == 0 && (int)pair < p.num_units) {
+    const int u = (int)pair;
+    int tpos, split;
+    if (u < p.full_units) decode_unit(u, p.split_k, &tpos, &split);
+    else tpos = p.full_units + (u - p.full_units) / p.tail_parts;
+    ptx::prefetch_l1(p.order + tpos);
+  }
   // Launched as a programmatic dependent: everything above (barriers, TMEM,
   // tensor-map prefetch) may overlap the previous kernel's tail; no global
-  // memory is touched before that kernel has completed.
+  // memory written by that kernel is touched before it has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   uint32_t issued = 0;

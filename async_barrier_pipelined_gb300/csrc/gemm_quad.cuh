@@ -319,8 +319,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   // A dependent launch (the split reduction) may be scheduled now; it waits
   // for this grid's completion before touching the partials.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // Launched as a programmatic dependent: no global memory is touched before
-  // the previous kernel has completed.
+  // The tile order was written by the host, not by the kernel this one
+  // waits for: its first entry for this cluster can be on its way meanwhile.
+  if (warp == 0 && lane == 0 && (int)cl < p.num_units) {
+    int tpos, split;
+    decode_unit((int)cl, p.split_k, &tpos, &split);
+    ptx::prefetch_l1(p.order + tpos);
+  }
+  // Launched as a programmatic dependent: no global memory written by the
+  // previous kernel is touched before it has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   uint32_t issued = 0;

@@ -48,15 +48,26 @@ GF16_HD uint32_t consumer_wait_parity(const RingPos& p) { return p.phase; }
 // k-block range [kb0, kb1) of split `s` out of `split_k` over `kblocks`
 // k-blocks: contiguous, non-empty when split_k <= kblocks, and covering
 // [0, kblocks) exactly once over s = 0 .. split_k-1.
+// (A kernel's first unit waits for this on one thread: one split needs no
+// division, and while (s + 1) * kblocks fits in 31 bits a 32-bit division
+// gives the same quotients as the 64-bit one, at a fraction of its cost.)
 GF16_HD void split_range(int kblocks, int split_k, int s, int* kb0, int* kb1) {
-  *kb0 = (int)(((int64_t)s * kblocks) / split_k);
-  *kb1 = (int)(((int64_t)(s + 1) * kblocks) / split_k);
+  if (split_k == 1) {
+    *kb0 = 0;
+    *kb1 = kblocks;
+  } else if (kblocks <= 46340) {  // s < split_k <= kblocks: (s + 1) * kblocks < 2^31
+    *kb0 = (int)((uint32_t)(s * kblocks) / (uint32_t)split_k);
+    *kb1 = (int)((uint32_t)((s + 1) * kblocks) / (uint32_t)split_k);
+  } else {
+    *kb0 = (int)(((int64_t)s * kblocks) / split_k);
+    *kb1 = (int)(((int64_t)(s + 1) * kblocks) / split_k);
+  }
 }
 
 // Work unit u -> (position in the tile order, split index).  The splits of
 // one tile are adjacent units, so they run side by side.
 GF16_HD void decode_unit(int u, int split_k, int* tile_pos, int* split) {
-  *tile_pos = u / split_k;
+  *tile_pos = split_k == 1 ? u : u / split_k;
   *split = u - (*tile_pos) * split_k;
 }
 

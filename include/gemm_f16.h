@@ -70,7 +70,10 @@ typedef enum gemm_f16_option {
     GEMM_F16_OPT_TIMEOUT_NS = 1,
     /* Order in which output tiles are handed to the persistent CTAs:
      * 0 = Morton (Z-order, "Xe2 ESIMD GEMM" page, "Tile walk order"), the
-     * default; 1 = row-major.  Results do not depend on it. */
+     * default; 1 = row-major.  A single-CTA launch whose work units all fit
+     * in one wave (one per CTA, all co-resident, so the order cannot change
+     * what shares the cache at a time) takes row-major order either way.
+     * Results do not depend on it. */
     GEMM_F16_OPT_TILE_ORDER = 2,
     /* TEST ONLY.  If >= 0, the producer of the given work unit expects the
      * bytes of its first stage but issues no copy for it, so that stage's
