@@ -24,11 +24,11 @@ __all__ = [
     "gemm_f16_tile_order", "gemm_f16_tile_shape", "Plan", "matmul",
     "OK", "ERR_INVALID_ARG", "ERR_MISALIGNED", "ERR_UNSUPPORTED_DEVICE",
     "ERR_OOM", "ERR_CUDA", "ERR_TIMEOUT", "ERR_SCRATCH_TOO_SMALL", "gemm_f16_run_noalloc", "gemm_f16_noalloc_status",
-    "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "OPT_ATTN_KERNEL", "OPT_ATTN_SPLIT", "OPT_A_REPACK", "INFO_NUM_SMS", "INFO_MAX_PAIRS", "INFO_MAX_QUADS",
+    "OPT_TIMEOUT_NS", "OPT_TILE_ORDER", "OPT_FAULT_UNIT", "OPT_KERNEL", "OPT_TILE_WIDTH", "OPT_SM_LIMIT", "OPT_ATTN_KERNEL", "OPT_ATTN_SPLIT", "OPT_A_REPACK", "OPT_KERNEL_TIMING", "INFO_NUM_SMS", "INFO_MAX_PAIRS", "INFO_MAX_QUADS",
     "gemm_f16_get_option", "gemm_f16_pair_tiles", "EXPORTED_SYMBOLS",
     "gemm_f16_run_ex", "gemm_f16_validate_ex", "attn_f16_fwd", "attn_f16_validate",
     "attn_f16_key_ranges", "gemm_f16_run_info", "gemm_f16_run_choice", "attn_f16_fwd_host", "attention_host",
-    "attention", "ATTN_HEAD_DIM",
+    "attention", "ATTN_HEAD_DIM", "gemm_f16_kernel_time",
     "LAYOUT_NN", "LAYOUT_TN", "LAYOUT_NT", "LAYOUT_TT",
 ]
 
@@ -50,6 +50,7 @@ OPT_SM_LIMIT = 6
 OPT_ATTN_KERNEL = 7
 OPT_ATTN_SPLIT = 8
 OPT_A_REPACK = 9
+OPT_KERNEL_TIMING = 10
 INFO_NUM_SMS = 100
 INFO_MAX_PAIRS = 101
 INFO_MAX_QUADS = 102
@@ -107,6 +108,7 @@ _SIGNATURES = {
                                      _c_int, _c_int, ctypes.POINTER(_c_int)]),
     "attn_f16_fwd_host": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                    _vp, ctypes.c_float, _vp]),
+    "gemm_f16_kernel_time": (_c_int, [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_c_i64)]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -283,6 +285,16 @@ def gemm_f16_run_choice(layout: int, M: int, N: int, K: int, lda: int, split_k: 
             "tile_width": info[3]}
 
 
+def gemm_f16_kernel_time(plan: int) -> tuple:
+    """(total milliseconds, launches) of the kernels timed since the last
+    read (OPT_KERNEL_TIMING); waits for the recorded events."""
+    ms = ctypes.c_double(0.0)
+    n = _c_i64(0)
+    _check(load().gemm_f16_kernel_time(plan, ctypes.byref(ms), ctypes.byref(n)),
+           "gemm_f16_kernel_time")
+    return ms.value, n.value
+
+
 def attn_f16_key_ranges(plan: int, batch: int, heads: int, seq_q: int, seq_kv: int) -> int:
     """Key ranges attn_f16_fwd would use for these sizes (1: no split)."""
     n = _c_int(0)
@@ -353,6 +365,11 @@ class Plan:
 
     def get_option(self, option: int) -> int:
         return gemm_f16_get_option(self.handle, option)
+
+    def kernel_time(self) -> tuple:
+        """(total milliseconds, launches) of the product / attention kernels
+        timed since the last read (see OPT_KERNEL_TIMING)."""
+        return gemm_f16_kernel_time(self.handle)
 
 
 def _stream_handle(stream) -> int:

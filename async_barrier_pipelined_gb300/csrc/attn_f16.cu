@@ -245,9 +245,13 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
     pdl.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    GF16_CUDA(cudaLaunchKernelEx(&cfg, attnp::attn_f16_fwd_pair_kernel, tmQ, tmK, tmV, tmO, tmP,
-                                 prm),
-              "launch attn_f16_fwd_pair_kernel");
+    cudaEvent_t t0;
+    if ((rc = timing_begin(p, cfg.stream, &t0))) return rc;
+    const cudaError_t le =
+        cudaLaunchKernelEx(&cfg, attnp::attn_f16_fwd_pair_kernel, tmQ, tmK, tmV, tmO, tmP, prm);
+    rc = timing_end(p, cfg.stream, t0, le == cudaSuccess);
+    GF16_CUDA(le, "launch attn_f16_fwd_pair_kernel");
+    if (rc) return rc;
     if (n_split > 1) {
       // One warp per query row of every item.
       cudaLaunchConfig_t ccfg = {};
@@ -283,8 +287,12 @@ int attn_f16_fwd(gemm_f16_plan_t p, int batch, int heads, int seq_q, int seq_kv,
   pdl.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &pdl;
   cfg.numAttrs = 1;
-  GF16_CUDA(cudaLaunchKernelEx(&cfg, attn::attn_f16_fwd_kernel, tmQ, tmK, tmV, tmO, prm),
-            "launch attn_f16_fwd_kernel");
+  cudaEvent_t t0;
+  if ((rc = timing_begin(p, cfg.stream, &t0))) return rc;
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, attn::attn_f16_fwd_kernel, tmQ, tmK, tmV, tmO, prm);
+  rc = timing_end(p, cfg.stream, t0, le == cudaSuccess);
+  GF16_CUDA(le, "launch attn_f16_fwd_kernel");
+  if (rc) return rc;
   return GEMM_F16_OK;
 }
 

@@ -1138,8 +1138,12 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
     void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmC, (void*)&tmW, (void*)&pp};
-    GF16_CUDA(cudaLaunchKernelExC(&cfg, (void*)quad::gemm_f16_quad_kernel, args),
-              "launch gemm_f16_quad_kernel");
+    cudaEvent_t t0;
+    if ((rc = timing_begin(p, stream, &t0))) return rc;
+    const cudaError_t le = cudaLaunchKernelExC(&cfg, (void*)quad::gemm_f16_quad_kernel, args);
+    rc = timing_end(p, stream, t0, le == cudaSuccess);
+    GF16_CUDA(le, "launch gemm_f16_quad_kernel");
+    if (rc) return rc;
   } else if (use_pair) {
     int64_t pair_cap = std::max(p->max_pairs, 1);
     if (p->sm_limit > 0) pair_cap = std::max<int64_t>(1, std::min<int64_t>(pair_cap, p->sm_limit / 2));
@@ -1190,7 +1194,12 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
     void* fn = pick_instance(layout, pair::gemm_f16_pair_kernel<0>, pair::gemm_f16_pair_kernel<1>,
                              pair::gemm_f16_pair_kernel<2>, pair::gemm_f16_pair_kernel<3>);
     void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmC, (void*)&tmW, (void*)&pp};
-    GF16_CUDA(cudaLaunchKernelExC(&cfg, fn, args), "launch gemm_f16_pair_kernel");
+    cudaEvent_t t0;
+    if ((rc = timing_begin(p, stream, &t0))) return rc;
+    const cudaError_t le = cudaLaunchKernelExC(&cfg, fn, args);
+    rc = timing_end(p, stream, t0, le == cudaSuccess);
+    GF16_CUDA(le, "launch gemm_f16_pair_kernel");
+    if (rc) return rc;
     if (tail_tiles > 0) {
       // P0 + P1 of each tail tile into C (a programmatic dependent launch).
       const int64_t groups = tail_tiles * 256 * 64;
@@ -1242,7 +1251,12 @@ int run_device(gemm_f16_plan_s* p, int layout, int M, int N, int K, const void* 
     void* fn = pick_instance(layout, gemm_f16_kernel<0>, gemm_f16_kernel<1>, gemm_f16_kernel<2>,
                              gemm_f16_kernel<3>);
     void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmC, (void*)&tmW, (void*)&prm};
-    GF16_CUDA(cudaLaunchKernelExC(&cfg, fn, args), "launch gemm_f16_kernel");
+    cudaEvent_t t0;
+    if ((rc = timing_begin(p, stream, &t0))) return rc;
+    const cudaError_t le = cudaLaunchKernelExC(&cfg, fn, args);
+    rc = timing_end(p, stream, t0, le == cudaSuccess);
+    GF16_CUDA(le, "launch gemm_f16_kernel");
+    if (rc) return rc;
   }
   }
 

@@ -133,6 +133,11 @@ struct gemm_f16_plan_s {
   int attn_slot = 0;
   gf16::host::TmapEntry tmaps[gf16::host::TMAP_CACHE];
   int tmap_used = 0, tmap_next = 0;
+  // GEMM_F16_OPT_KERNEL_TIMING: recorded (start, end) event pairs around
+  // product / attention kernel launches, and the idle events they reuse.
+  int kernel_timing = 0;
+  std::vector<cudaEvent_t> timing_marks;  // start, end, start, end, ...
+  std::vector<cudaEvent_t> timing_pool;
 };
 
 namespace gf16 {
@@ -147,6 +152,15 @@ void tmap_remember(gemm_f16_plan_s* p, const uint64_t (&key)[8], const CUtensorM
 int cached_encode_2d(gemm_f16_plan_s* p, CUtensorMap* map, CUtensorMapDataType dt, const void* ptr,
                      uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                      uint32_t box_outer, CUtensorMapSwizzle swz, CUtensorMapL2promotion promo);
+
+// Kernel timing records (GEMM_F16_OPT_KERNEL_TIMING).  timing_begin records
+// a start event on `stream` and returns it in *start (nullptr when timing is
+// off, the stream is capturing, or 65536 pairs are waiting); timing_end
+// records the matching end event after a successful launch, or returns the
+// start event to the pool when the launch failed (nothing for a nullptr
+// start).
+int timing_begin(gemm_f16_plan_s* p, cudaStream_t stream, cudaEvent_t* start);
+int timing_end(gemm_f16_plan_s* p, cudaStream_t stream, cudaEvent_t start, bool launched);
 
 // Per-translation-unit parts of gemm_f16_plan / gemm_f16_destroy, called
 // with the plan's device current.  init: kernel attributes and co-resident

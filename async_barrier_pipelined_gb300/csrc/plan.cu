@@ -121,6 +121,59 @@ int cached_encode_2d(gemm_f16_plan_s* p, CUtensorMap* map, CUtensorMapDataType d
   return GEMM_F16_OK;
 }
 
+constexpr size_t MAX_TIMING_PAIRS = 65536;
+
+static int timing_event(gemm_f16_plan_s* p, cudaEvent_t* ev) {
+  if (!p->timing_pool.empty()) {
+    *ev = p->timing_pool.back();
+    p->timing_pool.pop_back();
+    return GEMM_F16_OK;
+  }
+  GF16_CUDA(cudaEventCreate(ev), "cudaEventCreate(kernel timing)");
+  return GEMM_F16_OK;
+}
+
+int timing_begin(gemm_f16_plan_s* p, cudaStream_t stream, cudaEvent_t* start) {
+  *start = nullptr;
+  if (!p->kernel_timing || p->timing_marks.size() >= 2 * MAX_TIMING_PAIRS) return GEMM_F16_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  GF16_CUDA(cudaStreamIsCapturing(stream, &cs), "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone) return GEMM_F16_OK;
+  cudaEvent_t ev;
+  int rc = timing_event(p, &ev);
+  if (rc) return rc;
+  const cudaError_t e = cudaEventRecord(ev, stream);
+  if (e != cudaSuccess) {
+    p->timing_pool.push_back(ev);
+    return cuda_fail(e, "cudaEventRecord(kernel timing)");
+  }
+  *start = ev;
+  return GEMM_F16_OK;
+}
+
+int timing_end(gemm_f16_plan_s* p, cudaStream_t stream, cudaEvent_t start, bool launched) {
+  if (!start) return GEMM_F16_OK;
+  if (!launched) {
+    p->timing_pool.push_back(start);
+    return GEMM_F16_OK;
+  }
+  cudaEvent_t ev;
+  int rc = timing_event(p, &ev);
+  if (rc) {
+    p->timing_pool.push_back(start);
+    return rc;
+  }
+  const cudaError_t e = cudaEventRecord(ev, stream);
+  if (e != cudaSuccess) {
+    p->timing_pool.push_back(start);
+    p->timing_pool.push_back(ev);
+    return cuda_fail(e, "cudaEventRecord(kernel timing)");
+  }
+  p->timing_marks.push_back(start);
+  p->timing_marks.push_back(ev);
+  return GEMM_F16_OK;
+}
+
 }  // namespace host
 }  // namespace gf16
 
@@ -189,6 +242,8 @@ int gemm_f16_destroy(gemm_f16_plan_t p) {
     attn_plan_release(p);
     if (p->ws) cudaFree(p->ws);
     if (p->in_stream) cudaStreamDestroy(p->in_stream);
+    for (cudaEvent_t ev : p->timing_marks) cudaEventDestroy(ev);
+    for (cudaEvent_t ev : p->timing_pool) cudaEventDestroy(ev);
     if (p->status_host) cudaFreeHost(p->status_host);
   }
   delete p;
@@ -238,6 +293,10 @@ int gemm_f16_set_option(gemm_f16_plan_t p, int option, int64_t value) {
       if (value != 0 && value != 64 && value != 128 && value != 256) return GEMM_F16_ERR_INVALID_ARG;
       p->tile_width = (int)value;
       return GEMM_F16_OK;
+    case GEMM_F16_OPT_KERNEL_TIMING:
+      if (value != 0 && value != 1) return GEMM_F16_ERR_INVALID_ARG;
+      p->kernel_timing = (int)value;
+      return GEMM_F16_OK;
     case GEMM_F16_OPT_KERNEL:
       if (value < 0 || value > 3) return GEMM_F16_ERR_INVALID_ARG;
       if (value >= 2 && p->max_pairs <= 0) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
@@ -261,11 +320,40 @@ int gemm_f16_get_option(gemm_f16_plan_t p, int option, int64_t* value) {
     case GEMM_F16_OPT_ATTN_KERNEL: *value = p->attn_kernel; return GEMM_F16_OK;
     case GEMM_F16_OPT_ATTN_SPLIT: *value = p->attn_split; return GEMM_F16_OK;
     case GEMM_F16_OPT_A_REPACK: *value = p->a_repack; return GEMM_F16_OK;
+    case GEMM_F16_OPT_KERNEL_TIMING: *value = p->kernel_timing; return GEMM_F16_OK;
     case GEMM_F16_INFO_NUM_SMS: *value = p->num_sms; return GEMM_F16_OK;
     case GEMM_F16_INFO_MAX_PAIRS: *value = p->max_pairs; return GEMM_F16_OK;
     case GEMM_F16_INFO_MAX_QUADS: *value = p->max_quads; return GEMM_F16_OK;
     default: return GEMM_F16_ERR_INVALID_ARG;
   }
+}
+
+int gemm_f16_kernel_time(gemm_f16_plan_t p, double* total_ms, int64_t* launches) {
+  if (!p || !total_ms || !launches) return GEMM_F16_ERR_INVALID_ARG;
+  *total_ms = 0.0;
+  *launches = 0;
+  DeviceGuard g(p->device);
+  int rc = GEMM_F16_OK;
+  double sum = 0.0;
+  int64_t n = 0;
+  for (size_t i = 0; i + 1 < p->timing_marks.size(); i += 2) {
+    cudaEvent_t a = p->timing_marks[i], b = p->timing_marks[i + 1];
+    float ms = 0.0f;
+    cudaError_t e = cudaEventSynchronize(b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, a, b);
+    if (e != cudaSuccess) {
+      if (!rc) rc = cuda_fail(e, "kernel timing event");
+    } else {
+      sum += ms;
+      ++n;
+    }
+  }
+  for (cudaEvent_t ev : p->timing_marks) p->timing_pool.push_back(ev);
+  p->timing_marks.clear();
+  if (rc) return rc;
+  *total_ms = sum;
+  *launches = n;
+  return GEMM_F16_OK;
 }
 
 }  // extern "C"

@@ -19,7 +19,9 @@ torchrun each rank runs an independent replica on its own GPU (the GEMM has
 no exchange step, so there is no collective on the data path).
 
 Extra keys: roofline (dominant kernel vs the measured dense 16-bit tensor
-peak), cpu_baseline (the FP64 oracle on a bounded row sample, host cores,
+peak, or HBM bandwidth: its work per launch over the mean duration of its
+launches, timed with CUDA events on its own stream in a second pass of the
+timed region's steps; the whole step's figure beside it), cpu_baseline (the FP64 oracle on a bounded row sample, host cores,
 with the host's machine type and CPU model), e2e (same metric through
 gemm_f16_run_host with pinned host buffers, copies inside the timed region),
 clocks (nvidia-smi sampled under load), sustained (the same step re-timed
@@ -126,6 +128,31 @@ def load_peaks():
 def compulsory_bytes(w: si.Workload) -> int:
     """Bytes a GEMM must move at least: read A and B once, write C once (fp16)."""
     return 2 * (w.M * w.K + w.K * w.N + w.M * w.N)
+
+
+def kernel_bytes(w: si.Workload) -> int:
+    """Bytes the product kernel must move at least: read A and B once, then
+    write C (fp16), or with split_k > 1 the split_k FP32 partial tiles that
+    the reduction kernel adds."""
+    out = 4 * w.split_k * w.M * w.N if w.split_k > 1 else 2 * w.M * w.N
+    return 2 * (w.M * w.K + w.K * w.N) + out
+
+
+KERNEL_TIMING_NOTE = ("algorithmic work per launch / the product (or attention) kernel's "
+                      "duration per launch, the smaller of two CUDA-event upper bounds: "
+                      "kernel_ms_events (events on the launch stream directly around each "
+                      "launch, over the timed region's steps run again right after it; the "
+                      "event pair also serialises each launch behind the previous kernel) and "
+                      "the timed region's step time (all of a step's launches, overlapped); "
+                      "step_achieved divides by the step time")
+
+
+def kernel_duration(kms: float, ms_step: float):
+    """(ms per launch, which bound) for the roofline: both the event-pair
+    time and the step time bound the kernel's own duration from above."""
+    if kms <= ms_step:
+        return kms, "kernel events"
+    return ms_step, "timed-region step time"
 
 
 def _traffic_entry(workload: str):
@@ -336,6 +363,29 @@ def sustained_record(step, barrier, stream, dev, world, ms_step, flops_per_step,
             "seconds": ms * 1e-3,
             "frac_of_sustained_peak": value / world / peak_sustained if peak_sustained else None,
             "frac_of_burst_peak": value / world / peak_burst, "clocks": clocks}
+
+
+def kernel_timing_pass(g, plan, step, barrier, steps: int, start: int, world, dev):
+    """Mean duration of the dominant kernel's launches: the timed region's
+    steps run once more, right after it, with the library's kernel timing
+    records on (a CUDA event pair on the launch stream directly around each
+    product / attention kernel launch, read back with gemm_f16_kernel_time).
+    A separate pass because an event between two launches stops the next
+    kernel's set-up from overlapping the previous kernel (programmatic
+    dependent launch), which would slow the step being timed.  Returns
+    (ms per launch, max over ranks; launches timed on this rank)."""
+    plan.kernel_time()                      # forget earlier records
+    plan.set_option(g.OPT_KERNEL_TIMING, 1)
+    try:
+        for i in range(steps):
+            step(start + i)
+        barrier()
+    finally:
+        plan.set_option(g.OPT_KERNEL_TIMING, 0)
+    ms, n = plan.kernel_time()
+    if n <= 0:
+        raise RuntimeError("no kernel launch was timed")
+    return max_over_ranks(ms / n, world, dev), n
 
 
 def host_record() -> dict:
@@ -624,10 +674,19 @@ def run_attention(args):
                                      args.steps, peak_sus, peak)
         if plan.status() != 0:
             raise RuntimeError("device status error in the sustained region")
-    achieved = float(w.flops) / (ms_step * 1e-3) / 1e12
+    kms_ev, klaunches = kernel_timing_pass(g, plan, step, barrier, args.steps, 0, world, dev)
+    if plan.status() != 0:
+        raise RuntimeError("device status error in the kernel timing pass")
+    kms, kfrom = kernel_duration(kms_ev, ms_step)
+    achieved = float(w.flops) / (kms * 1e-3) / 1e12
+    step_achieved = float(w.flops) / (ms_step * 1e-3) / 1e12
     cbytes = 2.0 * w.D * w.B * w.H * (2 * w.Sq + 2 * w.Skv)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
+                "kernel_ms_per_launch": kms, "duration_from": kfrom, "kernel_ms_events": kms_ev,
+                "kernel_launches_timed": klaunches,
+                "step_achieved": step_achieved, "step_frac": step_achieved / peak,
+                "achieved_from": KERNEL_TIMING_NOTE,
                 "peak_source": f"{peak_kind} dense bf16 burst (fp16 runs at the same rate)",
                 "algorithmic_flops_per_launch": float(w.flops),
                 "traffic": load_traffic(w.name) if use_pair else None,
@@ -684,7 +743,8 @@ def run_attention(args):
                                        if graph is not None else "one host call per step")),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "sustained": sustained,
-            "gpu_launches": args.steps * launches_per_step, "pct_of_peak": 100.0 * achieved / peak,
+            "gpu_launches": args.steps * launches_per_step,
+            "pct_of_peak": 100.0 * step_achieved / peak,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -783,23 +843,37 @@ def run_ours(args):
                                      args.steps, peak_sus, peak)
         if plan.status() != 0:
             raise RuntimeError("device status error in the sustained region")
-    # Dominant kernel: the GEMM kernel.  For split workloads the step also
-    # holds the reduce launch; the figure is then the whole step's.  Bound:
-    # tensor if the workload's FLOP per compulsory byte is above the ridge
-    # point (tensor peak / HBM bandwidth), else HBM.
+    # Dominant kernel: the product kernel (single-CTA, pair or cluster of
+    # four), timed on its own in a second pass of the same steps; the step
+    # figures (all of a step's launches: repack, K-halves merge, split
+    # reduction) sit beside it.  Bound: tensor if the workload's FLOP per
+    # compulsory byte is above the ridge point (tensor peak / HBM
+    # bandwidth), else HBM.
+    kms_ev, klaunches = kernel_timing_pass(g, plan, step, barrier, args.steps, 0, world, dev)
+    if plan.status() != 0:
+        raise RuntimeError("device status error in the kernel timing pass")
+    kms, kfrom = kernel_duration(kms_ev, ms_step)
     cbytes = compulsory_bytes(w)
+    kbytes = kernel_bytes(w)
     ridge = peak * 1e12 / (peak_hbm * 1e9)
+    timing = {"kernel_ms_per_launch": kms, "duration_from": kfrom, "kernel_ms_events": kms_ev,
+              "kernel_launches_timed": klaunches, "achieved_from": KERNEL_TIMING_NOTE}
     if w.flops / cbytes >= ridge:
-        achieved = float(w.flops) / (ms_step * 1e-3) / 1e12
+        achieved = float(w.flops) / (kms * 1e-3) / 1e12
+        step_achieved = float(w.flops) / (ms_step * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak,
                     "peak_source": f"{peak_kind} dense bf16 burst (fp16 runs at the same rate)",
-                    "algorithmic_flops_per_launch": float(w.flops)}
+                    "algorithmic_flops_per_launch": float(w.flops), **timing,
+                    "step_achieved": step_achieved, "step_frac": step_achieved / peak}
     else:
-        achieved = cbytes / (ms_step * 1e-3) / 1e9
+        achieved = kbytes / (kms * 1e-3) / 1e9
+        step_achieved = cbytes / (ms_step * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_hbm, "unit": "GB/s",
                     "frac": achieved / peak_hbm, "peak_source": f"{peak_kind} HBM copy bandwidth",
-                    "algorithmic_bytes_per_launch": float(cbytes),
+                    "algorithmic_bytes_per_launch": float(kbytes), **timing,
+                    "step_achieved": step_achieved, "step_frac": step_achieved / peak_hbm,
+                    "step_algorithmic_bytes": float(cbytes),
                     "tflops": float(w.flops) / (ms_step * 1e-3) / 1e12}
     roofline["traffic"] = load_traffic(w.name)
     roofline["tensor_pipe_ncu"] = load_tensor_pipe(w.name)

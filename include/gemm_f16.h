@@ -145,7 +145,23 @@ typedef enum gemm_f16_option {
      * copies A once into plan-owned rows of whole lines (grown on the
      * stream like the split workspace, kept for later runs) and the product
      * reads that copy.  Results are bit-identical either way. */
-    GEMM_F16_OPT_A_REPACK = 9
+    GEMM_F16_OPT_A_REPACK = 9,
+    /* Kernel timing records: 0 = off (default), 1 = on.  While on, every
+     * gemm_f16_run / gemm_f16_run_ex / gemm_f16_run_host call records a pair
+     * of CUDA events on the launch stream directly before and after its
+     * product kernel (the single-CTA, pair or cluster-of-four kernel; not
+     * the repack of A, the K-halves merge or the split reduction), and every
+     * attn_f16_fwd / attn_f16_fwd_host call does the same around its
+     * attention kernel (not the merge of key ranges), so that
+     * gemm_f16_kernel_time can report the kernels' own durations.  The event
+     * between two launches stops a kernel from starting before the previous
+     * one on the stream has ended (the programmatic dependent launch that
+     * otherwise overlaps their set-up), so timed runs are a little slower
+     * back to back.  Nothing is recorded while the stream is being captured
+     * into a graph, or once 65536 pairs are waiting to be read.  Events come
+     * from a plan-owned pool that grows on demand (cudaEventCreate) and is
+     * freed with the plan. */
+    GEMM_F16_OPT_KERNEL_TIMING = 10
 } gemm_f16_option;
 
 /*
@@ -282,6 +298,18 @@ enum {
 
 /* Read an option's current value, or one of the GEMM_F16_INFO_* facts. */
 int gemm_f16_get_option(gemm_f16_plan_t plan, int option, int64_t *value);
+
+/*
+ * Durations of the kernels timed since the last call (GEMM_F16_OPT_KERNEL_TIMING):
+ * waits for each recorded pair's second event (cudaEventSynchronize), adds
+ * up the elapsed times, returns the events to the plan's pool and forgets
+ * the pairs.  *total_ms receives the sum in milliseconds and *launches the
+ * number of timed launches (0 and 0.0 when none was recorded).  Returns
+ * GEMM_F16_OK, GEMM_F16_ERR_INVALID_ARG for a null argument, or
+ * GEMM_F16_ERR_CUDA if an event cannot be read (the pairs are forgotten
+ * either way).
+ */
+int gemm_f16_kernel_time(gemm_f16_plan_t plan, double *total_ms, int64_t *launches);
 
 /* Static description of an error code (never NULL). */
 const char *gemm_f16_strerror(int code);

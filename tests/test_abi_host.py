@@ -86,6 +86,8 @@ def test_null_plan_is_rejected(lib):
     assert lib.gemm_f16_run(None, 8, 8, 8, P, 8, P, 8, P, 8, 1, None) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_status(None) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_set_option(None, 1, 5) == g.ERR_INVALID_ARG
+    ms, n = ctypes.c_double(1.0), ctypes.c_int64(1)
+    assert lib.gemm_f16_kernel_time(None, ctypes.byref(ms), ctypes.byref(n)) == g.ERR_INVALID_ARG
     assert lib.gemm_f16_destroy(None) == g.OK
 
 
