@@ -103,7 +103,7 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* statu
                                        unsigned long long timeout_ns, volatile int* abort_flag) {
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::mbar_try_wait_poll(bar, parity)) return true;
     if (*abort_flag) return false;
     if (ptx::globaltimer() - t0 > timeout_ns) {
       *abort_flag = 1;
@@ -116,7 +116,7 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* statu
 
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
                                            volatile int* abort_flag) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (ptx::mbar_try_wait_poll(bar, parity)) return true;
   return wait_slow(bar, parity, p.status, p.timeout_ns, abort_flag);
 }
 

@@ -154,7 +154,7 @@ __device__ __forceinline__ Item decode_unit(int u, const Params& p) {
 
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Params& p,
                                            volatile int* abort_flag) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (ptx::mbar_try_wait_poll(bar, parity)) return true;
   return attn::wait_slow(bar, parity, p.status, p.timeout_ns, abort_flag);
 }
 
@@ -165,7 +165,7 @@ __device__ __noinline__ bool wait_sleepy(uint32_t bar, uint32_t parity, const Pa
                                          volatile int* abort_flag) {
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::mbar_try_wait_poll(bar, parity)) return true;
     if (*abort_flag) return false;
     if (ptx::globaltimer() - t0 > p.timeout_ns) {
       *abort_flag = 1;
