@@ -158,6 +158,13 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   return attn::wait_slow(bar, parity, p.status, p.timeout_ns, abort_flag);
 }
 
+// The same wait suspending in hardware between checks (copy and MMA threads).
+__device__ __forceinline__ bool wait_phase_suspend(uint32_t bar, uint32_t parity, const Params& p,
+                                                   volatile int* abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return attn::wait_slow<true>(bar, parity, p.status, p.timeout_ns, abort_flag);
+}
+
 // A wait that sleeps between polls (256 ns), for the epilogue warps, which
 // wait most of an item for its row sums: polling at full rate would take
 // issue slots from the softmax, MMA and copy warps on the same schedulers.
@@ -218,7 +225,7 @@ __device__ __forceinline__ Issued producer_role(const CUtensorMap* tmQ, const CU
   bool ok = true;
   for (int u = cluster; u < p.n_units && ok; u += nclusters) {
     const Item w = decode_unit(u, p);
-    if (n.qloads > 0 && !wait_phase(b.q_empty, (n.qloads - 1) & 1u, p, abort_flag)) break;
+    if (n.qloads > 0 && !wait_phase_suspend(b.q_empty, (n.qloads - 1) & 1u, p, abort_flag)) break;
     if (rank == 0) ptx::mbar_arrive_expect_tx_relaxed(b.q_full, 2 * Q_BYTES);
 #pragma unroll
     for (int c = 0; c < HD / 64; ++c)
@@ -227,7 +234,7 @@ __device__ __forceinline__ Issued producer_role(const CUtensorMap* tmQ, const CU
     ++n.qloads;
     bool first = true;
     auto fill = [&](bool is_k, int j) -> bool {
-      if (!wait_phase(b.empty + 8 * pos.stage, producer_wait_parity(pos), p, abort_flag))
+      if (!wait_phase_suspend(b.empty + 8 * pos.stage, producer_wait_parity(pos), p, abort_flag))
         return false;
       if (rank == 0) ptx::mbar_arrive_expect_tx_relaxed(b.full + 8 * pos.stage, 2 * SLOT_BYTES);
       if (!(first && u == p.fault_unit && rank == 0)) {
@@ -271,9 +278,9 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
   // gs - 1 in registers; after an item's last S, q_empty hands Q back.
   auto issue_qk = [&](uint32_t gs, bool last_of_item) -> bool {
     if (gs > 0) {
-      if (!wait_phase(b.s_free, (gs - 1) & 1u, p, abort_flag)) return false;
+      if (!wait_phase_suspend(b.s_free, (gs - 1) & 1u, p, abort_flag)) return false;
     }
-    if (!wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag))
+    if (!wait_phase_suspend(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag))
       return false;
     ptx::tc_fence_after();
     const uint32_t k_addr = base + OFF_RING + pos.stage * SLOT_BYTES;
@@ -296,7 +303,7 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
   bool ok = true;
   for (int u = cluster; u < p.n_units && ok; u += nclusters, ++ki) {
     const int nb = decode_unit(u, p).nb;
-    if (!wait_phase(b.q_full, ki & 1u, p, abort_flag)) break;
+    if (!wait_phase_suspend(b.q_full, ki & 1u, p, abort_flag)) break;
     ptx::tc_fence_after();
     ok = issue_qk(g0, nb == 1);
     for (int j = 0; j < nb && ok; ++j) {
@@ -307,14 +314,14 @@ __device__ __forceinline__ void mma_role(const Params& p, uint32_t base, uint32_
       }
       // The split barrier's WAIT: both CTAs' P rows are in tensor memory.
       const uint32_t pb = gj & 1u;
-      if (!wait_phase(b.p_full + 8 * pb, (gj >> 1) & 1u, p, abort_flag) ||
-          !wait_phase(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag)) {
+      if (!wait_phase_suspend(b.p_full + 8 * pb, (gj >> 1) & 1u, p, abort_flag) ||
+          !wait_phase_suspend(b.full + 8 * pos.stage, consumer_wait_parity(pos), p, abort_flag)) {
         ok = false;
         break;
       }
       // The unit's first O += P V overwrites O: both CTAs' epilogue warps
       // must have read the previous unit's O.
-      if (j == 0 && ki > 0 && !wait_phase(b.o_free, (ki - 1) & 1u, p, abort_flag)) {
+      if (j == 0 && ki > 0 && !wait_phase_suspend(b.o_free, (ki - 1) & 1u, p, abort_flag)) {
         ok = false;
         break;
       }

@@ -69,8 +69,10 @@ __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
 }
 
 // try_wait without a suspend-time hint: the loops around it poll the
-// barrier.  The attention kernels keep this form (with the hint the 4 x 16 x
-// 4096^2 forward pass measured ~1.5 % slower, power-capped either way).
+// barrier.  The attention kernels' softmax and epilogue warps keep this form
+// (their waits are on the critical path of every key block; with the hint
+// the 4 x 16 x 4096^2 forward pass measured ~1.5 % slower, power-capped
+// either way).
 __device__ __forceinline__ bool mbar_try_wait_poll(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
