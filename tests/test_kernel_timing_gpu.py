@@ -130,3 +130,34 @@ def test_option_values(g):
                 plan.set_option(g.OPT_KERNEL_TIMING, bad)
         plan.set_option(g.OPT_KERNEL_TIMING, 1)
         assert plan.get_option(g.OPT_KERNEL_TIMING) == 1
+
+
+def test_layout_and_host_entry_points_record_their_product(g):
+    import torch
+    M, N, K = 640, 384, 704
+    w = si.custom(M, N, K, seed=21)
+    A_bits, B_bits = w.pair_bits(0)
+    want = oracle.gemm_f16(A_bits, B_bits)
+    with g.Plan(0) as plan:
+        plan.set_option(g.OPT_KERNEL_TIMING, 1)
+        # transposed A and B through gemm_f16_run_ex (matmul passes .t() views)
+        A = gpu_util.to_device(np.ascontiguousarray(A_bits.T)).t()
+        B = gpu_util.to_device(np.ascontiguousarray(B_bits.T)).t()
+        C = g.matmul(plan, A, B)
+        torch.cuda.synchronize()
+        parity.check(C.cpu().numpy().astype(np.float64), want, "TT with timing on")
+        ms, n = plan.kernel_time()
+        assert n == 1 and ms > 0.0
+        # host operands: the copies are not timed, the product is
+        hA = torch.from_numpy(A_bits.view(np.float16)).pin_memory()
+        hB = torch.from_numpy(B_bits.view(np.float16)).pin_memory()
+        hC = torch.empty((M, N), dtype=torch.float16).pin_memory()
+        s = torch.cuda.current_stream()
+        for _ in range(3):
+            g.gemm_f16_run_host(plan.handle, M, N, K, hA.data_ptr(), K, hB.data_ptr(), N,
+                                hC.data_ptr(), N, 1, int(s.cuda_stream))
+        s.synchronize()
+        assert plan.status() == g.OK
+        parity.check(hC.numpy().astype(np.float64), want, "host operands with timing on")
+        ms, n = plan.kernel_time()
+        assert n == 3 and ms > 0.0
