@@ -138,6 +138,11 @@ SWEEP = [
     (1, 1, 1), (1, 8, 8), (8, 1, 16), (7, 9, 13), (16, 16, 16), (33, 65, 17),
     (127, 255, 63), (129, 257, 65), (128, 256, 64), (200, 300, 100),
     (64, 1000, 72), (1000, 64, 200), (385, 513, 1000), (256, 264, 8),
+    # extreme aspect ratios at larger sizes: one row across nine column
+    # tiles of the cluster-of-four kernel, eight columns down many row
+    # tiles, K = 1, long K on thin outputs, a K one past a k-block
+    (1, 4104, 3000), (4000, 8, 3000), (2048, 2048, 1), (3, 1030, 4100),
+    (1030, 24, 4100), (520, 1536, 65),
 ]
 
 
