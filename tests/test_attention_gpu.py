@@ -152,7 +152,10 @@ def test_attn_4096_full(plan):
 
 
 SHAPES = [(1, 1, 1, 1), (1, 1, 1, 1000), (1, 1, 129, 65), (2, 2, 64, 64), (1, 3, 513, 127),
-          (3, 1, 257, 2049)]
+          (3, 1, 257, 2049),
+          # one query row against many keys (key split with a single row),
+          # many rows against one key, and many small heads
+          (1, 2, 1, 6000), (1, 1, 3000, 1), (4, 24, 33, 70)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
